@@ -1,0 +1,223 @@
+/*
+ * libpagedattn — paged KV-cache attention for one NVIDIA GB300 (sm_103a).
+ *
+ * The KV cache of every sequence lives in fixed-size physical blocks of
+ * `block_size` tokens; a per-sequence block table maps logical block
+ * floor(pos / block_size) to a physical block id, and the token sits at
+ * offset pos mod block_size inside it ("High-Throughput Local LLM
+ * Infrastructure: Architecting a Distributed Go API Gateway for vLLM &
+ * PagedAttention Clusters", section 1.2 "PagedAttention Mechanics & Virtual
+ * Page Tables"; "Inside vLLM: Anatomy of a High-Throughput LLM Inference
+ * System (2025)", section "Physical Block Mapping and Kernel Invocation").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All pointers named *_cache, q, k, v, out, block_tables, seq_lens,
+ *    ctx_lens, cu_q_lens, slot_mapping, seq_ids, positions and workspace are
+ *    DEVICE pointers on the current CUDA device, owned by the caller. The
+ *    library allocates nothing and keeps no pointer after a call returns.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream). Host-side argument errors return a negative
+ *    status BEFORE anything is launched, and then no output is touched.
+ *  - Errors found on the device (an out-of-range block id or slot, a
+ *    sequence longer than its table or than max_seq_len, a bounded wait that
+ *    ran out) never trap: the kernel skips the bad access, records the first
+ *    error code in a per-device status word and carries on. pa_get_status()
+ *    reads and clears that word. Rows hit by such an error hold unspecified
+ *    values.
+ *  - Cache layout: k_cache and v_cache are separate pools, each
+ *    [num_blocks][num_kv_heads][block_size][head_dim], contiguous, so one
+ *    (block, KV head) tile of block_size x head_dim elements is contiguous.
+ *  - q, k, v, out and the caches of one call share one dtype (pa_dtype).
+ *    Arithmetic is fp32 (scores, softmax, accumulation) whatever the I/O
+ *    dtype.
+ *  - Grouped-query attention: num_q_heads must be a multiple of
+ *    num_kv_heads; query head h reads KV head h / (num_q_heads/num_kv_heads).
+ *  - Device pointers to tensors must be 16-byte aligned.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_dtype {
+  PA_F32 = 0,
+  PA_F16 = 1,
+  PA_BF16 = 2
+} pa_dtype;
+
+/* Status codes. 0 is success; every error is negative. */
+#define PA_OK 0
+#define PA_ERR_ARG (-1)         /* null pointer, negative size, bad stride */
+#define PA_ERR_DTYPE (-2)       /* dtype not supported by this entry point  */
+#define PA_ERR_HEADS (-3)       /* num_q_heads not a multiple of num_kv_heads */
+#define PA_ERR_BLOCKSIZE (-4)   /* block_size must be 16 or 32              */
+#define PA_ERR_WORKSPACE (-5)   /* workspace null or smaller than required  */
+#define PA_ERR_ALIAS (-6)       /* copy_blocks: dst repeated or also a src  */
+#define PA_ERR_BLOCK_OOB (-7)   /* device: block id / slot outside the pool */
+#define PA_ERR_SEQLEN (-8)      /* device: length < 1, > table, > max given */
+#define PA_ERR_CUDA (-9)        /* a CUDA runtime call failed               */
+#define PA_ERR_UNSUPPORTED (-10)/* head_dim (or shape) not supported        */
+#define PA_ERR_TIMEOUT (-11)    /* device: a bounded wait ran out           */
+#define PA_ERR_ALIGN (-12)      /* a tensor pointer is not 16-byte aligned  */
+
+/* Human-readable name of a status code (static storage). */
+const char* pa_strerror(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int pa_version(void);
+
+/*
+ * pa_get_status — synchronise `stream`, return the first device-side error
+ * recorded since the last call (PA_OK if none), and clear it. The status
+ * word is per device and shared by all streams.
+ */
+int pa_get_status(void* stream);
+
+/*
+ * pa_slot_mapping — slot of every new token.
+ *   slot_mapping[t] = block_tables[seq_ids[t]][positions[t] / block_size]
+ *                     * block_size + positions[t] % block_size
+ * (logical block index and block offset of section 1.2 of the "High-
+ * Throughput Local LLM Infrastructure" page).
+ *   block_tables : int32 [num_seqs][max_blocks_per_seq]
+ *   seq_ids      : int32 [num_tokens], 0 <= seq_ids[t] < num_seqs
+ *   positions    : int32 [num_tokens], 0 <= positions[t] < max_blocks_per_seq*block_size
+ *   slot_mapping : int64 [num_tokens] (output)
+ * A token whose seq id, position or physical block (>= num_blocks) is out of
+ * range gets slot -1 and PA_ERR_BLOCK_OOB is recorded. num_tokens == 0 is a
+ * no-op.
+ */
+int pa_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t num_seqs,
+                    const int32_t* seq_ids, const int32_t* positions, int64_t num_tokens,
+                    int32_t block_size, int32_t num_blocks, int64_t* slot_mapping, void* stream);
+
+/*
+ * pa_reshape_and_cache — scatter new tokens' K and V into their cache slots
+ * (section 2.1 "PagedAttention Memory Allocation Life-Cycle", step 4: the
+ * kernels write new K/V into the assigned physical blocks).
+ *   k, v         : [num_tokens][num_kv_heads][head_dim], contiguous
+ *   slot_mapping : int64 [num_tokens]; slot s writes block s / block_size,
+ *                  offset s % block_size; s < 0 skips the token (padding);
+ *                  s >= num_blocks*block_size records PA_ERR_BLOCK_OOB and
+ *                  skips the token
+ *   k_cache, v_cache : the pools (layout above), updated in place
+ * Bit-exact copy. head_dim * sizeof(dtype) must be a multiple of 16.
+ * Two tokens with the same slot race (one of them wins).
+ */
+int pa_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                         void* k_cache, void* v_cache, int32_t num_blocks, int32_t block_size,
+                         int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype, void* stream);
+
+/*
+ * pa_copy_blocks — copy-on-write copies: for every pair, the whole K block
+ * and V block (all KV heads) dst <- src ("High-Throughput Local LLM
+ * Infrastructure...", section 1.2, "Reference Counting & Copy-on-Write";
+ * "03 - PagedAttention & the vLLM V1 Architecture", section "The block
+ * table walkthrough": the whole block is copied when a write inside it would
+ * diverge).
+ *   src_dst_pairs : HOST int64 [num_pairs][2] (src, dst). The pairs are
+ *                   validated on the host before any launch: every id in
+ *                   [0, num_blocks) else PA_ERR_BLOCK_OOB; no dst repeated
+ *                   and no dst equal to any src, else PA_ERR_ALIAS. They are
+ *                   passed to the kernel by value (no device copy), so the
+ *                   host array may be reused as soon as the call returns.
+ *   block_bytes   : bytes of one block of one pool
+ *                   (num_kv_heads*block_size*head_dim*sizeof(dtype)),
+ *                   a multiple of 16.
+ * Bit-exact. num_pairs == 0 is a no-op.
+ */
+int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst_pairs, int32_t num_pairs,
+                   int32_t num_blocks, int64_t block_bytes, void* stream);
+
+/*
+ * Split-KV partitioning of decode. A sequence of L keys is cut into
+ * ceil(L / partition_size) partitions; each is reduced to (m, l, o~)
+ * partials (running max, sum of exp(s - m), unnormalised output) in the
+ * workspace, and a second pass merges them:
+ *   out = sum_p exp(m_p - M) o~_p / sum_p exp(m_p - M) l_p,  M = max_p m_p.
+ * A sequence with one partition is written directly. partition_size must be
+ * a positive multiple of block_size, or 0 for the library's choice, which
+ * depends on (num_seqs, num_kv_heads, num_q_heads, block_size, max_seq_len)
+ * and the current device's SM count.
+ *
+ * pa_decode_partition_size returns the partition size a call with these
+ * arguments uses (resolving 0), or a negative status.
+ * pa_decode_workspace_size returns the workspace bytes pa_decode needs for
+ * these arguments (0 when no sequence can need more than one partition).
+ * The partials are fp32: num_seqs*num_q_heads*max_parts*(head_dim+2)*4
+ * bytes, max_parts = ceil(max_seq_len / partition_size).
+ */
+int32_t pa_decode_partition_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t block_size, int32_t max_seq_len, int32_t partition_size);
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t block_size, int32_t max_seq_len,
+                                int32_t partition_size);
+
+/*
+ * pa_decode — paged decode attention, one new query token per sequence
+ * ("03 - PagedAttention & the vLLM V1 Architecture", section "The attention
+ * kernel side": walk the block table, fetch each block's K and V tiles,
+ * compute softmax(Q K^T / sqrt(d)) V over the gathered tiles; the attention
+ * equation of "Inside vLLM...", section "Physical Block Mapping and Kernel
+ * Invocation").
+ *   q            : [num_seqs][num_q_heads][head_dim]
+ *   block_tables : int32 [num_seqs][max_blocks_per_seq]
+ *   seq_lens     : int32 [num_seqs]; sequence i attends to keys
+ *                  0 .. seq_lens[i]-1 (its newest token included: cache it
+ *                  with pa_reshape_and_cache first)
+ *   max_seq_len  : an upper bound of seq_lens (host value; sizes the grid);
+ *                  a longer sequence records PA_ERR_SEQLEN
+ *   scale        : multiplies q.k (usually 1/sqrt(head_dim))
+ *   out          : [num_seqs][num_q_heads][head_dim]
+ *   workspace    : device scratch of pa_decode_workspace_size() bytes (may be
+ *                  NULL when that is 0); contents need no initialisation
+ * Supported: block_size 16 or 32; fp16/bf16 with head_dim 64 or 128 (tensor-
+ * core path); fp32 with head_dim a multiple of 32 up to 256 (CUDA-core
+ * path). Each KV block is read once per KV head: all query heads of a GQA
+ * group are processed together.
+ */
+int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+              int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+              int32_t num_blocks, float scale, void* out, int32_t partition_size, void* workspace,
+              size_t workspace_bytes, pa_dtype dtype, void* stream);
+
+/*
+ * pa_chunked_prefill — attention of a mixed batch (prefill chunks and
+ * decode rows) over the paged context (chunked prefill: "Tech Radar: vLLM v1
+ * Production Engine Architecture...", section 3 "Dynamic Chunked Prefill").
+ *   q          : [total_q][num_q_heads][head_dim]; sequence i owns rows
+ *                cu_q_lens[i] .. cu_q_lens[i+1]-1
+ *   cu_q_lens  : int32 [num_seqs+1], cu_q_lens[0] = 0, non-decreasing
+ *   ctx_lens   : int32 [num_seqs]; tokens before sequence i's chunk. Row r
+ *                of the chunk sits at position ctx_lens[i] + r and attends to
+ *                keys 0 .. ctx_lens[i] + r (causal inside the chunk). The
+ *                chunk's own K/V must already be cached (pa_reshape_and_cache
+ *                of its tokens first).
+ *   max_q_len, max_kv_len : host upper bounds of the q_len and of
+ *                ctx_len + q_len over the batch (they size the grids)
+ *   out        : [total_q][num_q_heads][head_dim]
+ *   workspace  : pa_chunked_prefill_workspace_size() bytes
+ * Rows with q_len == 1 go through the decode path; longer chunks through a
+ * tcgen05 tensor-core kernel (fp16/bf16, head_dim 128).
+ */
+size_t pa_chunked_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t block_size, int32_t max_kv_len);
+int pa_chunked_prefill(const void* q, const int32_t* cu_q_lens, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* ctx_lens,
+                       int32_t num_seqs, int32_t max_q_len, int32_t max_kv_len, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                       float scale, void* out, void* workspace, size_t workspace_bytes, pa_dtype dtype,
+                       void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -1,0 +1,27 @@
+"""libpagedattn: paged KV-cache attention for one NVIDIA GB300 (sm_103a).
+
+The compute lives in hand-written CUDA kernels behind a C ABI
+(include/pagedattn.h, built into libpagedattn.so by build.build()); this
+package is the thin ctypes binding plus the host-side step helper.
+"""
+from ._binding import (  # noqa: F401
+    EXPORTS,
+    PA_BF16,
+    PA_F16,
+    PA_F32,
+    PagedAttnError,
+    exported_symbols,
+    load,
+    pa_chunked_prefill,
+    pa_chunked_prefill_workspace_size,
+    pa_copy_blocks,
+    pa_decode,
+    pa_decode_partition_size,
+    pa_decode_workspace_size,
+    pa_get_status,
+    pa_reshape_and_cache,
+    pa_slot_mapping,
+    pa_strerror,
+    pa_version,
+)
+from .builder import LIB_PATH, build  # noqa: F401

@@ -1,0 +1,340 @@
+// C-ABI entry points of libpagedattn: host-side argument checks, tensor-map
+// encoding, split-KV planning and dispatch to the kernel launchers.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+#include <unordered_set>
+#include <vector>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+// First device-side error since the last pa_get_status() (one word per device).
+__device__ int g_pa_status;
+
+namespace pa {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_status_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_encode_tried = false;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(pa_dtype dt) {
+  switch (dt) {
+    case PA_F32: return 4;
+    case PA_F16: return 2;
+    case PA_BF16: return 2;
+  }
+  return 0;
+}
+
+bool head_dim_supported(pa_dtype dt, int32_t d) {
+  if (dt == PA_F32) return d >= 32 && d <= 256 && d % 32 == 0;
+  return d == 64 || d == 128;
+}
+}  // namespace
+
+int* device_status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pa_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+int num_sms_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_num_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    g_num_sms[dev] = n;
+  }
+  return g_num_sms[dev];
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode_tried) {
+    g_encode_tried = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode;
+}
+
+int make_2d_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t cols, int64_t row_stride_elems,
+                       pa_dtype dt, int32_t box_rows, int32_t box_cols) {
+  auto fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  if (dt == PA_F32) return PA_ERR_DTYPE;
+  const CUtensorMapDataType t = dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t gstride[1] = {(cuuint64_t)row_stride_elems * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, t, 2, const_cast<void*>(base), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+int make_kv_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t head_dim, pa_dtype dt,
+                       int32_t box_rows) {
+  return make_2d_tensor_map(map, base, rows, head_dim, head_dim, dt, box_rows, 64);
+}
+
+static int32_t auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seq_len) {
+  const int32_t group = num_q_heads / num_kv_heads;
+  const int64_t units = (int64_t)num_seqs * num_kv_heads * ((group + 15) / 16);
+  // About four waves of two resident CTAs per SM before splitting stops.
+  const int64_t target = 8LL * num_sms_current_device();
+  int64_t parts = (target + units - 1) / units;
+  if (parts < 1) parts = 1;
+  const int64_t want = (max_seq_len + parts - 1) / parts;
+  int32_t part = 256;
+  while (part < want && part < 1024) part *= 2;
+  return part;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* pa_strerror(int s) {
+  switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_ARG: return "PA_ERR_ARG: invalid argument";
+    case PA_ERR_DTYPE: return "PA_ERR_DTYPE: dtype not supported here";
+    case PA_ERR_HEADS: return "PA_ERR_HEADS: num_q_heads is not a multiple of num_kv_heads";
+    case PA_ERR_BLOCKSIZE: return "PA_ERR_BLOCKSIZE: block_size must be 16 or 32";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing or too small";
+    case PA_ERR_ALIAS: return "PA_ERR_ALIAS: copy_blocks destination repeated or also a source";
+    case PA_ERR_BLOCK_OOB: return "PA_ERR_BLOCK_OOB: block id or slot outside the pool";
+    case PA_ERR_SEQLEN: return "PA_ERR_SEQLEN: sequence length out of range";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA runtime error";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: shape not supported";
+    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: a bounded device wait ran out";
+    case PA_ERR_ALIGN: return "PA_ERR_ALIGN: pointer not 16-byte aligned";
+  }
+  return "unknown status";
+}
+
+int pa_version(void) { return 100; }
+
+int pa_get_status(void* stream) {
+  int* p = device_status_ptr();
+  if (!p) return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  const int zero = 0;
+  if (v != 0 && cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return PA_ERR_CUDA;
+  return v;
+}
+
+int pa_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t num_seqs,
+                    const int32_t* seq_ids, const int32_t* positions, int64_t num_tokens, int32_t block_size,
+                    int32_t num_blocks, int64_t* slot_mapping, void* stream) {
+  if (num_tokens < 0 || num_seqs < 0 || max_blocks_per_seq < 1 || num_blocks < 1) return PA_ERR_ARG;
+  if (block_size != 16 && block_size != 32) return PA_ERR_BLOCKSIZE;
+  if (num_tokens == 0) return PA_OK;
+  if (!block_tables || !seq_ids || !positions || !slot_mapping) return PA_ERR_ARG;
+  int* st = device_status_ptr();
+  if (!st) return PA_ERR_CUDA;
+  return launch_slot_mapping(block_tables, max_blocks_per_seq, num_seqs, seq_ids, positions, num_tokens, block_size,
+                             num_blocks, slot_mapping, st, static_cast<cudaStream_t>(stream));
+}
+
+int pa_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                         void* k_cache, void* v_cache, int32_t num_blocks, int32_t block_size,
+                         int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype, void* stream) {
+  if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 1) return PA_ERR_ARG;
+  if (block_size != 16 && block_size != 32) return PA_ERR_BLOCKSIZE;
+  const int eb = elem_bytes(dtype);
+  if (!eb) return PA_ERR_DTYPE;
+  const int64_t row_bytes = (int64_t)head_dim * eb;
+  if (row_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+  int* st = device_status_ptr();
+  if (!st) return PA_ERR_CUDA;
+  return launch_reshape_and_cache(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, block_size,
+                                  num_kv_heads, (int32_t)row_bytes, st, static_cast<cudaStream_t>(stream));
+}
+
+int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst_pairs, int32_t num_pairs,
+                   int32_t num_blocks, int64_t block_bytes, void* stream) {
+  if (num_pairs < 0 || num_blocks < 1 || block_bytes <= 0) return PA_ERR_ARG;
+  if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !src_dst_pairs) return PA_ERR_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+  std::vector<int32_t> src(num_pairs), dst(num_pairs);
+  std::unordered_set<int64_t> dsts;
+  dsts.reserve(num_pairs * 2);
+  for (int32_t i = 0; i < num_pairs; ++i) {
+    const int64_t s = src_dst_pairs[2 * i], d = src_dst_pairs[2 * i + 1];
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) return PA_ERR_BLOCK_OOB;
+    if (!dsts.insert(d).second) return PA_ERR_ALIAS;
+    src[i] = (int32_t)s;
+    dst[i] = (int32_t)d;
+  }
+  for (int32_t i = 0; i < num_pairs; ++i)
+    if (dsts.count(src[i])) return PA_ERR_ALIAS;
+  return launch_copy_blocks(k_cache, v_cache, src.data(), dst.data(), num_pairs, block_bytes,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int32_t pa_decode_partition_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t block_size,
+                                 int32_t max_seq_len, int32_t partition_size) {
+  if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || max_seq_len < 0) return PA_ERR_ARG;
+  if (num_q_heads % num_kv_heads) return PA_ERR_HEADS;
+  if (block_size != 16 && block_size != 32) return PA_ERR_BLOCKSIZE;
+  if (partition_size < 0) return PA_ERR_ARG;
+  if (partition_size > 0) {
+    if (partition_size % block_size || partition_size > kMaxPartition) return PA_ERR_ARG;
+    return partition_size;
+  }
+  return auto_partition(num_seqs, num_q_heads, num_kv_heads, max_seq_len < 1 ? 1 : max_seq_len);
+}
+
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                int32_t block_size, int32_t max_seq_len, int32_t partition_size) {
+  const int32_t part =
+      pa_decode_partition_size(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, partition_size);
+  if (part <= 0 || head_dim < 1 || max_seq_len < 1) return 0;
+  const int64_t max_parts = (max_seq_len + part - 1) / part;
+  if (max_parts <= 1) return 0;
+  return (size_t)num_seqs * num_q_heads * max_parts * (head_dim + 2) * sizeof(float);
+}
+
+static int decode_common(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* lens, const int32_t* cu_q_lens,
+                         int32_t num_seqs, int32_t max_len, int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale, void* out,
+                         int32_t partition_size, void* workspace, size_t workspace_bytes, pa_dtype dtype,
+                         cudaStream_t stream) {
+  if (num_seqs < 0 || max_blocks_per_seq < 1 || num_blocks < 1 || head_dim < 1) return PA_ERR_ARG;
+  if (num_q_heads < 1 || num_kv_heads < 1) return PA_ERR_ARG;
+  if (num_q_heads % num_kv_heads) return PA_ERR_HEADS;
+  if (block_size != 16 && block_size != 32) return PA_ERR_BLOCKSIZE;
+  if (!elem_bytes(dtype)) return PA_ERR_DTYPE;
+  if (!head_dim_supported(dtype, head_dim)) return PA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return PA_ERR_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (max_len < 1) return PA_ERR_ARG;
+  if (num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+  if (!q || !k_cache || !v_cache || !block_tables || !lens || !out) return PA_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PA_ERR_ALIGN;
+  if ((int64_t)num_blocks * num_kv_heads * block_size >= (1LL << 31)) return PA_ERR_UNSUPPORTED;
+  const int32_t part =
+      pa_decode_partition_size(num_seqs, num_q_heads, num_kv_heads, block_size, max_len, partition_size);
+  if (part < 0) return part;
+  const int64_t max_parts = (max_len + part - 1) / part;
+  if (max_parts > 12288) return PA_ERR_ARG;
+  const size_t need = max_parts > 1 ? (size_t)num_seqs * num_q_heads * max_parts * (head_dim + 2) * sizeof(float) : 0;
+  if (need && (!workspace || workspace_bytes < need)) return PA_ERR_WORKSPACE;
+  if (need && !aligned16(workspace)) return PA_ERR_ALIGN;
+  int* st = device_status_ptr();
+  if (!st) return PA_ERR_CUDA;
+
+  DecodeParams p{};
+  p.q = q;
+  p.out = out;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.lens = lens;
+  p.cu_q_lens = cu_q_lens;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.head_dim = head_dim;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.group = num_q_heads / num_kv_heads;
+  p.partition = part;
+  p.max_parts = (int32_t)max_parts;
+  p.len_cap = max_len;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.part_o = need ? static_cast<float*>(workspace) : nullptr;
+  p.part_ml = need ? static_cast<float*>(workspace) + (size_t)num_seqs * num_q_heads * max_parts * head_dim : nullptr;
+  p.status = st;
+  return launch_decode(p, dtype, stream);
+}
+
+int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+              int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+              float scale, void* out, int32_t partition_size, void* workspace, size_t workspace_bytes,
+              pa_dtype dtype, void* stream) {
+  return decode_common(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
+                       max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out,
+                       partition_size, workspace, workspace_bytes, dtype, static_cast<cudaStream_t>(stream));
+}
+
+size_t pa_chunked_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t block_size, int32_t max_kv_len) {
+  return pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_kv_len, 0);
+}
+
+int pa_chunked_prefill(const void* q, const int32_t* cu_q_lens, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* ctx_lens,
+                       int32_t num_seqs, int32_t max_q_len, int32_t max_kv_len, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
+                       void* out, void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
+  if (num_seqs < 0 || max_q_len < 0 || max_kv_len < 0) return PA_ERR_ARG;
+  if (num_seqs == 0 || max_q_len == 0) return PA_OK;
+  if (!cu_q_lens || !ctx_lens) return PA_ERR_ARG;
+  if (dtype == PA_F32 && max_q_len > 1) return PA_ERR_DTYPE;
+  if (max_q_len > 1 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Decode rows (q_len == 1): the split-KV decode path, key count ctx + 1.
+  int rc = decode_common(q, k_cache, v_cache, block_tables, max_blocks_per_seq, ctx_lens, cu_q_lens, num_seqs,
+                         max_kv_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out, 0,
+                         workspace, workspace_bytes, dtype, s);
+  if (rc != PA_OK || max_q_len <= 1) return rc;
+  // Chunks (q_len > 1): tensor-core tiles.
+  PrefillParams p{};
+  p.q = q;
+  p.out = out;
+  p.block_tables = block_tables;
+  p.cu_q_lens = cu_q_lens;
+  p.ctx_lens = ctx_lens;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.head_dim = head_dim;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.group = num_q_heads / num_kv_heads;
+  p.max_q_len = max_q_len;
+  p.max_kv_len = max_kv_len;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = device_status_ptr();
+  return launch_prefill(p, k_cache, v_cache, dtype, s);
+}
+
+}  // extern "C"

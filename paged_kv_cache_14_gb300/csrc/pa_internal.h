@@ -1,0 +1,94 @@
+// Internal launch interface between the C-ABI layer (pa_api.cu) and the
+// kernel translation units. Not part of the public API.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pagedattn.h"
+
+namespace pa {
+
+// Largest partition (tokens) one decode CTA walks; bounds the shared-memory
+// copy of the partition's block ids.
+constexpr int kMaxPartition = 16384;
+// Pairs handed to one copy_blocks launch by value (kernel parameter space).
+constexpr int kCopyPairsPerLaunch = 1024;
+
+struct DecodeParams {
+  const void* q;
+  void* out;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* lens;       // seq_lens (decode) or ctx_lens (decode rows of a prefill batch)
+  const int32_t* cu_q_lens;  // nullptr for plain decode; else only rows with q_len == 1 run
+  int32_t max_blocks_per_seq;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t group;         // num_q_heads / num_kv_heads
+  int32_t rows_per_cta;  // query heads of one group handled by one CTA
+  int32_t row_groups;    // ceil(group / rows_per_cta)
+  int32_t partition;     // tokens per split-KV partition (multiple of block_size)
+  int32_t max_parts;     // grid.x; ceil(len_cap / partition)
+  int32_t len_cap;       // largest legal length (host bound)
+  float scale_log2;      // scale * log2(e)
+  float* part_o;         // [num_seqs][num_q_heads][max_parts][head_dim]
+  float* part_ml;        // [num_seqs][num_q_heads][max_parts][2] (m, l)
+  int* status;
+};
+
+struct PrefillParams {
+  const void* q;
+  void* out;
+  const int32_t* block_tables;
+  const int32_t* cu_q_lens;
+  const int32_t* ctx_lens;
+  int32_t max_blocks_per_seq;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t group;
+  int32_t max_q_len;
+  int32_t max_kv_len;
+  int32_t m_tiles;  // grid.x
+  float scale_log2;
+  int* status;
+};
+
+// Returns the device status word of the current device (nullptr on error).
+int* device_status_ptr();
+int num_sms_current_device();
+
+// Encode a 2-D tensor map over a KV pool seen as [num_blocks*num_kv_heads*block_size rows][head_dim],
+// box = [box_rows rows][64 elements] with 128-byte swizzle (16-bit dtypes only).
+int make_kv_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t head_dim, pa_dtype dt,
+                       int32_t box_rows);
+// Same view, generic box (inner box_cols elements), 128-byte swizzle.
+int make_2d_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t cols, int64_t row_stride_elems,
+                       pa_dtype dt, int32_t box_rows, int32_t box_cols);
+
+int launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t num_seqs,
+                        const int32_t* seq_ids, const int32_t* positions, int64_t num_tokens, int32_t block_size,
+                        int32_t num_blocks, int64_t* slot_mapping, int* status, cudaStream_t stream);
+int launch_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                             void* k_cache, void* v_cache, int32_t num_blocks, int32_t block_size,
+                             int32_t num_kv_heads, int32_t row_bytes, int* status, cudaStream_t stream);
+int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int32_t num_pairs,
+                       int64_t block_bytes, cudaStream_t stream);
+
+// Decode: split-KV main pass (+ merge pass when max_parts > 1).
+int launch_decode(const DecodeParams& p, pa_dtype dt, cudaStream_t stream);
+// Prefill chunks (q_len > 1) on the tensor-core path.
+int launch_prefill(const PrefillParams& p, const void* k_cache, const void* v_cache, pa_dtype dt,
+                   cudaStream_t stream);
+
+}  // namespace pa

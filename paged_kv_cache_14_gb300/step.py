@@ -1,0 +1,112 @@
+"""One pass of the paged-attention hot path on device tensors.
+
+A step is what a serving engine runs per layer per iteration on the KV side:
+  1. copy-on-write block copies (pa_copy_blocks) for blocks about to be
+     written while shared,
+  2. slot derivation for the new tokens (pa_slot_mapping),
+  3. the cache write of their K/V (pa_reshape_and_cache),
+  4. attention over the paged context: pa_decode when every sequence has one
+     new query token, pa_chunked_prefill otherwise.
+This module only sequences library calls on one stream and owns the device
+buffers the calls need (slot mapping, output, split-KV workspace), allocated
+once with PyTorch.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import _binding as pa
+
+
+class PagedStep:
+    def __init__(self, *, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 block_tables: torch.Tensor, kv_lens: torch.Tensor, q_lens_host: np.ndarray,
+                 kv_lens_host: np.ndarray, k_new: torch.Tensor, v_new: torch.Tensor,
+                 new_seq_ids: torch.Tensor, new_positions: torch.Tensor, cow_pairs_host: np.ndarray,
+                 scale: float, partition_size: int = 0, cu_q_lens: torch.Tensor | None = None,
+                 ctx_lens: torch.Tensor | None = None):
+        self.q, self.k_cache, self.v_cache = q, k_cache, v_cache
+        self.block_tables, self.kv_lens = block_tables, kv_lens
+        self.k_new, self.v_new = k_new, v_new
+        self.new_seq_ids, self.new_positions = new_seq_ids, new_positions
+        self.cow_pairs = np.ascontiguousarray(np.asarray(cow_pairs_host, dtype=np.int64).reshape(-1, 2))
+        self.scale = float(scale)
+        self.partition_size = int(partition_size)
+        q_lens_host = np.asarray(q_lens_host)
+        kv_lens_host = np.asarray(kv_lens_host)
+        self.is_decode = bool(np.all(q_lens_host == 1))
+        self.max_seq_len = int(kv_lens_host.max())
+        self.max_q_len = int(q_lens_host.max())
+        self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim = k_cache.shape
+        dev = q.device
+        self.slot_mapping = torch.empty(new_positions.shape[0], dtype=torch.int64, device=dev)
+        self.out = torch.empty_like(q)
+        n = kv_lens_host.shape[0]
+        hq = q.shape[1]
+        if self.is_decode:
+            need = pa.pa_decode_workspace_size(n, hq, self.num_kv_heads, self.head_dim, self.block_size,
+                                               self.max_seq_len, self.partition_size)
+        else:
+            need = pa.pa_chunked_prefill_workspace_size(n, hq, self.num_kv_heads, self.head_dim,
+                                                        self.block_size, self.max_seq_len)
+            self.cu_q_lens = cu_q_lens
+            self.ctx_lens = ctx_lens
+        self.workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+
+    @property
+    def launches(self) -> int:
+        """Kernel launches of one step (the library's own kernels)."""
+        n = 0
+        if self.cow_pairs.shape[0]:
+            n += -(-self.cow_pairs.shape[0] // 1024)
+        n += 2  # slot mapping, cache write
+        if self.is_decode:
+            part = pa.pa_decode_partition_size(self.kv_lens.shape[0], self.q.shape[1], self.num_kv_heads,
+                                               self.block_size, self.max_seq_len, self.partition_size)
+            n += 1 + (1 if -(-self.max_seq_len // part) > 1 else 0)
+        else:
+            part = pa.pa_decode_partition_size(self.kv_lens.shape[0], self.q.shape[1], self.num_kv_heads,
+                                               self.block_size, self.max_seq_len, 0)
+            n += 1 + (1 if -(-self.max_seq_len // part) > 1 else 0)
+            n += 1 if self.max_q_len > 1 else 0
+        return n
+
+    def run(self, stream=None) -> torch.Tensor:
+        if self.cow_pairs.shape[0]:
+            pa.pa_copy_blocks(self.k_cache, self.v_cache, self.cow_pairs, stream=stream)
+        pa.pa_slot_mapping(self.block_tables, self.new_seq_ids, self.new_positions, self.block_size,
+                           self.num_blocks, slot_mapping=self.slot_mapping, stream=stream)
+        pa.pa_reshape_and_cache(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
+                                stream=stream)
+        if self.is_decode:
+            pa.pa_decode(self.q, self.k_cache, self.v_cache, self.block_tables, self.kv_lens, self.max_seq_len,
+                         self.scale, out=self.out, partition_size=self.partition_size, workspace=self.workspace,
+                         stream=stream)
+        else:
+            pa.pa_chunked_prefill(self.q, self.cu_q_lens, self.k_cache, self.v_cache, self.block_tables,
+                                  self.ctx_lens, self.max_q_len, self.max_seq_len, self.scale, out=self.out,
+                                  workspace=self.workspace, stream=stream)
+        return self.out
+
+
+def step_from_host(batch, device="cuda", partition_size: int = 0) -> PagedStep:
+    """Build a PagedStep from a host-side batch object exposing the fields of
+    a seeded workload (q, caches, tables, lengths, new tokens, CoW pairs)."""
+    def dev(x, dtype=None):
+        t = torch.as_tensor(x)
+        if dtype is not None:
+            t = t.to(dtype)
+        return t.to(device, non_blocking=False).contiguous()
+
+    cu = np.zeros(batch.num_seqs + 1, dtype=np.int32)
+    np.cumsum(batch.q_lens, out=cu[1:])
+    return PagedStep(
+        q=dev(batch.q), k_cache=dev(batch.k_cache), v_cache=dev(batch.v_cache),
+        block_tables=dev(batch.block_tables, torch.int32), kv_lens=dev(batch.kv_lens, torch.int32),
+        q_lens_host=batch.q_lens, kv_lens_host=batch.kv_lens,
+        k_new=dev(batch.k_new), v_new=dev(batch.v_new),
+        new_seq_ids=dev(batch.new_seq_ids, torch.int32), new_positions=dev(batch.new_positions, torch.int32),
+        cow_pairs_host=batch.cow_pairs, scale=batch.scale, partition_size=partition_size,
+        cu_q_lens=dev(cu, torch.int32), ctx_lens=dev(batch.kv_lens - batch.q_lens, torch.int32),
+    )

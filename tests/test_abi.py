@@ -1,0 +1,120 @@
+"""The C-ABI library builds, loads and exports every entry point declared in
+include/pagedattn.h; host-side argument checks reject bad calls before any
+launch (no GPU needed for any of this)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import paged_kv_cache_14_gb300 as pa
+from paged_kv_cache_14_gb300 import builder as pabuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    srcs = [os.path.join(pabuild.CSRC, f) for f in os.listdir(pabuild.CSRC)] + [HEADER]
+    if not os.path.exists(pabuild.LIB_PATH) or os.path.getmtime(pabuild.LIB_PATH) < max(map(os.path.getmtime, srcs)):
+        pabuild.build()
+    return pa.load()
+
+
+def header_functions() -> list[str]:
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert header_functions() == sorted(pa.EXPORTS)
+
+
+def test_library_exports_every_header_symbol(lib):
+    got = pa.exported_symbols()
+    assert all(got.values()), {k: v for k, v in got.items() if not v}
+    assert pa.pa_version() == 100
+
+
+def test_strerror(lib):
+    assert pa.pa_strerror(0) == "PA_OK"
+    for code in range(-1, -13, -1):
+        assert pa.pa_strerror(code).startswith("PA_ERR_")
+
+
+def _decode_raw(lib, **over):
+    args = dict(q=0x1000, k=0x2000, v=0x3000, bt=0x4000, mb=4, sl=0x5000, n=2, maxlen=64, hq=8, hkv=2, d=128,
+                bs=16, nb=10, scale=0.1, out=0x6000, part=64, ws=None, wsb=0, dt=pa.PA_BF16, stream=None)
+    args.update(over)
+    a = args
+    return lib.pa_decode(a["q"], a["k"], a["v"], a["bt"], a["mb"], a["sl"], a["n"], a["maxlen"], a["hq"], a["hkv"],
+                         a["d"], a["bs"], a["nb"], a["scale"], a["out"], a["part"], a["ws"], a["wsb"], a["dt"],
+                         a["stream"])
+
+
+def test_decode_host_checks(lib):
+    assert _decode_raw(lib, hq=6, hkv=4) == -3          # PA_ERR_HEADS
+    assert _decode_raw(lib, bs=8) == -4                 # PA_ERR_BLOCKSIZE
+    assert _decode_raw(lib, bs=4) == -4
+    assert _decode_raw(lib, d=96) == -10                # PA_ERR_UNSUPPORTED (tensor-core path: 64/128)
+    assert _decode_raw(lib, dt=7) == -2                 # PA_ERR_DTYPE
+    assert _decode_raw(lib, n=0) == 0                   # empty batch: no-op
+    assert _decode_raw(lib, q=None) == -1               # PA_ERR_ARG
+    assert _decode_raw(lib, q=0x1004) == -12            # PA_ERR_ALIGN
+    assert _decode_raw(lib, scale=float("nan")) == -1
+    assert _decode_raw(lib, part=24) == -1              # partition not a multiple of block_size
+    assert _decode_raw(lib, maxlen=1000) == -5          # 16 partitions need a workspace
+    assert _decode_raw(lib, maxlen=1000, ws=0x7000, wsb=10) == -5
+
+
+def test_partition_and_workspace_sizes(lib):
+    assert pa.pa_decode_partition_size(4, 8, 2, 16, 1000, 64) == 64
+    assert pa.pa_decode_workspace_size(4, 8, 2, 128, 16, 1000, 64) == 4 * 8 * 16 * 130 * 4
+    assert pa.pa_decode_workspace_size(4, 8, 2, 128, 16, 64, 64) == 0
+    with pytest.raises(pa.PagedAttnError):
+        pa.pa_decode_partition_size(4, 8, 2, 16, 1000, 40)
+    # The automatic choice is a power of two in [256, 1024].
+    for n, L in [(1, 100), (256, 8192), (8, 131072)]:
+        p = pa.pa_decode_partition_size(n, 64, 8, 16, L, 0)
+        assert p in (256, 512, 1024)
+
+
+def test_copy_blocks_host_checks(lib):
+    def call(pairs, nb=10):
+        arr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+        return lib.pa_copy_blocks(0x1000, 0x2000, arr.ctypes.data_as(ctypes.c_void_p), arr.shape[0], nb, 4096,
+                                  None)
+    assert call([(1, 2), (2, 3)]) == -6                 # dst 2 is also a src
+    assert call([(1, 2), (4, 2)]) == -6                 # dst repeated
+    assert call([(1, 1)]) == -6                         # in-place
+    assert call([(1, 10)]) == -7                        # out of the pool
+    assert call([(-1, 3)]) == -7
+    assert lib.pa_copy_blocks(0x1000, 0x2000, None, 0, 10, 4096, None) == 0
+    assert lib.pa_copy_blocks(0x1000, 0x2000, None, 1, 10, 4096, None) == -1
+    assert lib.pa_copy_blocks(0x1000, 0x2000, None, 1, 10, 4100, None) == -10
+
+
+def test_cache_write_and_slot_host_checks(lib):
+    assert lib.pa_reshape_and_cache(0x1000, 0x2000, 0x3000, 4, 0x4000, 0x5000, 10, 16, 2, 128, 9, None) == -2
+    assert lib.pa_reshape_and_cache(0x1000, 0x2000, 0x3000, 4, 0x4000, 0x5000, 10, 12, 2, 128, 2, None) == -4
+    assert lib.pa_reshape_and_cache(0x1000, 0x2000, 0x3000, 4, 0x4000, 0x5000, 10, 16, 2, 4, 2, None) == -10
+    assert lib.pa_reshape_and_cache(0x1000, 0x2000, 0x3000, 0, 0x4000, 0x5000, 10, 16, 2, 128, 2, None) == 0
+    assert lib.pa_reshape_and_cache(0x1008, 0x2000, 0x3000, 4, 0x4000, 0x5000, 10, 16, 2, 128, 2, None) == -12
+    assert lib.pa_slot_mapping(0x1000, 4, 2, 0x2000, 0x3000, 0, 16, 10, 0x4000, None) == 0
+    assert lib.pa_slot_mapping(0x1000, 4, 2, 0x2000, 0x3000, 5, 48, 10, 0x4000, None) == -4
+
+
+def test_prefill_host_checks(lib):
+    f = lib.pa_chunked_prefill
+    # fp32 chunks are not on the tensor-core path.
+    assert f(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 4, 0x6000, 2, 8, 64, 8, 2, 128, 16, 10, 0.1, 0x7000, None, 0,
+             pa.PA_F32, None) == -2
+    assert f(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 4, 0x6000, 0, 8, 64, 8, 2, 128, 16, 10, 0.1, 0x7000, None, 0,
+             pa.PA_F16, None) == 0
+    assert f(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 4, 0x6000, 2, 8, 64, 8, 2, 64, 16, 10, 0.1, 0x7000, None, 0,
+             pa.PA_F16, None) == -10
