@@ -149,9 +149,12 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst_pairs, i
  * pa_decode_partition_size returns the partition size a call with these
  * arguments uses (resolving 0), or a negative status.
  * pa_decode_workspace_size returns the workspace bytes pa_decode needs for
- * these arguments (0 when no sequence can need more than one partition).
- * The partials are fp32: num_seqs*num_q_heads*max_parts*(head_dim+2)*4
- * bytes, max_parts = ceil(max_seq_len / partition_size).
+ * these arguments: a work list (about num_seqs*max_parts*4 bytes) plus,
+ * when a sequence can need
+ * more than one partition, fp32 partials of
+ * num_seqs*num_q_heads*max_parts*(head_dim+2)*4 bytes, with
+ * max_parts = ceil(max_seq_len / partition_size). It is never 0 for a
+ * non-empty batch.
  */
 int32_t pa_decode_partition_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t block_size, int32_t max_seq_len, int32_t partition_size);
@@ -175,8 +178,11 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t n
  *                  a longer sequence records PA_ERR_SEQLEN
  *   scale        : multiplies q.k (usually 1/sqrt(head_dim))
  *   out          : [num_seqs][num_q_heads][head_dim]
- *   workspace    : device scratch of pa_decode_workspace_size() bytes (may be
- *                  NULL when that is 0); contents need no initialisation
+ *   workspace    : device scratch of pa_decode_workspace_size() bytes,
+ *                  16-byte aligned; contents need no initialisation (every
+ *                  call rewrites what it uses). Two calls whose executions
+ *                  overlap on the device (different streams) must not share
+ *                  a workspace.
  * Supported: block_size 16 or 32; fp16/bf16 with head_dim 64 or 128 (tensor-
  * core path); fp32 with head_dim a multiple of 32 up to 256 (CUDA-core
  * path). Each KV block is read once per KV head: all query heads of a GQA

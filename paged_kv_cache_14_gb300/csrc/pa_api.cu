@@ -101,15 +101,18 @@ int make_kv_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t
 }
 
 static int32_t auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seq_len) {
+  // Work items are (sequence, partition, KV head group); the persistent
+  // decode kernel (two CTAs per SM) pulls them from a counter. Use the
+  // longest partition, at most 2048 tokens, that still gives about four
+  // items per resident CTA, assuming an average length of half the maximum.
+  // Longer partitions mean fewer per-item epilogues and partials; more items
+  // mean a shorter tail.
   const int32_t group = num_q_heads / num_kv_heads;
-  const int64_t units = (int64_t)num_seqs * num_kv_heads * ((group + 15) / 16);
-  // About four waves of two resident CTAs per SM before splitting stops.
+  const int64_t hr = (int64_t)num_kv_heads * ((group + 15) / 16);
   const int64_t target = 8LL * num_sms_current_device();
-  int64_t parts = (target + units - 1) / units;
-  if (parts < 1) parts = 1;
-  const int64_t want = (max_seq_len + parts - 1) / parts;
-  int32_t part = 256;
-  while (part < want && part < 1024) part *= 2;
+  const int64_t half = (max_seq_len + 1) / 2;
+  int32_t part = 2048;
+  while (part > 256 && (int64_t)num_seqs * hr * ((half + part - 1) / part) < target) part /= 2;
   return part;
 }
 
@@ -222,10 +225,9 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t n
                                 int32_t block_size, int32_t max_seq_len, int32_t partition_size) {
   const int32_t part =
       pa_decode_partition_size(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, partition_size);
-  if (part <= 0 || head_dim < 1 || max_seq_len < 1) return 0;
-  const int64_t max_parts = (max_seq_len + part - 1) / part;
-  if (max_parts <= 1) return 0;
-  return (size_t)num_seqs * num_q_heads * max_parts * (head_dim + 2) * sizeof(float);
+  if (part <= 0 || head_dim < 1 || num_seqs < 1) return 0;
+  const int64_t max_parts = ((max_seq_len < 1 ? 1 : max_seq_len) + part - 1) / part;
+  return decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_parts).total;
 }
 
 static int decode_common(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -252,9 +254,9 @@ static int decode_common(const void* q, const void* k_cache, const void* v_cache
   if (part < 0) return part;
   const int64_t max_parts = (max_len + part - 1) / part;
   if (max_parts > 12288) return PA_ERR_ARG;
-  const size_t need = max_parts > 1 ? (size_t)num_seqs * num_q_heads * max_parts * (head_dim + 2) * sizeof(float) : 0;
-  if (need && (!workspace || workspace_bytes < need)) return PA_ERR_WORKSPACE;
-  if (need && !aligned16(workspace)) return PA_ERR_ALIGN;
+  const DecodeWorkspace wl = decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_parts);
+  if (!workspace || workspace_bytes < wl.total) return PA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return PA_ERR_ALIGN;
   int* st = device_status_ptr();
   if (!st) return PA_ERR_CUDA;
 
@@ -278,8 +280,11 @@ static int decode_common(const void* q, const void* k_cache, const void* v_cache
   p.max_parts = (int32_t)max_parts;
   p.len_cap = max_len;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.part_o = need ? static_cast<float*>(workspace) : nullptr;
-  p.part_ml = need ? static_cast<float*>(workspace) + (size_t)num_seqs * num_q_heads * max_parts * head_dim : nullptr;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.work = reinterpret_cast<int32_t*>(ws + wl.work);
+  p.pairs = reinterpret_cast<int32_t*>(ws + wl.pairs);
+  p.part_o = max_parts > 1 ? reinterpret_cast<float*>(ws + wl.part_o) : nullptr;
+  p.part_ml = max_parts > 1 ? reinterpret_cast<float*>(ws + wl.part_ml) : nullptr;
   p.status = st;
   return launch_decode(p, dtype, stream);
 }

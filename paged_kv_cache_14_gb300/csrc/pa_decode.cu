@@ -1,61 +1,83 @@
 // Paged decode attention for sm_103a.
 //
-// One CTA handles one (split-KV partition, KV head [, query-row group],
-// sequence). It walks the sequence's block table over the partition and, for
-// every logical block, stages that block's K and V tiles for its KV head
-// (each tile is block_size x head_dim contiguous elements of the pool) into
-// shared memory with TMA. All query heads of the GQA group that share the KV
-// head are packed as the rows of one 16-row MMA tile, so every KV block is
-// read from HBM once per KV head ("03 - PagedAttention & the vLLM V1
-// Architecture", section "The attention kernel side": look up the block
-// table, fetch each block's K/V tiles, attend over the gathered tiles).
+// Work decomposition. A sequence of L keys is cut into split-KV partitions of
+// `partition` tokens; a work item is one (sequence, partition, KV head
+// [, query-row group]). A one-CTA plan kernel lists the items that exist
+// (sequence-major, so the sequences of a prefix-sharing group are processed
+// close together in time and read their shared blocks from L2) and resets
+// the work counter. The main kernel is persistent: each CTA pulls items from
+// the counter until none is left.
 //
-// Warp roles (160 threads): warp 4 is the producer (one lane issues the TMA
-// copies, ring of kStages stages guarded by full/empty mbarriers); warps 0-3
-// consume blocks round-robin, each keeping its own running max m, running
-// sum l and unnormalised output o for the 16 rows (online softmax), with
-// S = Q K^T and O += P V on warp-level tensor-core MMAs (m16n8k16, fp32
-// accumulate). At the end the four warps are merged through shared memory.
-// Decode is HBM-bound (about 8 flop per KV byte at GQA group 8), so the
-// warp-level MMA has ample headroom and tcgen05 tiles (M >= 64) would only
-// pad the 8 live rows.
+// Inside a CTA (160 threads): warp 4 is the producer. For every item it
+// copies the group's query rows into an item slot, then walks the sequence's
+// block table over the partition and stages each logical block's K and V
+// tiles for the item's KV head (block_size x head_dim contiguous elements of
+// the pool each) into a ring of shared-memory stages with 2-D TMA copies
+// (128-byte swizzle), one mbarrier per stage. It runs ahead across item
+// boundaries, so the ring never drains between items ("03 - PagedAttention &
+// the vLLM V1 Architecture", section "The attention kernel side": look the
+// block up in the table, fetch its K/V tiles, attend over the gathered
+// tiles).
 //
-// A partition writes the final output when it is the sequence's only one;
-// otherwise it writes fp32 partials (m, l, o~) and a merge kernel combines
-// them with log-sum-exp weights.
+// Warps 0-3 consume blocks round-robin. All query heads of the GQA group
+// sharing the KV head are the N columns of warp-level MMAs (m16n8k16, fp32
+// accumulate) with the block's 16 tokens as the M rows: S^T = K Q^T, an
+// online softmax per head column, then O^T += V^T P^T (P^T moves from the
+// accumulator layout to the B-operand layout with movmatrix). Every KV block
+// is therefore read once per KV head. Decode is HBM-bound (about 8 flop per
+// KV byte at group 8): the warp-level MMA has ample headroom, and tcgen05
+// tiles (M >= 64) would only pad the 8 live heads.
+//
+// The four warps' (m, l, o) are merged through shared memory. A sequence
+// with one partition is written directly; otherwise the item writes fp32
+// partials and a merge kernel combines the partitions of every (sequence,
+// query head) with log-sum-exp weights.
+//
+// fp32 I/O takes a CUDA-core path (exact fp32 FMAs, no TF32) with one CTA
+// per (partition, head group, sequence) and the same merge kernel.
 #include <math_constants.h>
+
+#include <type_traits>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
 namespace pa {
 
-template <int D, int BS>
-struct DecodeCfg {
-  static constexpr int kHalves = D / 64;                  // 128-byte swizzle boxes across head_dim
-  static constexpr int kTileBytes = BS * D * 2;           // one (block, KV head) tile of K or V
-  static constexpr int kStageBytes = 2 * kTileBytes;      // K tile + V tile
-  static constexpr int kStages = (65536 / kStageBytes) > 16 ? 16 : (65536 / kStageBytes);
-  static constexpr int kConsumerWarps = 4;
-  static constexpr int kThreads = (kConsumerWarps + 1) * 32;
-  static constexpr int kRows = 16;
-  static constexpr int kOStride = D + 4;  // fp32 merge-scratch row stride (bank spread)
-  static constexpr int kMaxIds = kMaxPartition / BS;
-  static constexpr size_t kStageRegion = (size_t)kStages * kStageBytes;
-  static constexpr size_t kMergeBytes = (size_t)kConsumerWarps * kRows * kOStride * 4;
-  static constexpr size_t kBarOff = kStageRegion;
-  static constexpr size_t kMlOff = kBarOff + 2 * kStages * 8;
-  static constexpr size_t kFlagOff = kMlOff + kConsumerWarps * kRows * 2 * 4;
-  static constexpr size_t kIdsOff = kFlagOff + 16;
-  static constexpr size_t kSmemBytes = kIdsOff + kMaxIds * 4 + 1024;  // + alignment slack
-  static_assert(kStages % kConsumerWarps == 0, "a stage must always belong to the same consumer warp");
-  static_assert(kMergeBytes <= kStageRegion, "merge scratch reuses the stage ring");
-};
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
 
-__device__ __forceinline__ uint32_t ld_u32(const void* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
-// Resolve the row of q / out and the key count of sequence `seq`.
-// Returns false when this sequence is not a decode row of this launch.
+// Named barrier over `threads` threads that also returns the OR of every
+// participant's predicate (the same value in all of them).
+__device__ __forceinline__ bool named_barrier_or(int id, int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Row of q / out and key count of sequence `seq`; false when the sequence
+// is not a decode row of this launch (a prefill chunk in a mixed batch).
 __device__ __forceinline__ bool decode_row(const DecodeParams& p, int seq, int& qrow, int& len) {
   if (p.cu_q_lens) {
     const int q0 = p.cu_q_lens[seq], q1 = p.cu_q_lens[seq + 1];
@@ -69,318 +91,497 @@ __device__ __forceinline__ bool decode_row(const DecodeParams& p, int seq, int& 
   return true;
 }
 
+__device__ __forceinline__ bool len_ok(const DecodeParams& p, int len) {
+  return len >= 1 && len <= p.len_cap && len <= p.max_blocks_per_seq * p.block_size;
+}
+
+// ---------------------------------------------------------------------------
+// Plan: list the (sequence, partition) pairs that exist, reset the counters.
+// One CTA of 1024 threads. Sequences with an illegal length get zero output
+// rows and PA_ERR_SEQLEN.
+// ---------------------------------------------------------------------------
 template <typename T>
-__device__ void write_zero_rows(const DecodeParams& p, int qrow, int h0, int nrows) {
-  T* out = static_cast<T*>(p.out);
-  for (int i = threadIdx.x; i < nrows * p.head_dim; i += blockDim.x) {
-    const int r = i / p.head_dim, d = i - r * p.head_dim;
-    out[((int64_t)qrow * p.num_q_heads + h0 + r) * p.head_dim + d] = T(0.0f);
+__global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p) {
+  __shared__ int32_t scan[1024];
+  const int N = p.num_seqs;
+  const int per = (N + 1023) / 1024;
+  const int s0 = min(N, (int)threadIdx.x * per), s1 = min(N, s0 + per);
+  int cnt = 0;
+  for (int s = s0; s < s1; ++s) {
+    int qrow, len;
+    if (!decode_row(p, s, qrow, len)) continue;
+    if (!len_ok(p, len)) {
+      record_error(p.status, PA_ERR_SEQLEN);
+      T* out = static_cast<T*>(p.out) + (int64_t)qrow * p.num_q_heads * p.head_dim;
+      for (int i = 0; i < p.num_q_heads * p.head_dim; ++i) out[i] = T(0.0f);
+      continue;
+    }
+    cnt += (len + p.partition - 1) / p.partition;
+  }
+  scan[threadIdx.x] = cnt;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {
+    const int v = threadIdx.x >= off ? scan[threadIdx.x - off] : 0;
+    __syncthreads();
+    scan[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int base = scan[threadIdx.x] - cnt;
+  for (int s = s0; s < s1; ++s) {
+    int qrow, len;
+    if (!decode_row(p, s, qrow, len) || !len_ok(p, len)) continue;
+    const int n = (len + p.partition - 1) / p.partition;
+    for (int part = 0; part < n; ++part) p.pairs[base++] = (s << 16) | part;
+  }
+  const int hr = p.num_kv_heads * p.row_groups;
+  if (threadIdx.x == 1023) {
+    p.work[0] = 0;
+    p.work[1] = scan[1023] * hr;
   }
 }
 
-template <typename T, int D, int BS>
-__global__ void __launch_bounds__(DecodeCfg<D, BS>::kThreads, 2)
+// ---------------------------------------------------------------------------
+// Persistent tensor-core decode kernel (fp16 / bf16).
+// ---------------------------------------------------------------------------
+// A stage holds one 16-token sub-tile of a (block, KV head) tile of K and of
+// V (a block of 32 tokens fills two stages). Stage s is only ever consumed
+// by consumer warp s % 4, so each stage's mbarrier is waited on in phase
+// order by one warp (a parity wait can never alias a phase not yet begun).
+template <int D, int BS, int NT>
+struct DecCfg {
+  static constexpr int kHalves = D / 64;              // 128-byte swizzle boxes across head_dim
+  static constexpr int kTile = 16 * D * 2;            // 16 tokens x head_dim of K (or V)
+  static constexpr int kStage = 2 * kTile;            // K + V
+  static constexpr int kStages = 65536 / kStage;      // 64 KB ring
+  static constexpr int kHeads = NT * 8;               // query heads per item (MMA N)
+  static constexpr int kConsumers = 4;
+  static constexpr int kThreads = (kConsumers + 1) * 32;
+  static constexpr int kSlots = 2;                    // item slots (metadata + query rows)
+  static constexpr int kQBytes = kHeads * D * 2;
+  static constexpr int kDp = D + 4;                   // fp32 scratch row stride (bank spread)
+  static constexpr size_t kRing = 0;
+  static constexpr size_t kQ = kRing + (size_t)kStages * kStage;
+  static constexpr size_t kScratch = kQ + (size_t)kSlots * kQBytes;
+  static constexpr size_t kMl = kScratch + (size_t)kConsumers * kHeads * kDp * 4;
+  static constexpr size_t kMeta = kMl + (size_t)kConsumers * kHeads * 2 * 4;
+  static constexpr size_t kValid = kMeta + (size_t)kSlots * 16 * 4;
+  static constexpr size_t kBars = (kValid + (size_t)kStages * 4 + 7) & ~size_t(7);
+  static constexpr size_t kFlags = kBars + (size_t)(2 * kStages + 2 * kSlots) * 8;
+  static constexpr size_t kSmem = kFlags + 16 + 1024;  // + alignment slack
+  static_assert(kStages % kConsumers == 0, "stage s belongs to consumer warp s % 4");
+  static_assert(BS % 16 == 0, "block size must be a multiple of 16");
+};
+
+struct ItemMeta {
+  int seq, qrow, h0, nrows, t_begin, t_end, nsub, jstart, part, n_parts, hg, pad[5];
+};
+
+template <typename T, int D, int BS, int NT>
+__global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                      const DecodeParams p) {
-  using C = DecodeCfg<D, BS>;
+  using C = DecCfg<D, BS, NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-
-  const int part = blockIdx.x;
-  const int kvh = blockIdx.y / p.row_groups;
-  const int rg = blockIdx.y - kvh * p.row_groups;
-  const int seq = blockIdx.z;
-  int qrow, len;
-  if (!decode_row(p, seq, qrow, len)) return;
-  const int h0 = kvh * p.group + rg * p.rows_per_cta;
-  const int nrows = min(p.rows_per_cta, p.group - rg * p.rows_per_cta);
-  if (len < 1 || len > p.len_cap || len > p.max_blocks_per_seq * BS) {
-    if (part == 0) {
-      if (threadIdx.x == 0) record_error(p.status, PA_ERR_SEQLEN);
-      write_zero_rows<T>(p, qrow, h0, nrows);
-    }
-    return;
-  }
-  const int n_parts = (len + p.partition - 1) / p.partition;
-  if (part >= n_parts) return;
-  const int t_begin = part * p.partition;
-  const int t_end = min(t_begin + p.partition, len);
-  const int nblk = (t_end - t_begin + BS - 1) / BS;
-
-  int32_t* ids = reinterpret_cast<int32_t*>(smem + C::kIdsOff);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  ItemMeta* meta = reinterpret_cast<ItemMeta*>(smem + C::kMeta);
+  int* stage_valid = reinterpret_cast<int*>(smem + C::kValid);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBars);
   uint64_t* empty = full + C::kStages;
-  float* ml = reinterpret_cast<float*>(smem + C::kMlOff);
-  int* abort_flag = reinterpret_cast<int*>(smem + C::kFlagOff);
+  uint64_t* ifull = empty + C::kStages;
+  uint64_t* iempty = ifull + C::kSlots;
+  float* scratch = reinterpret_cast<float*>(smem + C::kScratch);
+  float* ml = reinterpret_cast<float*>(smem + C::kMl);
 
-  {
-    const int32_t* bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq + t_begin / BS;
-    for (int j = threadIdx.x; j < nblk; j += blockDim.x) {
-      int id = bt[j];
-      if (id < 0 || id >= p.num_blocks) {
-        record_error(p.status, PA_ERR_BLOCK_OOB);
-        id = -1;
-      }
-      ids[j] = id;
-    }
-  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hr = p.num_kv_heads * p.row_groups;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
-    abort_flag[0] = 0;
-    abort_flag[1] = 0;  // loads issued by the producer
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(smem_u32(&ifull[s]), 1);
+      mbar_init(smem_u32(&iempty[s]), C::kConsumers);
+    }
     fence_barrier_init();
   }
+  // Query slots start zeroed: rows past a ragged group stay finite.
+  for (int i = threadIdx.x; i < C::kSlots * C::kQBytes / 16; i += blockDim.x)
+    reinterpret_cast<int4*>(smem + C::kQ)[i] = make_int4(0, 0, 0, 0);
   __syncthreads();
+  const uint32_t ring0 = smem_u32(smem + C::kRing);
 
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint32_t stage0 = smem_u32(smem);
-
-  // Per-consumer state (rows r0 = lane/4 and r0 + 8 of the 16-row tile).
-  const int r0 = lane >> 2;
-  const int cq = (lane & 3) * 2;
-  float o[D / 8][4];
-  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
-#pragma unroll
-  for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-
-  if (warp == C::kConsumerWarps) {
-    // ---------------- producer ----------------
+  if (warp == C::kConsumers) {
+    // =========================== producer ===========================
     if (lane == 0) {
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
-      int j = 0;
-      for (; j < nblk; ++j) {
-        const int s = j % C::kStages;
-        if (j >= C::kStages && !mbar_wait(smem_u32(&empty[s]), ((j / C::kStages) & 1) ^ 1, p.status)) {
-          atomicExch(&abort_flag[0], 1);
-          break;
-        }
-        const int id = ids[j];
-        const uint32_t fb = smem_u32(&full[s]);
-        if (id >= 0) {
-          mbar_arrive_expect_tx(fb, C::kStageBytes);
-          const int32_t row = (id * p.num_kv_heads + kvh) * BS;
-          const uint32_t kdst = stage0 + s * C::kStageBytes;
-          const uint32_t vdst = kdst + C::kTileBytes;
-#pragma unroll
-          for (int hf = 0; hf < C::kHalves; ++hf) {
-            tma_load_2d(kdst + hf * (BS * 128), &kmap, hf * 64, row, fb);
-            tma_load_2d(vdst + hf * (BS * 128), &vmap, hf * 64, row, fb);
-          }
-        } else {
-          mbar_arrive(fb);
-        }
-      }
-      abort_flag[1] = j;
     }
-  } else {
-    // ---------------- consumers ----------------
-    uint32_t qa[D / 16][4];
-    {
-      const T* qb = static_cast<const T*>(p.q) + ((int64_t)qrow * p.num_q_heads + h0) * D;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const int c = kk * 16 + cq;
-        qa[kk][0] = r0 < nrows ? ld_u32(qb + r0 * D + c) : 0u;
-        qa[kk][1] = r0 + 8 < nrows ? ld_u32(qb + (r0 + 8) * D + c) : 0u;
-        qa[kk][2] = r0 < nrows ? ld_u32(qb + r0 * D + c + 8) : 0u;
-        qa[kk][3] = r0 + 8 < nrows ? ld_u32(qb + (r0 + 8) * D + c + 8) : 0u;
-      }
+    const int total = p.work[1];
+    int next = 0;
+    if (lane == 0) next = atomicAdd(&p.work[0], 1);
+    next = __shfl_sync(0xffffffffu, next, 0);
+    // The (sequence, partition) pair and length of the next item are loaded
+    // one item ahead, so the item switch costs no dependent global loads.
+    int next_pr = 0, next_qrow = 0, next_len = 0;
+    if (next < total) {
+      next_pr = p.pairs[next / hr];
+      decode_row(p, next_pr >> 16, next_qrow, next_len);
     }
-    const float sl2 = p.scale_log2;
-    const int mi = lane >> 3, rr = lane & 7;
-    for (int j = warp; j < nblk; j += C::kConsumerWarps) {
-      const int s = j % C::kStages;
-      if (!mbar_wait(smem_u32(&full[s]), (j / C::kStages) & 1, p.status)) {
-        atomicExch(&abort_flag[0], 1);
+    int jg = 0;  // 16-token sub-tiles issued so far (global stage sequence)
+    bool bad = false;
+    constexpr int kSubPerBlock = BS / 16;
+    for (int it = 0;; ++it) {
+      const int item = next;
+      const int slot = it % C::kSlots;
+      if (lane == 0 && it >= C::kSlots &&
+          !mbar_wait(smem_u32(&iempty[slot]), ((it / C::kSlots) & 1) ^ 1, p.status))
+        bad = true;
+      bad = __shfl_sync(0xffffffffu, bad, 0);
+      if (bad) break;
+      if (item >= total) {
+        if (lane == 0) {
+          meta[slot].seq = -1;
+          mbar_arrive(smem_u32(&ifull[slot]));
+        }
         break;
       }
-      if (ids[j] >= 0) {
-        const uint32_t kb = stage0 + s * C::kStageBytes;
-        const uint32_t vb = kb + C::kTileBytes;
-#pragma unroll
-        for (int sub = 0; sub < BS / 16; ++sub) {
-          const int tok0 = t_begin + j * BS + sub * 16;
-          if (tok0 >= t_end) break;
-          float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-          {
-            const int tok = sub * 16 + (mi >> 1) * 8 + rr;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const int cg = kk * 2 + (mi & 1);
-              const uint32_t addr = kb + (cg >> 3) * (BS * 128) + tok * 128 + (((cg & 7) ^ (tok & 7)) << 4);
-              uint32_t b0, b1, b2, b3;
-              ldsm_x4(addr, b0, b1, b2, b3);
-              MmaOp<T>::run(sc[0], qa[kk], b0, b1);
-              MmaOp<T>::run(sc[1], qa[kk], b2, b3);
-            }
+      const int pr = next_pr, qrow = next_qrow, len = next_len;
+      if (lane == 0) next = atomicAdd(&p.work[0], 1);  // fetch the following item
+      const int hg = item - (item / hr) * hr;
+      const int seq = pr >> 16, part = pr & 0xffff;
+      const int kvh = hg / p.row_groups, rgi = hg - kvh * p.row_groups;
+      const int t_begin = part * p.partition;
+      const int t_end = min(t_begin + p.partition, len);
+      const int nsub = (t_end - t_begin + 15) / 16;
+      // Items are padded to a multiple of 4 sub-tiles with empty stages, so
+      // every item starts on stage 0 mod 4 and sub-tile u always lands on
+      // consumer warp u % 4: the summation order, hence the result, does not
+      // depend on which CTA ran the item or what it ran before.
+      const int nsub_pad = (nsub + 3) & ~3;
+      const int h0 = kvh * p.group + rgi * p.rows_per_cta;
+      const int nrows = min(p.rows_per_cta, p.group - rgi * p.rows_per_cta);
+      if (lane == 0) {
+        ItemMeta& m = meta[slot];
+        m.seq = seq;
+        m.qrow = qrow;
+        m.h0 = h0;
+        m.nrows = nrows;
+        m.t_begin = t_begin;
+        m.t_end = t_end;
+        m.nsub = nsub_pad;
+        m.jstart = jg;
+        m.part = part;
+        m.n_parts = (len + p.partition - 1) / p.partition;
+        m.hg = seq * hr + hg;
+        const uint32_t fb = smem_u32(&ifull[slot]);
+        mbar_arrive_expect_tx(fb, nrows * D * 2);
+        bulk_copy_g2s(smem_u32(smem + C::kQ + slot * C::kQBytes),
+                      static_cast<const T*>(p.q) + ((int64_t)qrow * p.num_q_heads + h0) * D, nrows * D * 2, fb);
+      }
+      const int32_t* bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq + t_begin / BS;
+      for (int ub = 0; ub < nsub_pad && !bad; ub += 32) {
+        // Lane k holds the physical block of sub-tile ub + k (-1: padding).
+        int id = -1;
+        if (ub + lane < nsub) {
+          id = bt[(ub + lane) / kSubPerBlock];
+          if (id < 0 || id >= p.num_blocks) {
+            record_error(p.status, PA_ERR_BLOCK_OOB);
+            id = -1;
           }
-          // Scale into log2 units and mask keys past the partition end.
+        }
+        const int cnt = min(32, nsub_pad - ub);
+        for (int k = 0; k < cnt; ++k) {
+          const int idk = __shfl_sync(0xffffffffu, id, k);
+          if (lane == 0) {
+            const int s = jg % C::kStages;
+            if (jg >= C::kStages && !mbar_wait(smem_u32(&empty[s]), ((jg / C::kStages) & 1) ^ 1, p.status)) {
+              bad = true;
+            } else {
+              stage_valid[s] = idk >= 0;
+              const uint32_t fb = smem_u32(&full[s]);
+              if (idk >= 0) {
+                mbar_arrive_expect_tx(fb, C::kStage);
+                const int32_t row = (idk * p.num_kv_heads + kvh) * BS + ((ub + k) % kSubPerBlock) * 16;
+                const uint32_t kd = ring0 + s * C::kStage;
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int tok = tok0 + nt * 8 + cq + (e & 1);
-              sc[nt][e] = tok < t_end ? sc[nt][e] * sl2 : -CUDART_INF_F;
-            }
-          // Online softmax (row max over the quad of lanes that share a row).
-          float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-          float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-          const bool dead0 = mn0 == -CUDART_INF_F, dead1 = mn1 == -CUDART_INF_F;
-          const float a0 = dead0 ? 1.f : exp2f(m0 - mn0);
-          const float a1 = dead1 ? 1.f : exp2f(m1 - mn1);
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            sc[nt][0] = dead0 ? 0.f : exp2f(sc[nt][0] - mn0);
-            sc[nt][1] = dead0 ? 0.f : exp2f(sc[nt][1] - mn0);
-            sc[nt][2] = dead1 ? 0.f : exp2f(sc[nt][2] - mn1);
-            sc[nt][3] = dead1 ? 0.f : exp2f(sc[nt][3] - mn1);
-          }
-          l0 = l0 * a0 + (sc[0][0] + sc[0][1]) + (sc[1][0] + sc[1][1]);
-          l1 = l1 * a1 + (sc[0][2] + sc[0][3]) + (sc[1][2] + sc[1][3]);
-          m0 = mn0;
-          m1 = mn1;
-#pragma unroll
-          for (int nt = 0; nt < D / 8; ++nt) {
-            o[nt][0] *= a0;
-            o[nt][1] *= a0;
-            o[nt][2] *= a1;
-            o[nt][3] *= a1;
-          }
-          // P as the A operand (the S accumulator layout is the A layout).
-          const uint32_t pa[4] = {MmaOp<T>::pack(sc[0][0], sc[0][1]), MmaOp<T>::pack(sc[0][2], sc[0][3]),
-                                  MmaOp<T>::pack(sc[1][0], sc[1][1]), MmaOp<T>::pack(sc[1][2], sc[1][3])};
-          // Keys past the end carry p = 0, but their V slots may hold any
-          // bits (NaN included): zero those V elements so 0 * V stays 0.
-          const bool tail = tok0 + 16 > t_end;
-          const int tlo = tok0 + cq;  // tokens held by the low / high halves of b0 (b1: +8)
-          const uint32_t keep0 = (tlo < t_end ? 0x0000ffffu : 0u) | (tlo + 1 < t_end ? 0xffff0000u : 0u);
-          const uint32_t keep1 = (tlo + 8 < t_end ? 0x0000ffffu : 0u) | (tlo + 9 < t_end ? 0xffff0000u : 0u);
-          {
-            const int tok = sub * 16 + (mi & 1) * 8 + rr;
-#pragma unroll
-            for (int np = 0; np < D / 16; ++np) {
-              const int cg = np * 2 + (mi >> 1);
-              const uint32_t addr = vb + (cg >> 3) * (BS * 128) + tok * 128 + (((cg & 7) ^ (tok & 7)) << 4);
-              uint32_t b0, b1, b2, b3;
-              ldsm_x4_t(addr, b0, b1, b2, b3);
-              if (tail) {
-                b0 &= keep0;
-                b1 &= keep1;
-                b2 &= keep0;
-                b3 &= keep1;
+                for (int hf = 0; hf < C::kHalves; ++hf) {
+                  tma_load_2d(kd + hf * 2048, &kmap, hf * 64, row, fb);
+                  tma_load_2d(kd + C::kTile + hf * 2048, &vmap, hf * 64, row, fb);
+                }
+              } else {
+                mbar_arrive(fb);
               }
-              MmaOp<T>::run(o[2 * np], pa, b0, b1);
-              MmaOp<T>::run(o[2 * np + 1], pa, b2, b3);
             }
+          }
+          bad = __shfl_sync(0xffffffffu, bad, 0);
+          if (bad) break;
+          ++jg;
+        }
+        if (ub == 0) {
+          // The counter has answered by now: load the next item's metadata
+          // while the rest of this item is issued.
+          next = __shfl_sync(0xffffffffu, next, 0);
+          if (next < total) {
+            next_pr = p.pairs[next / hr];
+            decode_row(p, next_pr >> 16, next_qrow, next_len);
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+      if (bad) break;
     }
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  }
-  __syncthreads();
-
-  if (abort_flag[0]) {
-    // A bounded wait ran out (recorded in the status word). Let every copy
-    // still in flight land before the CTA's shared memory is released.
-    if (threadIdx.x == 0) {
-      const int issued = abort_flag[1];
-      for (int s = 0; s < C::kStages && s < issued; ++s) {
-        const int last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
+    if (bad && lane == 0) {
+      // Let copies still in flight land before the CTA exits.
+      for (int s = 0; s < C::kStages && s < jg; ++s) {
+        const int last = s + ((jg - 1 - s) / C::kStages) * C::kStages;
         mbar_wait(smem_u32(&full[s]), (last / C::kStages) & 1, nullptr);
       }
     }
     return;
   }
 
-  // ---------------- merge the four consumer warps ----------------
-  if (warp < C::kConsumerWarps && (lane & 3) == 0) {
-    ml[(warp * 16 + r0) * 2 + 0] = m0;
-    ml[(warp * 16 + r0) * 2 + 1] = l0;
-    ml[(warp * 16 + r0 + 8) * 2 + 0] = m1;
-    ml[(warp * 16 + r0 + 8) * 2 + 1] = l1;
-  }
-  __syncthreads();
-  float* ob = reinterpret_cast<float*>(smem);
-  if (warp < C::kConsumerWarps) {
-    float M0 = -CUDART_INF_F, M1 = -CUDART_INF_F;
+  // =========================== consumers ===========================
+  const int ctid = threadIdx.x;  // 0..127
+  const int mi = lane >> 3, rr = lane & 7;
+  const int ti = lane & 3;   // column pair (heads 2ti, 2ti+1) of the accumulators
+  const int tr = lane >> 2;  // row (token / dim) of the accumulators
+  const float sl2 = p.scale_log2;
+  for (int it = 0;; ++it) {
+    const int slot = it % C::kSlots;
+    // A failed wait in any consumer warp ends all four together (the OR is
+    // the same in every thread, so no warp is left at a later barrier).
+    const bool waited = mbar_wait(smem_u32(&ifull[slot]), (it / C::kSlots) & 1, p.status);
+    if (named_barrier_or(1, C::kConsumers * 32, !waited)) break;
+    const ItemMeta mt = meta[slot];
+    if (mt.seq < 0) break;
+    // Q^T fragments (B operand: k = dims, n = heads) from the item slot.
+    uint32_t qf[D / 16][NT][2];
+    {
+      const uint32_t qs = smem_u32(smem + C::kQ + slot * C::kQBytes);
 #pragma unroll
-    for (int w = 0; w < C::kConsumerWarps; ++w) {
-      M0 = fmaxf(M0, ml[(w * 16 + r0) * 2]);
-      M1 = fmaxf(M1, ml[(w * 16 + r0 + 8) * 2]);
+      for (int kk = 0; kk < D / 16; kk += 2)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int head = nt * 8 + rr;
+          const int chunk = (kk + (mi >> 1)) * 2 + (mi & 1);
+          ldsm_x4(qs + head * (D * 2) + chunk * 16, qf[kk][nt][0], qf[kk][nt][1], qf[kk + 1][nt][0],
+                  qf[kk + 1][nt][1]);
+        }
     }
-    const float f0 = m0 == -CUDART_INF_F ? 0.f : exp2f(m0 - M0);
-    const float f1 = m1 == -CUDART_INF_F ? 0.f : exp2f(m1 - M1);
-    float* wb = ob + warp * 16 * C::kOStride;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&iempty[slot]));
+
+    float o[D / 16][NT][4];
 #pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) {
-      const int col = nt * 8 + cq;
-      *reinterpret_cast<float2*>(&wb[r0 * C::kOStride + col]) = make_float2(o[nt][0] * f0, o[nt][1] * f0);
-      *reinterpret_cast<float2*>(&wb[(r0 + 8) * C::kOStride + col]) = make_float2(o[nt][2] * f1, o[nt][3] * f1);
-    }
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < nrows * (D / 4); idx += blockDim.x) {
-    const int row = idx / (D / 4);
-    const int c4 = (idx - row * (D / 4)) * 4;
-    float M = -CUDART_INF_F;
+    for (int a = 0; a < D / 16; ++a)
 #pragma unroll
-    for (int w = 0; w < C::kConsumerWarps; ++w) M = fmaxf(M, ml[(w * 16 + row) * 2]);
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int nt = 0; nt < NT; ++nt) o[a][nt][0] = o[a][nt][1] = o[a][nt][2] = o[a][nt][3] = 0.f;
+    float m[NT][2], l[NT][2];
 #pragma unroll
-    for (int w = 0; w < C::kConsumerWarps; ++w) {
-      const float mw = ml[(w * 16 + row) * 2];
-      L += mw == -CUDART_INF_F ? 0.f : ml[(w * 16 + row) * 2 + 1] * exp2f(mw - M);
-      const float4 v = *reinterpret_cast<const float4*>(&ob[(w * 16 + row) * C::kOStride + c4]);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    if (n_parts == 1) {
-      const float inv = 1.f / L;
-      acc.x *= inv;
-      acc.y *= inv;
-      acc.z *= inv;
-      acc.w *= inv;
-      store4(static_cast<T*>(p.out) + ((int64_t)qrow * p.num_q_heads + h0 + row) * D + c4, acc);
-    } else {
-      const int64_t base = ((int64_t)seq * p.num_q_heads + h0 + row) * p.max_parts + part;
-      store4(p.part_o + base * D + c4, acc);
-      if (c4 == 0) {
-        p.part_ml[base * 2 + 0] = M;
-        p.part_ml[base * 2 + 1] = L;
+    for (int nt = 0; nt < NT; ++nt) m[nt][0] = m[nt][1] = -CUDART_INF_F, l[nt][0] = l[nt][1] = 0.f;
+
+    const int jend = mt.jstart + mt.nsub;
+    bool bad = false;
+    // This warp's sub-tiles: j = warp (mod 4), i.e. the stages it owns
+    // (jstart is a multiple of 4).
+    for (int j = mt.jstart + warp; j < jend; j += C::kConsumers) {
+      const int s = j % C::kStages;
+      if (!mbar_wait(smem_u32(&full[s]), (j / C::kStages) & 1, p.status)) {
+        bad = true;
+        break;
+      }
+      const bool valid = stage_valid[s] != 0;
+      // Copy the sub-tile's K and V fragments to registers and hand the
+      // stage back at once: the producer refills it while this warp
+      // computes, so the ring's bytes stay in flight.
+      uint32_t ka[D / 16][4], va[D / 16][4];
+      if (valid) {
+        const uint32_t kb = ring0 + s * C::kStage;
+        const uint32_t vb = kb + C::kTile;
+        const int tk_a = (mi & 1) * 8 + rr;   // K rows as the A operand (non-transposed)
+        const int tk_v = (mi >> 1) * 8 + rr;  // V rows, transposed into the A operand
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int cg = kk * 2 + (mi >> 1);
+          ldsm_x4(kb + (cg >> 3) * 2048 + tk_a * 128 + (((cg & 7) ^ (tk_a & 7)) << 4), ka[kk][0], ka[kk][1],
+                  ka[kk][2], ka[kk][3]);
+        }
+#pragma unroll
+        for (int a = 0; a < D / 16; ++a) {
+          const int cg = a * 2 + (mi & 1);
+          ldsm_x4_t(vb + (cg >> 3) * 2048 + tk_v * 128 + (((cg & 7) ^ (tk_v & 7)) << 4), va[a][0], va[a][1],
+                    va[a][2], va[a][3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+      if (valid) {
+        const int tok0 = mt.t_begin + (j - mt.jstart) * 16;
+        // S^T = K Q^T: rows = 16 tokens, columns = heads. Two accumulator
+        // chains over the head_dim halves shorten the dependent MMA chain.
+        float sc[NT][4], sc2[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = sc2[nt][0] = sc2[nt][1] = sc2[nt][2] = sc2[nt][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; kk += 2)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            MmaOp<T>::run(sc[nt], ka[kk], qf[kk][nt][0], qf[kk][nt][1]);
+            MmaOp<T>::run(sc2[nt], ka[kk + 1], qf[kk + 1][nt][0], qf[kk + 1][nt][1]);
+          }
+        // Scale to log2 units, mask keys past the partition end.
+        const int t_lo = tok0 + tr, t_hi = tok0 + tr + 8;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          sc[nt][0] = t_lo < mt.t_end ? (sc[nt][0] + sc2[nt][0]) * sl2 : -CUDART_INF_F;
+          sc[nt][1] = t_lo < mt.t_end ? (sc[nt][1] + sc2[nt][1]) * sl2 : -CUDART_INF_F;
+          sc[nt][2] = t_hi < mt.t_end ? (sc[nt][2] + sc2[nt][2]) * sl2 : -CUDART_INF_F;
+          sc[nt][3] = t_hi < mt.t_end ? (sc[nt][3] + sc2[nt][3]) * sl2 : -CUDART_INF_F;
+        }
+        // Online softmax per head column (max over the 16 tokens = over
+        // the 8 lanes that share lane % 4).
+        bool rescale = false;
+        float alpha[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            float mx = fmaxf(sc[nt][c], sc[nt][c + 2]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mn = fmaxf(m[nt][c], mx);
+            const bool dead = mn == -CUDART_INF_F;
+            alpha[nt][c] = dead ? 1.f : exp2f(m[nt][c] - mn);
+            rescale |= mn != m[nt][c];
+            const float p0 = dead ? 0.f : exp2f(sc[nt][c] - mn);
+            const float p1 = dead ? 0.f : exp2f(sc[nt][c + 2] - mn);
+            sc[nt][c] = p0;
+            sc[nt][c + 2] = p1;
+            l[nt][c] = l[nt][c] * alpha[nt][c] + (p0 + p1);
+            m[nt][c] = mn;
+          }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int a = 0; a < D / 16; ++a)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              o[a][nt][0] *= alpha[nt][0];
+              o[a][nt][1] *= alpha[nt][1];
+              o[a][nt][2] *= alpha[nt][0];
+              o[a][nt][3] *= alpha[nt][1];
+            }
+        }
+        // P^T as the B operand (k = tokens, n = heads).
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          pb[nt][0] = movmatrix_trans(MmaOp<T>::pack(sc[nt][0], sc[nt][1]));
+          pb[nt][1] = movmatrix_trans(MmaOp<T>::pack(sc[nt][2], sc[nt][3]));
+        }
+        // Keys past the end carry p = 0, but their V slots may hold any
+        // bits (NaN included): zero those V elements so 0 * V stays 0.
+        if (tok0 + 16 > mt.t_end) {
+          const int tk = tok0 + 2 * ti;
+          const uint32_t keep_lo = (tk < mt.t_end ? 0x0000ffffu : 0u) | (tk + 1 < mt.t_end ? 0xffff0000u : 0u);
+          const uint32_t keep_hi = (tk + 8 < mt.t_end ? 0x0000ffffu : 0u) | (tk + 9 < mt.t_end ? 0xffff0000u : 0u);
+#pragma unroll
+          for (int a = 0; a < D / 16; ++a) {
+            va[a][0] &= keep_lo;
+            va[a][1] &= keep_lo;
+            va[a][2] &= keep_hi;
+            va[a][3] &= keep_hi;
+          }
+        }
+        // O^T += V^T P^T: rows = head_dim (16 per m-tile), k = tokens.
+#pragma unroll
+        for (int a = 0; a < D / 16; ++a)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) MmaOp<T>::run(o[a][nt], va[a], pb[nt][0], pb[nt][1]);
       }
     }
+    if (named_barrier_or(1, C::kConsumers * 32, bad)) break;
+
+    // ---- merge the four warps: per head h, (m_w, l_w, o_w) ----
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float lv = l[nt][c];
+        lv += __shfl_xor_sync(0xffffffffu, lv, 4);
+        lv += __shfl_xor_sync(0xffffffffu, lv, 8);
+        lv += __shfl_xor_sync(0xffffffffu, lv, 16);
+        l[nt][c] = lv;
+        if (tr == 0) {
+          const int h = nt * 8 + 2 * ti + c;
+          ml[(warp * C::kHeads + h) * 2 + 0] = m[nt][c];
+          ml[(warp * C::kHeads + h) * 2 + 1] = lv;
+        }
+      }
+    named_barrier_sync(1, C::kConsumers * 32);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int h = nt * 8 + 2 * ti + c;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < C::kConsumers; ++w) M = fmaxf(M, ml[(w * C::kHeads + h) * 2]);
+        const float f = m[nt][c] == -CUDART_INF_F ? 0.f : exp2f(m[nt][c] - M);
+        float* row = scratch + (warp * C::kHeads + h) * C::kDp;
+#pragma unroll
+        for (int a = 0; a < D / 16; ++a) {
+          row[a * 16 + tr] = o[a][nt][c] * f;
+          row[a * 16 + tr + 8] = o[a][nt][c + 2] * f;
+        }
+      }
+    named_barrier_sync(1, C::kConsumers * 32);
+    const bool single = mt.n_parts == 1;
+    for (int idx = ctid; idx < mt.nrows * (D / 4); idx += C::kConsumers * 32) {
+      const int h = idx / (D / 4);
+      const int d4 = (idx - h * (D / 4)) * 4;
+      float M = -CUDART_INF_F;
+#pragma unroll
+      for (int w = 0; w < C::kConsumers; ++w) M = fmaxf(M, ml[(w * C::kHeads + h) * 2]);
+      float L = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < C::kConsumers; ++w) {
+        const float mw = ml[(w * C::kHeads + h) * 2];
+        L += mw == -CUDART_INF_F ? 0.f : ml[(w * C::kHeads + h) * 2 + 1] * exp2f(mw - M);
+        const float4 v = *reinterpret_cast<const float4*>(scratch + (w * C::kHeads + h) * C::kDp + d4);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      if (single) {
+        const float inv = 1.f / L;
+        store4(static_cast<T*>(p.out) + ((int64_t)mt.qrow * p.num_q_heads + mt.h0 + h) * D + d4,
+               make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+      } else {
+        const int64_t base = ((int64_t)mt.seq * p.num_q_heads + mt.h0 + h) * p.max_parts + mt.part;
+        __stcg(reinterpret_cast<float4*>(p.part_o + base * D + d4), acc);
+        if (d4 == 0) __stcg(reinterpret_cast<float2*>(p.part_ml + base * 2), make_float2(M, L));
+      }
+    }
+    named_barrier_sync(1, C::kConsumers * 32);
   }
 }
 
-// fp32 I/O: CUDA-core path (exact fp32 FMAs, no TF32). Four warps take the
-// partition's tokens round-robin; each lane holds head_dim/32 dimensions and
-// the dot products are reduced across the warp.
+// ---------------------------------------------------------------------------
+// fp32 I/O: CUDA-core path. One CTA per (partition, head group, sequence);
+// four warps take the partition's tokens round-robin, each lane holds
+// head_dim/32 dimensions and dot products are reduced across the warp.
+// ---------------------------------------------------------------------------
 template <int VEC>
 __global__ void __launch_bounds__(128) decode_simt_kernel(const DecodeParams p) {
   constexpr int D = VEC * 32;
   constexpr int ROWS = 8;
   constexpr int NW = 4;
   __shared__ int32_t ids[kMaxPartition / 16];
-  __shared__ float ml[NW][ROWS][2];
+  __shared__ float mls[NW][ROWS][2];
   __shared__ float ob[NW][ROWS][D];
 
   const int part = blockIdx.x;
@@ -390,15 +591,9 @@ __global__ void __launch_bounds__(128) decode_simt_kernel(const DecodeParams p) 
   const int BS = p.block_size;
   int qrow, len;
   if (!decode_row(p, seq, qrow, len)) return;
+  if (!len_ok(p, len)) return;  // reported and zeroed by the plan kernel
   const int h0 = kvh * p.group + rg * p.rows_per_cta;
   const int nrows = min(p.rows_per_cta, p.group - rg * p.rows_per_cta);
-  if (len < 1 || len > p.len_cap || len > p.max_blocks_per_seq * BS) {
-    if (part == 0) {
-      if (threadIdx.x == 0) record_error(p.status, PA_ERR_SEQLEN);
-      write_zero_rows<float>(p, qrow, h0, nrows);
-    }
-    return;
-  }
   const int n_parts = (len + p.partition - 1) / p.partition;
   if (part >= n_parts) return;
   const int t_begin = part * p.partition;
@@ -463,8 +658,8 @@ __global__ void __launch_bounds__(128) decode_simt_kernel(const DecodeParams p) 
   if (lane == 0) {
 #pragma unroll
     for (int g = 0; g < ROWS; ++g) {
-      ml[warp][g][0] = m[g];
-      ml[warp][g][1] = l[g];
+      mls[warp][g][0] = m[g];
+      mls[warp][g][1] = l[g];
     }
   }
   __syncthreads();
@@ -472,7 +667,7 @@ __global__ void __launch_bounds__(128) decode_simt_kernel(const DecodeParams p) 
   for (int g = 0; g < ROWS; ++g) {
     float M = -CUDART_INF_F;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, ml[w][g][0]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, mls[w][g][0]);
     const float f = m[g] == -CUDART_INF_F ? 0.f : exp2f(m[g] - M);
 #pragma unroll
     for (int v = 0; v < VEC; ++v) ob[warp][g][lane + 32 * v] = o[g][v] * f;
@@ -482,12 +677,12 @@ __global__ void __launch_bounds__(128) decode_simt_kernel(const DecodeParams p) 
     const int g = idx / D, d = idx - g * D;
     float M = -CUDART_INF_F;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, ml[w][g][0]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, mls[w][g][0]);
     float L = 0.f, acc = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
-      const float mw = ml[w][g][0];
-      L += mw == -CUDART_INF_F ? 0.f : ml[w][g][1] * exp2f(mw - M);
+      const float mw = mls[w][g][0];
+      L += mw == -CUDART_INF_F ? 0.f : mls[w][g][1] * exp2f(mw - M);
       acc += ob[w][g][d];
     }
     if (n_parts == 1) {
@@ -504,86 +699,124 @@ __global__ void __launch_bounds__(128) decode_simt_kernel(const DecodeParams p) 
 }
 
 // Split-KV merge: out = sum_p 2^(m_p - M) o~_p / sum_p 2^(m_p - M) l_p with
-// M = max_p m_p (scores are kept in log2 units). One CTA per (q head, seq).
+// M = max_p m_p (scores are kept in log2 units). One CTA per (q head,
+// sequence); the partitions' (m, l) pairs are read in parallel, the weights
+// kept in shared memory, and each thread accumulates head_dim / 128 columns.
 template <typename T>
 __global__ void __launch_bounds__(128) splitkv_merge_kernel(const DecodeParams p) {
+  extern __shared__ float wts[];  // [max_parts]
+  __shared__ float red[4];
   const int h = blockIdx.x;
   const int seq = blockIdx.y;
   int qrow, len;
-  if (!decode_row(p, seq, qrow, len)) return;
-  if (len < 1 || len > p.len_cap || len > p.max_blocks_per_seq * p.block_size) return;
+  if (!decode_row(p, seq, qrow, len) || !len_ok(p, len)) return;
   const int n = (len + p.partition - 1) / p.partition;
   if (n <= 1) return;
   const int64_t base = ((int64_t)seq * p.num_q_heads + h) * p.max_parts;
-  extern __shared__ float wts[];  // [max_parts]
-  __shared__ float red[2];
-  if (threadIdx.x < 32) {
-    float M = -CUDART_INF_F;
-    for (int i = threadIdx.x; i < n; i += 32) M = fmaxf(M, p.part_ml[(base + i) * 2]);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float M = -CUDART_INF_F;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) M = fmaxf(M, __ldcg(p.part_ml + (base + i) * 2));
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float L = 0.f;
-    for (int i = threadIdx.x; i < n; i += 32) {
-      const float w = exp2f(p.part_ml[(base + i) * 2] - M);
-      wts[i] = w;
-      L += w * p.part_ml[(base + i) * 2 + 1];
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    if (threadIdx.x == 0) red[0] = 1.f / L;
-  }
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) red[warp] = M;
   __syncthreads();
-  const float invL = red[0];
+  M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  __syncthreads();
+  float L = 0.f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const float2 mlv = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (base + i) * 2));
+    const float w = exp2f(mlv.x - M);
+    wts[i] = w;
+    L += w * mlv.y;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  if (lane == 0) red[warp] = L;
+  __syncthreads();
+  const float invL = 1.f / (red[0] + red[1] + red[2] + red[3]);
   const int D = p.head_dim;
   T* out = static_cast<T*>(p.out) + ((int64_t)qrow * p.num_q_heads + h) * D;
-  for (int d4 = threadIdx.x * 4; d4 < D; d4 += blockDim.x * 4) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < n; ++i) {
-      const float w = wts[i];
-      const float4 v = *reinterpret_cast<const float4*>(p.part_o + (base + i) * D + d4);
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    const float* src = p.part_o + base * D + d;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int i = 0;
+    for (; i + 3 < n; i += 4) {
+      a0 = fmaf(wts[i], __ldcg(src + (int64_t)i * D), a0);
+      a1 = fmaf(wts[i + 1], __ldcg(src + (int64_t)(i + 1) * D), a1);
+      a2 = fmaf(wts[i + 2], __ldcg(src + (int64_t)(i + 2) * D), a2);
+      a3 = fmaf(wts[i + 3], __ldcg(src + (int64_t)(i + 3) * D), a3);
     }
-    acc.x *= invL;
-    acc.y *= invL;
-    acc.z *= invL;
-    acc.w *= invL;
-    store4(out + d4, acc);
+    for (; i < n; ++i) a0 = fmaf(wts[i], __ldcg(src + (int64_t)i * D), a0);
+    out[d] = T(((a0 + a1) + (a2 + a3)) * invL);
   }
 }
 
-template <typename T, int D, int BS>
+static int launch_merge(const DecodeParams& p, pa_dtype dt, cudaStream_t stream) {
+  if (p.max_parts <= 1) return PA_OK;
+  const size_t wbytes = (size_t)p.max_parts * sizeof(float);
+  const dim3 grid(p.num_q_heads, p.num_seqs);
+  if (dt == PA_F32)
+    splitkv_merge_kernel<float><<<grid, 128, wbytes, stream>>>(p);
+  else if (dt == PA_BF16)
+    splitkv_merge_kernel<__nv_bfloat16><<<grid, 128, wbytes, stream>>>(p);
+  else
+    splitkv_merge_kernel<__half><<<grid, 128, wbytes, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+template <typename T, int D, int BS, int NT>
 static int launch_tc(const DecodeParams& p, cudaStream_t stream) {
-  using C = DecodeCfg<D, BS>;
-  const pa_dtype dt = sizeof(T) == 2 && std::is_same<T, __half>::value ? PA_F16 : PA_BF16;
+  using C = DecCfg<D, BS, NT>;
+  constexpr pa_dtype dt = std::is_same<T, __half>::value ? PA_F16 : PA_BF16;
   CUtensorMap kmap, vmap;
   const int64_t rows = (int64_t)p.num_blocks * p.num_kv_heads * BS;
-  int rc = make_kv_tensor_map(&kmap, p.k_cache, rows, D, dt, BS);
+  int rc = make_kv_tensor_map(&kmap, p.k_cache, rows, D, dt, 16);
   if (rc != PA_OK) return rc;
-  rc = make_kv_tensor_map(&vmap, p.v_cache, rows, D, dt, BS);
+  rc = make_kv_tensor_map(&vmap, p.v_cache, rows, D, dt, 16);
   if (rc != PA_OK) return rc;
-  auto kern = decode_tc_kernel<T, D, BS>;
+  auto kern = decode_tc_kernel<T, D, BS, NT>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes) !=
-        cudaSuccess)
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
       return PA_ERR_CUDA;
     attr_set[dev] = true;
   }
-  dim3 grid(p.max_parts, p.num_kv_heads * p.row_groups, p.num_seqs);
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(kmap, vmap, p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  decode_plan_kernel<T><<<1, 1024, 0, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  const int64_t upper = (int64_t)p.num_seqs * p.max_parts * p.num_kv_heads * p.row_groups;
+  const int64_t resident = (NT == 1 ? 2LL : 1LL) * num_sms_current_device();
+  const int ctas = (int)(upper < resident ? upper : resident);
+  kern<<<ctas, C::kThreads, C::kSmem, stream>>>(kmap, vmap, p);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  return launch_merge(p, dt, stream);
 }
 
 template <int VEC>
 static int launch_simt(const DecodeParams& p, cudaStream_t stream) {
+  decode_plan_kernel<float><<<1, 1024, 0, stream>>>(p);
   dim3 grid(p.max_parts, p.num_kv_heads * p.row_groups, p.num_seqs);
   decode_simt_kernel<VEC><<<grid, 128, 0, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  return launch_merge(p, PA_F32, stream);
+}
+
+template <typename T>
+static int launch_tc_dispatch(const DecodeParams& p, cudaStream_t stream) {
+  const int nt = p.rows_per_cta <= 8 ? 1 : 2;
+  const int key = ((p.head_dim == 64 ? 0 : 1) * 2 + (p.block_size == 16 ? 0 : 1)) * 2 + (nt - 1);
+  switch (key) {
+    case 0: return launch_tc<T, 64, 16, 1>(p, stream);
+    case 1: return launch_tc<T, 64, 16, 2>(p, stream);
+    case 2: return launch_tc<T, 64, 32, 1>(p, stream);
+    case 3: return launch_tc<T, 64, 32, 2>(p, stream);
+    case 4: return launch_tc<T, 128, 16, 1>(p, stream);
+    case 5: return launch_tc<T, 128, 16, 2>(p, stream);
+    case 6: return launch_tc<T, 128, 32, 1>(p, stream);
+    case 7: return launch_tc<T, 128, 32, 2>(p, stream);
+  }
+  return PA_ERR_UNSUPPORTED;
 }
 
 int launch_decode(const DecodeParams& p0, pa_dtype dt, cudaStream_t stream) {
@@ -592,40 +825,21 @@ int launch_decode(const DecodeParams& p0, pa_dtype dt, cudaStream_t stream) {
   p.rows_per_cta = p.group < rows_max ? p.group : rows_max;
   p.row_groups = (p.group + p.rows_per_cta - 1) / p.rows_per_cta;
   if ((int64_t)p.num_kv_heads * p.row_groups > 65535) return PA_ERR_UNSUPPORTED;
-  int rc = PA_ERR_UNSUPPORTED;
   if (dt == PA_F32) {
     switch (p.head_dim) {
-      case 32: rc = launch_simt<1>(p, stream); break;
-      case 64: rc = launch_simt<2>(p, stream); break;
-      case 96: rc = launch_simt<3>(p, stream); break;
-      case 128: rc = launch_simt<4>(p, stream); break;
-      case 160: rc = launch_simt<5>(p, stream); break;
-      case 192: rc = launch_simt<6>(p, stream); break;
-      case 224: rc = launch_simt<7>(p, stream); break;
-      case 256: rc = launch_simt<8>(p, stream); break;
-      default: return PA_ERR_UNSUPPORTED;
+      case 32: return launch_simt<1>(p, stream);
+      case 64: return launch_simt<2>(p, stream);
+      case 96: return launch_simt<3>(p, stream);
+      case 128: return launch_simt<4>(p, stream);
+      case 160: return launch_simt<5>(p, stream);
+      case 192: return launch_simt<6>(p, stream);
+      case 224: return launch_simt<7>(p, stream);
+      case 256: return launch_simt<8>(p, stream);
     }
-  } else {
-    const bool bf = dt == PA_BF16;
-    const int key = (p.head_dim == 64 ? 0 : p.head_dim == 128 ? 1 : 9) * 2 + (p.block_size == 16 ? 0 : 1);
-    switch (key) {
-      case 0: rc = bf ? launch_tc<__nv_bfloat16, 64, 16>(p, stream) : launch_tc<__half, 64, 16>(p, stream); break;
-      case 1: rc = bf ? launch_tc<__nv_bfloat16, 64, 32>(p, stream) : launch_tc<__half, 64, 32>(p, stream); break;
-      case 2: rc = bf ? launch_tc<__nv_bfloat16, 128, 16>(p, stream) : launch_tc<__half, 128, 16>(p, stream); break;
-      case 3: rc = bf ? launch_tc<__nv_bfloat16, 128, 32>(p, stream) : launch_tc<__half, 128, 32>(p, stream); break;
-      default: return PA_ERR_UNSUPPORTED;
-    }
+    return PA_ERR_UNSUPPORTED;
   }
-  if (rc != PA_OK || p.max_parts <= 1) return rc;
-  const size_t wbytes = (size_t)p.max_parts * sizeof(float);
-  dim3 grid(p.num_q_heads, p.num_seqs);
-  if (dt == PA_F32)
-    splitkv_merge_kernel<float><<<grid, 128, wbytes, stream>>>(p);
-  else if (dt == PA_BF16)
-    splitkv_merge_kernel<__nv_bfloat16><<<grid, 128, wbytes, stream>>>(p);
-  else
-    splitkv_merge_kernel<__half><<<grid, 128, wbytes, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  if (p.head_dim != 64 && p.head_dim != 128) return PA_ERR_UNSUPPORTED;
+  return dt == PA_BF16 ? launch_tc_dispatch<__nv_bfloat16>(p, stream) : launch_tc_dispatch<__half>(p, stream);
 }
 
 }  // namespace pa

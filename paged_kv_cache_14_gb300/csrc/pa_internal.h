@@ -40,8 +40,29 @@ struct DecodeParams {
   float scale_log2;      // scale * log2(e)
   float* part_o;         // [num_seqs][num_q_heads][max_parts][head_dim]
   float* part_ml;        // [num_seqs][num_q_heads][max_parts][2] (m, l)
+  int32_t* work;         // [0] next work item, [1] number of work items (written by the plan kernel)
+  int32_t* pairs;        // [num_seqs * max_parts] (seq << 16 | partition), in work order
   int* status;
 };
+
+// Split-KV workspace layout shared by the size query and the launch. Every
+// region starts on a 256-byte boundary.
+struct DecodeWorkspace {
+  size_t work, pairs, part_o, part_ml, total;
+};
+inline DecodeWorkspace decode_workspace_layout(int64_t num_seqs, int64_t num_q_heads, int64_t head_dim,
+                                               int64_t max_parts) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  DecodeWorkspace w{};
+  w.work = 0;
+  w.pairs = up(w.work + 16);
+  w.part_o = up(w.pairs + (size_t)num_seqs * max_parts * 4);
+  const size_t po = max_parts > 1 ? (size_t)num_seqs * num_q_heads * max_parts * head_dim * 4 : 0;
+  w.part_ml = up(w.part_o + po);
+  const size_t pm = max_parts > 1 ? (size_t)num_seqs * num_q_heads * max_parts * 2 * 4 : 0;
+  w.total = up(w.part_ml + pm);
+  return w;
+}
 
 struct PrefillParams {
   const void* q;

@@ -61,15 +61,12 @@ class PagedStep:
         if self.cow_pairs.shape[0]:
             n += -(-self.cow_pairs.shape[0] // 1024)
         n += 2  # slot mapping, cache write
-        if self.is_decode:
-            part = pa.pa_decode_partition_size(self.kv_lens.shape[0], self.q.shape[1], self.num_kv_heads,
-                                               self.block_size, self.max_seq_len, self.partition_size)
-            n += 1 + (1 if -(-self.max_seq_len // part) > 1 else 0)
-        else:
-            part = pa.pa_decode_partition_size(self.kv_lens.shape[0], self.q.shape[1], self.num_kv_heads,
-                                               self.block_size, self.max_seq_len, 0)
-            n += 1 + (1 if -(-self.max_seq_len // part) > 1 else 0)
-            n += 1 if self.max_q_len > 1 else 0
+        part = pa.pa_decode_partition_size(self.kv_lens.shape[0], self.q.shape[1], self.num_kv_heads,
+                                           self.block_size, self.max_seq_len,
+                                           self.partition_size if self.is_decode else 0)
+        n += 2 + (1 if -(-self.max_seq_len // part) > 1 else 0)  # plan, main, split-KV merge
+        if not self.is_decode and self.max_q_len > 1:
+            n += 1  # prefill chunks
         return n
 
     def run(self, stream=None) -> torch.Tensor:
