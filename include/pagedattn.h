@@ -65,6 +65,7 @@ typedef enum pa_dtype {
 #define PA_ERR_UNSUPPORTED (-10)/* head_dim (or shape) not supported        */
 #define PA_ERR_TIMEOUT (-11)    /* device: a bounded wait ran out           */
 #define PA_ERR_ALIGN (-12)      /* a tensor pointer is not 16-byte aligned  */
+#define PA_ERR_SCRATCH (-13)    /* pa_decode_noalloc: call needs more scratch than its fixed array */
 
 /* Human-readable name of a status code (static storage). */
 const char* pa_strerror(int status);
@@ -193,6 +194,32 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
               int32_t num_blocks, float scale, void* out, int32_t partition_size, void* workspace,
               size_t workspace_bytes, pa_dtype dtype, void* stream);
+
+/*
+ * pa_decode_noalloc — pa_decode for callers that cannot allocate device
+ * memory when they call (for example a plugin running inside another
+ * runtime's fixed memory pool, a serving loop that forbids cudaMalloc after
+ * start-up because it synchronises the device, or code that must not create
+ * allocations while a stream is being captured). The pages describe no such
+ * call; it exists for these callers only.
+ * Same arguments and results as pa_decode, without workspace arguments: the
+ * split-KV scratch is a fixed device array of
+ * pa_decode_noalloc_scratch_limit() bytes (64 MiB) inside the library, which
+ * every GPU that loads the library holds until the process exits. The call
+ * allocates nothing. A call whose pa_decode_workspace_size() exceeds the
+ * limit returns PA_ERR_SCRATCH before launching anything.
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call during set-up, before
+ * any stream capture. All calls share the one array and it keeps the last
+ * call's contents (nothing in it needs to start at zero): two calls whose
+ * executions overlap on the device, on different streams, race on it.
+ */
+size_t pa_decode_noalloc_scratch_limit(void);
+int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                      int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                      int32_t num_blocks, float scale, void* out, int32_t partition_size, pa_dtype dtype,
+                      void* stream);
 
 /*
  * pa_chunked_prefill — attention of a mixed batch (prefill chunks and

@@ -16,6 +16,8 @@ from ._binding import (  # noqa: F401
     pa_chunked_prefill_workspace_size,
     pa_copy_blocks,
     pa_decode,
+    pa_decode_noalloc,
+    pa_decode_noalloc_scratch_limit,
     pa_decode_partition_size,
     pa_decode_workspace_size,
     pa_get_status,

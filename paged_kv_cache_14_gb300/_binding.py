@@ -25,7 +25,8 @@ _DT = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
 EXPORTS = (
     "pa_strerror", "pa_version", "pa_get_status", "pa_slot_mapping", "pa_reshape_and_cache",
     "pa_copy_blocks", "pa_decode_partition_size", "pa_decode_workspace_size", "pa_decode",
-    "pa_chunked_prefill_workspace_size", "pa_chunked_prefill",
+    "pa_chunked_prefill_workspace_size", "pa_chunked_prefill", "pa_decode_noalloc_scratch_limit",
+    "pa_decode_noalloc",
 )
 
 _i32, _i64, _f32, _vp, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
@@ -62,6 +63,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "pa_chunked_prefill_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
         "pa_chunked_prefill": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                               _i32, _i32, _i32, _f32, _vp, _vp, _sz, ctypes.c_int, _vp]),
+        "pa_decode_noalloc_scratch_limit": (_sz, []),
+        "pa_decode_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                             _i32, _f32, _vp, _i32, ctypes.c_int, _vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -214,4 +218,25 @@ def pa_chunked_prefill(q: torch.Tensor, cu_q_lens: torch.Tensor, k_cache: torch.
         _cuda(ctx_lens, "ctx_lens", torch.int32), n, int(max_q_len), int(max_kv_len), hq, hkv, D, B, P,
         float(scale), _cuda(out, "out", dt), ws_ptr, ws_bytes, _DT[dt], _stream(stream))
     _check(rc, "pa_chunked_prefill")
+    return out
+
+
+def pa_decode_noalloc_scratch_limit() -> int:
+    return int(load().pa_decode_noalloc_scratch_limit())
+
+
+def pa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                      seq_lens: torch.Tensor, max_seq_len: int, scale: float, out: torch.Tensor,
+                      partition_size: int = 0, stream=None) -> torch.Tensor:
+    """pa_decode with the library's fixed scratch instead of a workspace.
+    `out` must be given: this path allocates nothing."""
+    N, hq, D = q.shape
+    P, hkv, B, _ = k_cache.shape
+    dt = q.dtype
+    rc = load().pa_decode_noalloc(
+        _cuda(q, "q", dt), _cuda(k_cache, "k_cache", dt), _cuda(v_cache, "v_cache", dt),
+        _cuda(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _cuda(seq_lens, "seq_lens", torch.int32), N, int(max_seq_len), hq, hkv, D, B, P, float(scale),
+        _cuda(out, "out", dt), int(partition_size), _DT[dt], _stream(stream))
+    _check(rc, "pa_decode_noalloc")
     return out

@@ -137,6 +137,7 @@ const char* pa_strerror(int s) {
     case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: shape not supported";
     case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: a bounded device wait ran out";
     case PA_ERR_ALIGN: return "PA_ERR_ALIGN: pointer not 16-byte aligned";
+    case PA_ERR_SCRATCH: return "PA_ERR_SCRATCH: the call needs more than pa_decode_noalloc's fixed scratch";
   }
   return "unknown status";
 }
