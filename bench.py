@@ -81,6 +81,20 @@ def decode_algorithmic_bytes(batch) -> dict:
     }
 
 
+def prefill_flops(batch) -> float:
+    """Tensor FLOPs of the chunk rows (q_len > 1): for every query row and
+    query head, 2*D for q.k and 2*D for p.v per key it attends to."""
+    f = 0.0
+    for i in range(batch.num_seqs):
+        ql = int(batch.q_lens[i])
+        if ql <= 1:
+            continue
+        ctx = int(batch.kv_lens[i]) - ql
+        keys = ql * ctx + ql * (ql + 1) // 2
+        f += 4.0 * batch.head_dim * batch.num_q_heads * keys
+    return f
+
+
 def step_extra_bytes(batch) -> int:
     """Bytes of the non-attention rows of a step: block copies (read + write
     of both pools), slot derivation and the cache write."""
@@ -167,6 +181,17 @@ def measured_peak_hbm() -> tuple[float, str]:
             return float(json.load(f)["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return 6800.0, "fallback"
+
+
+def measured_peak_tensor() -> tuple[float, str]:
+    """Dense 16-bit tensor peak (TFLOP/s): the measured cuBLAS bf16 burst
+    figure (fp16 has the same nominal rate, ratio 1)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (bf16 burst; fp16 nominal ratio 1)"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
 
 
 def profiled_traffic() -> float | None:
@@ -331,8 +356,12 @@ def native_arm(args) -> None:
                                slot_mapping=st.slot_mapping)
             pa.pa_reshape_and_cache(st.k_new, st.v_new, st.slot_mapping, st.k_cache, st.v_cache)
             ev[i][0].record(stream)
-            pa.pa_decode(st.q, st.k_cache, st.v_cache, st.block_tables, st.kv_lens, st.max_seq_len, st.scale,
-                         out=st.out, partition_size=st.partition_size, workspace=st.workspace)
+            if st.is_decode:
+                pa.pa_decode(st.q, st.k_cache, st.v_cache, st.block_tables, st.kv_lens, st.max_seq_len, st.scale,
+                             out=st.out, partition_size=st.partition_size, workspace=st.workspace)
+            else:
+                pa.pa_chunked_prefill(st.q, st.cu_q_lens, st.k_cache, st.v_cache, st.block_tables, st.ctx_lens,
+                                      st.max_q_len, st.max_seq_len, st.scale, out=st.out, workspace=st.workspace)
             ev[i][1].record(stream)
         stop.record(stream)
         barrier()
@@ -352,6 +381,13 @@ def native_arm(args) -> None:
         "new_seq_ids": torch.from_numpy(batch.new_seq_ids).pin_memory(),
         "new_positions": torch.from_numpy(batch.new_positions).pin_memory(),
     }
+    dev_of = {"q": st.q, "k_new": st.k_new, "v_new": st.v_new, "block_tables": st.block_tables,
+              "kv_lens": st.kv_lens, "new_seq_ids": st.new_seq_ids, "new_positions": st.new_positions}
+    if not st.is_decode:
+        host["cu_q_lens"] = torch.from_numpy(batch.cu_q_lens).pin_memory()
+        host["ctx_lens"] = torch.from_numpy(batch.ctx_lens).pin_memory()
+        dev_of["cu_q_lens"] = st.cu_q_lens
+        dev_of["ctx_lens"] = st.ctx_lens
     out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_host.numel() * out_host.element_size()
@@ -361,13 +397,8 @@ def native_arm(args) -> None:
     e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
     for _ in range(e2e_steps):
-        st.q.copy_(host["q"], non_blocking=True)
-        st.k_new.copy_(host["k_new"], non_blocking=True)
-        st.v_new.copy_(host["v_new"], non_blocking=True)
-        st.block_tables.copy_(host["block_tables"], non_blocking=True)
-        st.kv_lens.copy_(host["kv_lens"], non_blocking=True)
-        st.new_seq_ids.copy_(host["new_seq_ids"], non_blocking=True)
-        st.new_positions.copy_(host["new_positions"], non_blocking=True)
+        for name, t in host.items():
+            dev_of[name].copy_(t, non_blocking=True)
         st.run()
         out_host.copy_(st.out, non_blocking=True)
     e_stop.record(stream)
@@ -383,11 +414,15 @@ def native_arm(args) -> None:
     ms_step = ms_total / args.steps
 
     peak, peak_kind = measured_peak_hbm()
+    if not st.is_decode:
+        flops = prefill_flops(batch)
+        tpeak, tkind = measured_peak_tensor()
+        achieved_tf = flops / (dec_mean * 1e-3) / 1e12
     value = world * step_bytes / (ms_step * 1e-3) / 1e9
     e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
     dec_gbs = dec_bytes["total"] / (dec_mean * 1e-3) / 1e9
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and st.is_decode:
         res = run_oracle_sample(args.config, args.cpu_seconds, 1)[0]
         gbs, sps = oracle_rate(batch, res, per_seq_decode_bytes(batch))
         cpu = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -415,10 +450,15 @@ def native_arm(args) -> None:
                     2 * batch.k_cache.numel() * batch.k_cache.element_size() / 1e9),
                 "parallelism": f"replicas x{world}",
             },
-            "roofline": {"kernel": "paged decode (main + split-KV merge)", "bound": "hbm",
-                         "achieved": round(dec_gbs, 2), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": round(dec_gbs / peak, 4), "traffic": profiled_traffic(),
-                         "algorithmic_bytes": dec_bytes["total"], "ms_per_launch": round(dec_mean, 5)},
+            "roofline": ({"kernel": "paged decode (main + split-KV merge)", "bound": "hbm",
+                          "achieved": round(dec_gbs, 2), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                          "frac": round(dec_gbs / peak, 4), "traffic": profiled_traffic(),
+                          "algorithmic_bytes": dec_bytes["total"], "ms_per_launch": round(dec_mean, 5)}
+                         if st.is_decode else
+                         {"kernel": "chunked prefill call (tcgen05 chunk tiles + decode rows)", "bound": "tensor",
+                          "achieved": round(achieved_tf, 2), "peak": tpeak, "peak_kind": tkind,
+                          "unit": "TFLOP/s", "frac": round(achieved_tf / tpeak, 4), "traffic": None,
+                          "algorithmic_flops": flops, "ms_per_launch": round(dec_mean, 5)}),
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
                     "wall_ms_per_step": round(wall_ms, 5)},

@@ -227,27 +227,33 @@ int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, c
  * Production Engine Architecture...", section 3 "Dynamic Chunked Prefill").
  *   q          : [total_q][num_q_heads][head_dim]; sequence i owns rows
  *                cu_q_lens[i] .. cu_q_lens[i+1]-1
- *   cu_q_lens  : int32 [num_seqs+1], cu_q_lens[0] = 0, non-decreasing
+ *   cu_q_lens  : int32 [num_seqs+1], cu_q_lens[0] = 0, non-decreasing,
+ *                cu_q_lens[num_seqs] = total_q
  *   ctx_lens   : int32 [num_seqs]; tokens before sequence i's chunk. Row r
  *                of the chunk sits at position ctx_lens[i] + r and attends to
  *                keys 0 .. ctx_lens[i] + r (causal inside the chunk). The
  *                chunk's own K/V must already be cached (pa_reshape_and_cache
  *                of its tokens first).
  *   max_q_len, max_kv_len : host upper bounds of the q_len and of
- *                ctx_len + q_len over the batch (they size the grids)
+ *                ctx_len + q_len over the batch; a sequence above them
+ *                records PA_ERR_SEQLEN and is skipped
  *   out        : [total_q][num_q_heads][head_dim]
- *   workspace  : pa_chunked_prefill_workspace_size() bytes
- * Rows with q_len == 1 go through the decode path; longer chunks through a
- * tcgen05 tensor-core kernel (fp16/bf16, head_dim 128).
+ *   workspace  : pa_chunked_prefill_workspace_size() bytes, 16-byte aligned,
+ *                no initialisation needed; not shared by overlapping calls
+ * Rows with q_len == 1 go through the decode path (any supported dtype and
+ * head_dim); longer chunks through a tcgen05 tensor-core kernel that needs
+ * fp16/bf16, head_dim 128 and a power-of-two GQA group of at most 128
+ * (PA_ERR_DTYPE / PA_ERR_UNSUPPORTED otherwise).
  */
 size_t pa_chunked_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                                         int32_t head_dim, int32_t block_size, int32_t max_kv_len);
-int pa_chunked_prefill(const void* q, const int32_t* cu_q_lens, const void* k_cache, const void* v_cache,
-                       const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* ctx_lens,
-                       int32_t num_seqs, int32_t max_q_len, int32_t max_kv_len, int32_t num_q_heads,
-                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                       float scale, void* out, void* workspace, size_t workspace_bytes, pa_dtype dtype,
-                       void* stream);
+                                         int32_t head_dim, int32_t block_size, int32_t total_q,
+                                         int32_t max_kv_len);
+int pa_chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_lens, const void* k_cache,
+                       const void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* ctx_lens, int32_t num_seqs, int32_t max_q_len, int32_t max_kv_len,
+                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                       int32_t num_blocks, float scale, void* out, void* workspace, size_t workspace_bytes,
+                       pa_dtype dtype, void* stream);
 
 #ifdef __cplusplus
 }

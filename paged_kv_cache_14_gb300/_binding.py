@@ -60,9 +60,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "pa_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
         "pa_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                      _f32, _vp, _i32, _vp, _sz, ctypes.c_int, _vp]),
-        "pa_chunked_prefill_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
-        "pa_chunked_prefill": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
-                                              _i32, _i32, _i32, _f32, _vp, _vp, _sz, ctypes.c_int, _vp]),
+        "pa_chunked_prefill_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
+        "pa_chunked_prefill": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                              _i32, _i32, _i32, _i32, _f32, _vp, _vp, _sz, ctypes.c_int, _vp]),
         "pa_decode_noalloc_scratch_limit": (_sz, []),
         "pa_decode_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                              _i32, _f32, _vp, _i32, ctypes.c_int, _vp]),
@@ -192,9 +192,9 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, blo
 
 
 def pa_chunked_prefill_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
-                                      block_size: int, max_kv_len: int) -> int:
+                                      block_size: int, total_q: int, max_kv_len: int) -> int:
     return int(load().pa_chunked_prefill_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                                        block_size, max_kv_len))
+                                                        block_size, total_q, max_kv_len))
 
 
 def pa_chunked_prefill(q: torch.Tensor, cu_q_lens: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
@@ -207,13 +207,13 @@ def pa_chunked_prefill(q: torch.Tensor, cu_q_lens: torch.Tensor, k_cache: torch.
     dt = q.dtype
     if out is None:
         out = torch.empty_like(q)
-    need = pa_chunked_prefill_workspace_size(n, hq, hkv, D, B, max_kv_len)
+    need = pa_chunked_prefill_workspace_size(n, hq, hkv, D, B, T, max_kv_len)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     rc = load().pa_chunked_prefill(
-        _cuda(q, "q", dt), _cuda(cu_q_lens, "cu_q_lens", torch.int32), _cuda(k_cache, "k_cache", dt),
+        _cuda(q, "q", dt), T, _cuda(cu_q_lens, "cu_q_lens", torch.int32), _cuda(k_cache, "k_cache", dt),
         _cuda(v_cache, "v_cache", dt), _cuda(block_tables, "block_tables", torch.int32), block_tables.shape[1],
         _cuda(ctx_lens, "ctx_lens", torch.int32), n, int(max_q_len), int(max_kv_len), hq, hkv, D, B, P,
         float(scale), _cuda(out, "out", dt), ws_ptr, ws_bytes, _DT[dt], _stream(stream))

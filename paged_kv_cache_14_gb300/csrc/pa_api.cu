@@ -95,6 +95,22 @@ int make_2d_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+int make_3d_tensor_map(CUtensorMap* map, const void* base, int64_t d2, int64_t d1, int64_t d0, pa_dtype dt,
+                       int32_t b2, int32_t b1, int32_t b0) {
+  auto fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  if (dt == PA_F32) return PA_ERR_DTYPE;
+  const CUtensorMapDataType t = dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t gdim[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+  cuuint64_t gstride[2] = {(cuuint64_t)d0 * 2, (cuuint64_t)(d1 * d0 * 2)};
+  cuuint32_t box[3] = {(cuuint32_t)b0, (cuuint32_t)b1, (cuuint32_t)b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, t, 3, const_cast<void*>(base), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 int make_kv_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t head_dim, pa_dtype dt,
                        int32_t box_rows) {
   return make_2d_tensor_map(map, base, rows, head_dim, head_dim, dt, box_rows, 64);
@@ -301,27 +317,44 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
 }
 
 size_t pa_chunked_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                                         int32_t head_dim, int32_t block_size, int32_t max_kv_len) {
-  return pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_kv_len, 0);
+                                         int32_t head_dim, int32_t block_size, int32_t total_q, int32_t max_kv_len) {
+  const size_t dec =
+      pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_kv_len, 0);
+  if (dec == 0) return 0;
+  // + the chunk-tile work list: a counter pair and at most total_q tiles.
+  return dec + (((size_t)16 + (size_t)(total_q > 0 ? total_q : 0) * 4 + 255) & ~size_t(255));
 }
 
-int pa_chunked_prefill(const void* q, const int32_t* cu_q_lens, const void* k_cache, const void* v_cache,
-                       const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* ctx_lens,
-                       int32_t num_seqs, int32_t max_q_len, int32_t max_kv_len, int32_t num_q_heads,
-                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
-                       void* out, void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
-  if (num_seqs < 0 || max_q_len < 0 || max_kv_len < 0) return PA_ERR_ARG;
-  if (num_seqs == 0 || max_q_len == 0) return PA_OK;
+int pa_chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_lens, const void* k_cache,
+                       const void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* ctx_lens, int32_t num_seqs, int32_t max_q_len, int32_t max_kv_len,
+                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                       int32_t num_blocks, float scale, void* out, void* workspace, size_t workspace_bytes,
+                       pa_dtype dtype, void* stream) {
+  if (num_seqs < 0 || max_q_len < 0 || max_kv_len < 0 || total_q < 0) return PA_ERR_ARG;
+  if (num_seqs == 0 || max_q_len == 0 || total_q == 0) return PA_OK;
   if (!cu_q_lens || !ctx_lens) return PA_ERR_ARG;
   if (dtype == PA_F32 && max_q_len > 1) return PA_ERR_DTYPE;
-  if (max_q_len > 1 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (max_q_len > 1) {
+    if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads) return PA_ERR_HEADS;
+    const int32_t g = num_q_heads / num_kv_heads;
+    if (g > 128 || (g & (g - 1))) return PA_ERR_UNSUPPORTED;
+    if (max_q_len > total_q) return PA_ERR_ARG;
+  }
+  const size_t dec_ws =
+      pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_kv_len, 0);
+  if (!workspace ||
+      workspace_bytes < pa_chunked_prefill_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                          block_size, total_q, max_kv_len))
+    return PA_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // Decode rows (q_len == 1): the split-KV decode path, key count ctx + 1.
   int rc = decode_common(q, k_cache, v_cache, block_tables, max_blocks_per_seq, ctx_lens, cu_q_lens, num_seqs,
                          max_kv_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out, 0,
-                         workspace, workspace_bytes, dtype, s);
+                         workspace, dec_ws, dtype, s);
   if (rc != PA_OK || max_q_len <= 1) return rc;
-  // Chunks (q_len > 1): tensor-core tiles.
+  // Chunks (q_len > 1): tcgen05 tiles.
   PrefillParams p{};
   p.q = q;
   p.out = out;
@@ -338,7 +371,11 @@ int pa_chunked_prefill(const void* q, const int32_t* cu_q_lens, const void* k_ca
   p.group = num_q_heads / num_kv_heads;
   p.max_q_len = max_q_len;
   p.max_kv_len = max_kv_len;
+  p.total_q = total_q;
   p.scale_log2 = scale * 1.4426950408889634f;
+  uint8_t* pw = static_cast<uint8_t*>(workspace) + dec_ws;
+  p.work = reinterpret_cast<int32_t*>(pw);
+  p.pairs = reinterpret_cast<int32_t*>(pw + 16);
   p.status = device_status_ptr();
   return launch_prefill(p, k_cache, v_cache, dtype, s);
 }

@@ -80,8 +80,11 @@ struct PrefillParams {
   int32_t group;
   int32_t max_q_len;
   int32_t max_kv_len;
-  int32_t m_tiles;  // grid.x
+  int32_t total_q;   // rows of q / out
+  int32_t gshift;    // log2(group)
   float scale_log2;
+  int32_t* work;     // [0] next work item, [1] number of work items
+  int32_t* pairs;    // (seq << 16 | row tile), longest first
   int* status;
 };
 
@@ -93,6 +96,9 @@ int num_sms_current_device();
 // box = [box_rows rows][64 elements] with 128-byte swizzle (16-bit dtypes only).
 int make_kv_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t head_dim, pa_dtype dt,
                        int32_t box_rows);
+// 3-D map over a [d2][d1][d0] tensor (d0 contiguous), box [b2][b1][b0], 128-byte swizzle.
+int make_3d_tensor_map(CUtensorMap* map, const void* base, int64_t d2, int64_t d1, int64_t d0, pa_dtype dt,
+                       int32_t b2, int32_t b1, int32_t b0);
 // Same view, generic box (inner box_cols elements), 128-byte swizzle.
 int make_2d_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t cols, int64_t row_stride_elems,
                        pa_dtype dt, int32_t box_rows, int32_t box_cols);

@@ -1,13 +1,458 @@
-// Chunked-prefill attention on tcgen05 tensor cores (sm_103a).
+// Chunked-prefill attention over a paged context on tcgen05 tensor cores
+// (sm_103a). Chunked prefill splits a prompt into chunks that run alongside
+// decode rows ("Tech Radar: vLLM v1 Production Engine Architecture ...",
+// section 3 "Dynamic Chunked Prefill"); prefill is the tensor-core-bound
+// phase (same page, "The Prefill Phase (Compute-Bound)").
+//
+// Tiles. A chunk of q_len query rows of a sequence with ctx prior tokens is
+// cut into M = 128-row tiles of packed (query position, GQA head) rows: all G
+// query heads that share one KV head are consecutive rows, so every K/V tile
+// is read once per KV head and feeds a full 128-row MMA. Row r of the chunk
+// sits at position ctx + r and attends to keys 0 .. ctx + r.
+//
+// One persistent CTA (192 threads, two per SM) loops over work items (chunk
+// tile, KV head) listed by a plan kernel, longest first:
+//   warp 0  producer: TMA of the 128 query rows (3-D tensor map over
+//           [tokens][heads][head_dim], 128-byte swizzle), then for every
+//           64-token KV tile the four 16-token sub-tiles of K and V through
+//           the block table into a 2-stage ring;
+//   warp 1  owns the tensor memory (256 columns: S = 128x64 fp32 at column 0,
+//           O = 128x128 fp32 at column 128) and one lane issues the MMAs:
+//           S = Q K^T (K-major operands), then O += P V (P K-major from
+//           shared memory, V MN-major);
+//   warps 2-5  softmax: thread i owns row i (tensor-memory lane i): it loads
+//           its S row, applies the causal mask, keeps the running max and sum
+//           in registers, writes P (16-bit) into the swizzled P tile,
+//           rescales its O row in tensor memory when the max moved, and at
+//           the end normalises O and stores it.
+// Every mbarrier wait is time-bounded: on a timeout the kernel records
+// PA_ERR_TIMEOUT, lets outstanding copies and MMAs finish (bounded) and
+// returns; no wait can spin forever.
+#include <math_constants.h>
+
+#include <type_traits>
+
 #include "pa_common.cuh"
 #include "pa_internal.h"
+#include "pa_tcgen05.cuh"
 
 namespace pa {
 
-int launch_prefill(const PrefillParams& p, const void* k_cache, const void* v_cache, pa_dtype dt,
+namespace pf {
+constexpr int kM = 128;        // packed rows per tile (tensor-memory lanes)
+constexpr int kD = 128;        // head_dim
+constexpr int kN = 64;         // keys per KV tile
+constexpr int kThreads = 192;  // producer, MMA, 4 softmax warps
+constexpr int kQHalf = kM * 128;           // one 64-column half of Q: 128 rows x 128 B
+constexpr int kQBytes = 2 * kQHalf;        // 32 KB
+constexpr int kKVHalf = kN * 128;          // 64 rows x 128 B
+constexpr int kKBytes = 2 * kKVHalf;       // 16 KB
+constexpr int kStageBytes = 2 * kKBytes;   // K + V: 32 KB
+constexpr int kPBytes = kM * 128;          // 128 rows x 64 keys x 2 B
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kOffQ + kQBytes;
+constexpr int kOffP = kOffKV + 2 * kStageBytes;
+constexpr int kOffBar = kOffP + kPBytes;
+// bars: q_full, kv_full[2], kv_empty[2], s_full, s_free, p_full, o_done
+constexpr int kNumBars = 9;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, item, abort
+constexpr int kSmem = kOffMisc + 64;
+constexpr int kTmemCols = 256;
+constexpr int kColS = 0;
+constexpr int kColO = 128;
+}  // namespace pf
+
+// Plan: list (sequence, row tile) pairs of every chunk with q_len > 1,
+// ordered by decreasing number of KV tiles (longest items first), and reset
+// the item counter. One CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams p) {
+  constexpr int kBins = 2048;
+  __shared__ int hist[kBins];
+  __shared__ int total;
+  const int pp = pf::kM >> p.gshift;  // query positions per tile
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
+  if (threadIdx.x == 0) total = 0;
+  __syncthreads();
+  auto tiles_of = [&](int seq, int mt) -> int {
+    const int q0 = p.cu_q_lens[seq], ql = p.cu_q_lens[seq + 1] - q0;
+    const int ctx = p.ctx_lens[seq];
+    const int pos_hi = min((mt + 1) * pp, ql);
+    const int keys = ctx + pos_hi;
+    const int t = (keys + pf::kN - 1) / pf::kN;
+    return min(t, kBins - 1);
+  };
+  for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) {
+    const int ql = p.cu_q_lens[s + 1] - p.cu_q_lens[s];
+    if (ql <= 1) continue;
+    const int kv = p.ctx_lens[s] + ql;
+    if (p.ctx_lens[s] < 0 || kv > p.max_kv_len || kv > p.max_blocks_per_seq * p.block_size || ql > p.max_q_len) {
+      record_error(p.status, PA_ERR_SEQLEN);
+      continue;
+    }
+    const int nm = (ql + pp - 1) / pp;
+    for (int mt = 0; mt < nm; ++mt) atomicAdd(&hist[tiles_of(s, mt)], 1);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Exclusive scan from the longest bin down.
+    int run = 0;
+    for (int b = kBins - 1; b >= 0; --b) {
+      const int c = hist[b];
+      hist[b] = run;
+      run += c;
+    }
+    total = run;
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) {
+    const int ql = p.cu_q_lens[s + 1] - p.cu_q_lens[s];
+    if (ql <= 1) continue;
+    const int kv = p.ctx_lens[s] + ql;
+    if (p.ctx_lens[s] < 0 || kv > p.max_kv_len || kv > p.max_blocks_per_seq * p.block_size || ql > p.max_q_len)
+      continue;
+    const int nm = (ql + pp - 1) / pp;
+    for (int mt = 0; mt < nm; ++mt) {
+      const int slot = atomicAdd(&hist[tiles_of(s, mt)], 1);
+      p.pairs[slot] = (s << 16) | mt;
+    }
+  }
+  if (threadIdx.x == 0) {
+    p.work[0] = 0;
+    p.work[1] = total * p.num_kv_heads;
+  }
+}
+
+template <typename T, int BS>
+__global__ void __launch_bounds__(pf::kThreads, 2)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+  using namespace pf;
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  constexpr uint32_t kIdescS = idesc_f16(kM, kN, kBf16, false);  // S = Q K^T
+  constexpr uint32_t kIdescO = idesc_f16(kM, kD, kBf16, true);   // O += P V (V MN-major)
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  const uint32_t b_q = smem_u32(&bars[0]);
+  const uint32_t b_kvfull0 = smem_u32(&bars[1]);
+  const uint32_t b_kvempty0 = smem_u32(&bars[3]);
+  const uint32_t b_sfull = smem_u32(&bars[5]);
+  const uint32_t b_sfree = smem_u32(&bars[6]);
+  const uint32_t b_pfull = smem_u32(&bars[7]);
+  const uint32_t b_odone = smem_u32(&bars[8]);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(&misc[2]);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    if ((sbase & 1023u) != 0) record_error(p.status, PA_ERR_ALIGN);
+    mbar_init(b_q, 1);
+    mbar_init(b_kvfull0, 1);
+    mbar_init(b_kvfull0 + 8, 1);
+    mbar_init(b_kvempty0, 1);
+    mbar_init(b_kvempty0 + 8, 1);
+    mbar_init(b_sfull, 1);
+    mbar_init(b_sfree, 4);
+    mbar_init(b_pfull, 4);
+    mbar_init(b_odone, 1);
+    abort_flag[0] = (sbase & 1023u) != 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&misc[0]), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const int G = 1 << p.gshift;
+  const int pp = kM >> p.gshift;
+  const int total = p.work[1];
+
+  int tile_base = 0;  // KV tiles processed by this CTA before the current item
+  for (int it = 0;; ++it) {
+    if (threadIdx.x == 0) misc[1] = abort_flag[0] ? 0x7fffffff : atomicAdd(&p.work[0], 1);
+    __syncthreads();
+    const int item = (int)misc[1];
+    if (item >= total) break;
+    const int pr = p.pairs[item / p.num_kv_heads];
+    const int kvh = item - (item / p.num_kv_heads) * p.num_kv_heads;
+    const int seq = pr >> 16, mt = pr & 0xffff;
+    const int q0 = p.cu_q_lens[seq];
+    const int ql = p.cu_q_lens[seq + 1] - q0;
+    const int ctx = p.ctx_lens[seq];
+    const int kv_len = ctx + ql;
+    const int pos_lo = mt * pp;
+    const int pos_hi = min(pos_lo + pp, ql);
+    const int keys = ctx + pos_hi;  // keys the tile's last row needs
+    const int ntiles = (keys + kN - 1) / kN;
+    const int nblk_seq = (kv_len + BS - 1) / BS;
+
+    if (warp == 0) {
+      // =========================== producer ===========================
+      bool bad = false;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(b_q, kQBytes);
+        tma_load_3d(sbase + kOffQ, &qmap, 0, kvh * G, q0 + pos_lo, b_q);
+        tma_load_3d(sbase + kOffQ + kQHalf, &qmap, 64, kvh * G, q0 + pos_lo, b_q);
+      }
+      const int32_t* bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
+      for (int j = 0; j < ntiles; ++j) {
+        const int g = tile_base + j;
+        const int s = g & 1;
+        // Lanes 0..3: physical block of the tile's 16-token sub-tile `lane`.
+        int id = 0;
+        if (lane < 4) {
+          const int bi = (j * kN + lane * 16) / BS;
+          if (bi < nblk_seq) {
+            id = bt[bi];
+            if (id < 0 || id >= p.num_blocks) {
+              record_error(p.status, PA_ERR_BLOCK_OOB);
+              id = 0;
+            }
+          }
+        }
+        int ids[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ids[u] = __shfl_sync(0xffffffffu, id, u);
+        if (lane == 0) {
+          if (g >= 2 && !mbar_wait(b_kvempty0 + 8 * s, ((g >> 1) & 1) ^ 1, p.status)) {
+            bad = true;
+          } else {
+            const uint32_t fb = b_kvfull0 + 8 * s;
+            mbar_arrive_expect_tx(fb, kStageBytes);
+            const uint32_t kdst = sbase + kOffKV + s * kStageBytes;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int row = (ids[u] * p.num_kv_heads + kvh) * BS + ((j * kN + u * 16) % BS);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                tma_load_2d(kdst + h * kKVHalf + u * 2048, &kmap, h * 64, row, fb);
+                tma_load_2d(kdst + kKBytes + h * kKVHalf + u * 2048, &vmap, h * 64, row, fb);
+              }
+            }
+          }
+        }
+        bad = __shfl_sync(0xffffffffu, bad, 0);
+        if (bad) {
+          abort_flag[0] = 1;
+          // Let the copies already issued land before the CTA moves on.
+          if (lane == 0) {
+            mbar_wait(b_q, it & 1, nullptr);
+            for (int jj = max(0, j - 2); jj < j; ++jj)
+              mbar_wait(b_kvfull0 + 8 * ((tile_base + jj) & 1), ((tile_base + jj) >> 1) & 1, nullptr);
+          }
+          break;
+        }
+      }
+    } else if (warp == 1) {
+      // ============================= MMA =============================
+      if (lane == 0) {
+        bool bad = !mbar_wait(b_q, it & 1, p.status);
+        uint32_t last_bar = 0, last_phase = 0;  // the last commit: it covers every MMA issued before it
+        for (int j = 0; j < ntiles && !bad; ++j) {
+          const int g = tile_base + j;
+          const int s = g & 1;
+          if (!mbar_wait(b_kvfull0 + 8 * s, (g >> 1) & 1, p.status)) { bad = true; break; }
+          if (g > 0 && !mbar_wait(b_sfree, (g - 1) & 1, p.status)) { bad = true; break; }
+          tc_fence_after();
+          const uint32_t kst = sbase + kOffKV + s * kStageBytes;
+#pragma unroll
+          for (int k = 0; k < kD / 16; ++k) {
+            const uint64_t ad = sdesc_sw128(sbase + kOffQ + (k >> 2) * kQHalf + (k & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(kst + (k >> 2) * kKVHalf + (k & 3) * 32, 16, 1024);
+            tc_mma_f16(tmem + kColS, ad, bd, kIdescS, k > 0);
+          }
+          tc_commit(b_sfull);
+          last_bar = b_sfull;
+          last_phase = g & 1;
+          if (!mbar_wait(b_pfull, g & 1, p.status)) { bad = true; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kN / 16; ++k) {
+            const uint64_t ad = sdesc_sw128(sbase + kOffP + k * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(kst + kKBytes + k * 2048, kKVHalf, 1024);
+            tc_mma_f16(tmem + kColO, ad, bd, kIdescO, (j > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(b_odone);
+          tc_commit(b_kvempty0 + 8 * s);
+          last_bar = b_odone;
+          last_phase = g & 1;
+        }
+        if (bad) {
+          abort_flag[0] = 1;
+          // Let issued MMAs finish before tensor memory is released.
+          if (last_bar) mbar_wait(last_bar, last_phase, nullptr);
+        }
+      }
+      __syncwarp();
+    } else {
+      // =========================== softmax ===========================
+      const int q = warp & 3;             // tensor-memory lane quarter of this warp
+      const int row = q * 32 + lane;      // packed row owned by this thread
+      const uint32_t tl = (uint32_t)(q * 32) << 16;
+      const int pos = pos_lo + (row >> p.gshift);
+      const int head = row & (G - 1);
+      const int lim = min(ctx + pos, kv_len - 1);  // last key this row may see
+      const float sl2 = p.scale_log2;
+      float m = -CUDART_INF_F, l = 0.f;
+      bool bad = false;
+      for (int j = 0; j < ntiles; ++j) {
+        const int g = tile_base + j;
+        if (!mbar_wait(b_sfull, g & 1, p.status)) { bad = true; break; }
+        tc_fence_after();
+        uint32_t sr[2][32];
+        tmem_ld32(tmem + tl + kColS, sr[0]);
+        tmem_ld32(tmem + tl + kColS + 32, sr[1]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_sfree);
+        const int k0 = j * kN;
+        float mx = -CUDART_INF_F;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int key = k0 + h * 32 + c;
+            const float v = key <= lim ? __uint_as_float(sr[h][c]) * sl2 : -CUDART_INF_F;
+            sr[h][c] = __float_as_uint(v);
+            mx = fmaxf(mx, v);
+          }
+        const float mn = fmaxf(m, mx);
+        const float alpha = exp2f(m - mn);  // m = -inf on the first tile: alpha = 0
+        float rs = 0.f;
+        uint32_t pk[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float a = exp2f(__uint_as_float(sr[h][c]) - mn);
+            const float b = exp2f(__uint_as_float(sr[h][c + 1]) - mn);
+            rs += a + b;
+            pk[h * 16 + c / 2] = MmaOp<T>::pack(a, b);
+          }
+        l = l * alpha + rs;
+        m = mn;
+        // PV of the previous tile must be done before P and O are touched.
+        if (j > 0 && !mbar_wait(b_odone, (g - 1) & 1, p.status)) { bad = true; break; }
+        tc_fence_after();
+        const int s = g & 1;
+        if (k0 + kN > kv_len) {
+          // Keys past the sequence end carry p = 0, but their V slots may
+          // hold any bits (NaN included): zero those V rows.
+          if (!mbar_wait(b_kvfull0 + 8 * s, (g >> 1) & 1, p.status)) { bad = true; break; }
+          uint8_t* vst = smem + kOffKV + s * kStageBytes + kKBytes;
+          const int first = max(kv_len - k0, 0);
+          for (int idx = threadIdx.x - 64; idx < (kN - first) * 16; idx += 128) {
+            const int r = first + idx / 16, c = idx % 16;  // row, 16-byte chunk over both halves
+            *reinterpret_cast<int4*>(vst + (c >> 3) * kKVHalf + r * 128 + (c & 7) * 16) = make_int4(0, 0, 0, 0);
+          }
+        }
+        // P row (64 keys, 16-bit) into the 128-byte-swizzled K-major P tile.
+        uint8_t* prow = smem + kOffP + row * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        fence_async_shared();
+        // Rescale the O row when the running max moved (warp-uniform).
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t orow[32];
+            tmem_ld32(tmem + tl + kColO + cc * 32, orow);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) orow[c] = __float_as_uint(__uint_as_float(orow[c]) * alpha);
+            tmem_st32(tmem + tl + kColO + cc * 32, orow);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_pfull);
+      }
+      if (!bad && mbar_wait(b_odone, (tile_base + ntiles - 1) & 1, p.status)) {
+        tc_fence_after();
+        const float inv = 1.f / l;
+        T* orow = static_cast<T*>(p.out) + ((int64_t)(q0 + pos) * p.num_q_heads + kvh * G + head) * kD;
+        const bool valid = pos < ql;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + tl + kColO + cc * 32, ov);
+          tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+              store4(orow + cc * 32 + c,
+                     make_float4(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv,
+                                 __uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv));
+          }
+        }
+      } else {
+        bad = true;
+      }
+      if (bad) abort_flag[0] = 1;
+      tc_fence_before();
+    }
+    tile_base += ntiles;
+    __syncthreads();
+    if (abort_flag[0]) break;
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <typename T, int BS>
+static int launch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                 const PrefillParams& p, int ctas, cudaStream_t stream) {
+  auto kern = prefill_tc_kernel<T, BS>;
+  static bool attr_set[64] = {};  // one flag per device for this instantiation
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pf::kSmem) != cudaSuccess)
+      return PA_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  kern<<<ctas, pf::kThreads, pf::kSmem, stream>>>(qmap, kmap, vmap, p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int launch_prefill(const PrefillParams& p0, const void* k_cache, const void* v_cache, pa_dtype dt,
                    cudaStream_t stream) {
-  (void)p; (void)k_cache; (void)v_cache; (void)dt; (void)stream;
-  return PA_ERR_UNSUPPORTED;
+  PrefillParams p = p0;
+  if (p.head_dim != pf::kD) return PA_ERR_UNSUPPORTED;
+  if (p.group < 1 || p.group > pf::kM || (p.group & (p.group - 1))) return PA_ERR_UNSUPPORTED;
+  int gs = 0;
+  while ((1 << gs) < p.group) ++gs;
+  p.gshift = gs;
+  CUtensorMap qmap, kmap, vmap;
+  {
+    // q seen as [total_q][num_q_heads][head_dim]; box = 64 columns x G heads x 128/G positions.
+    int rc = make_3d_tensor_map(&qmap, p.q, p.total_q, p.num_q_heads, pf::kD, dt, pf::kM / p.group, p.group, 64);
+    if (rc != PA_OK) return rc;
+    const int64_t rows = (int64_t)p.num_blocks * p.num_kv_heads * p.block_size;
+    rc = make_kv_tensor_map(&kmap, k_cache, rows, pf::kD, dt, 16);
+    if (rc != PA_OK) return rc;
+    rc = make_kv_tensor_map(&vmap, v_cache, rows, pf::kD, dt, 16);
+    if (rc != PA_OK) return rc;
+  }
+  prefill_plan_kernel<<<1, 1024, 0, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  const int64_t upper = (int64_t)(p.total_q > 0 ? p.total_q : 1) * p.num_kv_heads;
+  const int64_t resident = 2LL * num_sms_current_device();
+  const int ctas = (int)(upper < resident ? upper : resident);
+  const bool bf = dt == PA_BF16;
+  if (p.block_size == 16)
+    return bf ? launch_prefill_kernel<__nv_bfloat16, 16>(qmap, kmap, vmap, p, ctas, stream)
+              : launch_prefill_kernel<__half, 16>(qmap, kmap, vmap, p, ctas, stream);
+  return bf ? launch_prefill_kernel<__nv_bfloat16, 32>(qmap, kmap, vmap, p, ctas, stream)
+            : launch_prefill_kernel<__half, 32>(qmap, kmap, vmap, p, ctas, stream);
 }
 
 }  // namespace pa

@@ -49,7 +49,7 @@ class PagedStep:
                                                self.max_seq_len, self.partition_size)
         else:
             need = pa.pa_chunked_prefill_workspace_size(n, hq, self.num_kv_heads, self.head_dim,
-                                                        self.block_size, self.max_seq_len)
+                                                        self.block_size, q.shape[0], self.max_seq_len)
             self.cu_q_lens = cu_q_lens
             self.ctx_lens = ctx_lens
         self.workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
@@ -66,7 +66,7 @@ class PagedStep:
                                            self.partition_size if self.is_decode else 0)
         n += 2 + (1 if -(-self.max_seq_len // part) > 1 else 0)  # plan, main, split-KV merge
         if not self.is_decode and self.max_q_len > 1:
-            n += 1  # prefill chunks
+            n += 2  # prefill plan, prefill chunks
         return n
 
     def run(self, stream=None) -> torch.Tensor:

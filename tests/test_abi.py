@@ -114,10 +114,18 @@ def test_cache_write_and_slot_host_checks(lib):
 
 def test_prefill_host_checks(lib):
     f = lib.pa_chunked_prefill
-    # fp32 chunks are not on the tensor-core path.
-    assert f(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 4, 0x6000, 2, 8, 64, 8, 2, 128, 16, 10, 0.1, 0x7000, None, 0,
-             pa.PA_F32, None) == -2
-    assert f(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 4, 0x6000, 0, 8, 64, 8, 2, 128, 16, 10, 0.1, 0x7000, None, 0,
-             pa.PA_F16, None) == 0
-    assert f(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 4, 0x6000, 2, 8, 64, 8, 2, 64, 16, 10, 0.1, 0x7000, None, 0,
-             pa.PA_F16, None) == -10
+
+    def call(**o):
+        a = dict(q=0x1000, tq=64, cu=0x2000, k=0x3000, v=0x4000, bt=0x5000, mb=4, ctx=0x6000, n=2, mq=8, mkv=64,
+                 hq=8, hkv=2, d=128, bs=16, nb=10, scale=0.1, out=0x7000, ws=None, wsb=0, dt=pa.PA_F16)
+        a.update(o)
+        return f(a["q"], a["tq"], a["cu"], a["k"], a["v"], a["bt"], a["mb"], a["ctx"], a["n"], a["mq"], a["mkv"],
+                 a["hq"], a["hkv"], a["d"], a["bs"], a["nb"], a["scale"], a["out"], a["ws"], a["wsb"], a["dt"], None)
+    assert call(dt=pa.PA_F32) == -2          # fp32 chunks are not on the tensor-core path
+    assert call(n=0) == 0                    # empty batch
+    assert call(tq=0) == 0
+    assert call(d=64) == -10                 # chunk kernel needs head_dim 128
+    assert call(hq=12, hkv=4) == -10         # group 3 is not a power of two
+    assert call(hq=6, hkv=4) == -3
+    assert call(mq=100, tq=64) == -1         # max_q_len above total_q
+    assert call() == -5                      # workspace required
