@@ -119,16 +119,16 @@ int make_kv_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t
 static int32_t auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seq_len) {
   // Work items are (sequence, partition, KV head group); the persistent
   // decode kernel (two CTAs per SM) pulls them from a counter. Use the
-  // longest partition, at most 2048 tokens, that still gives about four
-  // items per resident CTA, assuming an average length of half the maximum.
-  // Longer partitions mean fewer per-item epilogues and partials; more items
-  // mean a shorter tail.
+  // longest partition (at most 4096 tokens, and at most half the longest
+  // sequence so long sequences still split) that gives about four items per
+  // SM, assuming an average length of half the maximum. Longer partitions
+  // mean fewer per-item epilogues and partials; more items, a shorter tail.
   const int32_t group = num_q_heads / num_kv_heads;
   const int64_t hr = (int64_t)num_kv_heads * ((group + 15) / 16);
-  const int64_t target = 8LL * num_sms_current_device();
+  const int64_t target = 4LL * num_sms_current_device();
   const int64_t half = (max_seq_len + 1) / 2;
-  int32_t part = 2048;
-  while (part > 256 && (int64_t)num_seqs * hr * ((half + part - 1) / part) < target) part /= 2;
+  int32_t part = 4096;
+  while (part > 256 && (part > half || (int64_t)num_seqs * hr * ((half + part - 1) / part) < target)) part /= 2;
   return part;
 }
 

@@ -42,6 +42,16 @@
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
+// Bytes of the K/V stage ring of one decode CTA.
+#ifndef PA_DECODE_RING_BYTES
+#define PA_DECODE_RING_BYTES 65536
+#endif
+// Work order of the decode plan: 1 = first partitions sequence-major, then
+// the rest longest first; 0 = all partitions sequence-major.
+#ifndef PA_DECODE_PLAN_ORDER
+#define PA_DECODE_PLAN_ORDER 1
+#endif
+
 namespace pa {
 
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
@@ -102,11 +112,26 @@ __device__ __forceinline__ bool len_ok(const DecodeParams& p, int len) {
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p) {
+  // Work order: the first partition of every sequence in sequence order
+  // (the sequences of a prefix-sharing group are adjacent, so the CTAs that
+  // read a shared prefix run at the same time and hit in L2), then every
+  // other partition from the longest to the shortest, so the last items
+  // pulled from the counter are short and the tail is short.
+  constexpr int kBins = 1024;  // later partitions binned by length, 16 tokens per bin, longest first
   __shared__ int32_t scan[1024];
+  __shared__ int32_t hist[kBins];
   const int N = p.num_seqs;
+  const int P = p.partition;
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  auto bin_of = [&](int len, int part) {
+    if (!PA_DECODE_PLAN_ORDER) return 0;
+    const int plen = min(P, len - part * P);
+    return min((P - plen) >> 4, kBins - 1);
+  };
   const int per = (N + 1023) / 1024;
   const int s0 = min(N, (int)threadIdx.x * per), s1 = min(N, s0 + per);
-  int cnt = 0;
+  int cnt0 = 0;
   for (int s = s0; s < s1; ++s) {
     int qrow, len;
     if (!decode_row(p, s, qrow, len)) continue;
@@ -116,9 +141,11 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
       for (int i = 0; i < p.num_q_heads * p.head_dim; ++i) out[i] = T(0.0f);
       continue;
     }
-    cnt += (len + p.partition - 1) / p.partition;
+    ++cnt0;
+    const int n = (len + P - 1) / P;
+    for (int part = 1; part < n; ++part) atomicAdd(&hist[bin_of(len, part)], 1);
   }
-  scan[threadIdx.x] = cnt;
+  scan[threadIdx.x] = cnt0;
   __syncthreads();
   for (int off = 1; off < 1024; off <<= 1) {
     const int v = threadIdx.x >= off ? scan[threadIdx.x - off] : 0;
@@ -126,17 +153,30 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
     scan[threadIdx.x] += v;
     __syncthreads();
   }
-  int base = scan[threadIdx.x] - cnt;
+  const int total0 = scan[1023];
+  int base0 = scan[threadIdx.x] - cnt0;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = total0;
+    for (int b = 0; b < kBins; ++b) {
+      const int c = hist[b];
+      hist[b] = run;
+      run += c;
+    }
+    scan[0] = run;  // total number of (sequence, partition) pairs
+  }
+  __syncthreads();
+  const int total = scan[0];
   for (int s = s0; s < s1; ++s) {
     int qrow, len;
     if (!decode_row(p, s, qrow, len) || !len_ok(p, len)) continue;
-    const int n = (len + p.partition - 1) / p.partition;
-    for (int part = 0; part < n; ++part) p.pairs[base++] = (s << 16) | part;
+    p.pairs[base0++] = s << 16;
+    const int n = (len + P - 1) / P;
+    for (int part = 1; part < n; ++part) p.pairs[atomicAdd(&hist[bin_of(len, part)], 1)] = (s << 16) | part;
   }
-  const int hr = p.num_kv_heads * p.row_groups;
-  if (threadIdx.x == 1023) {
+  if (threadIdx.x == 0) {
     p.work[0] = 0;
-    p.work[1] = scan[1023] * hr;
+    p.work[1] = total * p.num_kv_heads * p.row_groups;
   }
 }
 
@@ -152,13 +192,13 @@ struct DecCfg {
   static constexpr int kHalves = D / 64;              // 128-byte swizzle boxes across head_dim
   static constexpr int kTile = 16 * D * 2;            // 16 tokens x head_dim of K (or V)
   static constexpr int kStage = 2 * kTile;            // K + V
-  static constexpr int kStages = 65536 / kStage;      // 64 KB ring
+  static constexpr int kStages = PA_DECODE_RING_BYTES / kStage;
   static constexpr int kHeads = NT * 8;               // query heads per item (MMA N)
   static constexpr int kConsumers = 4;
   static constexpr int kThreads = (kConsumers + 1) * 32;
   static constexpr int kSlots = 2;                    // item slots (metadata + query rows)
   static constexpr int kQBytes = kHeads * D * 2;
-  static constexpr int kDp = D + 4;                   // fp32 scratch row stride (bank spread)
+  static constexpr int kDp = D + 4;                   // fp32 scratch row stride (+4: bank spread)
   static constexpr size_t kRing = 0;
   static constexpr size_t kQ = kRing + (size_t)kStages * kStage;
   static constexpr size_t kScratch = kQ + (size_t)kSlots * kQBytes;

@@ -81,10 +81,12 @@ def test_partition_and_workspace_sizes(lib):
     assert 0 < small <= 4096  # one partition: no partials, only the work list
     with pytest.raises(pa.PagedAttnError):
         pa.pa_decode_partition_size(4, 8, 2, 16, 1000, 40)
-    # The automatic choice is a power of two in [256, 2048].
-    for n, L in [(1, 100), (256, 8192), (8, 131072)]:
+    # The automatic choice is a power of two in [256, 4096], at most half the
+    # longest sequence once that is above 512.
+    for n, L in [(1, 100), (256, 8192), (8, 131072), (64, 4096)]:
         p = pa.pa_decode_partition_size(n, 64, 8, 16, L, 0)
-        assert p in (256, 512, 1024, 2048)
+        assert p in (256, 512, 1024, 2048, 4096)
+        assert L <= 512 or p <= L // 2
 
 
 def test_copy_blocks_host_checks(lib):
