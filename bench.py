@@ -325,7 +325,9 @@ def native_arm(args) -> None:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     pa.load()
     batch = make_config(args.config)
-    st = step_from_host(batch, partition_size=args.partition)
+    shared = args.decode == "shared_prefix" or (
+        args.decode == "auto" and batch.is_decode and batch.prefix_lens is not None and bool(batch.prefix_lens.any()))
+    st = step_from_host(batch, partition_size=args.partition, shared_prefix=shared)
     dec_bytes = decode_algorithmic_bytes(batch)
     step_bytes = dec_bytes["total"] + step_extra_bytes(batch)
     stream = torch.cuda.current_stream()
@@ -356,12 +358,7 @@ def native_arm(args) -> None:
                                slot_mapping=st.slot_mapping)
             pa.pa_reshape_and_cache(st.k_new, st.v_new, st.slot_mapping, st.k_cache, st.v_cache)
             ev[i][0].record(stream)
-            if st.is_decode:
-                pa.pa_decode(st.q, st.k_cache, st.v_cache, st.block_tables, st.kv_lens, st.max_seq_len, st.scale,
-                             out=st.out, partition_size=st.partition_size, workspace=st.workspace)
-            else:
-                pa.pa_chunked_prefill(st.q, st.cu_q_lens, st.k_cache, st.v_cache, st.block_tables, st.ctx_lens,
-                                      st.max_q_len, st.max_seq_len, st.scale, out=st.out, workspace=st.workspace)
+            st.attend()
             ev[i][1].record(stream)
         stop.record(stream)
         barrier()
@@ -383,6 +380,11 @@ def native_arm(args) -> None:
     }
     dev_of = {"q": st.q, "k_new": st.k_new, "v_new": st.v_new, "block_tables": st.block_tables,
               "kv_lens": st.kv_lens, "new_seq_ids": st.new_seq_ids, "new_positions": st.new_positions}
+    if st.shared_prefix:
+        host["group_starts"] = torch.from_numpy(batch.group_starts).pin_memory()
+        host["prefix_lens"] = torch.from_numpy(batch.prefix_lens).pin_memory()
+        dev_of["group_starts"] = st.group_starts
+        dev_of["prefix_lens"] = st.prefix_lens
     if not st.is_decode:
         host["cu_q_lens"] = torch.from_numpy(batch.cu_q_lens).pin_memory()
         host["ctx_lens"] = torch.from_numpy(batch.ctx_lens).pin_memory()
@@ -444,13 +446,17 @@ def native_arm(args) -> None:
                 "cow_pairs": int(len(batch.cow_pairs)), "partition": pa.pa_decode_partition_size(
                     batch.num_seqs, batch.num_q_heads, batch.num_kv_heads, batch.block_size, batch.max_seq_len,
                     args.partition),
-                "step": "copy_blocks + slot_mapping + reshape_and_cache + decode (+ split-KV merge)",
+                "step": "copy_blocks + slot_mapping + reshape_and_cache + " + (
+                    "pa_decode_shared_prefix" if st.shared_prefix else
+                    "pa_decode" if st.is_decode else "pa_chunked_prefill"),
                 "step_bytes": step_bytes, "decode_bytes": dec_bytes,
                 "l2": "inputs larger than L2 (KV pools %.2f GB vs 129 MB L2); no flush" % (
                     2 * batch.k_cache.numel() * batch.k_cache.element_size() / 1e9),
                 "parallelism": f"replicas x{world}",
             },
-            "roofline": ({"kernel": "paged decode (main + split-KV merge)", "bound": "hbm",
+            "roofline": ({"kernel": ("paged decode, shared-prefix (prefix check + tcgen05 prefix pass + split-KV "
+                                     "suffix decode + merge)" if st.shared_prefix else
+                                     "paged decode (plan + main + split-KV merge)"), "bound": "hbm",
                           "achieved": round(dec_gbs, 2), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                           "frac": round(dec_gbs / peak, 4), "traffic": profiled_traffic(),
                           "algorithmic_bytes": dec_bytes["total"], "ms_per_launch": round(dec_mean, 5)}
@@ -479,6 +485,8 @@ def main():
     ap.add_argument("--impl", choices=("native", "reference"), default="native")
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--partition", type=int, default=0)
+    ap.add_argument("--decode", choices=("auto", "plain", "shared_prefix"), default="auto",
+                    help="auto: shared-prefix decode when the workload's sequences share prefix blocks")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

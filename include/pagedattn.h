@@ -196,6 +196,44 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
               size_t workspace_bytes, pa_dtype dtype, void* stream);
 
 /*
+ * pa_decode_shared_prefix — pa_decode for batches in which groups of
+ * consecutive sequences share leading KV blocks through their block tables
+ * (prefix caching or parallel sampling: several tables name the same
+ * refcounted physical blocks, "High-Throughput Local LLM Infrastructure...",
+ * section 1.2 "Reference Counting & Copy-on-Write"; "Inside vLLM...",
+ * section "Zero-Copy Branching and Parallel Sampling"). The result is the
+ * same attention as pa_decode; what changes is the work: each group's shared
+ * blocks are read once per KV head for all its members, in one tcgen05
+ * tensor-core pass whose rows are (member, query head), and each member's
+ * private suffix goes through the split-KV decode kernel; the two are merged
+ * with log-sum-exp weights.
+ *   group_starts : int32 [num_groups+1] device; group g is the sequences
+ *                  group_starts[g] .. group_starts[g+1]-1 (consecutive;
+ *                  group_starts[0] = 0, group_starts[num_groups] = num_seqs)
+ *   prefix_lens  : int32 [num_seqs] device; a hint: sequence i shares its
+ *                  first prefix_lens[i] tokens with its group. A hint is used
+ *                  only if it is a positive multiple of block_size, shorter
+ *                  than seq_lens[i], and the first prefix_lens[i]/block_size
+ *                  table entries of sequence i equal those of the group member
+ *                  with the longest hint; otherwise it is ignored for that
+ *                  sequence (same result, no saving). Malformed group_starts
+ *                  record PA_ERR_ARG and disable every hint.
+ *   workspace    : pa_decode_shared_prefix_workspace_size() bytes.
+ * Other arguments as pa_decode. fp16/bf16, head_dim 128, GQA group a power
+ * of two up to 128 (up to 128/group members per tensor-core tile; larger
+ * groups take several tiles).
+ */
+size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                              int32_t head_dim, int32_t block_size, int32_t max_seq_len,
+                                              int32_t partition_size, int32_t num_groups);
+int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                            int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                            int32_t max_seq_len, const int32_t* group_starts, const int32_t* prefix_lens,
+                            int32_t num_groups, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t num_blocks, float scale, void* out, int32_t partition_size,
+                            void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream);
+
+/*
  * pa_decode_noalloc — pa_decode for callers that cannot allocate device
  * memory when they call (for example a plugin running inside another
  * runtime's fixed memory pool, a serving loop that forbids cudaMalloc after

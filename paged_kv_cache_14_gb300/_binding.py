@@ -25,8 +25,8 @@ _DT = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
 EXPORTS = (
     "pa_strerror", "pa_version", "pa_get_status", "pa_slot_mapping", "pa_reshape_and_cache",
     "pa_copy_blocks", "pa_decode_partition_size", "pa_decode_workspace_size", "pa_decode",
-    "pa_chunked_prefill_workspace_size", "pa_chunked_prefill", "pa_decode_noalloc_scratch_limit",
-    "pa_decode_noalloc",
+    "pa_chunked_prefill_workspace_size", "pa_chunked_prefill", "pa_decode_shared_prefix_workspace_size",
+    "pa_decode_shared_prefix", "pa_decode_noalloc_scratch_limit", "pa_decode_noalloc",
 )
 
 _i32, _i64, _f32, _vp, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
@@ -63,6 +63,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "pa_chunked_prefill_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
         "pa_chunked_prefill": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                               _i32, _i32, _i32, _i32, _f32, _vp, _vp, _sz, ctypes.c_int, _vp]),
+        "pa_decode_shared_prefix_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]),
+        "pa_decode_shared_prefix": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _vp, _vp, _i32, _i32,
+                                                   _i32, _i32, _i32, _i32, _f32, _vp, _i32, _vp, _sz, ctypes.c_int,
+                                                   _vp]),
         "pa_decode_noalloc_scratch_limit": (_sz, []),
         "pa_decode_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                              _i32, _f32, _vp, _i32, ctypes.c_int, _vp]),
@@ -218,6 +222,40 @@ def pa_chunked_prefill(q: torch.Tensor, cu_q_lens: torch.Tensor, k_cache: torch.
         _cuda(ctx_lens, "ctx_lens", torch.int32), n, int(max_q_len), int(max_kv_len), hq, hkv, D, B, P,
         float(scale), _cuda(out, "out", dt), ws_ptr, ws_bytes, _DT[dt], _stream(stream))
     _check(rc, "pa_chunked_prefill")
+    return out
+
+
+def pa_decode_shared_prefix_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                                           block_size: int, max_seq_len: int, partition_size: int,
+                                           num_groups: int) -> int:
+    return int(load().pa_decode_shared_prefix_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                             block_size, max_seq_len, partition_size, num_groups))
+
+
+def pa_decode_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                            group_starts: torch.Tensor, prefix_lens: torch.Tensor, scale: float,
+                            out: torch.Tensor | None = None, partition_size: int = 0,
+                            workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    N, hq, D = q.shape
+    P, hkv, B, _ = k_cache.shape
+    G = group_starts.shape[0] - 1
+    dt = q.dtype
+    if out is None:
+        out = torch.empty_like(q)
+    need = pa_decode_shared_prefix_workspace_size(N, hq, hkv, D, B, max_seq_len, partition_size, G)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load().pa_decode_shared_prefix(
+        _cuda(q, "q", dt), _cuda(k_cache, "k_cache", dt), _cuda(v_cache, "v_cache", dt),
+        _cuda(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _cuda(seq_lens, "seq_lens", torch.int32), N, int(max_seq_len),
+        _cuda(group_starts, "group_starts", torch.int32), _cuda(prefix_lens, "prefix_lens", torch.int32), G,
+        hq, hkv, D, B, P, float(scale), _cuda(out, "out", dt), int(partition_size), ws_ptr, ws_bytes, _DT[dt],
+        _stream(stream))
+    _check(rc, "pa_decode_shared_prefix")
     return out
 
 

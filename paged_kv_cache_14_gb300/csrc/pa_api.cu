@@ -247,12 +247,15 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t n
   return decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_parts).total;
 }
 
-static int decode_common(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
-                         int32_t max_blocks_per_seq, const int32_t* lens, const int32_t* cu_q_lens,
-                         int32_t num_seqs, int32_t max_len, int32_t num_q_heads, int32_t num_kv_heads,
-                         int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale, void* out,
-                         int32_t partition_size, void* workspace, size_t workspace_bytes, pa_dtype dtype,
-                         cudaStream_t stream) {
+// Checks and parameter block of a decode launch. extra_slots = 1 reserves a
+// partial slot per (sequence, head) for the prefix pass of shared-prefix
+// decode. On success *wl is the decode workspace layout.
+static int decode_prepare(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                          int32_t max_blocks_per_seq, const int32_t* lens, const int32_t* cu_q_lens,
+                          int32_t num_seqs, int32_t max_len, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale, void* out,
+                          int32_t partition_size, int32_t extra_slots, void* workspace, size_t workspace_bytes,
+                          pa_dtype dtype, DecodeParams* dp, DecodeWorkspace* wl) {
   if (num_seqs < 0 || max_blocks_per_seq < 1 || num_blocks < 1 || head_dim < 1) return PA_ERR_ARG;
   if (num_q_heads < 1 || num_kv_heads < 1) return PA_ERR_ARG;
   if (num_q_heads % num_kv_heads) return PA_ERR_HEADS;
@@ -269,10 +272,10 @@ static int decode_common(const void* q, const void* k_cache, const void* v_cache
   const int32_t part =
       pa_decode_partition_size(num_seqs, num_q_heads, num_kv_heads, block_size, max_len, partition_size);
   if (part < 0) return part;
-  const int64_t max_parts = (max_len + part - 1) / part;
+  const int64_t max_parts = (max_len + part - 1) / part + extra_slots;
   if (max_parts > 12288) return PA_ERR_ARG;
-  const DecodeWorkspace wl = decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_parts);
-  if (!workspace || workspace_bytes < wl.total) return PA_ERR_WORKSPACE;
+  *wl = decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_parts);
+  if (!workspace || workspace_bytes < wl->total) return PA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return PA_ERR_ALIGN;
   int* st = device_status_ptr();
   if (!st) return PA_ERR_CUDA;
@@ -298,11 +301,29 @@ static int decode_common(const void* q, const void* k_cache, const void* v_cache
   p.len_cap = max_len;
   p.scale_log2 = scale * 1.4426950408889634f;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.work = reinterpret_cast<int32_t*>(ws + wl.work);
-  p.pairs = reinterpret_cast<int32_t*>(ws + wl.pairs);
-  p.part_o = max_parts > 1 ? reinterpret_cast<float*>(ws + wl.part_o) : nullptr;
-  p.part_ml = max_parts > 1 ? reinterpret_cast<float*>(ws + wl.part_ml) : nullptr;
+  p.work = reinterpret_cast<int32_t*>(ws + wl->work);
+  p.pairs = reinterpret_cast<int32_t*>(ws + wl->pairs);
+  p.part_o = max_parts > 1 ? reinterpret_cast<float*>(ws + wl->part_o) : nullptr;
+  p.part_ml = max_parts > 1 ? reinterpret_cast<float*>(ws + wl->part_ml) : nullptr;
+  p.prefix = nullptr;
+  p.slot0 = extra_slots;
   p.status = st;
+  *dp = p;
+  return PA_OK;
+}
+
+static int decode_common(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* lens, const int32_t* cu_q_lens,
+                         int32_t num_seqs, int32_t max_len, int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale, void* out,
+                         int32_t partition_size, void* workspace, size_t workspace_bytes, pa_dtype dtype,
+                         cudaStream_t stream) {
+  DecodeParams p;
+  DecodeWorkspace wl;
+  const int rc = decode_prepare(q, k_cache, v_cache, block_tables, max_blocks_per_seq, lens, cu_q_lens, num_seqs,
+                                max_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out,
+                                partition_size, 0, workspace, workspace_bytes, dtype, &p, &wl);
+  if (rc != PA_OK || num_seqs == 0) return rc;
   return launch_decode(p, dtype, stream);
 }
 
@@ -314,6 +335,86 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
   return decode_common(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
                        max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out,
                        partition_size, workspace, workspace_bytes, dtype, static_cast<cudaStream_t>(stream));
+}
+
+size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                              int32_t head_dim, int32_t block_size, int32_t max_seq_len,
+                                              int32_t partition_size, int32_t num_groups) {
+  const int32_t part =
+      pa_decode_partition_size(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, partition_size);
+  if (part <= 0 || head_dim < 1 || num_seqs < 1 || num_groups < 1) return 0;
+  const int64_t max_parts = ((max_seq_len < 1 ? 1 : max_seq_len) + part - 1) / part + 1;
+  return decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_parts).total +
+         cascade_workspace_layout(num_seqs, num_groups).total;
+}
+
+int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                            int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                            int32_t max_seq_len, const int32_t* group_starts, const int32_t* prefix_lens,
+                            int32_t num_groups, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t num_blocks, float scale, void* out, int32_t partition_size,
+                            void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
+  if (num_seqs < 0 || num_groups < 0) return PA_ERR_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (num_groups < 1 || num_groups > num_seqs || !group_starts || !prefix_lens) return PA_ERR_ARG;
+  if (dtype == PA_F32) return PA_ERR_DTYPE;
+  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads) return PA_ERR_HEADS;
+  const int32_t g = num_q_heads / num_kv_heads;
+  if (g > 128 || (g & (g - 1))) return PA_ERR_UNSUPPORTED;
+  const size_t need = pa_decode_shared_prefix_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                            block_size, max_seq_len, partition_size, num_groups);
+  if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+  DecodeParams dp;
+  DecodeWorkspace wl;
+  int rc = decode_prepare(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
+                          max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out,
+                          partition_size, 1, workspace, workspace_bytes, dtype, &dp, &wl);
+  if (rc != PA_OK) return rc;
+  const CascadeWorkspace cw = cascade_workspace_layout(num_seqs, num_groups);
+  uint8_t* cbase = static_cast<uint8_t*>(workspace) + wl.total;
+  int32_t* prefix = reinterpret_cast<int32_t*>(cbase + cw.prefix);
+  int32_t* group_ref = reinterpret_cast<int32_t*>(cbase + cw.group_ref);
+  int32_t* group_of_seq = reinterpret_cast<int32_t*>(cbase + cw.group_of);
+  int32_t* pwork = reinterpret_cast<int32_t*>(cbase + cw.work);
+  int32_t* ppairs = reinterpret_cast<int32_t*>(cbase + cw.pairs);
+  int32_t* pkeys = reinterpret_cast<int32_t*>(cbase + cw.pair_keys);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  dp.prefix = prefix;
+  // 1. Verify the hints and list the prefix pass's work.
+  rc = launch_cascade_prep(dp, group_starts, prefix_lens, num_groups, 128 / g, prefix, group_ref, group_of_seq,
+                           pwork, ppairs, pkeys, s);
+  if (rc != PA_OK) return rc;
+  // 2. Prefix pass (tcgen05): every group's shared blocks once for all its
+  //    members, partials into slot 0.
+  PrefillParams pp{};
+  pp.q = q;
+  pp.out = out;
+  pp.block_tables = block_tables;
+  pp.max_blocks_per_seq = max_blocks_per_seq;
+  pp.num_seqs = num_seqs;
+  pp.num_q_heads = num_q_heads;
+  pp.num_kv_heads = num_kv_heads;
+  pp.head_dim = head_dim;
+  pp.block_size = block_size;
+  pp.num_blocks = num_blocks;
+  pp.group = g;
+  pp.total_q = num_seqs;
+  pp.scale_log2 = dp.scale_log2;
+  pp.work = pwork;
+  pp.pairs = ppairs;
+  pp.group_starts = group_starts;
+  pp.prefix = prefix;
+  pp.group_ref = group_ref;
+  pp.pair_keys = pkeys;
+  pp.part_o = dp.part_o;
+  pp.part_ml = dp.part_ml;
+  pp.max_parts = dp.max_parts;
+  pp.status = dp.status;
+  rc = launch_prefix_pass(pp, k_cache, v_cache, dtype, s);
+  if (rc != PA_OK) return rc;
+  // 3. Suffix decode (split-KV over the private keys) and the merge.
+  return launch_decode(dp, dtype, s);
 }
 
 size_t pa_chunked_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,

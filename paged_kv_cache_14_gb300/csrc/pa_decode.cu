@@ -142,8 +142,9 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
       continue;
     }
     ++cnt0;
-    const int n = (len + P - 1) / P;
-    for (int part = 1; part < n; ++part) atomicAdd(&hist[bin_of(len, part)], 1);
+    const int sl = len - (p.prefix ? p.prefix[s] : 0);  // keys left to the suffix pass
+    const int n = (sl + P - 1) / P;
+    for (int part = 1; part < n; ++part) atomicAdd(&hist[bin_of(sl, part)], 1);
   }
   scan[threadIdx.x] = cnt0;
   __syncthreads();
@@ -171,8 +172,9 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
     int qrow, len;
     if (!decode_row(p, s, qrow, len) || !len_ok(p, len)) continue;
     p.pairs[base0++] = s << 16;
-    const int n = (len + P - 1) / P;
-    for (int part = 1; part < n; ++part) p.pairs[atomicAdd(&hist[bin_of(len, part)], 1)] = (s << 16) | part;
+    const int sl = len - (p.prefix ? p.prefix[s] : 0);
+    const int n = (sl + P - 1) / P;
+    for (int part = 1; part < n; ++part) p.pairs[atomicAdd(&hist[bin_of(sl, part)], 1)] = (s << 16) | part;
   }
   if (threadIdx.x == 0) {
     p.work[0] = 0;
@@ -263,10 +265,11 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
     next = __shfl_sync(0xffffffffu, next, 0);
     // The (sequence, partition) pair and length of the next item are loaded
     // one item ahead, so the item switch costs no dependent global loads.
-    int next_pr = 0, next_qrow = 0, next_len = 0;
+    int next_pr = 0, next_qrow = 0, next_len = 0, next_pfx = 0;
     if (next < total) {
       next_pr = p.pairs[next / hr];
       decode_row(p, next_pr >> 16, next_qrow, next_len);
+      next_pfx = p.prefix ? p.prefix[next_pr >> 16] : 0;
     }
     int jg = 0;  // 16-token sub-tiles issued so far (global stage sequence)
     bool bad = false;
@@ -286,12 +289,12 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
         }
         break;
       }
-      const int pr = next_pr, qrow = next_qrow, len = next_len;
+      const int pr = next_pr, qrow = next_qrow, len = next_len, pfx = next_pfx;
       if (lane == 0) next = atomicAdd(&p.work[0], 1);  // fetch the following item
       const int hg = item - (item / hr) * hr;
       const int seq = pr >> 16, part = pr & 0xffff;
       const int kvh = hg / p.row_groups, rgi = hg - kvh * p.row_groups;
-      const int t_begin = part * p.partition;
+      const int t_begin = pfx + part * p.partition;  // the suffix starts after the shared prefix
       const int t_end = min(t_begin + p.partition, len);
       const int nsub = (t_end - t_begin + 15) / 16;
       // Items are padded to a multiple of 4 sub-tiles with empty stages, so
@@ -311,8 +314,10 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
         m.t_end = t_end;
         m.nsub = nsub_pad;
         m.jstart = jg;
-        m.part = part;
-        m.n_parts = (len + p.partition - 1) / p.partition;
+        m.part = p.slot0 + part;
+        // Partials of this (sequence, head): the suffix partitions, plus the
+        // prefix pass's when there is a shared prefix.
+        m.n_parts = (len - pfx + p.partition - 1) / p.partition + (pfx > 0 ? 1 : 0);
         m.hg = seq * hr + hg;
         const uint32_t fb = smem_u32(&ifull[slot]);
         mbar_arrive_expect_tx(fb, nrows * D * 2);
@@ -365,6 +370,7 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
           if (next < total) {
             next_pr = p.pairs[next / hr];
             decode_row(p, next_pr >> 16, next_qrow, next_len);
+            next_pfx = p.prefix ? p.prefix[next_pr >> 16] : 0;
           }
         }
       }
@@ -750,9 +756,12 @@ __global__ void __launch_bounds__(128) splitkv_merge_kernel(const DecodeParams p
   const int seq = blockIdx.y;
   int qrow, len;
   if (!decode_row(p, seq, qrow, len) || !len_ok(p, len)) return;
-  const int n = (len + p.partition - 1) / p.partition;
-  if (n <= 1) return;
-  const int64_t base = ((int64_t)seq * p.num_q_heads + h) * p.max_parts;
+  const int pfx = p.prefix ? p.prefix[seq] : 0;
+  const int ns = (len - pfx + p.partition - 1) / p.partition;  // suffix partitions
+  if (pfx == 0 && ns <= 1) return;                              // written directly
+  const int first = pfx > 0 ? 0 : p.slot0;                      // slot 0 holds the prefix pass
+  const int n = p.slot0 + ns - first;
+  const int64_t base = ((int64_t)seq * p.num_q_heads + h) * p.max_parts + first;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float M = -CUDART_INF_F;
   for (int i = threadIdx.x; i < n; i += blockDim.x) M = fmaxf(M, __ldcg(p.part_ml + (base + i) * 2));

@@ -42,6 +42,11 @@ struct DecodeParams {
   float* part_ml;        // [num_seqs][num_q_heads][max_parts][2] (m, l)
   int32_t* work;         // [0] next work item, [1] number of work items (written by the plan kernel)
   int32_t* pairs;        // [num_seqs * max_parts] (seq << 16 | partition), in work order
+  // Shared-prefix (cascade) decode: tokens [0, prefix[i]) of sequence i were
+  // attended by the prefix pass, whose partial sits in slot 0; the suffix
+  // partitions use slots 1.. . nullptr / 0 for plain decode.
+  const int32_t* prefix;
+  int32_t slot0;
   int* status;
 };
 
@@ -84,9 +89,38 @@ struct PrefillParams {
   int32_t gshift;    // log2(group)
   float scale_log2;
   int32_t* work;     // [0] next work item, [1] number of work items
-  int32_t* pairs;    // (seq << 16 | row tile), longest first
+  int32_t* pairs;    // (seq << 16 | row tile), longest first; prefix pass: (group << 16 | member tile)
+  // Prefix pass of shared-prefix decode (null for chunked prefill): rows are
+  // (group member, GQA head); keys are the group's shared blocks, read
+  // through the table of the member with the longest verified prefix; the
+  // result is a partial (m, l, o~) in slot 0 of every member.
+  const int32_t* group_starts;  // [num_groups + 1]
+  const int32_t* prefix;        // [num_seqs] verified shared-prefix lengths
+  const int32_t* group_ref;     // [num_groups] member whose table covers the group prefix
+  const int32_t* pair_keys;     // [pairs] keys of the pair's tile (max prefix of its members)
+  float* part_o;
+  float* part_ml;
+  int32_t max_parts;
   int* status;
 };
+
+// Workspace of shared-prefix decode, after the decode workspace (which is
+// laid out with max_parts + 1 partial slots).
+struct CascadeWorkspace {
+  size_t prefix, group_of, group_ref, work, pairs, pair_keys, total;
+};
+inline CascadeWorkspace cascade_workspace_layout(int64_t num_seqs, int64_t num_groups) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  CascadeWorkspace w{};
+  w.prefix = 0;
+  w.group_of = up(w.prefix + (size_t)num_seqs * 4);
+  w.group_ref = up(w.group_of + (size_t)num_seqs * 4);
+  w.work = up(w.group_ref + (size_t)num_groups * 4);
+  w.pairs = up(w.work + 16);
+  w.pair_keys = up(w.pairs + (size_t)num_seqs * 4);
+  w.total = up(w.pair_keys + (size_t)num_seqs * 4);
+  return w;
+}
 
 // Returns the device status word of the current device (nullptr on error).
 int* device_status_ptr();
@@ -117,5 +151,13 @@ int launch_decode(const DecodeParams& p, pa_dtype dt, cudaStream_t stream);
 // Prefill chunks (q_len > 1) on the tensor-core path.
 int launch_prefill(const PrefillParams& p, const void* k_cache, const void* v_cache, pa_dtype dt,
                    cudaStream_t stream);
+// Prefix pass of shared-prefix decode on the same tensor-core kernel.
+int launch_prefix_pass(const PrefillParams& p, const void* k_cache, const void* v_cache, pa_dtype dt,
+                       cudaStream_t stream);
+// Shared-prefix verification and the prefix pass's work list (one CTA).
+int launch_cascade_prep(const DecodeParams& dp, const int32_t* group_starts, const int32_t* prefix_in,
+                        int32_t num_groups, int32_t members_per_tile, int32_t* prefix_out, int32_t* group_ref,
+                        int32_t* group_of_seq, int32_t* work, int32_t* pairs, int32_t* pair_keys,
+                        cudaStream_t stream);
 
 }  // namespace pa

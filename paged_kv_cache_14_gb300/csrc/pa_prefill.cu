@@ -122,7 +122,11 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
   }
 }
 
-template <typename T, int BS>
+// PREFIX = false: chunked prefill (causal rows, normalised output).
+// PREFIX = true: prefix pass of shared-prefix decode (rows = group members x
+// GQA heads, each row masked to its own verified prefix, fp32 partial
+// (m, l, o~) written to slot 0 of the member's partials).
+template <typename T, int BS, bool PREFIX>
 __global__ void __launch_bounds__(pf::kThreads, 2)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
@@ -176,16 +180,32 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
     __syncthreads();
     const int item = (int)misc[1];
     if (item >= total) break;
-    const int pr = p.pairs[item / p.num_kv_heads];
-    const int kvh = item - (item / p.num_kv_heads) * p.num_kv_heads;
-    const int seq = pr >> 16, mt = pr & 0xffff;
-    const int q0 = p.cu_q_lens[seq];
-    const int ql = p.cu_q_lens[seq + 1] - q0;
-    const int ctx = p.ctx_lens[seq];
-    const int kv_len = ctx + ql;
+    const int pi = item / p.num_kv_heads;
+    const int pr = p.pairs[pi];
+    const int kvh = item - pi * p.num_kv_heads;
+    const int mt = pr & 0xffff;
+    // Tile geometry. Chunk: rows are query positions pos_lo.. of sequence
+    // `seq`; prefix pass: rows are members m_lo.. of group `grp`, keys are
+    // the group's shared prefix read through the reference member's table.
+    int seq, q_z, q0 = 0, ql = 0, ctx = 0, kv_len, keys, grp = 0, s0 = 0, m_hi = 0;
     const int pos_lo = mt * pp;
-    const int pos_hi = min(pos_lo + pp, ql);
-    const int keys = ctx + pos_hi;  // keys the tile's last row needs
+    if constexpr (!PREFIX) {
+      seq = pr >> 16;
+      q0 = p.cu_q_lens[seq];
+      ql = p.cu_q_lens[seq + 1] - q0;
+      ctx = p.ctx_lens[seq];
+      kv_len = ctx + ql;
+      keys = ctx + min(pos_lo + pp, ql);  // keys the tile's last row needs
+      q_z = q0 + pos_lo;
+    } else {
+      grp = pr >> 16;
+      s0 = p.group_starts[grp];
+      m_hi = min(pos_lo + pp, p.group_starts[grp + 1] - s0);
+      seq = p.group_ref[grp];
+      keys = p.pair_keys[pi];
+      kv_len = keys;
+      q_z = s0 + pos_lo;
+    }
     const int ntiles = (keys + kN - 1) / kN;
     const int nblk_seq = (kv_len + BS - 1) / BS;
 
@@ -194,8 +214,8 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
       bool bad = false;
       if (lane == 0) {
         mbar_arrive_expect_tx(b_q, kQBytes);
-        tma_load_3d(sbase + kOffQ, &qmap, 0, kvh * G, q0 + pos_lo, b_q);
-        tma_load_3d(sbase + kOffQ + kQHalf, &qmap, 64, kvh * G, q0 + pos_lo, b_q);
+        tma_load_3d(sbase + kOffQ, &qmap, 0, kvh * G, q_z, b_q);
+        tma_load_3d(sbase + kOffQ + kQHalf, &qmap, 64, kvh * G, q_z, b_q);
       }
       const int32_t* bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
       for (int j = 0; j < ntiles; ++j) {
@@ -292,9 +312,14 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
       const int q = warp & 3;             // tensor-memory lane quarter of this warp
       const int row = q * 32 + lane;      // packed row owned by this thread
       const uint32_t tl = (uint32_t)(q * 32) << 16;
-      const int pos = pos_lo + (row >> p.gshift);
+      const int pos = pos_lo + (row >> p.gshift);  // query position (chunk) or group member (prefix)
       const int head = row & (G - 1);
-      const int lim = min(ctx + pos, kv_len - 1);  // last key this row may see
+      int lim;  // last key this row may see (-1: none)
+      if constexpr (!PREFIX) {
+        lim = min(ctx + pos, kv_len - 1);
+      } else {
+        lim = pos < m_hi ? p.prefix[s0 + pos] - 1 : -1;
+      }
       const float sl2 = p.scale_log2;
       float m = -CUDART_INF_F, l = 0.f;
       bool bad = false;
@@ -321,15 +346,17 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
             mx = fmaxf(mx, v);
           }
         const float mn = fmaxf(m, mx);
-        const float alpha = exp2f(m - mn);  // m = -inf on the first tile: alpha = 0
+        const bool dead = mn == -CUDART_INF_F;  // no key seen yet (a row without keys)
+        const float alpha = dead ? 1.f : exp2f(m - mn);  // m = -inf on the first tile: alpha = 0
+        const float msub = dead ? 0.f : mn;
         float rs = 0.f;
         uint32_t pk[32];
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            const float a = exp2f(__uint_as_float(sr[h][c]) - mn);
-            const float b = exp2f(__uint_as_float(sr[h][c + 1]) - mn);
+            const float a = exp2f(__uint_as_float(sr[h][c]) - msub);
+            const float b = exp2f(__uint_as_float(sr[h][c + 1]) - msub);
             rs += a + b;
             pk[h * 16 + c / 2] = MmaOp<T>::pack(a, b);
           }
@@ -376,21 +403,42 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
       }
       if (!bad && mbar_wait(b_odone, (tile_base + ntiles - 1) & 1, p.status)) {
         tc_fence_after();
-        const float inv = 1.f / l;
-        T* orow = static_cast<T*>(p.out) + ((int64_t)(q0 + pos) * p.num_q_heads + kvh * G + head) * kD;
-        const bool valid = pos < ql;
+        if constexpr (!PREFIX) {
+          const float inv = 1.f / l;
+          T* orow = static_cast<T*>(p.out) + ((int64_t)(q0 + pos) * p.num_q_heads + kvh * G + head) * kD;
+          const bool valid = pos < ql;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t ov[32];
-          tmem_ld32(tmem + tl + kColO + cc * 32, ov);
-          tmem_ld_wait();
-          if (valid) {
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t ov[32];
+            tmem_ld32(tmem + tl + kColO + cc * 32, ov);
+            tmem_ld_wait();
+            if (valid) {
 #pragma unroll
-            for (int c = 0; c < 32; c += 4)
-              store4(orow + cc * 32 + c,
-                     make_float4(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv,
-                                 __uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv));
+              for (int c = 0; c < 32; c += 4)
+                store4(orow + cc * 32 + c,
+                       make_float4(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv,
+                                   __uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv));
+            }
           }
+        } else {
+          // Partial of the prefix: running max m (log2 units), l = sum 2^(s - m)
+          // and o~ = sum 2^(s - m) v, into slot 0 of the member's partials.
+          const bool valid = lim >= 0;
+          const int64_t base = ((int64_t)(s0 + pos) * p.num_q_heads + kvh * G + head) * p.max_parts;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t ov[32];
+            tmem_ld32(tmem + tl + kColO + cc * 32, ov);
+            tmem_ld_wait();
+            if (valid) {
+#pragma unroll
+              for (int c = 0; c < 32; c += 4)
+                __stcg(reinterpret_cast<float4*>(p.part_o + base * kD + cc * 32 + c),
+                       make_float4(__uint_as_float(ov[c]), __uint_as_float(ov[c + 1]), __uint_as_float(ov[c + 2]),
+                                   __uint_as_float(ov[c + 3])));
+            }
+          }
+          if (valid) __stcg(reinterpret_cast<float2*>(p.part_ml + base * 2), make_float2(m, l));
         }
       } else {
         bad = true;
@@ -407,10 +455,10 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <typename T, int BS>
+template <typename T, int BS, bool PREFIX>
 static int launch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                  const PrefillParams& p, int ctas, cudaStream_t stream) {
-  auto kern = prefill_tc_kernel<T, BS>;
+  auto kern = prefill_tc_kernel<T, BS, PREFIX>;
   static bool attr_set[64] = {};  // one flag per device for this instantiation
   int dev = 0;
   cudaGetDevice(&dev);
@@ -421,6 +469,17 @@ static int launch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& kma
   }
   kern<<<ctas, pf::kThreads, pf::kSmem, stream>>>(qmap, kmap, vmap, p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+template <bool PREFIX>
+static int dispatch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                   const PrefillParams& p, int ctas, pa_dtype dt, cudaStream_t stream) {
+  const bool bf = dt == PA_BF16;
+  if (p.block_size == 16)
+    return bf ? launch_prefill_kernel<__nv_bfloat16, 16, PREFIX>(qmap, kmap, vmap, p, ctas, stream)
+              : launch_prefill_kernel<__half, 16, PREFIX>(qmap, kmap, vmap, p, ctas, stream);
+  return bf ? launch_prefill_kernel<__nv_bfloat16, 32, PREFIX>(qmap, kmap, vmap, p, ctas, stream)
+            : launch_prefill_kernel<__half, 32, PREFIX>(qmap, kmap, vmap, p, ctas, stream);
 }
 
 int launch_prefill(const PrefillParams& p0, const void* k_cache, const void* v_cache, pa_dtype dt,
@@ -447,12 +506,31 @@ int launch_prefill(const PrefillParams& p0, const void* k_cache, const void* v_c
   const int64_t upper = (int64_t)(p.total_q > 0 ? p.total_q : 1) * p.num_kv_heads;
   const int64_t resident = 2LL * num_sms_current_device();
   const int ctas = (int)(upper < resident ? upper : resident);
-  const bool bf = dt == PA_BF16;
-  if (p.block_size == 16)
-    return bf ? launch_prefill_kernel<__nv_bfloat16, 16>(qmap, kmap, vmap, p, ctas, stream)
-              : launch_prefill_kernel<__half, 16>(qmap, kmap, vmap, p, ctas, stream);
-  return bf ? launch_prefill_kernel<__nv_bfloat16, 32>(qmap, kmap, vmap, p, ctas, stream)
-            : launch_prefill_kernel<__half, 32>(qmap, kmap, vmap, p, ctas, stream);
+  return dispatch_prefill_kernel<false>(qmap, kmap, vmap, p, ctas, dt, stream);
+}
+
+int launch_prefix_pass(const PrefillParams& p0, const void* k_cache, const void* v_cache, pa_dtype dt,
+                       cudaStream_t stream) {
+  PrefillParams p = p0;
+  if (p.head_dim != pf::kD) return PA_ERR_UNSUPPORTED;
+  if (p.group < 1 || p.group > pf::kM || (p.group & (p.group - 1))) return PA_ERR_UNSUPPORTED;
+  int gs = 0;
+  while ((1 << gs) < p.group) ++gs;
+  p.gshift = gs;
+  CUtensorMap qmap, kmap, vmap;
+  // Decode queries [num_seqs][num_q_heads][head_dim]: members of a group are
+  // consecutive sequences, so a tile is one box of 128/G sequences x G heads.
+  int rc = make_3d_tensor_map(&qmap, p.q, p.num_seqs, p.num_q_heads, pf::kD, dt, pf::kM / p.group, p.group, 64);
+  if (rc != PA_OK) return rc;
+  const int64_t rows = (int64_t)p.num_blocks * p.num_kv_heads * p.block_size;
+  rc = make_kv_tensor_map(&kmap, k_cache, rows, pf::kD, dt, 16);
+  if (rc != PA_OK) return rc;
+  rc = make_kv_tensor_map(&vmap, v_cache, rows, pf::kD, dt, 16);
+  if (rc != PA_OK) return rc;
+  const int64_t upper = (int64_t)p.num_seqs * p.num_kv_heads;
+  const int64_t resident = 2LL * num_sms_current_device();
+  const int ctas = (int)(upper < resident ? upper : resident);
+  return dispatch_prefill_kernel<true>(qmap, kmap, vmap, p, ctas, dt, stream);
 }
 
 }  // namespace pa

@@ -25,7 +25,8 @@ class PagedStep:
                  kv_lens_host: np.ndarray, k_new: torch.Tensor, v_new: torch.Tensor,
                  new_seq_ids: torch.Tensor, new_positions: torch.Tensor, cow_pairs_host: np.ndarray,
                  scale: float, partition_size: int = 0, cu_q_lens: torch.Tensor | None = None,
-                 ctx_lens: torch.Tensor | None = None):
+                 ctx_lens: torch.Tensor | None = None, group_starts: torch.Tensor | None = None,
+                 prefix_lens: torch.Tensor | None = None):
         self.q, self.k_cache, self.v_cache = q, k_cache, v_cache
         self.block_tables, self.kv_lens = block_tables, kv_lens
         self.k_new, self.v_new = k_new, v_new
@@ -52,6 +53,14 @@ class PagedStep:
                                                         self.block_size, q.shape[0], self.max_seq_len)
             self.cu_q_lens = cu_q_lens
             self.ctx_lens = ctx_lens
+        # Shared-prefix decode when the batch names groups that share blocks.
+        self.group_starts, self.prefix_lens = group_starts, prefix_lens
+        self.shared_prefix = bool(self.is_decode and group_starts is not None and prefix_lens is not None
+                                  and group_starts.shape[0] - 1 < n)
+        if self.shared_prefix:
+            need = max(need, pa.pa_decode_shared_prefix_workspace_size(
+                n, hq, self.num_kv_heads, self.head_dim, self.block_size, self.max_seq_len, self.partition_size,
+                group_starts.shape[0] - 1))
         self.workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
 
     @property
@@ -64,6 +73,9 @@ class PagedStep:
         part = pa.pa_decode_partition_size(self.kv_lens.shape[0], self.q.shape[1], self.num_kv_heads,
                                            self.block_size, self.max_seq_len,
                                            self.partition_size if self.is_decode else 0)
+        if self.shared_prefix:
+            n += 5  # prefix check, prefix pass, plan, suffix decode, merge
+            return n
         n += 2 + (1 if -(-self.max_seq_len // part) > 1 else 0)  # plan, main, split-KV merge
         if not self.is_decode and self.max_q_len > 1:
             n += 2  # prefill plan, prefill chunks
@@ -76,7 +88,17 @@ class PagedStep:
                            self.num_blocks, slot_mapping=self.slot_mapping, stream=stream)
         pa.pa_reshape_and_cache(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
                                 stream=stream)
-        if self.is_decode:
+        self.attend(stream)
+        return self.out
+
+    def attend(self, stream=None) -> torch.Tensor:
+        """The attention call of the step alone."""
+        if self.shared_prefix:
+            pa.pa_decode_shared_prefix(self.q, self.k_cache, self.v_cache, self.block_tables, self.kv_lens,
+                                       self.max_seq_len, self.group_starts, self.prefix_lens, self.scale,
+                                       out=self.out, partition_size=self.partition_size, workspace=self.workspace,
+                                       stream=stream)
+        elif self.is_decode:
             pa.pa_decode(self.q, self.k_cache, self.v_cache, self.block_tables, self.kv_lens, self.max_seq_len,
                          self.scale, out=self.out, partition_size=self.partition_size, workspace=self.workspace,
                          stream=stream)
@@ -87,9 +109,10 @@ class PagedStep:
         return self.out
 
 
-def step_from_host(batch, device="cuda", partition_size: int = 0) -> PagedStep:
+def step_from_host(batch, device="cuda", partition_size: int = 0, shared_prefix: bool = False) -> PagedStep:
     """Build a PagedStep from a host-side batch object exposing the fields of
-    a seeded workload (q, caches, tables, lengths, new tokens, CoW pairs)."""
+    a seeded workload (q, caches, tables, lengths, new tokens, CoW pairs).
+    With shared_prefix, decode uses the batch's prefix-sharing groups."""
     def dev(x, dtype=None):
         t = torch.as_tensor(x)
         if dtype is not None:
@@ -106,4 +129,6 @@ def step_from_host(batch, device="cuda", partition_size: int = 0) -> PagedStep:
         new_seq_ids=dev(batch.new_seq_ids, torch.int32), new_positions=dev(batch.new_positions, torch.int32),
         cow_pairs_host=batch.cow_pairs, scale=batch.scale, partition_size=partition_size,
         cu_q_lens=dev(cu, torch.int32), ctx_lens=dev(batch.kv_lens - batch.q_lens, torch.int32),
+        group_starts=dev(batch.group_starts, torch.int32) if shared_prefix else None,
+        prefix_lens=dev(batch.prefix_lens, torch.int32) if shared_prefix else None,
     )

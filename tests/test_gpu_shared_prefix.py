@@ -1,0 +1,96 @@
+"""Shared-prefix (cascade) decode on the GPU: the same attention as plain
+decode, computed as one tcgen05 pass over each group's shared blocks plus a
+split-KV pass over every member's private suffix, merged with log-sum-exp
+weights. Checked against the fp64 oracle and against pa_decode."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import assert_attention_close, oracle_caches_after_step, oracle_decode, to_f64
+from workloads import build_batch, make_config
+
+pytestmark = pytest.mark.gpu
+
+
+def _device_step(lib, b):
+    from paged_kv_cache_14_gb300.step import step_from_host
+    st = step_from_host(b)
+    st.run()  # copy-on-write, slots, cache write, plain decode
+    assert lib.pa_get_status() == 0
+    return st
+
+
+def _shared(lib, st, b, group_starts=None, prefix_lens=None, partition=0):
+    gs = torch.from_numpy(b.group_starts if group_starts is None else group_starts).cuda()
+    pl = torch.from_numpy(b.prefix_lens if prefix_lens is None else prefix_lens).cuda()
+    out = lib.pa_decode_shared_prefix(st.q, st.k_cache, st.v_cache, st.block_tables, st.kv_lens, st.max_seq_len,
+                                      gs, pl, b.scale, partition_size=partition)
+    return out
+
+
+CASES = [
+    # dtype, B, Hq, Hkv, lens, group, prefix tokens
+    ("bf16", 16, 64, 8, [5, 64, 64, 65, 200, 31, 1000, 129, 17, 80], 4, 64),
+    ("f16", 32, 64, 8, [40, 300, 1000, 2000, 33, 64, 65, 999], 8, 256),
+    ("bf16", 16, 32, 8, [300] * 20 + [20, 700], 20, 256),      # group 4: 20 members > 32/tile? no: 32/tile
+    ("bf16", 16, 64, 8, list(range(100, 100 + 37 * 45, 45)), 37, 512),  # 37 members: 3 tiles of 16
+    ("f16", 16, 128, 8, [129, 400, 1024, 77], 2, 128),        # group 16: 8 members per tile
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-B{c[1]}-G{c[2] // c[3]}-grp{c[5]}")
+@pytest.mark.parametrize("partition", [0, 64])
+def test_shared_prefix_matches_oracle_and_decode(lib, case, partition):
+    dtype, B, hq, hkv, lens, grp, pref = case
+    b = build_batch(name="cascade", seed=CASES.index(case) + 70, dtype=dtype, block_size=B, num_q_heads=hq,
+                    num_kv_heads=hkv, head_dim=128, q_lens=np.ones(len(lens), np.int32), kv_lens=lens,
+                    share_group=grp, share_prefix_tokens=pref, cow_per_seq=True)
+    assert (b.prefix_lens > 0).any()
+    st = _device_step(lib, b)
+    ref_plain = to_f64(st.out)
+    out = to_f64(_shared(lib, st, b, partition=partition * (B // 16)))
+    assert lib.pa_get_status() == 0
+    kc, vc, _ = oracle_caches_after_step(b)
+    assert_attention_close(out, oracle_decode(b, kc, vc), dtype, f"{case} vs oracle")
+    assert_attention_close(out, ref_plain, dtype, f"{case} vs pa_decode")
+
+
+def test_shared_prefix_bad_hints_still_correct(lib):
+    lens = [300, 300, 900, 64, 500, 33]
+    b = build_batch(name="cascade_bad", seed=81, dtype="bf16", block_size=16, num_q_heads=64, num_kv_heads=8,
+                    head_dim=128, q_lens=np.ones(6, np.int32), kv_lens=lens, share_group=3,
+                    share_prefix_tokens=256, cow_per_seq=True)
+    st = _device_step(lib, b)
+    kc, vc, _ = oracle_caches_after_step(b)
+    ref = oracle_decode(b, kc, vc)
+    pl = b.prefix_lens.copy()
+    pl[0] = 288            # claims a private block as shared: rejected by the table check
+    pl[1] = 17             # not a multiple of the block size: ignored
+    pl[4] = lens[4]        # the whole sequence: ignored (the newest token is private)
+    out = to_f64(_shared(lib, st, b, prefix_lens=pl))
+    assert lib.pa_get_status() == 0
+    assert_attention_close(out, ref, "bf16", "bad hints")
+    # Malformed groups: every hint is dropped and the call records PA_ERR_ARG.
+    gs = b.group_starts.copy()
+    gs[1], gs[2] = gs[2], gs[1]
+    out = to_f64(_shared(lib, st, b, group_starts=gs))
+    assert lib.pa_get_status() == -1
+    assert_attention_close(out, ref, "bf16", "malformed groups")
+
+
+@pytest.mark.slow
+def test_llama3_70b_prefix_config_shared_prefix(lib):
+    b = make_config("llama3_70b_prefix_bf16")
+    st = _device_step(lib, b)
+    plain = st.out.clone()
+    out = _shared(lib, st, b)
+    assert lib.pa_get_status() == 0
+    assert_attention_close(to_f64(out), to_f64(plain), "bf16", "shared-prefix vs pa_decode, full size")
+    kr, vr, _ = oracle_caches_after_step(b)
+    rng = np.random.default_rng(12)
+    order = np.argsort(b.kv_lens)
+    pick = sorted(set([int(order[0]), int(order[-1]), 0, 15, 16]) | set(rng.choice(256, 10, replace=False).tolist()))
+    ref = oracle_decode(b, kr, vr, seqs=pick)
+    assert_attention_close(to_f64(out)[pick], ref[pick], "bf16", "shared-prefix vs oracle, full size")

@@ -67,6 +67,12 @@ class PagedBatch:
     new_positions: np.ndarray
     cow_pairs: np.ndarray
     meta: dict = field(default_factory=dict)
+    # Prefix-sharing structure: group g is sequences group_starts[g] ..
+    # group_starts[g+1]-1; sequence i's first prefix_lens[i] tokens use the
+    # group's shared physical blocks (after its copy-on-write). Without
+    # sharing every sequence is its own group with prefix 0.
+    group_starts: np.ndarray | None = None
+    prefix_lens: np.ndarray | None = None
 
     @property
     def num_seqs(self) -> int:
@@ -242,6 +248,15 @@ def build_batch(
         k_new = torch.empty((t_new, num_kv_heads, head_dim), dtype=td)
         v_new = torch.empty((t_new, num_kv_heads, head_dim), dtype=td)
 
+    if share_group:
+        group_starts = np.minimum(np.arange(0, n_groups + 1) * share_group, n).astype(np.int32)
+        # Blocks still shared after the copy-on-write of the last shared one.
+        shared_after = shared_counts - (1 if n_cow else 0)
+        prefix_lens = (shared_after * B).astype(np.int32)
+    else:
+        group_starts = np.arange(0, n + 1, dtype=np.int32)
+        prefix_lens = np.zeros(n, dtype=np.int32)
+
     meta = dict(
         seed=seed, need_blocks=need, share_group=share_group,
         share_prefix_tokens=share_prefix_tokens, hot_key_frac=hot_key_frac,
@@ -253,6 +268,7 @@ def build_batch(
         num_blocks=pool_size, block_tables=tables, q_lens=q_lens, kv_lens=kv_lens,
         q=q, k_cache=k_cache, v_cache=v_cache, k_new=k_new, v_new=v_new,
         new_seq_ids=new_seq_ids, new_positions=new_positions, cow_pairs=cow, meta=meta,
+        group_starts=group_starts, prefix_lens=prefix_lens,
     )
 
 
