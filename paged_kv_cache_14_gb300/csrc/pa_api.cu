@@ -381,9 +381,11 @@ int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_ca
   int32_t* pkeys = reinterpret_cast<int32_t*>(cbase + cw.pair_keys);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   dp.prefix = prefix;
-  // 1. Verify the hints and list the prefix pass's work.
-  rc = launch_cascade_prep(dp, group_starts, prefix_lens, num_groups, 128 / g, prefix, group_ref, group_of_seq,
-                           pwork, ppairs, pkeys, s);
+  decode_set_rows(dp, dtype);
+  // 1. Verify the hints, list the prefix pass's work and the suffix decode's.
+  rc = launch_cascade_prep(dp, dtype, group_starts, prefix_lens, num_groups, 128 / g, prefix, group_ref,
+                           group_of_seq, pwork, ppairs, pkeys, s);
+  dp.planned = 1;
   if (rc != PA_OK) return rc;
   // 2. Prefix pass (tcgen05): every group's shared blocks once for all its
   //    members, partials into slot 0.

@@ -14,6 +14,7 @@
 // speed, never correctness.
 #include "pa_common.cuh"
 #include "pa_internal.h"
+#include "pa_plan.cuh"
 
 namespace pa {
 
@@ -26,6 +27,7 @@ __device__ __forceinline__ int group_of(const int32_t* group_starts, int num_gro
   return lo;
 }
 
+template <typename T>
 __global__ void __launch_bounds__(1024) cascade_prep_kernel(const DecodeParams p, const int32_t* group_starts,
                                                             const int32_t* prefix_in, int32_t num_groups,
                                                             int32_t members_per_tile, int32_t* prefix_out,
@@ -74,11 +76,10 @@ __global__ void __launch_bounds__(1024) cascade_prep_kernel(const DecodeParams p
     const int nb = prefix_out[s] / B;
     const int32_t* a = p.block_tables + (int64_t)s * p.max_blocks_per_seq;
     const int32_t* b = p.block_tables + (int64_t)r * p.max_blocks_per_seq;
-    for (int j = c; j < nb; j += 4)
-      if (a[j] != b[j]) {
-        prefix_out[s] = 0;
-        break;
-      }
+    bool mismatch = false;  // no early exit: the loads stay independent
+#pragma unroll 8
+    for (int j = c; j < nb; j += 4) mismatch |= a[j] != b[j];
+    if (mismatch) prefix_out[s] = 0;
   }
   __syncthreads();
   // 4. Prefix-pass work: one pair per (group, tile of consecutive members)
@@ -101,14 +102,21 @@ __global__ void __launch_bounds__(1024) cascade_prep_kernel(const DecodeParams p
     work[0] = 0;
     work[1] = count * p.num_kv_heads;
   }
+  // 5. The suffix decode's work list, from the verified prefixes.
+  decode_plan_body<T>(p);
 }
 
-int launch_cascade_prep(const DecodeParams& dp, const int32_t* group_starts, const int32_t* prefix_in,
+int launch_cascade_prep(const DecodeParams& dp, pa_dtype dt, const int32_t* group_starts, const int32_t* prefix_in,
                         int32_t num_groups, int32_t members_per_tile, int32_t* prefix_out, int32_t* group_ref,
                         int32_t* group_of_seq, int32_t* work, int32_t* pairs, int32_t* pair_keys,
                         cudaStream_t stream) {
-  cascade_prep_kernel<<<1, 1024, 0, stream>>>(dp, group_starts, prefix_in, num_groups, members_per_tile,
-                                              prefix_out, group_ref, group_of_seq, work, pairs, pair_keys);
+  if (dt == PA_BF16)
+    cascade_prep_kernel<__nv_bfloat16><<<1, 1024, 0, stream>>>(dp, group_starts, prefix_in, num_groups,
+                                                               members_per_tile, prefix_out, group_ref, group_of_seq,
+                                                               work, pairs, pair_keys);
+  else
+    cascade_prep_kernel<__half><<<1, 1024, 0, stream>>>(dp, group_starts, prefix_in, num_groups, members_per_tile,
+                                                        prefix_out, group_ref, group_of_seq, work, pairs, pair_keys);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -41,17 +41,12 @@
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
+#include "pa_plan.cuh"
 
 // Bytes of the K/V stage ring of one decode CTA.
 #ifndef PA_DECODE_RING_BYTES
 #define PA_DECODE_RING_BYTES 65536
 #endif
-// Work order of the decode plan: 1 = first partitions sequence-major, then
-// the rest longest first; 0 = all partitions sequence-major.
-#ifndef PA_DECODE_PLAN_ORDER
-#define PA_DECODE_PLAN_ORDER 1
-#endif
-
 namespace pa {
 
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
@@ -86,101 +81,11 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
       : "memory");
 }
 
-// Row of q / out and key count of sequence `seq`; false when the sequence
-// is not a decode row of this launch (a prefill chunk in a mixed batch).
-__device__ __forceinline__ bool decode_row(const DecodeParams& p, int seq, int& qrow, int& len) {
-  if (p.cu_q_lens) {
-    const int q0 = p.cu_q_lens[seq], q1 = p.cu_q_lens[seq + 1];
-    if (q1 - q0 != 1) return false;
-    qrow = q0;
-    len = p.lens[seq] + 1;
-  } else {
-    qrow = seq;
-    len = p.lens[seq];
-  }
-  return true;
-}
-
-__device__ __forceinline__ bool len_ok(const DecodeParams& p, int len) {
-  return len >= 1 && len <= p.len_cap && len <= p.max_blocks_per_seq * p.block_size;
-}
-
-// ---------------------------------------------------------------------------
-// Plan: list the (sequence, partition) pairs that exist, reset the counters.
-// One CTA of 1024 threads. Sequences with an illegal length get zero output
-// rows and PA_ERR_SEQLEN.
-// ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p) {
-  // Work order: the first partition of every sequence in sequence order
-  // (the sequences of a prefix-sharing group are adjacent, so the CTAs that
-  // read a shared prefix run at the same time and hit in L2), then every
-  // other partition from the longest to the shortest, so the last items
-  // pulled from the counter are short and the tail is short.
-  constexpr int kBins = 1024;  // later partitions binned by length, 16 tokens per bin, longest first
-  __shared__ int32_t scan[1024];
-  __shared__ int32_t hist[kBins];
-  const int N = p.num_seqs;
-  const int P = p.partition;
-  for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
-  auto bin_of = [&](int len, int part) {
-    if (!PA_DECODE_PLAN_ORDER) return 0;
-    const int plen = min(P, len - part * P);
-    return min((P - plen) >> 4, kBins - 1);
-  };
-  const int per = (N + 1023) / 1024;
-  const int s0 = min(N, (int)threadIdx.x * per), s1 = min(N, s0 + per);
-  int cnt0 = 0;
-  for (int s = s0; s < s1; ++s) {
-    int qrow, len;
-    if (!decode_row(p, s, qrow, len)) continue;
-    if (!len_ok(p, len)) {
-      record_error(p.status, PA_ERR_SEQLEN);
-      T* out = static_cast<T*>(p.out) + (int64_t)qrow * p.num_q_heads * p.head_dim;
-      for (int i = 0; i < p.num_q_heads * p.head_dim; ++i) out[i] = T(0.0f);
-      continue;
-    }
-    ++cnt0;
-    const int sl = len - (p.prefix ? p.prefix[s] : 0);  // keys left to the suffix pass
-    const int n = (sl + P - 1) / P;
-    for (int part = 1; part < n; ++part) atomicAdd(&hist[bin_of(sl, part)], 1);
-  }
-  scan[threadIdx.x] = cnt0;
-  __syncthreads();
-  for (int off = 1; off < 1024; off <<= 1) {
-    const int v = threadIdx.x >= off ? scan[threadIdx.x - off] : 0;
-    __syncthreads();
-    scan[threadIdx.x] += v;
-    __syncthreads();
-  }
-  const int total0 = scan[1023];
-  int base0 = scan[threadIdx.x] - cnt0;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = total0;
-    for (int b = 0; b < kBins; ++b) {
-      const int c = hist[b];
-      hist[b] = run;
-      run += c;
-    }
-    scan[0] = run;  // total number of (sequence, partition) pairs
-  }
-  __syncthreads();
-  const int total = scan[0];
-  for (int s = s0; s < s1; ++s) {
-    int qrow, len;
-    if (!decode_row(p, s, qrow, len) || !len_ok(p, len)) continue;
-    p.pairs[base0++] = s << 16;
-    const int sl = len - (p.prefix ? p.prefix[s] : 0);
-    const int n = (sl + P - 1) / P;
-    for (int part = 1; part < n; ++part) p.pairs[atomicAdd(&hist[bin_of(sl, part)], 1)] = (s << 16) | part;
-  }
-  if (threadIdx.x == 0) {
-    p.work[0] = 0;
-    p.work[1] = total * p.num_kv_heads * p.row_groups;
-  }
+  decode_plan_body<T>(p);
 }
+
 
 // ---------------------------------------------------------------------------
 // Persistent tensor-core decode kernel (fp16 / bf16).
@@ -214,8 +119,15 @@ struct DecCfg {
   static_assert(BS % 16 == 0, "block size must be a multiple of 16");
 };
 
+// How an item's result leaves the CTA.
+enum ItemOut : int {
+  kOutPartial = 0,     // fp32 partial into its slot (merged later)
+  kOutDirect = 1,      // the sequence's only partition: normalised output
+  kOutWithPrefix = 2,  // the only suffix partition: merged here with the prefix pass's partial (slot 0)
+};
+
 struct ItemMeta {
-  int seq, qrow, h0, nrows, t_begin, t_end, nsub, jstart, part, n_parts, hg, pad[5];
+  int seq, qrow, h0, nrows, t_begin, t_end, nsub, jstart, part, n_parts, hg, out_mode, pad[4];
 };
 
 template <typename T, int D, int BS, int NT>
@@ -315,9 +227,9 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
         m.nsub = nsub_pad;
         m.jstart = jg;
         m.part = p.slot0 + part;
-        // Partials of this (sequence, head): the suffix partitions, plus the
-        // prefix pass's when there is a shared prefix.
-        m.n_parts = (len - pfx + p.partition - 1) / p.partition + (pfx > 0 ? 1 : 0);
+        const int ns = (len - pfx + p.partition - 1) / p.partition;  // suffix partitions
+        m.n_parts = ns + (pfx > 0 ? 1 : 0);
+        m.out_mode = ns > 1 ? kOutPartial : (pfx > 0 ? kOutWithPrefix : kOutDirect);
         m.hg = seq * hr + hg;
         const uint32_t fb = smem_u32(&ifull[slot]);
         mbar_arrive_expect_tx(fb, nrows * D * 2);
@@ -583,7 +495,6 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
         }
       }
     named_barrier_sync(1, C::kConsumers * 32);
-    const bool single = mt.n_parts == 1;
     for (int idx = ctid; idx < mt.nrows * (D / 4); idx += C::kConsumers * 32) {
       const int h = idx / (D / 4);
       const int d4 = (idx - h * (D / 4)) * 4;
@@ -602,7 +513,19 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
         acc.z += v.z;
         acc.w += v.w;
       }
-      if (single) {
+      if (mt.out_mode == kOutWithPrefix) {
+        // Merge with the prefix pass's partial (written by an earlier
+        // launch on this stream): M' = max(M, m0), weights 2^(M - M'), 2^(m0 - M').
+        const int64_t b0 = ((int64_t)mt.seq * p.num_q_heads + mt.h0 + h) * p.max_parts;
+        const float2 ml0 = __ldcg(reinterpret_cast<const float2*>(p.part_ml + b0 * 2));
+        const float4 o0 = __ldcg(reinterpret_cast<const float4*>(p.part_o + b0 * D + d4));
+        const float Mx = fmaxf(M, ml0.x);
+        const float w1 = exp2f(M - Mx), w0 = exp2f(ml0.x - Mx);
+        const float inv = 1.f / (L * w1 + ml0.y * w0);
+        store4(static_cast<T*>(p.out) + ((int64_t)mt.qrow * p.num_q_heads + mt.h0 + h) * D + d4,
+               make_float4((acc.x * w1 + o0.x * w0) * inv, (acc.y * w1 + o0.y * w0) * inv,
+                           (acc.z * w1 + o0.z * w0) * inv, (acc.w * w1 + o0.w * w0) * inv));
+      } else if (mt.out_mode == kOutDirect) {
         const float inv = 1.f / L;
         store4(static_cast<T*>(p.out) + ((int64_t)mt.qrow * p.num_q_heads + mt.h0 + h) * D + d4,
                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
@@ -745,71 +668,65 @@ __global__ void __launch_bounds__(128) decode_simt_kernel(const DecodeParams p) 
 }
 
 // Split-KV merge: out = sum_p 2^(m_p - M) o~_p / sum_p 2^(m_p - M) l_p with
-// M = max_p m_p (scores are kept in log2 units). One CTA per (q head,
-// sequence); the partitions' (m, l) pairs are read in parallel, the weights
-// kept in shared memory, and each thread accumulates head_dim / 128 columns.
+// M = max_p m_p (scores are kept in log2 units). One warp per (sequence,
+// query head), eight heads per CTA: lanes reduce the partitions' (m, l)
+// pairs, then each lane accumulates four head_dim columns over the
+// partitions with coalesced 16-byte loads.
 template <typename T>
-__global__ void __launch_bounds__(128) splitkv_merge_kernel(const DecodeParams p) {
-  extern __shared__ float wts[];  // [max_parts]
-  __shared__ float red[4];
-  const int h = blockIdx.x;
+__global__ void __launch_bounds__(256) splitkv_merge_kernel(const DecodeParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x * 8 + warp;
   const int seq = blockIdx.y;
+  if (h >= p.num_q_heads) return;
   int qrow, len;
   if (!decode_row(p, seq, qrow, len) || !len_ok(p, len)) return;
   const int pfx = p.prefix ? p.prefix[seq] : 0;
   const int ns = (len - pfx + p.partition - 1) / p.partition;  // suffix partitions
-  if (pfx == 0 && ns <= 1) return;                              // written directly
+  if (ns <= 1) return;  // written by the decode kernel (alone, or merged with the prefix partial)
   const int first = pfx > 0 ? 0 : p.slot0;                      // slot 0 holds the prefix pass
   const int n = p.slot0 + ns - first;
   const int64_t base = ((int64_t)seq * p.num_q_heads + h) * p.max_parts + first;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* ml = p.part_ml + base * 2;
   float M = -CUDART_INF_F;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) M = fmaxf(M, __ldcg(p.part_ml + (base + i) * 2));
+  for (int i = lane; i < n; i += 32) M = fmaxf(M, __ldcg(ml + 2 * i));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  if (lane == 0) red[warp] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  __syncthreads();
   float L = 0.f;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const float2 mlv = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (base + i) * 2));
-    const float w = exp2f(mlv.x - M);
-    wts[i] = w;
-    L += w * mlv.y;
+  for (int i = lane; i < n; i += 32) {
+    const float2 v = __ldcg(reinterpret_cast<const float2*>(ml + 2 * i));
+    L += v.x == -CUDART_INF_F ? 0.f : exp2f(v.x - M) * v.y;
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  if (lane == 0) red[warp] = L;
-  __syncthreads();
-  const float invL = 1.f / (red[0] + red[1] + red[2] + red[3]);
+  const float invL = 1.f / L;
   const int D = p.head_dim;
   T* out = static_cast<T*>(p.out) + ((int64_t)qrow * p.num_q_heads + h) * D;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    const float* src = p.part_o + base * D + d;
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    int i = 0;
-    for (; i + 3 < n; i += 4) {
-      a0 = fmaf(wts[i], __ldcg(src + (int64_t)i * D), a0);
-      a1 = fmaf(wts[i + 1], __ldcg(src + (int64_t)(i + 1) * D), a1);
-      a2 = fmaf(wts[i + 2], __ldcg(src + (int64_t)(i + 2) * D), a2);
-      a3 = fmaf(wts[i + 3], __ldcg(src + (int64_t)(i + 3) * D), a3);
+  for (int d4 = lane * 4; d4 < D; d4 += 128) {
+    const float* src = p.part_o + base * D + d4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int i = 0; i < n; ++i) {
+      const float mi = __ldcg(ml + 2 * i);
+      const float w = mi == -CUDART_INF_F ? 0.f : exp2f(mi - M);
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (int64_t)i * D));
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
     }
-    for (; i < n; ++i) a0 = fmaf(wts[i], __ldcg(src + (int64_t)i * D), a0);
-    out[d] = T(((a0 + a1) + (a2 + a3)) * invL);
+    store4(out + d4, make_float4(acc.x * invL, acc.y * invL, acc.z * invL, acc.w * invL));
   }
 }
 
 static int launch_merge(const DecodeParams& p, pa_dtype dt, cudaStream_t stream) {
   if (p.max_parts <= 1) return PA_OK;
-  const size_t wbytes = (size_t)p.max_parts * sizeof(float);
-  const dim3 grid(p.num_q_heads, p.num_seqs);
+  const dim3 grid((p.num_q_heads + 7) / 8, p.num_seqs);
   if (dt == PA_F32)
-    splitkv_merge_kernel<float><<<grid, 128, wbytes, stream>>>(p);
+    splitkv_merge_kernel<float><<<grid, 256, 0, stream>>>(p);
   else if (dt == PA_BF16)
-    splitkv_merge_kernel<__nv_bfloat16><<<grid, 128, wbytes, stream>>>(p);
+    splitkv_merge_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(p);
   else
-    splitkv_merge_kernel<__half><<<grid, 128, wbytes, stream>>>(p);
+    splitkv_merge_kernel<__half><<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -832,8 +749,10 @@ static int launch_tc(const DecodeParams& p, cudaStream_t stream) {
       return PA_ERR_CUDA;
     attr_set[dev] = true;
   }
-  decode_plan_kernel<T><<<1, 1024, 0, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (!p.planned) {
+    decode_plan_kernel<T><<<1, 1024, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  }
   const int64_t upper = (int64_t)p.num_seqs * p.max_parts * p.num_kv_heads * p.row_groups;
   const int64_t resident = (NT == 1 ? 2LL : 1LL) * num_sms_current_device();
   const int ctas = (int)(upper < resident ? upper : resident);
@@ -868,11 +787,15 @@ static int launch_tc_dispatch(const DecodeParams& p, cudaStream_t stream) {
   return PA_ERR_UNSUPPORTED;
 }
 
-int launch_decode(const DecodeParams& p0, pa_dtype dt, cudaStream_t stream) {
-  DecodeParams p = p0;
+void decode_set_rows(DecodeParams& p, pa_dtype dt) {
   const int rows_max = dt == PA_F32 ? 8 : 16;
   p.rows_per_cta = p.group < rows_max ? p.group : rows_max;
   p.row_groups = (p.group + p.rows_per_cta - 1) / p.rows_per_cta;
+}
+
+int launch_decode(const DecodeParams& p0, pa_dtype dt, cudaStream_t stream) {
+  DecodeParams p = p0;
+  decode_set_rows(p, dt);
   if ((int64_t)p.num_kv_heads * p.row_groups > 65535) return PA_ERR_UNSUPPORTED;
   if (dt == PA_F32) {
     switch (p.head_dim) {

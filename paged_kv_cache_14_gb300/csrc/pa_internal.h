@@ -47,8 +47,13 @@ struct DecodeParams {
   // partitions use slots 1.. . nullptr / 0 for plain decode.
   const int32_t* prefix;
   int32_t slot0;
+  int32_t planned;       // the work list is already built (by the shared-prefix preparation)
   int* status;
 };
+
+// Rows of a query-head group handled per decode work item (depends on dtype).
+void decode_set_rows(DecodeParams& p, pa_dtype dt);
+
 
 // Split-KV workspace layout shared by the size query and the launch. Every
 // region starts on a 256-byte boundary.
@@ -155,7 +160,9 @@ int launch_prefill(const PrefillParams& p, const void* k_cache, const void* v_ca
 int launch_prefix_pass(const PrefillParams& p, const void* k_cache, const void* v_cache, pa_dtype dt,
                        cudaStream_t stream);
 // Shared-prefix verification and the prefix pass's work list (one CTA).
-int launch_cascade_prep(const DecodeParams& dp, const int32_t* group_starts, const int32_t* prefix_in,
+// Also builds the suffix decode's work list (dp.prefix must point at
+// prefix_out); the caller then launches the decode with dp.planned = 1.
+int launch_cascade_prep(const DecodeParams& dp, pa_dtype dt, const int32_t* group_starts, const int32_t* prefix_in,
                         int32_t num_groups, int32_t members_per_tile, int32_t* prefix_out, int32_t* group_ref,
                         int32_t* group_of_seq, int32_t* work, int32_t* pairs, int32_t* pair_keys,
                         cudaStream_t stream);

@@ -51,14 +51,18 @@ constexpr int kStageBytes = 2 * kKBytes;   // K + V: 32 KB
 constexpr int kPBytes = kM * 128;          // 128 rows x 64 keys x 2 B
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kQBytes;
-constexpr int kOffP = kOffKV + 2 * kStageBytes;
-constexpr int kOffBar = kOffP + kPBytes;
-// bars: q_full, kv_full[2], kv_empty[2], s_full, s_free, p_full, o_done
-constexpr int kNumBars = 9;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, item, abort
-constexpr int kSmem = kOffMisc + 64;
 constexpr int kTmemCols = 256;
-constexpr int kColS = 0;
+// Layout past the K/V ring of NS stages.
+template <int NS>
+struct Layout {
+  static constexpr int kOffP = kOffKV + NS * kStageBytes;
+  static constexpr int kOffBar = kOffP + kPBytes;
+  // bars: q_full, kv_full[NS], kv_empty[NS], s_full[2], s_free[2], p_full, o_done
+  static constexpr int kNumBars = 1 + 2 * NS + 6;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, item, abort
+  static constexpr int kSmem = kOffMisc + 64;
+};
+constexpr int kColS = 0;  // two S buffers: columns 0..63 and 64..127 (tile g uses buffer g & 1)
 constexpr int kColO = 128;
 }  // namespace pf
 
@@ -126,23 +130,27 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
 // PREFIX = true: prefix pass of shared-prefix decode (rows = group members x
 // GQA heads, each row masked to its own verified prefix, fp32 partial
 // (m, l, o~) written to slot 0 of the member's partials).
-template <typename T, int BS, bool PREFIX>
-__global__ void __launch_bounds__(pf::kThreads, 2)
+template <typename T, int BS, bool PREFIX, int NS>
+__global__ void __launch_bounds__(pf::kThreads, NS <= 2 ? 2 : 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
   using namespace pf;
+  using Lay = Layout<NS>;
+  constexpr int kOffP = Lay::kOffP;
+  constexpr int kOffBar = Lay::kOffBar;
+  constexpr int kOffMisc = Lay::kOffMisc;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   constexpr uint32_t kIdescS = idesc_f16(kM, kN, kBf16, false);  // S = Q K^T
   constexpr uint32_t kIdescO = idesc_f16(kM, kD, kBf16, true);   // O += P V (V MN-major)
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   const uint32_t b_q = smem_u32(&bars[0]);
-  const uint32_t b_kvfull0 = smem_u32(&bars[1]);
-  const uint32_t b_kvempty0 = smem_u32(&bars[3]);
-  const uint32_t b_sfull = smem_u32(&bars[5]);
-  const uint32_t b_sfree = smem_u32(&bars[6]);
-  const uint32_t b_pfull = smem_u32(&bars[7]);
-  const uint32_t b_odone = smem_u32(&bars[8]);
+  const uint32_t b_kvfull0 = smem_u32(&bars[1]);        // + 8 * stage
+  const uint32_t b_kvempty0 = smem_u32(&bars[1 + NS]);  // + 8 * stage
+  const uint32_t b_sfull0 = smem_u32(&bars[1 + 2 * NS]);  // + 8 * buffer
+  const uint32_t b_sfree0 = smem_u32(&bars[3 + 2 * NS]);  // + 8 * buffer
+  const uint32_t b_pfull = smem_u32(&bars[5 + 2 * NS]);
+  const uint32_t b_odone = smem_u32(&bars[6 + 2 * NS]);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(&misc[2]);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -151,12 +159,14 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
   if (threadIdx.x == 0) {
     if ((sbase & 1023u) != 0) record_error(p.status, PA_ERR_ALIGN);
     mbar_init(b_q, 1);
-    mbar_init(b_kvfull0, 1);
-    mbar_init(b_kvfull0 + 8, 1);
-    mbar_init(b_kvempty0, 1);
-    mbar_init(b_kvempty0 + 8, 1);
-    mbar_init(b_sfull, 1);
-    mbar_init(b_sfree, 4);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(b_kvfull0 + 8 * i, 1);
+      mbar_init(b_kvempty0 + 8 * i, 1);
+    }
+    mbar_init(b_sfull0, 1);
+    mbar_init(b_sfull0 + 8, 1);
+    mbar_init(b_sfree0, 4);
+    mbar_init(b_sfree0 + 8, 4);
     mbar_init(b_pfull, 4);
     mbar_init(b_odone, 1);
     abort_flag[0] = (sbase & 1023u) != 0;
@@ -220,7 +230,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
       const int32_t* bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
       for (int j = 0; j < ntiles; ++j) {
         const int g = tile_base + j;
-        const int s = g & 1;
+        const int s = g % NS;
         // Lanes 0..3: physical block of the tile's 16-token sub-tile `lane`.
         int id = 0;
         if (lane < 4) {
@@ -237,7 +247,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
 #pragma unroll
         for (int u = 0; u < 4; ++u) ids[u] = __shfl_sync(0xffffffffu, id, u);
         if (lane == 0) {
-          if (g >= 2 && !mbar_wait(b_kvempty0 + 8 * s, ((g >> 1) & 1) ^ 1, p.status)) {
+          if (g >= NS && !mbar_wait(b_kvempty0 + 8 * s, ((g / NS) & 1) ^ 1, p.status)) {
             bad = true;
           } else {
             const uint32_t fb = b_kvfull0 + 8 * s;
@@ -260,8 +270,8 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
           // Let the copies already issued land before the CTA moves on.
           if (lane == 0) {
             mbar_wait(b_q, it & 1, nullptr);
-            for (int jj = max(0, j - 2); jj < j; ++jj)
-              mbar_wait(b_kvfull0 + 8 * ((tile_base + jj) & 1), ((tile_base + jj) >> 1) & 1, nullptr);
+            for (int jj = max(0, j - NS); jj < j; ++jj)
+              mbar_wait(b_kvfull0 + 8 * ((tile_base + jj) % NS), ((tile_base + jj) / NS) & 1, nullptr);
           }
           break;
         }
@@ -271,24 +281,35 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
       if (lane == 0) {
         bool bad = !mbar_wait(b_q, it & 1, p.status);
         uint32_t last_bar = 0, last_phase = 0;  // the last commit: it covers every MMA issued before it
-        for (int j = 0; j < ntiles && !bad; ++j) {
-          const int g = tile_base + j;
-          const int s = g & 1;
-          if (!mbar_wait(b_kvfull0 + 8 * s, (g >> 1) & 1, p.status)) { bad = true; break; }
-          if (g > 0 && !mbar_wait(b_sfree, (g - 1) & 1, p.status)) { bad = true; break; }
+        // S for tile g goes to TMEM buffer g & 1; S of the next tile is issued
+        // before waiting for this tile's P, so the tensor core computes it
+        // while the softmax warps work.
+        auto issue_s = [&](int g) -> bool {
+          const int st = g % NS;  // K/V stage
+          const int sb = g & 1;   // S buffer
+          if (!mbar_wait(b_kvfull0 + 8 * st, (g / NS) & 1, p.status)) return false;
+          if (g >= 2 && !mbar_wait(b_sfree0 + 8 * sb, ((g >> 1) & 1) ^ 1, p.status)) return false;
           tc_fence_after();
-          const uint32_t kst = sbase + kOffKV + s * kStageBytes;
+          const uint32_t kst = sbase + kOffKV + st * kStageBytes;
 #pragma unroll
           for (int k = 0; k < kD / 16; ++k) {
             const uint64_t ad = sdesc_sw128(sbase + kOffQ + (k >> 2) * kQHalf + (k & 3) * 32, 16, 1024);
             const uint64_t bd = sdesc_sw128(kst + (k >> 2) * kKVHalf + (k & 3) * 32, 16, 1024);
-            tc_mma_f16(tmem + kColS, ad, bd, kIdescS, k > 0);
+            tc_mma_f16(tmem + kColS + sb * kN, ad, bd, kIdescS, k > 0);
           }
-          tc_commit(b_sfull);
-          last_bar = b_sfull;
-          last_phase = g & 1;
+          tc_commit(b_sfull0 + 8 * sb);
+          last_bar = b_sfull0 + 8 * sb;
+          last_phase = (g >> 1) & 1;
+          return true;
+        };
+        if (!bad && ntiles > 0) bad = !issue_s(tile_base);
+        for (int j = 0; j < ntiles && !bad; ++j) {
+          const int g = tile_base + j;
+          const int s = g % NS;
+          if (j + 1 < ntiles && !issue_s(g + 1)) { bad = true; break; }
           if (!mbar_wait(b_pfull, g & 1, p.status)) { bad = true; break; }
           tc_fence_after();
+          const uint32_t kst = sbase + kOffKV + s * kStageBytes;
 #pragma unroll
           for (int k = 0; k < kN / 16; ++k) {
             const uint64_t ad = sdesc_sw128(sbase + kOffP + k * 32, 16, 1024);
@@ -325,15 +346,16 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
       bool bad = false;
       for (int j = 0; j < ntiles; ++j) {
         const int g = tile_base + j;
-        if (!mbar_wait(b_sfull, g & 1, p.status)) { bad = true; break; }
+        const int sb = g & 1;  // S buffer of this tile
+        if (!mbar_wait(b_sfull0 + 8 * sb, (g >> 1) & 1, p.status)) { bad = true; break; }
         tc_fence_after();
         uint32_t sr[2][32];
-        tmem_ld32(tmem + tl + kColS, sr[0]);
-        tmem_ld32(tmem + tl + kColS + 32, sr[1]);
+        tmem_ld32(tmem + tl + kColS + sb * kN, sr[0]);
+        tmem_ld32(tmem + tl + kColS + sb * kN + 32, sr[1]);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(b_sfree);
+        if (lane == 0) mbar_arrive(b_sfree0 + 8 * sb);
         const int k0 = j * kN;
         float mx = -CUDART_INF_F;
 #pragma unroll
@@ -365,11 +387,11 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
         // PV of the previous tile must be done before P and O are touched.
         if (j > 0 && !mbar_wait(b_odone, (g - 1) & 1, p.status)) { bad = true; break; }
         tc_fence_after();
-        const int s = g & 1;
+        const int s = g % NS;
         if (k0 + kN > kv_len) {
           // Keys past the sequence end carry p = 0, but their V slots may
           // hold any bits (NaN included): zero those V rows.
-          if (!mbar_wait(b_kvfull0 + 8 * s, (g >> 1) & 1, p.status)) { bad = true; break; }
+          if (!mbar_wait(b_kvfull0 + 8 * s, (g / NS) & 1, p.status)) { bad = true; break; }
           uint8_t* vst = smem + kOffKV + s * kStageBytes + kKBytes;
           const int first = max(kv_len - k0, 0);
           for (int idx = threadIdx.x - 64; idx < (kN - first) * 16; idx += 128) {
@@ -458,16 +480,20 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
 template <typename T, int BS, bool PREFIX>
 static int launch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                  const PrefillParams& p, int ctas, cudaStream_t stream) {
-  auto kern = prefill_tc_kernel<T, BS, PREFIX>;
+  // Chunked prefill: 2 stages, two CTAs per SM. Prefix pass (few items, one
+  // CTA per SM): 4 stages to keep more K/V in flight per CTA.
+  constexpr int NS = PREFIX ? 4 : 2;
+  constexpr int kSmemBytes = pf::Layout<NS>::kSmem;
+  auto kern = prefill_tc_kernel<T, BS, PREFIX, NS>;
   static bool attr_set[64] = {};  // one flag per device for this instantiation
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pf::kSmem) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
       return PA_ERR_CUDA;
     attr_set[dev] = true;
   }
-  kern<<<ctas, pf::kThreads, pf::kSmem, stream>>>(qmap, kmap, vmap, p);
+  kern<<<ctas, pf::kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -528,7 +554,7 @@ int launch_prefix_pass(const PrefillParams& p0, const void* k_cache, const void*
   rc = make_kv_tensor_map(&vmap, v_cache, rows, pf::kD, dt, 16);
   if (rc != PA_OK) return rc;
   const int64_t upper = (int64_t)p.num_seqs * p.num_kv_heads;
-  const int64_t resident = 2LL * num_sms_current_device();
+  const int64_t resident = num_sms_current_device();
   const int ctas = (int)(upper < resident ? upper : resident);
   return dispatch_prefill_kernel<true>(qmap, kmap, vmap, p, ctas, dt, stream);
 }
