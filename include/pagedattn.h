@@ -221,7 +221,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
  *   workspace    : pa_decode_shared_prefix_workspace_size() bytes.
  * Other arguments as pa_decode. fp16/bf16, head_dim 128, GQA group a power
  * of two up to 128 (up to 128/group members per tensor-core tile; larger
- * groups take several tiles).
+ * groups take several tiles), scale > 0.
  */
 size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                               int32_t head_dim, int32_t block_size, int32_t max_seq_len,
@@ -280,8 +280,8 @@ int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, c
  *                no initialisation needed; not shared by overlapping calls
  * Rows with q_len == 1 go through the decode path (any supported dtype and
  * head_dim); longer chunks through a tcgen05 tensor-core kernel that needs
- * fp16/bf16, head_dim 128 and a power-of-two GQA group of at most 128
- * (PA_ERR_DTYPE / PA_ERR_UNSUPPORTED otherwise).
+ * fp16/bf16, head_dim 128, a power-of-two GQA group of at most 128
+ * (PA_ERR_DTYPE / PA_ERR_UNSUPPORTED otherwise) and scale > 0 (PA_ERR_ARG).
  */
 size_t pa_chunked_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t block_size, int32_t total_q,

@@ -184,6 +184,37 @@ __device__ __forceinline__ void store4(__half* p, float4 v) {
   *reinterpret_cast<uint2*>(p) = u;
 }
 
+// Exclusive prefix sum of one int per thread over a CTA of 1024 threads
+// (warp shuffles, then one warp over the 32 warp totals). `scratch` is 33
+// ints of shared memory; *total receives the sum. Contains __syncthreads.
+__device__ __forceinline__ int block_exclusive_scan_1024(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    const int sv = scratch[lane];
+    int t = sv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    scratch[lane] = t - sv;
+    if (lane == 31) scratch[32] = t;
+  }
+  __syncthreads();
+  *total = scratch[32];
+  const int r = x - v + scratch[w];
+  __syncthreads();
+  return r;
+}
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }

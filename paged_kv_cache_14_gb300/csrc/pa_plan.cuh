@@ -48,7 +48,7 @@ __device__ __forceinline__ void decode_plan_body(const DecodeParams& p) {
   // other partition from the longest to the shortest, so the last items
   // pulled from the counter are short and the tail is short.
   constexpr int kBins = 1024;  // later partitions binned by length, 16 tokens per bin, longest first
-  __shared__ int32_t scan[1024];
+  __shared__ int32_t scan[33];
   __shared__ int32_t hist[kBins];
   const int N = p.num_seqs;
   const int P = p.partition;
@@ -79,28 +79,15 @@ __device__ __forceinline__ void decode_plan_body(const DecodeParams& p) {
     if (!p.prefix) ++cnt0;
     for (int part = first_binned; part < n; ++part) atomicAdd(&hist[bin_of(sl, part)], 1);
   }
-  scan[threadIdx.x] = cnt0;
+  int total0;
+  int base0 = block_exclusive_scan_1024(cnt0, scan, &total0);
+  // Bins in ascending order (longest partitions first), after the first
+  // partitions: one bin per thread.
+  int nbin_total;
+  const int bin_off = block_exclusive_scan_1024(hist[threadIdx.x], scan, &nbin_total);
+  hist[threadIdx.x] = total0 + bin_off;
   __syncthreads();
-  for (int off = 1; off < 1024; off <<= 1) {
-    const int v = threadIdx.x >= off ? scan[threadIdx.x - off] : 0;
-    __syncthreads();
-    scan[threadIdx.x] += v;
-    __syncthreads();
-  }
-  const int total0 = scan[1023];
-  int base0 = scan[threadIdx.x] - cnt0;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = total0;
-    for (int b = 0; b < kBins; ++b) {
-      const int c = hist[b];
-      hist[b] = run;
-      run += c;
-    }
-    scan[0] = run;  // total number of (sequence, partition) pairs
-  }
-  __syncthreads();
-  const int total = scan[0];
+  const int total = total0 + nbin_total;
   for (int s = s0; s < s1; ++s) {
     int qrow, len;
     if (!decode_row(p, s, qrow, len) || !len_ok(p, len)) continue;

@@ -97,17 +97,19 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
     for (int mt = 0; mt < nm; ++mt) atomicAdd(&hist[tiles_of(s, mt)], 1);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    // Exclusive scan from the longest bin down.
-    int run = 0;
-    for (int b = kBins - 1; b >= 0; --b) {
-      const int c = hist[b];
-      hist[b] = run;
-      run += c;
-    }
-    total = run;
+  {
+    // Exclusive scan from the longest bin down: thread t owns bins
+    // kBins-1-2t and kBins-2-2t.
+    __shared__ int scratch[33];
+    const int b0 = kBins - 1 - 2 * threadIdx.x, b1 = b0 - 1;
+    const int c0 = hist[b0], c1 = hist[b1];
+    int tot;
+    const int off = block_exclusive_scan_1024(c0 + c1, scratch, &tot);
+    hist[b0] = off;
+    hist[b1] = off + c0;
+    if (threadIdx.x == 0) total = tot;
+    __syncthreads();
   }
-  __syncthreads();
   for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) {
     const int ql = p.cu_q_lens[s + 1] - p.cu_q_lens[s];
     if (ql <= 1) continue;
@@ -357,33 +359,50 @@ __global__ void __launch_bounds__(pf::kThreads, NS <= 2 ? 2 : 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(b_sfree0 + 8 * sb);
         const int k0 = j * kN;
+        // Raw-score row max (scale > 0 keeps the order); the causal / prefix
+        // mask is skipped when the whole tile is visible to every row of the warp.
+        const bool full_vis = __all_sync(0xffffffffu, k0 + kN - 1 <= lim);
         float mx = -CUDART_INF_F;
+        if (full_vis) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+          for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int key = k0 + h * 32 + c;
-            const float v = key <= lim ? __uint_as_float(sr[h][c]) * sl2 : -CUDART_INF_F;
-            sr[h][c] = __float_as_uint(v);
-            mx = fmaxf(mx, v);
-          }
-        const float mn = fmaxf(m, mx);
-        const bool dead = mn == -CUDART_INF_F;  // no key seen yet (a row without keys)
-        const float alpha = dead ? 1.f : exp2f(m - mn);  // m = -inf on the first tile: alpha = 0
-        const float msub = dead ? 0.f : mn;
+            for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(sr[h][c]));
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int key = k0 + h * 32 + c;
+              const float v = key <= lim ? __uint_as_float(sr[h][c]) : -CUDART_INF_F;
+              sr[h][c] = __float_as_uint(v);
+              mx = fmaxf(mx, v);
+            }
+        }
+        // Exponentials are taken against m (raw units). It only moves up when
+        // the row max exceeds it by more than 2^8 in probability (then O and l
+        // are rescaled); below that, p <= 256 stays exact enough in fp32 and
+        // representable in the 16-bit P tile, and O / l is unchanged.
+        float alpha = 1.f;
+        if (m == -CUDART_INF_F) {
+          m = mx;  // first keys of this row (still -inf for a row without keys)
+        } else if ((mx - m) * sl2 > 8.f) {
+          alpha = exp2f((m - mx) * sl2);
+          m = mx;
+        }
+        const float neg = m == -CUDART_INF_F ? 0.f : -m * sl2;
         float rs = 0.f;
         uint32_t pk[32];
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            const float a = exp2f(__uint_as_float(sr[h][c]) - msub);
-            const float b = exp2f(__uint_as_float(sr[h][c + 1]) - msub);
+            const float a = exp2f(fmaf(__uint_as_float(sr[h][c]), sl2, neg));
+            const float b = exp2f(fmaf(__uint_as_float(sr[h][c + 1]), sl2, neg));
             rs += a + b;
             pk[h * 16 + c / 2] = MmaOp<T>::pack(a, b);
           }
         l = l * alpha + rs;
-        m = mn;
         // PV of the previous tile must be done before P and O are touched.
         if (j > 0 && !mbar_wait(b_odone, (g - 1) & 1, p.status)) { bad = true; break; }
         tc_fence_after();
@@ -443,8 +462,9 @@ __global__ void __launch_bounds__(pf::kThreads, NS <= 2 ? 2 : 1)
             }
           }
         } else {
-          // Partial of the prefix: running max m (log2 units), l = sum 2^(s - m)
-          // and o~ = sum 2^(s - m) v, into slot 0 of the member's partials.
+          // Partial of the prefix in log2 units: reference max m*scale*log2(e),
+          // l = sum 2^(s - m) and o~ = sum 2^(s - m) v, into slot 0 of the
+          // member's partials.
           const bool valid = lim >= 0;
           const int64_t base = ((int64_t)(s0 + pos) * p.num_q_heads + kvh * G + head) * p.max_parts;
 #pragma unroll
@@ -460,7 +480,7 @@ __global__ void __launch_bounds__(pf::kThreads, NS <= 2 ? 2 : 1)
                                    __uint_as_float(ov[c + 3])));
             }
           }
-          if (valid) __stcg(reinterpret_cast<float2*>(p.part_ml + base * 2), make_float2(m, l));
+          if (valid) __stcg(reinterpret_cast<float2*>(p.part_ml + base * 2), make_float2(m * sl2, l));
         }
       } else {
         bad = true;
