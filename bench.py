@@ -209,6 +209,23 @@ def profiled_traffic() -> float | None:
     return float(m_tr.group(1)) if sha == m_sha.group(1) else None
 
 
+def reduce_max_over_ranks(values, world: int, device="cpu") -> list[float]:
+    """Elementwise max of per-rank timings (the slowest rank sets the step
+    time); a no-op for one rank. The only collective of the bench: timing
+    bookkeeping, not data."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def weak_scaling_value(world: int, bytes_per_step: float, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank moves bytes_per_step per step (replicas)."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 def dist_info():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -409,10 +426,7 @@ def native_arm(args) -> None:
     wall_ms = (time.perf_counter() - t0) * 1000.0 / e2e_steps
 
     # Max over ranks.
-    vals = torch.tensor([ms_total, e2e_ms, statistics.mean(dec_ms)], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    ms_total, e2e_ms, dec_mean = vals.tolist()
+    ms_total, e2e_ms, dec_mean = reduce_max_over_ranks([ms_total, e2e_ms, statistics.mean(dec_ms)], world, "cuda")
     ms_step = ms_total / args.steps
 
     peak, peak_kind = measured_peak_hbm()
@@ -420,8 +434,8 @@ def native_arm(args) -> None:
         flops = prefill_flops(batch)
         tpeak, tkind = measured_peak_tensor()
         achieved_tf = flops / (dec_mean * 1e-3) / 1e12
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
-    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    value = weak_scaling_value(world, step_bytes, ms_step)
+    e2e_value = weak_scaling_value(world, step_bytes, e2e_ms)
     dec_gbs = dec_bytes["total"] / (dec_mean * 1e-3) / 1e9
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and st.is_decode:

@@ -1,0 +1,55 @@
+"""The bench's multi-rank path on CPU with gloo (world size 2): each rank is
+an independent replica; the step time is the max over ranks and the value
+counts every rank's bytes (weak scaling). No GPU needed."""
+from __future__ import annotations
+
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank: int, world: int, port: int, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+        mine = [1.0 + rank, 10.0 - rank, 0.5 * (rank + 1)]
+        got = bench.reduce_max_over_ranks(mine, world, "cpu")
+        dist.barrier()
+        q.put((rank, got, bench.weak_scaling_value(world, 2e9, got[0])))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_reduce_and_value_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, got, value in res:
+        assert got == [2.0, 10.0, 1.0]  # elementwise max over the two ranks
+        # 2 replicas x 2 GB each in 2 ms -> 2000 GB/s
+        assert abs(value - 2 * 2e9 / 2e-3 / 1e9) < 1e-6
+
+
+def test_single_rank_is_identity():
+    import bench
+    assert bench.reduce_max_over_ranks([3.0, 4.0], 1) == [3.0, 4.0]
+    assert bench.weak_scaling_value(1, 1e9, 1.0) == pytest.approx(1000.0)
