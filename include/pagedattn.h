@@ -293,6 +293,72 @@ int pa_chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_lens,
                        int32_t num_blocks, float scale, void* out, void* workspace, size_t workspace_bytes,
                        pa_dtype dtype, void* stream);
 
+/*
+ * FP8 (e4m3) KV cache with per-block scales ("Tech Radar: vLLM v1 Production
+ * Engine Architecture...", section 2, "Hopper TMA Warp Specialization & FP8
+ * Kernel Integration", item 3 "FP8 Block-Quantized Caching": keys and values
+ * are quantized dynamically to 8-bit floating point at block boundaries,
+ * halving the bytes per token; "High-Throughput Local LLM Infrastructure...",
+ * section 6, Q5: e4m3).
+ *   k_cache, v_cache : uint8 pools [num_blocks][num_kv_heads][block_size][head_dim]
+ *                      of e4m3 codes (OCP FP8 E4M3: bias 7, no infinity,
+ *                      largest finite 448)
+ *   kv_scales        : float32 [num_blocks][num_kv_heads][2], 16-byte aligned:
+ *                      the K (index 0) and V (index 1) scale of every (block,
+ *                      KV head) tile. Stored value = e4m3 value * scale.
+ * Scale rule of a cache write, per (block, KV head, pool), with a = the
+ * largest |x| the call writes into the block and o_min the lowest offset it
+ * writes there: s_old = 0 if o_min == 0 (the write starts the block afresh),
+ * else the stored scale; s_new = max(s_old, fl32(a / 448)); if s_new > s_old
+ * > 0 the codes at offsets < o_min are re-encoded as e4m3(fl32(value *
+ * fl32(s_old / s_new))); each new row is encoded as e4m3(fl32(x / s_new))
+ * (code 0 when s_new == 0). e4m3() rounds to nearest, ties to even, and
+ * saturates at +-448. Codes at offsets above the written ones are untouched.
+ */
+
+/*
+ * pa_reshape_and_cache_fp8 — cache write into the e4m3 pools.
+ *   k, v         : [num_tokens][num_kv_heads][head_dim] of dtype (fp32, fp16
+ *                  or bf16), 16-byte aligned
+ *   slot_mapping : int64 [num_tokens], as for pa_reshape_and_cache. All the
+ *                  tokens a call writes into one block must be consecutive
+ *                  entries of slot_mapping (entries with slot < 0 may sit
+ *                  between them): the order in which a batch lists each
+ *                  sequence's new tokens. Tokens of one block split into two
+ *                  separate runs race on that block's codes and scale (the
+ *                  result is unspecified; nothing outside the block is
+ *                  touched).
+ * head_dim must be 64 or 128 (PA_ERR_UNSUPPORTED). Bit-exact (see the rule
+ * above). Two tokens with the same slot: the later one in the list wins.
+ */
+int pa_reshape_and_cache_fp8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                             void* k_cache, void* v_cache, float* kv_scales, int32_t num_blocks, int32_t block_size,
+                             int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype, void* stream);
+
+/*
+ * pa_copy_blocks_fp8 — copy-on-write for the e4m3 pools: for every pair the
+ * whole K and V block and the block's 2 * num_kv_heads scales, dst <- src.
+ * Pairs are validated as for pa_copy_blocks (HOST array, PA_ERR_BLOCK_OOB,
+ * PA_ERR_ALIAS). Bit-exact.
+ */
+int pa_copy_blocks_fp8(void* k_cache, void* v_cache, float* kv_scales, const int64_t* src_dst_pairs,
+                       int32_t num_pairs, int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                       int32_t head_dim, void* stream);
+
+/*
+ * pa_decode_fp8 — pa_decode over the e4m3 pools: every stored value is the
+ * e4m3 code times its (block, KV head) scale, and the attention is that of
+ * pa_decode on those values. q and out are fp16 or bf16 (dtype;
+ * PA_ERR_DTYPE otherwise); head_dim must be 128 (PA_ERR_UNSUPPORTED). The
+ * workspace is pa_decode_workspace_size() bytes, as for pa_decode. Codes are
+ * widened to fp16 exactly; scores, softmax and accumulation are fp32.
+ */
+int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const float* kv_scales,
+                  const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                  int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t block_size, int32_t num_blocks, float scale, void* out, int32_t partition_size,
+                  void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

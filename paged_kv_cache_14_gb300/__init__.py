@@ -15,7 +15,9 @@ from ._binding import (  # noqa: F401
     pa_chunked_prefill,
     pa_chunked_prefill_workspace_size,
     pa_copy_blocks,
+    pa_copy_blocks_fp8,
     pa_decode,
+    pa_decode_fp8,
     pa_decode_noalloc,
     pa_decode_noalloc_scratch_limit,
     pa_decode_partition_size,
@@ -24,6 +26,7 @@ from ._binding import (  # noqa: F401
     pa_decode_workspace_size,
     pa_get_status,
     pa_reshape_and_cache,
+    pa_reshape_and_cache_fp8,
     pa_slot_mapping,
     pa_strerror,
     pa_version,

@@ -27,6 +27,7 @@ EXPORTS = (
     "pa_copy_blocks", "pa_decode_partition_size", "pa_decode_workspace_size", "pa_decode",
     "pa_chunked_prefill_workspace_size", "pa_chunked_prefill", "pa_decode_shared_prefix_workspace_size",
     "pa_decode_shared_prefix", "pa_decode_noalloc_scratch_limit", "pa_decode_noalloc",
+    "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8", "pa_decode_fp8",
 )
 
 _i32, _i64, _f32, _vp, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
@@ -70,6 +71,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "pa_decode_noalloc_scratch_limit": (_sz, []),
         "pa_decode_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                              _i32, _f32, _vp, _i32, ctypes.c_int, _vp]),
+        "pa_reshape_and_cache_fp8": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                                    ctypes.c_int, _vp]),
+        "pa_copy_blocks_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp]),
+        "pa_decode_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                         _i32, _f32, _vp, _i32, _vp, _sz, ctypes.c_int, _vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -277,4 +283,58 @@ def pa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         _cuda(seq_lens, "seq_lens", torch.int32), N, int(max_seq_len), hq, hkv, D, B, P, float(scale),
         _cuda(out, "out", dt), int(partition_size), _DT[dt], _stream(stream))
     _check(rc, "pa_decode_noalloc")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# e4m3 KV cache: uint8 code pools [P, Hkv, B, D] and float32 scales
+# [P, Hkv, 2] (K, V) per (block, KV head).
+# ---------------------------------------------------------------------------
+
+def pa_reshape_and_cache_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                             k_cache: torch.Tensor, v_cache: torch.Tensor, kv_scales: torch.Tensor,
+                             stream=None) -> None:
+    P, hkv, B, D = k_cache.shape
+    dt = k.dtype
+    rc = load().pa_reshape_and_cache_fp8(
+        _cuda(k, "k", dt), _cuda(v, "v", dt), _cuda(slot_mapping, "slot_mapping", torch.int64), k.shape[0],
+        _cuda(k_cache, "k_cache", torch.uint8), _cuda(v_cache, "v_cache", torch.uint8),
+        _cuda(kv_scales, "kv_scales", torch.float32), P, B, hkv, D, _DT[dt], _stream(stream))
+    _check(rc, "pa_reshape_and_cache_fp8")
+
+
+def pa_copy_blocks_fp8(k_cache: torch.Tensor, v_cache: torch.Tensor, kv_scales: torch.Tensor, src_dst_pairs,
+                       stream=None) -> None:
+    """src_dst_pairs: HOST int64 [n, 2] (numpy array, list or CPU tensor)."""
+    pairs = np.ascontiguousarray(np.asarray(src_dst_pairs, dtype=np.int64).reshape(-1, 2))
+    P, hkv, B, D = k_cache.shape
+    rc = load().pa_copy_blocks_fp8(
+        _cuda(k_cache, "k_cache", torch.uint8), _cuda(v_cache, "v_cache", torch.uint8),
+        _cuda(kv_scales, "kv_scales", torch.float32), pairs.ctypes.data_as(ctypes.c_void_p), pairs.shape[0], P, B,
+        hkv, D, _stream(stream))
+    _check(rc, "pa_copy_blocks_fp8")
+
+
+def pa_decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, kv_scales: torch.Tensor,
+                  block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int, scale: float,
+                  out: torch.Tensor | None = None, partition_size: int = 0, workspace: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    N, hq, D = q.shape
+    P, hkv, B, D2 = k_cache.shape
+    if D2 != D:
+        raise ValueError("q and k_cache head_dim differ")
+    dt = q.dtype
+    if out is None:
+        out = torch.empty_like(q)
+    need = pa_decode_workspace_size(N, hq, hkv, D, B, max_seq_len, partition_size)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load().pa_decode_fp8(
+        _cuda(q, "q", dt), _cuda(k_cache, "k_cache", torch.uint8), _cuda(v_cache, "v_cache", torch.uint8),
+        _cuda(kv_scales, "kv_scales", torch.float32), _cuda(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _cuda(seq_lens, "seq_lens", torch.int32), N, int(max_seq_len), hq, hkv, D, B, P,
+        float(scale), _cuda(out, "out", dt), int(partition_size), ws_ptr, ws_bytes, _DT[dt], _stream(stream))
+    _check(rc, "pa_decode_fp8")
     return out

@@ -111,6 +111,19 @@ int make_3d_tensor_map(CUtensorMap* map, const void* base, int64_t d2, int64_t d
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+int make_u8_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t head_dim, int32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  cuuint64_t gdim[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+  cuuint64_t gstride[1] = {(cuuint64_t)head_dim};
+  cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 int make_kv_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t head_dim, pa_dtype dt,
                        int32_t box_rows) {
   return make_2d_tensor_map(map, base, rows, head_dim, head_dim, dt, box_rows, 64);
@@ -335,6 +348,63 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
   return decode_common(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
                        max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out,
                        partition_size, workspace, workspace_bytes, dtype, static_cast<cudaStream_t>(stream));
+}
+
+int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const float* kv_scales,
+                  const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                  int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t block_size, int32_t num_blocks, float scale, void* out, int32_t partition_size,
+                  void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+  DecodeParams p;
+  DecodeWorkspace wl;
+  const int rc = decode_prepare(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
+                                max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out,
+                                partition_size, 0, workspace, workspace_bytes, dtype, &p, &wl);
+  if (rc != PA_OK || num_seqs == 0) return rc;
+  if (!kv_scales) return PA_ERR_ARG;
+  if (!aligned16(kv_scales)) return PA_ERR_ALIGN;
+  p.kv_scales = kv_scales;
+  return launch_decode(p, dtype, static_cast<cudaStream_t>(stream));
+}
+
+int pa_reshape_and_cache_fp8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                             void* k_cache, void* v_cache, float* kv_scales, int32_t num_blocks, int32_t block_size,
+                             int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype, void* stream) {
+  if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 1) return PA_ERR_ARG;
+  if (block_size != 16 && block_size != 32) return PA_ERR_BLOCKSIZE;
+  if (!elem_bytes(dtype)) return PA_ERR_DTYPE;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache || !kv_scales) return PA_ERR_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(kv_scales))
+    return PA_ERR_ALIGN;
+  int* st = device_status_ptr();
+  if (!st) return PA_ERR_CUDA;
+  return launch_reshape_and_cache_fp8(k, v, slot_mapping, num_tokens, static_cast<uint8_t*>(k_cache),
+                                      static_cast<uint8_t*>(v_cache), kv_scales, num_blocks, block_size,
+                                      num_kv_heads, head_dim, dtype, st, static_cast<cudaStream_t>(stream));
+}
+
+int pa_copy_blocks_fp8(void* k_cache, void* v_cache, float* kv_scales, const int64_t* src_dst_pairs,
+                       int32_t num_pairs, int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                       int32_t head_dim, void* stream) {
+  if (num_pairs < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 1) return PA_ERR_ARG;
+  if (block_size != 16 && block_size != 32) return PA_ERR_BLOCKSIZE;
+  if (num_pairs == 0) return PA_OK;
+  if (!kv_scales) return PA_ERR_ARG;
+  const int64_t block_bytes = (int64_t)num_kv_heads * block_size * head_dim;
+  // Codes first (validates the pairs), then the scales of the same pairs.
+  const int rc = pa_copy_blocks(k_cache, v_cache, src_dst_pairs, num_pairs, num_blocks, block_bytes, stream);
+  if (rc != PA_OK) return rc;
+  std::vector<int32_t> src(num_pairs), dst(num_pairs);
+  for (int32_t i = 0; i < num_pairs; ++i) {
+    src[i] = (int32_t)src_dst_pairs[2 * i];
+    dst[i] = (int32_t)src_dst_pairs[2 * i + 1];
+  }
+  return launch_copy_scales(kv_scales, src.data(), dst.data(), num_pairs, num_kv_heads,
+                            static_cast<cudaStream_t>(stream));
 }
 
 size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,

@@ -6,6 +6,11 @@
 
 namespace pa {
 
+struct CopyPairsScales {
+  int32_t src[kCopyPairsPerLaunch];
+  int32_t dst[kCopyPairsPerLaunch];
+};
+
 // slot = block_tables[seq][pos / B] * B + pos % B (logical block index and
 // block offset, section 1.2 of the "High-Throughput Local LLM
 // Infrastructure" page).
@@ -59,6 +64,172 @@ __global__ void reshape_and_cache_kernel(const uint8_t* __restrict__ k, const ui
       vd[i] = vs[i];
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// e4m3 cache write with one scale per (block, KV head) and pool. The rows a
+// call writes into one block are consecutive entries of the slot mapping
+// (padding entries may sit between them); the first of them leads a warp
+// per (KV head, pool) that
+//   1. takes a = the largest |x| of the run's rows and the lowest written
+//      offset o_min;
+//   2. forms s_new = max(s_old, a / 448), with s_old = 0 when the run
+//      touches offset 0 (the block starts afresh), else the stored scale;
+//   3. if the scale grew (and s_old > 0), re-encodes the codes at offsets
+//      below o_min (the tokens already in the block) with ratio s_old / s_new;
+//   4. encodes every row of the run as e4m3(x / s_new) and stores s_new.
+// Each step is one IEEE single-precision operation (division and product
+// rounded to nearest) followed by the round-to-nearest-even, saturating
+// conversion to e4m3, so the codes are reproducible bit for bit.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_c(uint16_t c) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(c));
+  return d;
+}
+
+// Two floats to two e4m3 codes: lo in the low byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int VEC>
+__device__ __forceinline__ void store_codes(uint8_t* dst, const uint32_t (&c)[VEC / 2]) {
+  if constexpr (VEC == 2) {
+    *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(c[0]);
+  } else if constexpr (VEC == 4) {
+    *reinterpret_cast<uint32_t*>(dst) = c[0] | (c[1] << 16);
+  }
+}
+
+template <int VEC>
+__device__ __forceinline__ void load_codes(const uint8_t* src, float (&x)[VEC]) {
+  uint32_t w;
+  if constexpr (VEC == 2) w = *reinterpret_cast<const uint16_t*>(src);
+  else w = *reinterpret_cast<const uint32_t*>(src);
+#pragma unroll
+  for (int i = 0; i < VEC; i += 2) {
+    const uint32_t h2 = e4m3x2_to_f16x2_c(static_cast<uint16_t>(w >> (8 * i)));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+    x[i] = f.x;
+    x[i + 1] = f.y;
+  }
+}
+
+template <typename TI, int VEC>
+__global__ void __launch_bounds__(256) reshape_and_cache_fp8_kernel(
+    const TI* __restrict__ k, const TI* __restrict__ v, const int64_t* __restrict__ slot_mapping, int64_t num_tokens,
+    uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache, float* __restrict__ kv_scales, int32_t num_blocks,
+    int32_t block_size, int32_t num_kv_heads, int* status) {
+  constexpr int D = VEC * 32;
+  constexpr unsigned kFull = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t cap = (int64_t)num_blocks * block_size;
+  const int64_t total = num_tokens * num_kv_heads * 2;
+  for (int64_t w = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); w < total; w += warps) {
+    const int64_t t = w / (num_kv_heads * 2);
+    const int rem = (int)(w - t * num_kv_heads * 2);
+    const int h = rem >> 1, pool = rem & 1;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;  // padding token
+    if (slot >= cap) {
+      if (lane == 0 && rem == 0) record_error(status, PA_ERR_BLOCK_OOB);
+      continue;
+    }
+    const int64_t blk = slot / block_size;
+    // Lead only if the nearest earlier token with a valid slot lies in
+    // another block (or there is none).
+    bool leader = true;
+    for (int64_t base = t - 1; base >= 0; base -= 32) {
+      const int64_t j = base - lane;
+      const int64_t sj = j >= 0 ? slot_mapping[j] : -1;
+      const unsigned ok = __ballot_sync(kFull, j >= 0 && sj >= 0 && sj < cap);
+      if (ok) {
+        const int64_t sf = __shfl_sync(kFull, sj, __ffs(ok) - 1);  // lowest lane = latest token
+        leader = sf / block_size != blk;
+        break;
+      }
+    }
+    if (!leader) continue;
+    const TI* src = pool == 0 ? k : v;
+    uint8_t* codes = (pool == 0 ? k_cache : v_cache) + (blk * num_kv_heads + h) * (int64_t)block_size * D;
+    // 1. The run's rows: amax and the lowest offset; `end` = one past the run.
+    float amax = 0.f;
+    int omin = block_size;
+    int64_t end = num_tokens;
+    for (int64_t base = t; base < num_tokens; base += 32) {
+      const int64_t j = base + lane;
+      const int64_t sj = j < num_tokens ? slot_mapping[j] : -1;
+      const bool okj = j < num_tokens && sj >= 0 && sj < cap;
+      const unsigned other = __ballot_sync(kFull, okj && sj / block_size != blk);
+      const int lim = other ? __ffs(other) - 1 : 32;
+      unsigned mem = __ballot_sync(kFull, okj && sj / block_size == blk && lane < lim);
+      while (mem) {
+        const int ln = __ffs(mem) - 1;
+        mem &= mem - 1;
+        const int64_t sm = __shfl_sync(kFull, sj, ln);
+        omin = min(omin, (int)(sm - blk * block_size));
+        const TI* row = src + ((base + ln) * num_kv_heads + h) * D + lane * VEC;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) amax = fmaxf(amax, fabsf(to_f32(row[i])));
+      }
+      if (other) {
+        end = base + lim;
+        break;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+    // 2. The block's new scale.
+    float* sp = kv_scales + (blk * num_kv_heads + h) * 2 + pool;
+    const float s_old = omin == 0 ? 0.f : *sp;
+    const float s_new = fmaxf(s_old, __fdiv_rn(amax, 448.f));
+    // 3. Re-encode the tokens already in the block if the scale grew.
+    if (s_new > s_old && s_old > 0.f && omin > 0) {
+      const float r = __fdiv_rn(s_old, s_new);
+      for (int o = 0; o < omin; ++o) {
+        uint8_t* cp = codes + (int64_t)o * D + lane * VEC;
+        float x[VEC];
+        load_codes<VEC>(cp, x);
+        uint32_t c[VEC / 2];
+#pragma unroll
+        for (int i = 0; i < VEC; i += 2) c[i / 2] = f32x2_to_e4m3x2(__fmul_rn(x[i], r), __fmul_rn(x[i + 1], r));
+        store_codes<VEC>(cp, c);
+      }
+    }
+    // 4. Encode the run's rows.
+    for (int64_t base = t; base < end; base += 32) {
+      const int64_t j = base + lane;
+      const int64_t sj = j < end ? slot_mapping[j] : -1;
+      unsigned mem = __ballot_sync(kFull, j < end && sj >= 0 && sj < cap && sj / block_size == blk);
+      while (mem) {
+        const int ln = __ffs(mem) - 1;
+        mem &= mem - 1;
+        const int64_t sm = __shfl_sync(kFull, sj, ln);
+        const TI* row = src + ((base + ln) * num_kv_heads + h) * D + lane * VEC;
+        uint32_t c[VEC / 2];
+#pragma unroll
+        for (int i = 0; i < VEC; i += 2) {
+          const float x0 = to_f32(row[i]), x1 = to_f32(row[i + 1]);
+          c[i / 2] = s_new > 0.f ? f32x2_to_e4m3x2(__fdiv_rn(x0, s_new), __fdiv_rn(x1, s_new)) : 0u;
+        }
+        store_codes<VEC>(codes + (sm - blk * block_size) * D + lane * VEC, c);
+      }
+    }
+    if (lane == 0) *sp = s_new;
+  }
+}
+
+// grid = num_pairs: the 2 * num_kv_heads scales of block dst <- those of src.
+__global__ void __launch_bounds__(256) copy_scales_kernel(float* __restrict__ kv_scales,
+                                                          const __grid_constant__ CopyPairsScales pairs,
+                                                          int32_t per_block) {
+  const float* src = kv_scales + (int64_t)pairs.src[blockIdx.x] * per_block;
+  float* dst = kv_scales + (int64_t)pairs.dst[blockIdx.x] * per_block;
+  for (int i = threadIdx.x; i < per_block; i += blockDim.x) dst[i] = src[i];
 }
 
 struct CopyPairs {
@@ -126,6 +297,43 @@ int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const i
     }
     copy_blocks_kernel<<<dim3(n, 2), 256, 0, stream>>>(static_cast<uint8_t*>(k_cache),
                                                        static_cast<uint8_t*>(v_cache), pairs, block_bytes);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+int launch_reshape_and_cache_fp8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                                 uint8_t* k_cache, uint8_t* v_cache, float* kv_scales, int32_t num_blocks,
+                                 int32_t block_size, int32_t num_kv_heads, int32_t head_dim, pa_dtype dt,
+                                 int* status, cudaStream_t stream) {
+  const int64_t warps = num_tokens * num_kv_heads * 2;
+  const int grid = grid_for(warps, 8);
+#define PA_RC8(TI, VEC)                                                                                          \
+  reshape_and_cache_fp8_kernel<TI, VEC><<<grid, 256, 0, stream>>>(                                               \
+      static_cast<const TI*>(k), static_cast<const TI*>(v), slot_mapping, num_tokens, k_cache, v_cache, kv_scales, \
+      num_blocks, block_size, num_kv_heads, status)
+  const bool d128 = head_dim == 128;
+  if (dt == PA_BF16) {
+    if (d128) PA_RC8(__nv_bfloat16, 4); else PA_RC8(__nv_bfloat16, 2);
+  } else if (dt == PA_F16) {
+    if (d128) PA_RC8(__half, 4); else PA_RC8(__half, 2);
+  } else {
+    if (d128) PA_RC8(float, 4); else PA_RC8(float, 2);
+  }
+#undef PA_RC8
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int launch_copy_scales(float* kv_scales, const int32_t* src, const int32_t* dst, int32_t num_pairs,
+                       int32_t num_kv_heads, cudaStream_t stream) {
+  for (int32_t base = 0; base < num_pairs; base += kCopyPairsPerLaunch) {
+    const int32_t n = num_pairs - base < kCopyPairsPerLaunch ? num_pairs - base : kCopyPairsPerLaunch;
+    CopyPairsScales pairs;
+    for (int32_t i = 0; i < n; ++i) {
+      pairs.src[i] = src[base + i];
+      pairs.dst[i] = dst[base + i];
+    }
+    copy_scales_kernel<<<n, 256, 0, stream>>>(kv_scales, pairs, 2 * num_kv_heads);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;

@@ -55,6 +55,14 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
   return d;
 }
 
+// Two e4m3 codes (low byte first) to an fp16 pair (low half first); exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
+  uint32_t d;
+  const uint16_t c = static_cast<uint16_t>(codes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(c));
+  return d;
+}
+
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -94,10 +102,12 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
 // V (a block of 32 tokens fills two stages). Stage s is only ever consumed
 // by consumer warp s % 4, so each stage's mbarrier is waited on in phase
 // order by one warp (a parity wait can never alias a phase not yet begun).
-template <int D, int BS, int NT>
+template <int D, int BS, int NT, bool KV8 = false>
 struct DecCfg {
-  static constexpr int kHalves = D / 64;              // 128-byte swizzle boxes across head_dim
-  static constexpr int kTile = 16 * D * 2;            // 16 tokens x head_dim of K (or V)
+  static constexpr int kEsz = KV8 ? 1 : 2;            // bytes per cached element
+  static constexpr int kBoxCols = 128 / kEsz;         // elements in one 128-byte TMA box row
+  static constexpr int kHalves = D * kEsz / 128;      // 128-byte swizzle boxes across head_dim
+  static constexpr int kTile = 16 * D * kEsz;         // 16 tokens x head_dim of K (or V)
   static constexpr int kStage = 2 * kTile;            // K + V
   static constexpr int kStages = PA_DECODE_RING_BYTES / kStage;
   static constexpr int kHeads = NT * 8;               // query heads per item (MMA N)
@@ -114,7 +124,8 @@ struct DecCfg {
   static constexpr size_t kValid = kMeta + (size_t)kSlots * 16 * 4;
   static constexpr size_t kBars = (kValid + (size_t)kStages * 4 + 7) & ~size_t(7);
   static constexpr size_t kFlags = kBars + (size_t)(2 * kStages + 2 * kSlots) * 8;
-  static constexpr size_t kSmem = kFlags + 16 + 1024;  // + alignment slack
+  static constexpr size_t kScl = kFlags + 16;          // e4m3 cache: (K, V) scale of each stage's block
+  static constexpr size_t kSmem = kScl + (KV8 ? (size_t)kStages * 8 : 0) + 1024;  // + alignment slack
   static_assert(kStages % kConsumers == 0, "stage s belongs to consumer warp s % 4");
   static_assert(BS % 16 == 0, "block size must be a multiple of 16");
 };
@@ -130,11 +141,11 @@ struct ItemMeta {
   int seq, qrow, h0, nrows, t_begin, t_end, nsub, jstart, part, n_parts, hg, out_mode, pad[4];
 };
 
-template <typename T, int D, int BS, int NT>
-__global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
+template <typename T, int D, int BS, int NT, bool KV8>
+__global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 : 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                      const DecodeParams p) {
-  using C = DecCfg<D, BS, NT>;
+  using C = DecCfg<D, BS, NT, KV8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   ItemMeta* meta = reinterpret_cast<ItemMeta*>(smem + C::kMeta);
@@ -145,6 +156,7 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
   uint64_t* iempty = ifull + C::kSlots;
   float* scratch = reinterpret_cast<float*>(smem + C::kScratch);
   float* ml = reinterpret_cast<float*>(smem + C::kMl);
+  float2* stage_scale = reinterpret_cast<float2*>(smem + C::kScl);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hr = p.num_kv_heads * p.row_groups;
@@ -238,24 +250,35 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
       }
       const int32_t* bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq + t_begin / BS;
       for (int ub = 0; ub < nsub_pad && !bad; ub += 32) {
-        // Lane k holds the physical block of sub-tile ub + k (-1: padding).
+        // Lane k holds the physical block of sub-tile ub + k (-1: padding)
+        // and, for an e4m3 cache, that block's (K, V) scales.
         int id = -1;
+        float2 bsc = make_float2(0.f, 0.f);
         if (ub + lane < nsub) {
           id = bt[(ub + lane) / kSubPerBlock];
           if (id < 0 || id >= p.num_blocks) {
             record_error(p.status, PA_ERR_BLOCK_OOB);
             id = -1;
           }
+          if constexpr (KV8) {
+            if (id >= 0) bsc = __ldg(reinterpret_cast<const float2*>(p.kv_scales) + (int64_t)id * p.num_kv_heads + kvh);
+          }
         }
         const int cnt = min(32, nsub_pad - ub);
         for (int k = 0; k < cnt; ++k) {
           const int idk = __shfl_sync(0xffffffffu, id, k);
+          float2 sck = make_float2(0.f, 0.f);
+          if constexpr (KV8) {
+            sck.x = __shfl_sync(0xffffffffu, bsc.x, k);
+            sck.y = __shfl_sync(0xffffffffu, bsc.y, k);
+          }
           if (lane == 0) {
             const int s = jg % C::kStages;
             if (jg >= C::kStages && !mbar_wait(smem_u32(&empty[s]), ((jg / C::kStages) & 1) ^ 1, p.status)) {
               bad = true;
             } else {
               stage_valid[s] = idk >= 0;
+              if constexpr (KV8) stage_scale[s] = sck;  // published by the arrive below
               const uint32_t fb = smem_u32(&full[s]);
               if (idk >= 0) {
                 mbar_arrive_expect_tx(fb, C::kStage);
@@ -263,8 +286,8 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
                 const uint32_t kd = ring0 + s * C::kStage;
 #pragma unroll
                 for (int hf = 0; hf < C::kHalves; ++hf) {
-                  tma_load_2d(kd + hf * 2048, &kmap, hf * 64, row, fb);
-                  tma_load_2d(kd + C::kTile + hf * 2048, &vmap, hf * 64, row, fb);
+                  tma_load_2d(kd + hf * 2048, &kmap, hf * C::kBoxCols, row, fb);
+                  tma_load_2d(kd + C::kTile + hf * 2048, &vmap, hf * C::kBoxCols, row, fb);
                 }
               } else {
                 mbar_arrive(fb);
@@ -314,7 +337,10 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
     if (mt.seq < 0) break;
     // Q^T fragments (B operand: k = dims, n = heads) from the item slot.
     uint32_t qf[D / 16][NT][2];
-    {
+    // e4m3 cache: 2^e for the head of each accumulator column, undoing the
+    // power-of-two scaling that brought that head's query row into fp16.
+    float qsh[NT][2];
+    if constexpr (!KV8) {
       const uint32_t qs = smem_u32(smem + C::kQ + slot * C::kQBytes);
 #pragma unroll
       for (int kk = 0; kk < D / 16; kk += 2)
@@ -325,6 +351,46 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
           ldsm_x4(qs + head * (D * 2) + chunk * 16, qf[kk][nt][0], qf[kk][nt][1], qf[kk + 1][nt][0],
                   qf[kk + 1][nt][1]);
         }
+    } else {
+      // The e4m3 K fragments hold head_dim elements 16c + 4t .. 16c + 4t + 3
+      // of a token in MMA k slots (2t, 2t+1, 2t+8, 2t+9) (see below), so the
+      // query takes the same order: lane (g, t) reads 4 consecutive elements
+      // of head g per 16-wide chunk. The MMA runs in fp16; a bf16 query row
+      // is scaled by 2^-e (e from its largest magnitude) so that it fits
+      // fp16's range with bf16's precision, and the scores are scaled back.
+      const uint8_t* qs = smem + C::kQ + slot * C::kQBytes;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const T* row = reinterpret_cast<const T*>(qs) + (nt * 8 + tr) * D;
+        float v[D / 16][4];
+        float amax = 0.f;
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(row + c * 16 + 4 * ti);
+          const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            v[c][i] = to_f32(e[i]);
+            amax = fmaxf(amax, fabsf(v[c][i]));
+          }
+        }
+        int sh = 0;
+        if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+          int ex = 0;
+          frexpf(amax, &ex);
+          sh = amax > 0.f ? ex - 15 : 0;  // amax * 2^-sh in [2^14, 2^15)
+        }
+        const float mul = ldexpf(1.f, -sh);
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+          qf[c][nt][0] = MmaOp<__half>::pack(v[c][0] * mul, v[c][1] * mul);
+          qf[c][nt][1] = MmaOp<__half>::pack(v[c][2] * mul, v[c][3] * mul);
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) qsh[nt][c] = ldexpf(1.f, __shfl_sync(0xffffffffu, sh, (2 * ti + c) * 4));
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&iempty[slot]));
@@ -337,6 +403,11 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
     float m[NT][2], l[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) m[nt][0] = m[nt][1] = -CUDART_INF_F, l[nt][0] = l[nt][1] = 0.f;
+    // e4m3 cache: O accumulates p * s_V(block) * 2^kap * code, with kap the
+    // largest exponent that keeps s_V * 2^kap <= 2^15 for every block seen
+    // so far (so p * s_V * 2^kap fits fp16); kap only decreases, and O is
+    // rescaled by the exact power of two when it does.
+    int kap = 1 << 20;
 
     const int jend = mt.jstart + mt.nsub;
     bool bad = false;
@@ -353,49 +424,94 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
       // stage back at once: the producer refills it while this warp
       // computes, so the ring's bytes stay in flight.
       uint32_t ka[D / 16][4], va[D / 16][4];
+      float2 bscale = make_float2(0.f, 0.f);
       if (valid) {
         const uint32_t kb = ring0 + s * C::kStage;
         const uint32_t vb = kb + C::kTile;
-        const int tk_a = (mi & 1) * 8 + rr;   // K rows as the A operand (non-transposed)
-        const int tk_v = (mi >> 1) * 8 + rr;  // V rows, transposed into the A operand
+        if constexpr (!KV8) {
+          const int tk_a = (mi & 1) * 8 + rr;   // K rows as the A operand (non-transposed)
+          const int tk_v = (mi >> 1) * 8 + rr;  // V rows, transposed into the A operand
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int cg = kk * 2 + (mi >> 1);
-          ldsm_x4(kb + (cg >> 3) * 2048 + tk_a * 128 + (((cg & 7) ^ (tk_a & 7)) << 4), ka[kk][0], ka[kk][1],
-                  ka[kk][2], ka[kk][3]);
-        }
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int cg = kk * 2 + (mi >> 1);
+            ldsm_x4(kb + (cg >> 3) * 2048 + tk_a * 128 + (((cg & 7) ^ (tk_a & 7)) << 4), ka[kk][0], ka[kk][1],
+                    ka[kk][2], ka[kk][3]);
+          }
 #pragma unroll
-        for (int a = 0; a < D / 16; ++a) {
-          const int cg = a * 2 + (mi & 1);
-          ldsm_x4_t(vb + (cg >> 3) * 2048 + tk_v * 128 + (((cg & 7) ^ (tk_v & 7)) << 4), va[a][0], va[a][1],
-                    va[a][2], va[a][3]);
+          for (int a = 0; a < D / 16; ++a) {
+            const int cg = a * 2 + (mi & 1);
+            ldsm_x4_t(vb + (cg >> 3) * 2048 + tk_v * 128 + (((cg & 7) ^ (tk_v & 7)) << 4), va[a][0], va[a][1],
+                      va[a][2], va[a][3]);
+          }
+        } else {
+          // 8x16-byte matrices: lane group mi reads tokens (mi & 1) * 8 + rr
+          // of 16-byte chunk 2q + (mi >> 1). The raw codes go to ka/va[2q..]
+          // and are widened after the stage is released.
+          const int tk = (mi & 1) * 8 + rr;
+#pragma unroll
+          for (int q2 = 0; q2 < D / 32; ++q2) {
+            const int cg = 2 * q2 + (mi >> 1);
+            const uint32_t off = (cg >> 3) * 2048 + tk * 128 + (((cg & 7) ^ (tk & 7)) << 4);
+            ldsm_x4(kb + off, ka[2 * q2][0], ka[2 * q2][1], ka[2 * q2][2], ka[2 * q2][3]);
+            ldsm_x4_t(vb + off, va[2 * q2][0], va[2 * q2][1], va[2 * q2][2], va[2 * q2][3]);
+          }
+          bscale = stage_scale[s];
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
       if (valid) {
         const int tok0 = mt.t_begin + (j - mt.jstart) * 16;
+        if constexpr (KV8) {
+          // K: matrix (tokens 0-7 | 8-15) x (chunk 2q | 2q+1) gives lane (g, t)
+          // elements 4t..4t+3 of token g (or g+8). Widen to fp16 pairs:
+          // A rows g / g+8, k slots (2t, 2t+1) <- elements (4t, 4t+1),
+          // k slots (2t+8, 2t+9) <- elements (4t+2, 4t+3).
+          // V (transposed load): lane (g, t) gets elements (2g, 2g+1) of
+          // tokens 2t and 2t+1; a byte permute pairs the tokens per element,
+          // so A row g <- element 2g and row g+8 <- element 2g+1 of the
+          // chunk, k slots = the tokens.
+#pragma unroll
+          for (int q2 = D / 32 - 1; q2 >= 0; --q2) {
+            const uint32_t k0 = ka[2 * q2][0], k1 = ka[2 * q2][1], k2 = ka[2 * q2][2], k3 = ka[2 * q2][3];
+            ka[2 * q2][0] = e4m3x2_to_f16x2(k0 & 0xffffu);
+            ka[2 * q2][1] = e4m3x2_to_f16x2(k1 & 0xffffu);
+            ka[2 * q2][2] = e4m3x2_to_f16x2(k0 >> 16);
+            ka[2 * q2][3] = e4m3x2_to_f16x2(k1 >> 16);
+            ka[2 * q2 + 1][0] = e4m3x2_to_f16x2(k2 & 0xffffu);
+            ka[2 * q2 + 1][1] = e4m3x2_to_f16x2(k3 & 0xffffu);
+            ka[2 * q2 + 1][2] = e4m3x2_to_f16x2(k2 >> 16);
+            ka[2 * q2 + 1][3] = e4m3x2_to_f16x2(k3 >> 16);
+          }
+        }
         // S^T = K Q^T: rows = 16 tokens, columns = heads. Two accumulator
         // chains over the head_dim halves shorten the dependent MMA chain.
         float sc[NT][4], sc2[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
           sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = sc2[nt][0] = sc2[nt][1] = sc2[nt][2] = sc2[nt][3] = 0.f;
+        using MT = typename std::conditional<KV8, __half, T>::type;
 #pragma unroll
         for (int kk = 0; kk < D / 16; kk += 2)
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            MmaOp<T>::run(sc[nt], ka[kk], qf[kk][nt][0], qf[kk][nt][1]);
-            MmaOp<T>::run(sc2[nt], ka[kk + 1], qf[kk + 1][nt][0], qf[kk + 1][nt][1]);
+            MmaOp<MT>::run(sc[nt], ka[kk], qf[kk][nt][0], qf[kk][nt][1]);
+            MmaOp<MT>::run(sc2[nt], ka[kk + 1], qf[kk + 1][nt][0], qf[kk + 1][nt][1]);
           }
-        // Scale to log2 units, mask keys past the partition end.
+        // Scale to log2 units (and, for e4m3, by the block's K scale and the
+        // query rows' exponents), mask keys past the partition end.
+        float fs[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) fs[nt][c] = KV8 ? sl2 * bscale.x * qsh[nt][c] : sl2;
         const int t_lo = tok0 + tr, t_hi = tok0 + tr + 8;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          sc[nt][0] = t_lo < mt.t_end ? (sc[nt][0] + sc2[nt][0]) * sl2 : -CUDART_INF_F;
-          sc[nt][1] = t_lo < mt.t_end ? (sc[nt][1] + sc2[nt][1]) * sl2 : -CUDART_INF_F;
-          sc[nt][2] = t_hi < mt.t_end ? (sc[nt][2] + sc2[nt][2]) * sl2 : -CUDART_INF_F;
-          sc[nt][3] = t_hi < mt.t_end ? (sc[nt][3] + sc2[nt][3]) * sl2 : -CUDART_INF_F;
+          sc[nt][0] = t_lo < mt.t_end ? (sc[nt][0] + sc2[nt][0]) * fs[nt][0] : -CUDART_INF_F;
+          sc[nt][1] = t_lo < mt.t_end ? (sc[nt][1] + sc2[nt][1]) * fs[nt][1] : -CUDART_INF_F;
+          sc[nt][2] = t_hi < mt.t_end ? (sc[nt][2] + sc2[nt][2]) * fs[nt][0] : -CUDART_INF_F;
+          sc[nt][3] = t_hi < mt.t_end ? (sc[nt][3] + sc2[nt][3]) * fs[nt][1] : -CUDART_INF_F;
         }
         // Online softmax per head column (max over the 16 tokens = over
         // the 8 lanes that share lane % 4).
@@ -420,6 +536,24 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
             l[nt][c] = l[nt][c] * alpha[nt][c] + (p0 + p1);
             m[nt][c] = mn;
           }
+        // e4m3: the weight of this block's V codes, p * s_V * 2^kap.
+        float fv = 1.f;
+        if constexpr (KV8) {
+          fv = 0.f;
+          if (bscale.y > 0.f) {
+            int ex = 0;
+            frexpf(bscale.y, &ex);  // s_V in [2^(ex-1), 2^ex)
+            const int kmax = 15 - ex;
+            if (kmax < kap) {
+              const float r = ldexpf(1.f, kmax - kap);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) alpha[nt][0] *= r, alpha[nt][1] *= r;
+              rescale = true;
+              kap = kmax;
+            }
+            fv = ldexpf(bscale.y, kap);
+          }
+        }
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
           for (int a = 0; a < D / 16; ++a)
@@ -435,8 +569,28 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
         uint32_t pb[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          pb[nt][0] = movmatrix_trans(MmaOp<T>::pack(sc[nt][0], sc[nt][1]));
-          pb[nt][1] = movmatrix_trans(MmaOp<T>::pack(sc[nt][2], sc[nt][3]));
+          if constexpr (KV8) {
+            pb[nt][0] = movmatrix_trans(MmaOp<__half>::pack(sc[nt][0] * fv, sc[nt][1] * fv));
+            pb[nt][1] = movmatrix_trans(MmaOp<__half>::pack(sc[nt][2] * fv, sc[nt][3] * fv));
+          } else {
+            pb[nt][0] = movmatrix_trans(MmaOp<T>::pack(sc[nt][0], sc[nt][1]));
+            pb[nt][1] = movmatrix_trans(MmaOp<T>::pack(sc[nt][2], sc[nt][3]));
+          }
+        }
+        if constexpr (KV8) {
+#pragma unroll
+          for (int q2 = D / 32 - 1; q2 >= 0; --q2) {
+            const uint32_t v0 = __byte_perm(va[2 * q2][0], 0, 0x3120), v1 = __byte_perm(va[2 * q2][1], 0, 0x3120);
+            const uint32_t v2 = __byte_perm(va[2 * q2][2], 0, 0x3120), v3 = __byte_perm(va[2 * q2][3], 0, 0x3120);
+            va[2 * q2][0] = e4m3x2_to_f16x2(v0 & 0xffffu);
+            va[2 * q2][1] = e4m3x2_to_f16x2(v0 >> 16);
+            va[2 * q2][2] = e4m3x2_to_f16x2(v1 & 0xffffu);
+            va[2 * q2][3] = e4m3x2_to_f16x2(v1 >> 16);
+            va[2 * q2 + 1][0] = e4m3x2_to_f16x2(v2 & 0xffffu);
+            va[2 * q2 + 1][1] = e4m3x2_to_f16x2(v2 >> 16);
+            va[2 * q2 + 1][2] = e4m3x2_to_f16x2(v3 & 0xffffu);
+            va[2 * q2 + 1][3] = e4m3x2_to_f16x2(v3 >> 16);
+          }
         }
         // Keys past the end carry p = 0, but their V slots may hold any
         // bits (NaN included): zero those V elements so 0 * V stays 0.
@@ -456,7 +610,7 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
 #pragma unroll
         for (int a = 0; a < D / 16; ++a)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) MmaOp<T>::run(o[a][nt], va[a], pb[nt][0], pb[nt][1]);
+          for (int nt = 0; nt < NT; ++nt) MmaOp<MT>::run(o[a][nt], va[a], pb[nt][0], pb[nt][1]);
       }
     }
     if (named_barrier_or(1, C::kConsumers * 32, bad)) break;
@@ -486,12 +640,20 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT>::kThreads, NT == 1 ? 2 : 1)
         float M = -CUDART_INF_F;
 #pragma unroll
         for (int w = 0; w < C::kConsumers; ++w) M = fmaxf(M, ml[(w * C::kHeads + h) * 2]);
-        const float f = m[nt][c] == -CUDART_INF_F ? 0.f : exp2f(m[nt][c] - M);
+        float f = m[nt][c] == -CUDART_INF_F ? 0.f : exp2f(m[nt][c] - M);
         float* row = scratch + (warp * C::kHeads + h) * C::kDp;
+        if constexpr (KV8) {
+          // O rows: m-row tr <-> element 16a + 2tr, m-row tr + 8 <-> 16a + 2tr + 1.
+          f *= ldexpf(1.f, -kap);
 #pragma unroll
-        for (int a = 0; a < D / 16; ++a) {
-          row[a * 16 + tr] = o[a][nt][c] * f;
-          row[a * 16 + tr + 8] = o[a][nt][c + 2] * f;
+          for (int a = 0; a < D / 16; ++a)
+            *reinterpret_cast<float2*>(row + a * 16 + 2 * tr) = make_float2(o[a][nt][c] * f, o[a][nt][c + 2] * f);
+        } else {
+#pragma unroll
+          for (int a = 0; a < D / 16; ++a) {
+            row[a * 16 + tr] = o[a][nt][c] * f;
+            row[a * 16 + tr + 8] = o[a][nt][c + 2] * f;
+          }
         }
       }
     named_barrier_sync(1, C::kConsumers * 32);
@@ -730,17 +892,24 @@ static int launch_merge(const DecodeParams& p, pa_dtype dt, cudaStream_t stream)
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-template <typename T, int D, int BS, int NT>
+template <typename T, int D, int BS, int NT, bool KV8>
 static int launch_tc(const DecodeParams& p, cudaStream_t stream) {
-  using C = DecCfg<D, BS, NT>;
+  using C = DecCfg<D, BS, NT, KV8>;
   constexpr pa_dtype dt = std::is_same<T, __half>::value ? PA_F16 : PA_BF16;
   CUtensorMap kmap, vmap;
   const int64_t rows = (int64_t)p.num_blocks * p.num_kv_heads * BS;
-  int rc = make_kv_tensor_map(&kmap, p.k_cache, rows, D, dt, 16);
+  int rc;
+  if constexpr (KV8) {
+    rc = make_u8_tensor_map(&kmap, p.k_cache, rows, D, 16);
+    if (rc != PA_OK) return rc;
+    rc = make_u8_tensor_map(&vmap, p.v_cache, rows, D, 16);
+  } else {
+    rc = make_kv_tensor_map(&kmap, p.k_cache, rows, D, dt, 16);
+    if (rc != PA_OK) return rc;
+    rc = make_kv_tensor_map(&vmap, p.v_cache, rows, D, dt, 16);
+  }
   if (rc != PA_OK) return rc;
-  rc = make_kv_tensor_map(&vmap, p.v_cache, rows, D, dt, 16);
-  if (rc != PA_OK) return rc;
-  auto kern = decode_tc_kernel<T, D, BS, NT>;
+  auto kern = decode_tc_kernel<T, D, BS, NT, KV8>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -773,16 +942,26 @@ static int launch_simt(const DecodeParams& p, cudaStream_t stream) {
 template <typename T>
 static int launch_tc_dispatch(const DecodeParams& p, cudaStream_t stream) {
   const int nt = p.rows_per_cta <= 8 ? 1 : 2;
+  if (p.kv_scales) {  // e4m3 cache: head_dim 128 only
+    if (p.head_dim != 128) return PA_ERR_UNSUPPORTED;
+    switch ((p.block_size == 16 ? 0 : 1) * 2 + (nt - 1)) {
+      case 0: return launch_tc<T, 128, 16, 1, true>(p, stream);
+      case 1: return launch_tc<T, 128, 16, 2, true>(p, stream);
+      case 2: return launch_tc<T, 128, 32, 1, true>(p, stream);
+      case 3: return launch_tc<T, 128, 32, 2, true>(p, stream);
+    }
+    return PA_ERR_UNSUPPORTED;
+  }
   const int key = ((p.head_dim == 64 ? 0 : 1) * 2 + (p.block_size == 16 ? 0 : 1)) * 2 + (nt - 1);
   switch (key) {
-    case 0: return launch_tc<T, 64, 16, 1>(p, stream);
-    case 1: return launch_tc<T, 64, 16, 2>(p, stream);
-    case 2: return launch_tc<T, 64, 32, 1>(p, stream);
-    case 3: return launch_tc<T, 64, 32, 2>(p, stream);
-    case 4: return launch_tc<T, 128, 16, 1>(p, stream);
-    case 5: return launch_tc<T, 128, 16, 2>(p, stream);
-    case 6: return launch_tc<T, 128, 32, 1>(p, stream);
-    case 7: return launch_tc<T, 128, 32, 2>(p, stream);
+    case 0: return launch_tc<T, 64, 16, 1, false>(p, stream);
+    case 1: return launch_tc<T, 64, 16, 2, false>(p, stream);
+    case 2: return launch_tc<T, 64, 32, 1, false>(p, stream);
+    case 3: return launch_tc<T, 64, 32, 2, false>(p, stream);
+    case 4: return launch_tc<T, 128, 16, 1, false>(p, stream);
+    case 5: return launch_tc<T, 128, 16, 2, false>(p, stream);
+    case 6: return launch_tc<T, 128, 32, 1, false>(p, stream);
+    case 7: return launch_tc<T, 128, 32, 2, false>(p, stream);
   }
   return PA_ERR_UNSUPPORTED;
 }
@@ -798,6 +977,7 @@ int launch_decode(const DecodeParams& p0, pa_dtype dt, cudaStream_t stream) {
   decode_set_rows(p, dt);
   if ((int64_t)p.num_kv_heads * p.row_groups > 65535) return PA_ERR_UNSUPPORTED;
   if (dt == PA_F32) {
+    if (p.kv_scales) return PA_ERR_DTYPE;
     switch (p.head_dim) {
       case 32: return launch_simt<1>(p, stream);
       case 64: return launch_simt<2>(p, stream);

@@ -48,6 +48,9 @@ struct DecodeParams {
   const int32_t* prefix;
   int32_t slot0;
   int32_t planned;       // the work list is already built (by the shared-prefix preparation)
+  // e4m3 KV cache: (K, V) scale per (block, KV head), float32
+  // [num_blocks][num_kv_heads][2]; nullptr when the pools hold q's dtype.
+  const float* kv_scales;
   int* status;
 };
 
@@ -135,6 +138,8 @@ int num_sms_current_device();
 // box = [box_rows rows][64 elements] with 128-byte swizzle (16-bit dtypes only).
 int make_kv_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t head_dim, pa_dtype dt,
                        int32_t box_rows);
+// Same view of an e4m3 (one byte per element) pool: box = [box_rows rows][128 elements].
+int make_u8_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t head_dim, int32_t box_rows);
 // 3-D map over a [d2][d1][d0] tensor (d0 contiguous), box [b2][b1][b0], 128-byte swizzle.
 int make_3d_tensor_map(CUtensorMap* map, const void* base, int64_t d2, int64_t d1, int64_t d0, pa_dtype dt,
                        int32_t b2, int32_t b1, int32_t b0);
@@ -150,6 +155,15 @@ int launch_reshape_and_cache(const void* k, const void* v, const int64_t* slot_m
                              int32_t num_kv_heads, int32_t row_bytes, int* status, cudaStream_t stream);
 int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int32_t num_pairs,
                        int64_t block_bytes, cudaStream_t stream);
+// e4m3 cache write: per (run of consecutive tokens in one block, KV head,
+// pool) one warp computes the block's new scale and encodes the rows.
+int launch_reshape_and_cache_fp8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                                 uint8_t* k_cache, uint8_t* v_cache, float* kv_scales, int32_t num_blocks,
+                                 int32_t block_size, int32_t num_kv_heads, int32_t head_dim, pa_dtype dt,
+                                 int* status, cudaStream_t stream);
+// The (K, V) scales of whole blocks, dst <- src.
+int launch_copy_scales(float* kv_scales, const int32_t* src, const int32_t* dst, int32_t num_pairs,
+                       int32_t num_kv_heads, cudaStream_t stream);
 
 // Decode: split-KV main pass (+ merge pass when max_parts > 1).
 int launch_decode(const DecodeParams& p, pa_dtype dt, cudaStream_t stream);

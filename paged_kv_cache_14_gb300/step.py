@@ -26,8 +26,11 @@ class PagedStep:
                  new_seq_ids: torch.Tensor, new_positions: torch.Tensor, cow_pairs_host: np.ndarray,
                  scale: float, partition_size: int = 0, cu_q_lens: torch.Tensor | None = None,
                  ctx_lens: torch.Tensor | None = None, group_starts: torch.Tensor | None = None,
-                 prefix_lens: torch.Tensor | None = None):
+                 prefix_lens: torch.Tensor | None = None, kv_scales: torch.Tensor | None = None):
         self.q, self.k_cache, self.v_cache = q, k_cache, v_cache
+        # e4m3 cache: k_cache / v_cache hold uint8 codes, kv_scales the
+        # float32 (K, V) scale of every (block, KV head).
+        self.kv_scales = kv_scales
         self.block_tables, self.kv_lens = block_tables, kv_lens
         self.k_new, self.v_new = k_new, v_new
         self.new_seq_ids, self.new_positions = new_seq_ids, new_positions
@@ -62,13 +65,15 @@ class PagedStep:
                 n, hq, self.num_kv_heads, self.head_dim, self.block_size, self.max_seq_len, self.partition_size,
                 group_starts.shape[0] - 1))
         self.workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        if kv_scales is not None and (self.shared_prefix or not self.is_decode):
+            raise ValueError("the e4m3 cache is supported by plain decode only")
 
     @property
     def launches(self) -> int:
         """Kernel launches of one step (the library's own kernels)."""
         n = 0
         if self.cow_pairs.shape[0]:
-            n += -(-self.cow_pairs.shape[0] // 1024)
+            n += -(-self.cow_pairs.shape[0] // 1024) * (2 if self.kv_scales is not None else 1)
         n += 2  # slot mapping, cache write
         part = pa.pa_decode_partition_size(self.kv_lens.shape[0], self.q.shape[1], self.num_kv_heads,
                                            self.block_size, self.max_seq_len,
@@ -82,18 +87,30 @@ class PagedStep:
         return n
 
     def run(self, stream=None) -> torch.Tensor:
+        fp8 = self.kv_scales is not None
         if self.cow_pairs.shape[0]:
-            pa.pa_copy_blocks(self.k_cache, self.v_cache, self.cow_pairs, stream=stream)
+            if fp8:
+                pa.pa_copy_blocks_fp8(self.k_cache, self.v_cache, self.kv_scales, self.cow_pairs, stream=stream)
+            else:
+                pa.pa_copy_blocks(self.k_cache, self.v_cache, self.cow_pairs, stream=stream)
         pa.pa_slot_mapping(self.block_tables, self.new_seq_ids, self.new_positions, self.block_size,
                            self.num_blocks, slot_mapping=self.slot_mapping, stream=stream)
-        pa.pa_reshape_and_cache(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
-                                stream=stream)
+        if fp8:
+            pa.pa_reshape_and_cache_fp8(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
+                                        self.kv_scales, stream=stream)
+        else:
+            pa.pa_reshape_and_cache(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
+                                    stream=stream)
         self.attend(stream)
         return self.out
 
     def attend(self, stream=None) -> torch.Tensor:
         """The attention call of the step alone."""
-        if self.shared_prefix:
+        if self.kv_scales is not None:
+            pa.pa_decode_fp8(self.q, self.k_cache, self.v_cache, self.kv_scales, self.block_tables, self.kv_lens,
+                             self.max_seq_len, self.scale, out=self.out, partition_size=self.partition_size,
+                             workspace=self.workspace, stream=stream)
+        elif self.shared_prefix:
             pa.pa_decode_shared_prefix(self.q, self.k_cache, self.v_cache, self.block_tables, self.kv_lens,
                                        self.max_seq_len, self.group_starts, self.prefix_lens, self.scale,
                                        out=self.out, partition_size=self.partition_size, workspace=self.workspace,
@@ -109,10 +126,13 @@ class PagedStep:
         return self.out
 
 
-def step_from_host(batch, device="cuda", partition_size: int = 0, shared_prefix: bool = False) -> PagedStep:
+def step_from_host(batch, device="cuda", partition_size: int = 0, shared_prefix: bool = False,
+                   fp8_pool=None) -> PagedStep:
     """Build a PagedStep from a host-side batch object exposing the fields of
     a seeded workload (q, caches, tables, lengths, new tokens, CoW pairs).
-    With shared_prefix, decode uses the batch's prefix-sharing groups."""
+    With shared_prefix, decode uses the batch's prefix-sharing groups. With
+    fp8_pool = (k_codes, v_codes, kv_scales) the step runs on an e4m3 cache
+    holding those codes instead of the batch's 16-bit pools."""
     def dev(x, dtype=None):
         t = torch.as_tensor(x)
         if dtype is not None:
@@ -121,8 +141,9 @@ def step_from_host(batch, device="cuda", partition_size: int = 0, shared_prefix:
 
     cu = np.zeros(batch.num_seqs + 1, dtype=np.int32)
     np.cumsum(batch.q_lens, out=cu[1:])
+    kc, vc, sc = (batch.k_cache, batch.v_cache, None) if fp8_pool is None else fp8_pool
     return PagedStep(
-        q=dev(batch.q), k_cache=dev(batch.k_cache), v_cache=dev(batch.v_cache),
+        q=dev(batch.q), k_cache=dev(kc), v_cache=dev(vc), kv_scales=None if sc is None else dev(sc),
         block_tables=dev(batch.block_tables, torch.int32), kv_lens=dev(batch.kv_lens, torch.int32),
         q_lens_host=batch.q_lens, kv_lens_host=batch.kv_lens,
         k_new=dev(batch.k_new), v_new=dev(batch.v_new),

@@ -8,6 +8,7 @@ from .generate import (  # noqa: F401
     TORCH_DTYPES,
     PagedBatch,
     build_batch,
+    e4m3_pool,
     make_config,
     random_lengths,
 )

@@ -363,6 +363,29 @@ def make_config(name: str, with_values: bool = True) -> PagedBatch:
     return CONFIGS[name](with_values=with_values)
 
 
+def e4m3_pool(seed: int, num_blocks: int, num_kv_heads: int, block_size: int, head_dim: int,
+              log2_scale_range: tuple[float, float] = (-10.0, -7.0)):
+    """A synthetic e4m3 KV pool drawn directly as codes: K and V codes uniform
+    over the 254 byte values that are not e4m3 NaN patterns (0x7F, 0xFF), and
+    one K and one V scale per (block, KV head), log-uniform over
+    2^log2_scale_range (the default keeps stored magnitudes below 448 * 2^-7
+    = 3.5, like unit-normal data).
+    Returns (k_codes, v_codes) uint8 [P, Hkv, B, D] and kv_scales float32
+    [P, Hkv, 2] (CPU tensors). Random structure only: no value is encoded."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 4093]))
+    shape = (num_blocks, num_kv_heads, block_size, head_dim)
+
+    def codes():
+        r = rng.integers(0, 254, size=shape, dtype=np.int32)   # 0..253
+        r = r + (r >= 0x7F)                                      # skip 0x7F; 0xFF is never reached
+        return torch.from_numpy(r.astype(np.uint8))
+
+    k, v = codes(), codes()
+    lo, hi = log2_scale_range
+    sc = np.exp2(rng.uniform(lo, hi, size=(num_blocks, num_kv_heads, 2))).astype(np.float32)
+    return k, v, torch.from_numpy(sc)
+
+
 def random_lengths(seed: int, n: int, lo: int, hi: int) -> np.ndarray:
     """Uniform integer lengths in [lo, hi] (structure helper for small cases)."""
     rng = np.random.default_rng(np.random.SeedSequence([seed, 77]))
