@@ -39,6 +39,7 @@ if ROOT not in sys.path:
 
 DEFAULT_CONFIG = "llama3_70b_prefix_bf16"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_llama3_70b_prefix_bf16.md")
+PROFILE_SUMMARY_FP8 = os.path.join(ROOT, "profiles", "decode_e4m3_llama3_70b_prefix.md")
 DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_14_gb300", "csrc", "pa_decode.cu")
 
 
@@ -46,13 +47,15 @@ DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_14_gb300", "csrc", "pa_decode.cu
 # Algorithmic bytes (metric bookkeeping on host arrays).
 # ---------------------------------------------------------------------------
 
-def decode_algorithmic_bytes(batch) -> dict:
+def decode_algorithmic_bytes(batch, kv_esize: int | None = None) -> dict:
     """Bytes decode must move: every distinct live (physical block, KV head)
     tile once, counting its valid tokens (the largest count any sequence
     reading it uses), for K and V; plus q, out, the block-table entries read
-    and seq_lens."""
+    and seq_lens. kv_esize = 1 for an e4m3 cache, which adds the (K, V)
+    scale pair (8 bytes) of every distinct live tile."""
     B = batch.block_size
     esize = batch.q.element_size()
+    kv_es = esize if kv_esize is None else kv_esize
     valid = {}
     whole = set()
     entries = 0
@@ -68,10 +71,12 @@ def decode_algorithmic_bytes(batch) -> dict:
                 valid[phys] = v
             whole.add(phys)
     kv_tok = sum(valid.values())
-    per_tok = 2 * batch.num_kv_heads * batch.head_dim * esize
+    per_tok = 2 * batch.num_kv_heads * batch.head_dim * kv_es
     q_bytes = batch.q.numel() * esize
     out_bytes = q_bytes
     meta = entries * 4 + batch.num_seqs * 4
+    if kv_esize is not None and kv_esize == 1:
+        meta += len(valid) * batch.num_kv_heads * 8
     logical_tok = int(np.sum(batch.kv_lens))
     return {
         "kv_bytes": kv_tok * per_tok,
@@ -95,16 +100,19 @@ def prefill_flops(batch) -> float:
     return f
 
 
-def step_extra_bytes(batch) -> int:
+def step_extra_bytes(batch, kv_esize: int | None = None) -> int:
     """Bytes of the non-attention rows of a step: block copies (read + write
-    of both pools), slot derivation and the cache write."""
+    of both pools), slot derivation and the cache write (new rows read in the
+    I/O dtype, written in the cache's; an e4m3 cache adds its scales)."""
     esize = batch.q.element_size()
-    block_bytes = batch.num_kv_heads * batch.block_size * batch.head_dim * esize
-    copies = len(batch.cow_pairs) * 2 * 2 * block_bytes
+    kv_es = esize if kv_esize is None else kv_esize
+    block_bytes = batch.num_kv_heads * batch.block_size * batch.head_dim * kv_es
+    scales = 8 * batch.num_kv_heads if kv_es == 1 else 0
+    copies = len(batch.cow_pairs) * 2 * (2 * block_bytes + scales)
     t = len(batch.new_positions)
     slots = t * (4 + 4 + 4 + 8)
-    row = batch.num_kv_heads * batch.head_dim * esize
-    write = t * (8 + 2 * 2 * row)
+    row = batch.num_kv_heads * batch.head_dim
+    write = t * (8 + 2 * row * (esize + kv_es) + 2 * scales)
     return copies + slots + write
 
 
@@ -194,11 +202,11 @@ def measured_peak_tensor() -> tuple[float, str]:
         return 1900.0, "fallback"
 
 
-def profiled_traffic() -> float | None:
-    """DRAM bytes per decode launch from the committed ncu summary, if the
+def profiled_traffic(summary: str = PROFILE_SUMMARY) -> float | None:
+    """DRAM bytes per decode launch from a committed ncu summary, if the
     decode source has not changed since it was captured."""
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(summary).read()
     except OSError:
         return None
     m_sha = re.search(r"decode_source_sha256:\s*([0-9a-f]{64})", text)
@@ -241,12 +249,36 @@ ORACLE_SNIPPET = r"""
 import json, sys, time, numpy as np
 sys.path.insert(0, {root!r})
 import oracle
-from workloads import make_config
+import oracle.fp8_kv as f8
+from workloads import make_config, e4m3_pool
 b = make_config({config!r})
-kc = b.k_cache.clone(); vc = b.v_cache.clone()
-oracle.copy_blocks(kc, vc, b.cow_pairs)
-slots = oracle.slot_mapping(b.block_tables, b.new_seq_ids, b.new_positions, b.block_size)
-oracle.reshape_and_cache(b.k_new, b.v_new, slots, kc, vc, b.block_size)
+fp8 = {fp8!r}
+if fp8:
+    kc, vc, sc = (x.numpy() for x in e4m3_pool(b.meta.get("seed", 0), b.num_blocks, b.num_kv_heads,
+                                               b.block_size, b.head_dim))
+    f8.copy_blocks_fp8(kc, vc, sc, b.cow_pairs)
+    slots = oracle.slot_mapping(b.block_tables, b.new_seq_ids, b.new_positions, b.block_size)
+    f8.reshape_and_cache_fp8(b.k_new.float().numpy(), b.v_new.float().numpy(), slots, kc, vc, sc, b.block_size)
+else:
+    kc = b.k_cache.clone(); vc = b.v_cache.clone()
+    oracle.copy_blocks(kc, vc, b.cow_pairs)
+    slots = oracle.slot_mapping(b.block_tables, b.new_seq_ids, b.new_positions, b.block_size)
+    oracle.reshape_and_cache(b.k_new, b.v_new, slots, kc, vc, b.block_size)
+
+
+def decode_one(i):
+    if not fp8:
+        return oracle.decode(b.q, kc, vc, b.block_tables, b.kv_lens, b.scale, b.block_size, seqs=[i])
+    # e4m3: dequantise the sequence's blocks, then the same decode.
+    nb = -(-int(b.kv_lens[i]) // b.block_size)
+    blocks = b.block_tables[i][:nb]
+    kd = f8.dequantize(kc[blocks], sc[blocks, :, 0])
+    vd = f8.dequantize(vc[blocks], sc[blocks, :, 1])
+    tables = np.zeros_like(b.block_tables)
+    tables[i, :nb] = np.arange(nb)
+    return oracle.decode(b.q, kd, vd, tables, b.kv_lens, b.scale, b.block_size, seqs=[i])
+
+
 rng = np.random.default_rng(123)
 order = rng.permutation(b.num_seqs)
 budget = {budget!r}
@@ -254,7 +286,7 @@ results = []
 for rep in range({reps!r}):
     t0 = time.perf_counter(); done = []; toks = 0
     for i in order:
-        oracle.decode(b.q, kc, vc, b.block_tables, b.kv_lens, b.scale, b.block_size, seqs=[int(i)])
+        decode_one(int(i))
         done.append(int(i)); toks += int(b.kv_lens[i])
         if time.perf_counter() - t0 > budget:
             break
@@ -265,12 +297,12 @@ print("ORACLE_JSON " + json.dumps(results))
 """
 
 
-def run_oracle_sample(config: str, budget_s: float, reps: int) -> list[dict]:
+def run_oracle_sample(config: str, budget_s: float, reps: int, fp8: bool = False) -> list[dict]:
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
-    code = ORACLE_SNIPPET.format(root=ROOT, config=config, budget=budget_s, reps=reps)
+    code = ORACLE_SNIPPET.format(root=ROOT, config=config, budget=budget_s, reps=reps, fp8=fp8)
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
     for line in r.stdout.splitlines():
         if line.startswith("ORACLE_JSON "):
@@ -286,9 +318,9 @@ def oracle_rate(batch, res: dict, per_seq_bytes: np.ndarray) -> tuple[float, flo
     return byts / res["seconds"] / 1e9, len(seqs) / res["seconds"]
 
 
-def per_seq_decode_bytes(batch) -> np.ndarray:
+def per_seq_decode_bytes(batch, kv_esize: int | None = None) -> np.ndarray:
     esize = batch.q.element_size()
-    per_tok = 2 * batch.num_kv_heads * batch.head_dim * esize
+    per_tok = 2 * batch.num_kv_heads * batch.head_dim * (esize if kv_esize is None else kv_esize)
     qo = 2 * batch.num_q_heads * batch.head_dim * esize
     return batch.kv_lens.astype(np.float64) * per_tok + qo
 
@@ -334,7 +366,7 @@ def native_arm(args) -> None:
 
     import paged_kv_cache_14_gb300 as pa
     from paged_kv_cache_14_gb300.step import step_from_host
-    from workloads import make_config
+    from workloads import e4m3_pool, make_config
 
     rank, world, local = dist_info()
     torch.cuda.set_device(local)
@@ -342,11 +374,17 @@ def native_arm(args) -> None:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     pa.load()
     batch = make_config(args.config)
-    shared = args.decode == "shared_prefix" or (
-        args.decode == "auto" and batch.is_decode and batch.prefix_lens is not None and bool(batch.prefix_lens.any()))
-    st = step_from_host(batch, partition_size=args.partition, shared_prefix=shared)
-    dec_bytes = decode_algorithmic_bytes(batch)
-    step_bytes = dec_bytes["total"] + step_extra_bytes(batch)
+    fp8 = args.kv_cache == "e4m3"
+    if fp8 and (args.decode == "shared_prefix" or not batch.is_decode):
+        raise SystemExit("the e4m3 cache runs plain decode only")
+    shared = not fp8 and (args.decode == "shared_prefix" or (
+        args.decode == "auto" and batch.is_decode and batch.prefix_lens is not None and bool(batch.prefix_lens.any())))
+    pool = e4m3_pool(batch.meta["seed"], batch.num_blocks, batch.num_kv_heads, batch.block_size,
+                     batch.head_dim) if fp8 else None
+    st = step_from_host(batch, partition_size=args.partition, shared_prefix=shared, fp8_pool=pool)
+    kv_es = 1 if fp8 else None
+    dec_bytes = decode_algorithmic_bytes(batch, kv_es)
+    step_bytes = dec_bytes["total"] + step_extra_bytes(batch, kv_es)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -369,11 +407,7 @@ def native_arm(args) -> None:
         barrier()
         start.record(stream)
         for i in range(args.steps):
-            if st.cow_pairs.shape[0]:
-                pa.pa_copy_blocks(st.k_cache, st.v_cache, st.cow_pairs)
-            pa.pa_slot_mapping(st.block_tables, st.new_seq_ids, st.new_positions, st.block_size, st.num_blocks,
-                               slot_mapping=st.slot_mapping)
-            pa.pa_reshape_and_cache(st.k_new, st.v_new, st.slot_mapping, st.k_cache, st.v_cache)
+            st.prepare()
             ev[i][0].record(stream)
             st.attend()
             ev[i][1].record(stream)
@@ -439,18 +473,20 @@ def native_arm(args) -> None:
     dec_gbs = dec_bytes["total"] / (dec_mean * 1e-3) / 1e9
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and st.is_decode:
-        res = run_oracle_sample(args.config, args.cpu_seconds, 1)[0]
-        gbs, sps = oracle_rate(batch, res, per_seq_decode_bytes(batch))
+        res = run_oracle_sample(args.config, args.cpu_seconds, 1, fp8=fp8)[0]
+        gbs, sps = oracle_rate(batch, res, per_seq_decode_bytes(batch, kv_es))
         cpu = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"decode of {len(res['seqs'])} of {batch.num_seqs} sequences "
-                         f"({res['tokens']} keys) in {res['seconds']:.1f} s, fp64 numpy, 1 thread",
+                         f"({res['tokens']} keys) in {res['seconds']:.1f} s, fp64 numpy, 1 thread"
+                         + (" (e4m3 pools dequantised per sequence)" if fp8 else ""),
                "seq_steps_per_s": round(sps, 4)}
     if rank == 0:
         line = {
             "metric": "paged decode attention HBM GB/s (% of GB300 peak) & seq-steps/s at 70B layer",
             "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": batch.dtype, "data": "synthetic (seeded)",
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else batch.dtype,
+            "data": "synthetic (seeded)" + (", e4m3 pools drawn as codes + per-block scales" if fp8 else ""),
             "pct_of_peak": round(100.0 * value / world / peak, 2),
             "seq_steps_per_s": round(world * batch.num_seqs / (ms_step * 1e-3), 1),
             "config": {
@@ -460,19 +496,24 @@ def native_arm(args) -> None:
                 "cow_pairs": int(len(batch.cow_pairs)), "partition": pa.pa_decode_partition_size(
                     batch.num_seqs, batch.num_q_heads, batch.num_kv_heads, batch.block_size, batch.max_seq_len,
                     args.partition),
-                "step": "copy_blocks + slot_mapping + reshape_and_cache + " + (
-                    "pa_decode_shared_prefix" if st.shared_prefix else
-                    "pa_decode" if st.is_decode else "pa_chunked_prefill"),
+                "kv_cache": ("e4m3 codes + fp32 (K, V) scale per (block, KV head); q/out " + batch.dtype)
+                if fp8 else batch.dtype,
+                "step": ("copy_blocks_fp8 + slot_mapping + reshape_and_cache_fp8 + pa_decode_fp8" if fp8 else
+                         "copy_blocks + slot_mapping + reshape_and_cache + " + (
+                             "pa_decode_shared_prefix" if st.shared_prefix else
+                             "pa_decode" if st.is_decode else "pa_chunked_prefill")),
                 "step_bytes": step_bytes, "decode_bytes": dec_bytes,
                 "l2": "inputs larger than L2 (KV pools %.2f GB vs 129 MB L2); no flush" % (
-                    2 * batch.k_cache.numel() * batch.k_cache.element_size() / 1e9),
+                    2 * st.k_cache.numel() * st.k_cache.element_size() / 1e9),
                 "parallelism": f"replicas x{world}",
             },
             "roofline": ({"kernel": ("paged decode, shared-prefix (prefix check + tcgen05 prefix pass + split-KV "
                                      "suffix decode + merge)" if st.shared_prefix else
+                                     "paged decode over the e4m3 cache (plan + main + split-KV merge)" if fp8 else
                                      "paged decode (plan + main + split-KV merge)"), "bound": "hbm",
                           "achieved": round(dec_gbs, 2), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                          "frac": round(dec_gbs / peak, 4), "traffic": profiled_traffic(),
+                          "frac": round(dec_gbs / peak, 4),
+                          "traffic": profiled_traffic(PROFILE_SUMMARY_FP8 if fp8 else PROFILE_SUMMARY),
                           "algorithmic_bytes": dec_bytes["total"], "ms_per_launch": round(dec_mean, 5)}
                          if st.is_decode else
                          {"kernel": "chunked prefill call (tcgen05 chunk tiles + decode rows)", "bound": "tensor",
@@ -501,6 +542,8 @@ def main():
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--decode", choices=("auto", "plain", "shared_prefix"), default="auto",
                     help="auto: shared-prefix decode when the workload's sequences share prefix blocks")
+    ap.add_argument("--kv-cache", choices=("native", "e4m3"), default="native",
+                    help="native: the pools hold q's dtype; e4m3: e4m3 codes with per-block scales")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

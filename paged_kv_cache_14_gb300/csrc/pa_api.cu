@@ -114,11 +114,13 @@ int make_3d_tensor_map(CUtensorMap* map, const void* base, int64_t d2, int64_t d
 int make_u8_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t head_dim, int32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return PA_ERR_CUDA;
-  cuuint64_t gdim[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+  // The copy moves bytes unchanged, so the rows are described as 16-bit
+  // elements (half as many per row): the same 128-byte box rows and swizzle.
+  cuuint64_t gdim[2] = {(cuuint64_t)head_dim / 2, (cuuint64_t)rows};
   cuuint64_t gstride[1] = {(cuuint64_t)head_dim};
-  cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, estr,
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), gdim, gstride, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;

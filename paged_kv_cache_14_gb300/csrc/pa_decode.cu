@@ -55,12 +55,23 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
   return d;
 }
 
-// Two e4m3 codes (low byte first) to an fp16 pair (low half first); exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
-  uint32_t d;
-  const uint16_t c = static_cast<uint16_t>(codes);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(c));
-  return d;
+// Four e4m3 codes (byte 0 first) to two fp16 pairs: lo <- bytes 0, 1 and
+// hi <- bytes 2, 3 (low half first); exact.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t codes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\t"
+      "mov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(codes));
+}
+
+// 2^x with the hardware approximation (inputs here are <= 0 or -inf; the
+// result's relative error is a few ulp, results below 2^-126 flush to 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
@@ -98,16 +109,22 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p)
 // ---------------------------------------------------------------------------
 // Persistent tensor-core decode kernel (fp16 / bf16).
 // ---------------------------------------------------------------------------
-// A stage holds one 16-token sub-tile of a (block, KV head) tile of K and of
-// V (a block of 32 tokens fills two stages). Stage s is only ever consumed
-// by consumer warp s % 4, so each stage's mbarrier is waited on in phase
-// order by one warp (a parity wait can never alias a phase not yet begun).
+// A stage holds 16 tokens (bf16/fp16 cache) or 32 tokens (e4m3 cache) of a
+// sequence's K and V for one KV head: one or two 16-token sub-tiles, each a
+// slice of one (block, KV head) tile (a 32-token block fills two sub-tiles;
+// the two sub-tiles of an e4m3 stage may come from two blocks). Either way a
+// stage is 8 KB at head_dim 128. Stage s is only ever consumed by consumer
+// warp s % 4, so each stage's mbarrier is waited on in phase order by one
+// warp (a parity wait can never alias a phase not yet begun).
 template <int D, int BS, int NT, bool KV8 = false>
 struct DecCfg {
   static constexpr int kEsz = KV8 ? 1 : 2;            // bytes per cached element
   static constexpr int kBoxCols = 128 / kEsz;         // elements in one 128-byte TMA box row
   static constexpr int kHalves = D * kEsz / 128;      // 128-byte swizzle boxes across head_dim
-  static constexpr int kTile = 16 * D * kEsz;         // 16 tokens x head_dim of K (or V)
+  static constexpr int kSubTiles = KV8 ? 2 : 1;       // 16-token sub-tiles per stage
+  static constexpr int kStageTok = 16 * kSubTiles;    // tokens per stage
+  static constexpr int kSub = 16 * D * kEsz;          // bytes of one sub-tile of K (or V)
+  static constexpr int kTile = kSubTiles * kSub;      // K (or V) bytes of a stage
   static constexpr int kStage = 2 * kTile;            // K + V
   static constexpr int kStages = PA_DECODE_RING_BYTES / kStage;
   static constexpr int kHeads = NT * 8;               // query heads per item (MMA N)
@@ -124,8 +141,9 @@ struct DecCfg {
   static constexpr size_t kValid = kMeta + (size_t)kSlots * 16 * 4;
   static constexpr size_t kBars = (kValid + (size_t)kStages * 4 + 7) & ~size_t(7);
   static constexpr size_t kFlags = kBars + (size_t)(2 * kStages + 2 * kSlots) * 8;
-  static constexpr size_t kScl = kFlags + 16;          // e4m3 cache: (K, V) scale of each stage's block
-  static constexpr size_t kSmem = kScl + (KV8 ? (size_t)kStages * 8 : 0) + 1024;  // + alignment slack
+  // e4m3 cache: (K, V) scales of the blocks of each stage's two sub-tiles.
+  static constexpr size_t kScl = (kFlags + 16 + 15) & ~size_t(15);
+  static constexpr size_t kSmem = kScl + (KV8 ? (size_t)kStages * 16 : 0) + 1024;  // + alignment slack
   static_assert(kStages % kConsumers == 0, "stage s belongs to consumer warp s % 4");
   static_assert(BS % 16 == 0, "block size must be a multiple of 16");
 };
@@ -156,7 +174,7 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
   uint64_t* iempty = ifull + C::kSlots;
   float* scratch = reinterpret_cast<float*>(smem + C::kScratch);
   float* ml = reinterpret_cast<float*>(smem + C::kMl);
-  float2* stage_scale = reinterpret_cast<float2*>(smem + C::kScl);
+  float4* stage_scale = reinterpret_cast<float4*>(smem + C::kScl);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hr = p.num_kv_heads * p.row_groups;
@@ -195,8 +213,10 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
       decode_row(p, next_pr >> 16, next_qrow, next_len);
       next_pfx = p.prefix ? p.prefix[next_pr >> 16] : 0;
     }
-    int jg = 0;  // 16-token sub-tiles issued so far (global stage sequence)
+    int jg = 0;  // stages issued so far (global stage sequence)
     bool bad = false;
+    unsigned fail_mask = 0;  // lanes of the group whose slot wait ran out
+    int fail_n = 0;          // size of that group
     constexpr int kSubPerBlock = BS / 16;
     for (int it = 0;; ++it) {
       const int item = next;
@@ -220,9 +240,10 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
       const int kvh = hg / p.row_groups, rgi = hg - kvh * p.row_groups;
       const int t_begin = pfx + part * p.partition;  // the suffix starts after the shared prefix
       const int t_end = min(t_begin + p.partition, len);
-      const int nsub = (t_end - t_begin + 15) / 16;
-      // Items are padded to a multiple of 4 sub-tiles with empty stages, so
-      // every item starts on stage 0 mod 4 and sub-tile u always lands on
+      const int nsub16 = (t_end - t_begin + 15) / 16;                 // 16-token sub-tiles
+      const int nsub = (nsub16 + C::kSubTiles - 1) / C::kSubTiles;    // stages
+      // Items are padded to a multiple of 4 stages with empty stages, so
+      // every item starts on stage 0 mod 4 and stage u always lands on
       // consumer warp u % 4: the summation order, hence the result, does not
       // depend on which CTA ran the item or what it ran before.
       const int nsub_pad = (nsub + 3) & ~3;
@@ -250,53 +271,86 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
       }
       const int32_t* bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq + t_begin / BS;
       for (int ub = 0; ub < nsub_pad && !bad; ub += 32) {
-        // Lane k holds the physical block of sub-tile ub + k (-1: padding)
-        // and, for an e4m3 cache, that block's (K, V) scales.
-        int id = -1;
-        float2 bsc = make_float2(0.f, 0.f);
-        if (ub + lane < nsub) {
-          id = bt[(ub + lane) / kSubPerBlock];
-          if (id < 0 || id >= p.num_blocks) {
-            record_error(p.status, PA_ERR_BLOCK_OOB);
-            id = -1;
-          }
-          if constexpr (KV8) {
-            if (id >= 0) bsc = __ldg(reinterpret_cast<const float2*>(p.kv_scales) + (int64_t)id * p.num_kv_heads + kvh);
+        // Lane k holds the physical blocks of the sub-tiles of stage ub + k
+        // (-1: padding) and, for an e4m3 cache, those blocks' (K, V) scales.
+        int id[C::kSubTiles];
+        float2 bsc[C::kSubTiles];
+#pragma unroll
+        for (int h = 0; h < C::kSubTiles; ++h) {
+          id[h] = -1;
+          bsc[h] = make_float2(0.f, 0.f);
+          const int sub = (ub + lane) * C::kSubTiles + h;
+          if (sub < nsub16) {
+            id[h] = bt[sub / kSubPerBlock];
+            if (id[h] < 0 || id[h] >= p.num_blocks) {
+              record_error(p.status, PA_ERR_BLOCK_OOB);
+              id[h] = -1;
+            }
+            if constexpr (KV8) {
+              if (id[h] >= 0)
+                bsc[h] = __ldg(reinterpret_cast<const float2*>(p.kv_scales) + (int64_t)id[h] * p.num_kv_heads + kvh);
+            }
           }
         }
         const int cnt = min(32, nsub_pad - ub);
-        for (int k = 0; k < cnt; ++k) {
-          const int idk = __shfl_sync(0xffffffffu, id, k);
-          float2 sck = make_float2(0.f, 0.f);
-          if constexpr (KV8) {
-            sck.x = __shfl_sync(0xffffffffu, bsc.x, k);
-            sck.y = __shfl_sync(0xffffffffu, bsc.y, k);
+        // Issue the batch in groups of up to kStages stages, one lane per
+        // stage: each lane waits for its own ring slot (all distinct within
+        // a group, so no parity wait can alias an older phase), publishes
+        // the stage's validity (and scales) and issues its copies, so a
+        // single pass of the warp issues a whole group.
+        for (int g = 0; g < cnt; g += C::kStages) {
+          const int n = min(C::kStages, cnt - g);
+          const int src = g + (lane < n ? lane : 0);
+          int idk[C::kSubTiles];
+          float2 sck[C::kSubTiles];
+#pragma unroll
+          for (int h = 0; h < C::kSubTiles; ++h) {
+            idk[h] = __shfl_sync(0xffffffffu, id[h], src);
+            sck[h] = make_float2(0.f, 0.f);
+            if constexpr (KV8) {
+              sck[h].x = __shfl_sync(0xffffffffu, bsc[h].x, src);
+              sck[h].y = __shfl_sync(0xffffffffu, bsc[h].y, src);
+            }
           }
-          if (lane == 0) {
-            const int s = jg % C::kStages;
-            if (jg >= C::kStages && !mbar_wait(smem_u32(&empty[s]), ((jg / C::kStages) & 1) ^ 1, p.status)) {
-              bad = true;
+          bool failed = false;
+          if (lane < n) {
+            const int j = jg + lane;
+            const int s = j % C::kStages;
+            if (j >= C::kStages && !mbar_wait(smem_u32(&empty[s]), ((j / C::kStages) & 1) ^ 1, p.status)) {
+              failed = true;
             } else {
-              stage_valid[s] = idk >= 0;
-              if constexpr (KV8) stage_scale[s] = sck;  // published by the arrive below
+              int vmask = 0;
+#pragma unroll
+              for (int h = 0; h < C::kSubTiles; ++h) vmask |= (idk[h] >= 0 ? 1 : 0) << h;
+              stage_valid[s] = vmask;
+              if constexpr (KV8) stage_scale[s] = make_float4(sck[0].x, sck[0].y, sck[1].x, sck[1].y);  // published by the arrive below
               const uint32_t fb = smem_u32(&full[s]);
-              if (idk >= 0) {
-                mbar_arrive_expect_tx(fb, C::kStage);
-                const int32_t row = (idk * p.num_kv_heads + kvh) * BS + ((ub + k) % kSubPerBlock) * 16;
+              if (vmask) {
+                mbar_arrive_expect_tx(fb, __popc(vmask) * 2 * C::kSub);
                 const uint32_t kd = ring0 + s * C::kStage;
 #pragma unroll
-                for (int hf = 0; hf < C::kHalves; ++hf) {
-                  tma_load_2d(kd + hf * 2048, &kmap, hf * C::kBoxCols, row, fb);
-                  tma_load_2d(kd + C::kTile + hf * 2048, &vmap, hf * C::kBoxCols, row, fb);
+                for (int h = 0; h < C::kSubTiles; ++h) {
+                  if (idk[h] < 0) continue;
+                  const int sub = (ub + g + lane) * C::kSubTiles + h;
+                  const int32_t row = (idk[h] * p.num_kv_heads + kvh) * BS + (sub % kSubPerBlock) * 16;
+#pragma unroll
+                  for (int hf = 0; hf < C::kHalves; ++hf) {
+                    tma_load_2d(kd + h * C::kSub + hf * 2048, &kmap, hf * C::kBoxCols, row, fb);
+                    tma_load_2d(kd + C::kTile + h * C::kSub + hf * 2048, &vmap, hf * C::kBoxCols, row, fb);
+                  }
                 }
               } else {
                 mbar_arrive(fb);
               }
             }
           }
-          bad = __shfl_sync(0xffffffffu, bad, 0);
-          if (bad) break;
-          ++jg;
+          fail_mask = __ballot_sync(0xffffffffu, failed);
+          if (fail_mask) {
+            fail_n = n;
+            bad = true;
+            break;
+          }
+          jg += n;
         }
         if (ub == 0) {
           // The counter has answered by now: load the next item's metadata
@@ -311,12 +365,16 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
       }
       if (bad) break;
     }
-    if (bad && lane == 0) {
-      // Let copies still in flight land before the CTA exits.
-      for (int s = 0; s < C::kStages && s < jg; ++s) {
-        const int last = s + ((jg - 1 - s) / C::kStages) * C::kStages;
-        mbar_wait(smem_u32(&full[s]), (last / C::kStages) & 1, nullptr);
-      }
+    if (bad && lane < C::kStages) {
+      // Let copies still in flight land before the CTA exits: lane s waits
+      // for the last stage issued on ring slot s. Stages before jg were all
+      // issued; of a group that failed (stages jg .. jg + fail_n - 1) only
+      // those whose lane did not fail.
+      const int sl = lane;
+      const int off = ((sl - jg) % C::kStages + C::kStages) % C::kStages;  // slot sl's place in that group
+      int last = jg + off;
+      if (off >= fail_n || ((fail_mask >> off) & 1u)) last -= C::kStages;
+      if (last >= 0) mbar_wait(smem_u32(&full[sl]), (last / C::kStages) & 1, nullptr);
     }
     return;
   }
@@ -406,29 +464,31 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
     // e4m3 cache: O accumulates p * s_V(block) * 2^kap * code, with kap the
     // largest exponent that keeps s_V * 2^kap <= 2^15 for every block seen
     // so far (so p * s_V * 2^kap fits fp16); kap only decreases, and O is
-    // rescaled by the exact power of two when it does.
-    int kap = 1 << 20;
+    // rescaled by the exact power of two when it does. kap_unset until the
+    // first block with a non-zero V scale.
+    constexpr int kap_unset = 1 << 20;
+    int kap = kap_unset;
+    float pw = 0.f;  // 2^kap
 
     const int jend = mt.jstart + mt.nsub;
     bool bad = false;
-    // This warp's sub-tiles: j = warp (mod 4), i.e. the stages it owns
-    // (jstart is a multiple of 4).
-    for (int j = mt.jstart + warp; j < jend; j += C::kConsumers) {
-      const int s = j % C::kStages;
-      if (!mbar_wait(smem_u32(&full[s]), (j / C::kStages) & 1, p.status)) {
-        bad = true;
-        break;
-      }
-      const bool valid = stage_valid[s] != 0;
-      // Copy the sub-tile's K and V fragments to registers and hand the
-      // stage back at once: the producer refills it while this warp
-      // computes, so the ring's bytes stay in flight.
-      uint32_t ka[D / 16][4], va[D / 16][4];
-      float2 bscale = make_float2(0.f, 0.f);
-      if (valid) {
-        const uint32_t kb = ring0 + s * C::kStage;
-        const uint32_t vb = kb + C::kTile;
-        if constexpr (!KV8) {
+    if constexpr (!KV8) {
+      // This warp's sub-tiles: j = warp (mod 4), i.e. the stages it owns
+      // (jstart is a multiple of 4).
+      for (int j = mt.jstart + warp; j < jend; j += C::kConsumers) {
+        const int s = j % C::kStages;
+        if (!mbar_wait(smem_u32(&full[s]), (j / C::kStages) & 1, p.status)) {
+          bad = true;
+          break;
+        }
+        const bool valid = stage_valid[s] != 0;
+        // Copy the sub-tile's K and V fragments to registers and hand the
+        // stage back at once: the producer refills it while this warp
+        // computes, so the ring's bytes stay in flight.
+        uint32_t ka[D / 16][4], va[D / 16][4];
+        if (valid) {
+          const uint32_t kb = ring0 + s * C::kStage;
+          const uint32_t vb = kb + C::kTile;
           const int tk_a = (mi & 1) * 8 + rr;   // K rows as the A operand (non-transposed)
           const int tk_v = (mi >> 1) * 8 + rr;  // V rows, transposed into the A operand
 #pragma unroll
@@ -443,75 +503,32 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
             ldsm_x4_t(vb + (cg >> 3) * 2048 + tk_v * 128 + (((cg & 7) ^ (tk_v & 7)) << 4), va[a][0], va[a][1],
                       va[a][2], va[a][3]);
           }
-        } else {
-          // 8x16-byte matrices: lane group mi reads tokens (mi & 1) * 8 + rr
-          // of 16-byte chunk 2q + (mi >> 1). The raw codes go to ka/va[2q..]
-          // and are widened after the stage is released.
-          const int tk = (mi & 1) * 8 + rr;
-#pragma unroll
-          for (int q2 = 0; q2 < D / 32; ++q2) {
-            const int cg = 2 * q2 + (mi >> 1);
-            const uint32_t off = (cg >> 3) * 2048 + tk * 128 + (((cg & 7) ^ (tk & 7)) << 4);
-            ldsm_x4(kb + off, ka[2 * q2][0], ka[2 * q2][1], ka[2 * q2][2], ka[2 * q2][3]);
-            ldsm_x4_t(vb + off, va[2 * q2][0], va[2 * q2][1], va[2 * q2][2], va[2 * q2][3]);
-          }
-          bscale = stage_scale[s];
         }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-      if (valid) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        if (!valid) continue;
         const int tok0 = mt.t_begin + (j - mt.jstart) * 16;
-        if constexpr (KV8) {
-          // K: matrix (tokens 0-7 | 8-15) x (chunk 2q | 2q+1) gives lane (g, t)
-          // elements 4t..4t+3 of token g (or g+8). Widen to fp16 pairs:
-          // A rows g / g+8, k slots (2t, 2t+1) <- elements (4t, 4t+1),
-          // k slots (2t+8, 2t+9) <- elements (4t+2, 4t+3).
-          // V (transposed load): lane (g, t) gets elements (2g, 2g+1) of
-          // tokens 2t and 2t+1; a byte permute pairs the tokens per element,
-          // so A row g <- element 2g and row g+8 <- element 2g+1 of the
-          // chunk, k slots = the tokens.
-#pragma unroll
-          for (int q2 = D / 32 - 1; q2 >= 0; --q2) {
-            const uint32_t k0 = ka[2 * q2][0], k1 = ka[2 * q2][1], k2 = ka[2 * q2][2], k3 = ka[2 * q2][3];
-            ka[2 * q2][0] = e4m3x2_to_f16x2(k0 & 0xffffu);
-            ka[2 * q2][1] = e4m3x2_to_f16x2(k1 & 0xffffu);
-            ka[2 * q2][2] = e4m3x2_to_f16x2(k0 >> 16);
-            ka[2 * q2][3] = e4m3x2_to_f16x2(k1 >> 16);
-            ka[2 * q2 + 1][0] = e4m3x2_to_f16x2(k2 & 0xffffu);
-            ka[2 * q2 + 1][1] = e4m3x2_to_f16x2(k3 & 0xffffu);
-            ka[2 * q2 + 1][2] = e4m3x2_to_f16x2(k2 >> 16);
-            ka[2 * q2 + 1][3] = e4m3x2_to_f16x2(k3 >> 16);
-          }
-        }
         // S^T = K Q^T: rows = 16 tokens, columns = heads. Two accumulator
         // chains over the head_dim halves shorten the dependent MMA chain.
         float sc[NT][4], sc2[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
           sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = sc2[nt][0] = sc2[nt][1] = sc2[nt][2] = sc2[nt][3] = 0.f;
-        using MT = typename std::conditional<KV8, __half, T>::type;
 #pragma unroll
         for (int kk = 0; kk < D / 16; kk += 2)
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            MmaOp<MT>::run(sc[nt], ka[kk], qf[kk][nt][0], qf[kk][nt][1]);
-            MmaOp<MT>::run(sc2[nt], ka[kk + 1], qf[kk + 1][nt][0], qf[kk + 1][nt][1]);
+            MmaOp<T>::run(sc[nt], ka[kk], qf[kk][nt][0], qf[kk][nt][1]);
+            MmaOp<T>::run(sc2[nt], ka[kk + 1], qf[kk + 1][nt][0], qf[kk + 1][nt][1]);
           }
-        // Scale to log2 units (and, for e4m3, by the block's K scale and the
-        // query rows' exponents), mask keys past the partition end.
-        float fs[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int c = 0; c < 2; ++c) fs[nt][c] = KV8 ? sl2 * bscale.x * qsh[nt][c] : sl2;
+        // Scale to log2 units, mask keys past the partition end.
         const int t_lo = tok0 + tr, t_hi = tok0 + tr + 8;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          sc[nt][0] = t_lo < mt.t_end ? (sc[nt][0] + sc2[nt][0]) * fs[nt][0] : -CUDART_INF_F;
-          sc[nt][1] = t_lo < mt.t_end ? (sc[nt][1] + sc2[nt][1]) * fs[nt][1] : -CUDART_INF_F;
-          sc[nt][2] = t_hi < mt.t_end ? (sc[nt][2] + sc2[nt][2]) * fs[nt][0] : -CUDART_INF_F;
-          sc[nt][3] = t_hi < mt.t_end ? (sc[nt][3] + sc2[nt][3]) * fs[nt][1] : -CUDART_INF_F;
+          sc[nt][0] = t_lo < mt.t_end ? (sc[nt][0] + sc2[nt][0]) * sl2 : -CUDART_INF_F;
+          sc[nt][1] = t_lo < mt.t_end ? (sc[nt][1] + sc2[nt][1]) * sl2 : -CUDART_INF_F;
+          sc[nt][2] = t_hi < mt.t_end ? (sc[nt][2] + sc2[nt][2]) * sl2 : -CUDART_INF_F;
+          sc[nt][3] = t_hi < mt.t_end ? (sc[nt][3] + sc2[nt][3]) * sl2 : -CUDART_INF_F;
         }
         // Online softmax per head column (max over the 16 tokens = over
         // the 8 lanes that share lane % 4).
@@ -536,24 +553,6 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
             l[nt][c] = l[nt][c] * alpha[nt][c] + (p0 + p1);
             m[nt][c] = mn;
           }
-        // e4m3: the weight of this block's V codes, p * s_V * 2^kap.
-        float fv = 1.f;
-        if constexpr (KV8) {
-          fv = 0.f;
-          if (bscale.y > 0.f) {
-            int ex = 0;
-            frexpf(bscale.y, &ex);  // s_V in [2^(ex-1), 2^ex)
-            const int kmax = 15 - ex;
-            if (kmax < kap) {
-              const float r = ldexpf(1.f, kmax - kap);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) alpha[nt][0] *= r, alpha[nt][1] *= r;
-              rescale = true;
-              kap = kmax;
-            }
-            fv = ldexpf(bscale.y, kap);
-          }
-        }
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
           for (int a = 0; a < D / 16; ++a)
@@ -569,28 +568,8 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
         uint32_t pb[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          if constexpr (KV8) {
-            pb[nt][0] = movmatrix_trans(MmaOp<__half>::pack(sc[nt][0] * fv, sc[nt][1] * fv));
-            pb[nt][1] = movmatrix_trans(MmaOp<__half>::pack(sc[nt][2] * fv, sc[nt][3] * fv));
-          } else {
-            pb[nt][0] = movmatrix_trans(MmaOp<T>::pack(sc[nt][0], sc[nt][1]));
-            pb[nt][1] = movmatrix_trans(MmaOp<T>::pack(sc[nt][2], sc[nt][3]));
-          }
-        }
-        if constexpr (KV8) {
-#pragma unroll
-          for (int q2 = D / 32 - 1; q2 >= 0; --q2) {
-            const uint32_t v0 = __byte_perm(va[2 * q2][0], 0, 0x3120), v1 = __byte_perm(va[2 * q2][1], 0, 0x3120);
-            const uint32_t v2 = __byte_perm(va[2 * q2][2], 0, 0x3120), v3 = __byte_perm(va[2 * q2][3], 0, 0x3120);
-            va[2 * q2][0] = e4m3x2_to_f16x2(v0 & 0xffffu);
-            va[2 * q2][1] = e4m3x2_to_f16x2(v0 >> 16);
-            va[2 * q2][2] = e4m3x2_to_f16x2(v1 & 0xffffu);
-            va[2 * q2][3] = e4m3x2_to_f16x2(v1 >> 16);
-            va[2 * q2 + 1][0] = e4m3x2_to_f16x2(v2 & 0xffffu);
-            va[2 * q2 + 1][1] = e4m3x2_to_f16x2(v2 >> 16);
-            va[2 * q2 + 1][2] = e4m3x2_to_f16x2(v3 & 0xffffu);
-            va[2 * q2 + 1][3] = e4m3x2_to_f16x2(v3 >> 16);
-          }
+          pb[nt][0] = movmatrix_trans(MmaOp<T>::pack(sc[nt][0], sc[nt][1]));
+          pb[nt][1] = movmatrix_trans(MmaOp<T>::pack(sc[nt][2], sc[nt][3]));
         }
         // Keys past the end carry p = 0, but their V slots may hold any
         // bits (NaN included): zero those V elements so 0 * V stays 0.
@@ -610,7 +589,184 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
 #pragma unroll
         for (int a = 0; a < D / 16; ++a)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) MmaOp<MT>::run(o[a][nt], va[a], pb[nt][0], pb[nt][1]);
+          for (int nt = 0; nt < NT; ++nt) MmaOp<T>::run(o[a][nt], va[a], pb[nt][0], pb[nt][1]);
+      }
+    } else {
+      // e4m3 cache: a stage holds two 16-token sub-tiles (halves), so the
+      // softmax reductions and the bookkeeping are paid once per 32 tokens
+      // and the two halves' MMA chains overlap.
+      for (int j = mt.jstart + warp; j < jend; j += C::kConsumers) {
+        const int s = j % C::kStages;
+        if (!mbar_wait(smem_u32(&full[s]), (j / C::kStages) & 1, p.status)) {
+          bad = true;
+          break;
+        }
+        const int vmask = stage_valid[s];
+        const bool valid0 = (vmask & 1) != 0, valid1 = (vmask & 2) != 0;
+        // Raw codes of both halves: 8x16-byte matrices, lane group mi reads
+        // tokens (mi & 1) * 8 + rr of 16-byte chunk 2q + (mi >> 1).
+        uint32_t kr[2][D / 32][4], vr[2][D / 32][4];
+        float2 bs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        {
+          const int tk = (mi & 1) * 8 + rr;
+          const float4 sc4 = stage_scale[s];
+          bs[0] = make_float2(sc4.x, sc4.y);
+          bs[1] = make_float2(sc4.z, sc4.w);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (!(h ? valid1 : valid0)) continue;
+            const uint32_t kb = ring0 + s * C::kStage + h * C::kSub, vb = kb + C::kTile;
+#pragma unroll
+            for (int q2 = 0; q2 < D / 32; ++q2) {
+              const int cg = 2 * q2 + (mi >> 1);
+              const uint32_t off = (cg >> 3) * 2048 + tk * 128 + (((cg & 7) ^ (tk & 7)) << 4);
+              ldsm_x4(kb + off, kr[h][q2][0], kr[h][q2][1], kr[h][q2][2], kr[h][q2][3]);
+              ldsm_x4_t(vb + off, vr[h][q2][0], vr[h][q2][1], vr[h][q2][2], vr[h][q2][3]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        if (!valid0 && !valid1) continue;
+        const int tok0 = mt.t_begin + (j - mt.jstart) * 32;
+        // S^T per half: K widened to fp16 pairs (A rows g / g+8; k slots
+        // (2t, 2t+1) <- elements (4t, 4t+1), (2t+8, 2t+9) <- (4t+2, 4t+3)
+        // of the 16-element chunk), times the query in the same order.
+        float sc[2][NT][4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float acc[NT][4], acc2[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = acc2[nt][0] = acc2[nt][1] = acc2[nt][2] =
+                acc2[nt][3] = 0.f;
+          if (h ? valid1 : valid0) {
+#pragma unroll
+            for (int q2 = 0; q2 < D / 32; ++q2) {
+              uint32_t a0[4], a1[4];
+              e4m3x4_to_f16x4(kr[h][q2][0], a0[0], a0[2]);
+              e4m3x4_to_f16x4(kr[h][q2][1], a0[1], a0[3]);
+              e4m3x4_to_f16x4(kr[h][q2][2], a1[0], a1[2]);
+              e4m3x4_to_f16x4(kr[h][q2][3], a1[1], a1[3]);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                MmaOp<__half>::run(acc[nt], a0, qf[2 * q2][nt][0], qf[2 * q2][nt][1]);
+                MmaOp<__half>::run(acc2[nt], a1, qf[2 * q2 + 1][nt][0], qf[2 * q2 + 1][nt][1]);
+              }
+            }
+          }
+          // Scale by the block's K scale, the query rows' exponents and
+          // log2(e) * softmax scale; mask keys past the partition end.
+          const int t_lo = tok0 + 16 * h + tr, t_hi = t_lo + 8;
+          const bool vh = h ? valid1 : valid0;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const float f0 = sl2 * bs[h].x * qsh[nt][0], f1 = sl2 * bs[h].x * qsh[nt][1];
+            sc[h][nt][0] = vh && t_lo < mt.t_end ? (acc[nt][0] + acc2[nt][0]) * f0 : -CUDART_INF_F;
+            sc[h][nt][1] = vh && t_lo < mt.t_end ? (acc[nt][1] + acc2[nt][1]) * f1 : -CUDART_INF_F;
+            sc[h][nt][2] = vh && t_hi < mt.t_end ? (acc[nt][2] + acc2[nt][2]) * f0 : -CUDART_INF_F;
+            sc[h][nt][3] = vh && t_hi < mt.t_end ? (acc[nt][3] + acc2[nt][3]) * f1 : -CUDART_INF_F;
+          }
+        }
+        // Online softmax per head column over the 32 tokens.
+        bool rescale = false;
+        float alpha[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            float mx = fmaxf(fmaxf(sc[0][nt][c], sc[0][nt][c + 2]), fmaxf(sc[1][nt][c], sc[1][nt][c + 2]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mn = fmaxf(m[nt][c], mx);
+            const bool dead = mn == -CUDART_INF_F;
+            alpha[nt][c] = dead ? 1.f : fast_exp2(m[nt][c] - mn);
+            rescale |= mn != m[nt][c];
+            float ps = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float p0 = dead ? 0.f : fast_exp2(sc[h][nt][c] - mn);
+              const float p1 = dead ? 0.f : fast_exp2(sc[h][nt][c + 2] - mn);
+              sc[h][nt][c] = p0;
+              sc[h][nt][c + 2] = p1;
+              ps += p0 + p1;
+            }
+            l[nt][c] = l[nt][c] * alpha[nt][c] + ps;
+            m[nt][c] = mn;
+          }
+        // The weight of each half's V codes is p * s_V * 2^kap; lower kap
+        // first if a half's V scale needs it.
+        float fv[2];
+        {
+          const float smax = fmaxf(valid0 ? bs[0].y : 0.f, valid1 ? bs[1].y : 0.f);
+          if (smax > 0.f) {
+            // smax in [2^(ex-1), 2^ex) with ex from the exponent field (a
+            // subnormal counts as ex = -126, which keeps smax * 2^kap below 2^15).
+            const int ex = (int)((__float_as_uint(smax) >> 23) & 0xffu) - 126;
+            const int kmax = min(15 - ex, 127);
+            if (kmax < kap) {
+              const int d = kap == kap_unset ? -1000 : kmax - kap;
+              const float r = d < -126 ? 0.f : __uint_as_float((uint32_t)(d + 127) << 23);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) alpha[nt][0] *= r, alpha[nt][1] *= r;
+              rescale = true;
+              kap = kmax;
+              pw = __uint_as_float((uint32_t)(kmax + 127) << 23);
+            }
+          }
+          fv[0] = valid0 ? bs[0].y * pw : 0.f;
+          fv[1] = valid1 ? bs[1].y * pw : 0.f;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int a = 0; a < D / 16; ++a)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              o[a][nt][0] *= alpha[nt][0];
+              o[a][nt][1] *= alpha[nt][1];
+              o[a][nt][2] *= alpha[nt][0];
+              o[a][nt][3] *= alpha[nt][1];
+            }
+        }
+        // O^T += V^T P^T per half. V (transposed load): lane (g, t) holds
+        // elements (2g, 2g+1) of tokens 2t and 2t+1; a byte permute pairs
+        // the tokens per element, so A row g <- element 2g and row g+8 <-
+        // element 2g+1 of the chunk, k slots = the tokens.
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (!(h ? valid1 : valid0)) continue;
+          uint32_t pb[NT][2];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            pb[nt][0] = movmatrix_trans(MmaOp<__half>::pack(sc[h][nt][0] * fv[h], sc[h][nt][1] * fv[h]));
+            pb[nt][1] = movmatrix_trans(MmaOp<__half>::pack(sc[h][nt][2] * fv[h], sc[h][nt][3] * fv[h]));
+          }
+          const int th = tok0 + 16 * h;
+          uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
+          if (th + 16 > mt.t_end) {
+            // Keys past the end carry p = 0, but their V codes may hold any
+            // bits (NaN included): zero those V elements so 0 * V stays 0.
+            const int tk = th + 2 * ti;
+            keep_lo = (tk < mt.t_end ? 0x0000ffffu : 0u) | (tk + 1 < mt.t_end ? 0xffff0000u : 0u);
+            keep_hi = (tk + 8 < mt.t_end ? 0x0000ffffu : 0u) | (tk + 9 < mt.t_end ? 0xffff0000u : 0u);
+          }
+#pragma unroll
+          for (int q2 = 0; q2 < D / 32; ++q2) {
+            uint32_t a0[4], a1[4];
+            e4m3x4_to_f16x4(__byte_perm(vr[h][q2][0], 0, 0x3120), a0[0], a0[1]);
+            e4m3x4_to_f16x4(__byte_perm(vr[h][q2][1], 0, 0x3120), a0[2], a0[3]);
+            e4m3x4_to_f16x4(__byte_perm(vr[h][q2][2], 0, 0x3120), a1[0], a1[1]);
+            e4m3x4_to_f16x4(__byte_perm(vr[h][q2][3], 0, 0x3120), a1[2], a1[3]);
+            a0[0] &= keep_lo, a0[1] &= keep_lo, a0[2] &= keep_hi, a0[3] &= keep_hi;
+            a1[0] &= keep_lo, a1[1] &= keep_lo, a1[2] &= keep_hi, a1[3] &= keep_hi;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              MmaOp<__half>::run(o[2 * q2][nt], a0, pb[nt][0], pb[nt][1]);
+              MmaOp<__half>::run(o[2 * q2 + 1][nt], a1, pb[nt][0], pb[nt][1]);
+            }
+          }
+        }
       }
     }
     if (named_barrier_or(1, C::kConsumers * 32, bad)) break;
@@ -644,7 +800,7 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
         float* row = scratch + (warp * C::kHeads + h) * C::kDp;
         if constexpr (KV8) {
           // O rows: m-row tr <-> element 16a + 2tr, m-row tr + 8 <-> 16a + 2tr + 1.
-          f *= ldexpf(1.f, -kap);
+          f = pw > 0.f ? f / pw : 0.f;  // undo 2^kap (exact: a power of two)
 #pragma unroll
           for (int a = 0; a < D / 16; ++a)
             *reinterpret_cast<float2*>(row + a * 16 + 2 * tr) = make_float2(o[a][nt][c] * f, o[a][nt][c + 2] * f);

@@ -138,7 +138,7 @@ int num_sms_current_device();
 // box = [box_rows rows][64 elements] with 128-byte swizzle (16-bit dtypes only).
 int make_kv_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t head_dim, pa_dtype dt,
                        int32_t box_rows);
-// Same view of an e4m3 (one byte per element) pool: box = [box_rows rows][128 elements].
+// Same view of an e4m3 (one byte per element) pool: box = [box_rows rows][128 bytes].
 int make_u8_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t head_dim, int32_t box_rows);
 // 3-D map over a [d2][d1][d0] tensor (d0 contiguous), box [b2][b1][b0], 128-byte swizzle.
 int make_3d_tensor_map(CUtensorMap* map, const void* base, int64_t d2, int64_t d1, int64_t d0, pa_dtype dt,

@@ -6,7 +6,10 @@ A step is what a serving engine runs per layer per iteration on the KV side:
   2. slot derivation for the new tokens (pa_slot_mapping),
   3. the cache write of their K/V (pa_reshape_and_cache),
   4. attention over the paged context: pa_decode when every sequence has one
-     new query token, pa_chunked_prefill otherwise.
+     new query token (pa_decode_shared_prefix when sequences share prefix
+     blocks), pa_chunked_prefill otherwise.
+With an e4m3 cache the same step runs pa_copy_blocks_fp8,
+pa_reshape_and_cache_fp8 and pa_decode_fp8.
 This module only sequences library calls on one stream and owns the device
 buffers the calls need (slot mapping, output, split-KV workspace), allocated
 once with PyTorch.
@@ -87,6 +90,12 @@ class PagedStep:
         return n
 
     def run(self, stream=None) -> torch.Tensor:
+        self.prepare(stream)
+        self.attend(stream)
+        return self.out
+
+    def prepare(self, stream=None) -> None:
+        """The step's cache side: copy-on-write copies, slots, cache write."""
         fp8 = self.kv_scales is not None
         if self.cow_pairs.shape[0]:
             if fp8:
@@ -101,8 +110,6 @@ class PagedStep:
         else:
             pa.pa_reshape_and_cache(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
                                     stream=stream)
-        self.attend(stream)
-        return self.out
 
     def attend(self, stream=None) -> torch.Tensor:
         """The attention call of the step alone."""
