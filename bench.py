@@ -38,8 +38,12 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 DEFAULT_CONFIG = "llama3_70b_prefix_bf16"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_llama3_70b_prefix_bf16.md")
-PROFILE_SUMMARY_FP8 = os.path.join(ROOT, "profiles", "decode_e4m3_llama3_70b_prefix.md")
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def profile_summary(config: str, fp8: bool) -> str:
+    """The committed ncu summary of the decode kernel on this workload."""
+    return os.path.join(PROFILES, f"decode_e4m3_{config}.md" if fp8 else f"decode_{config}.md")
 DECODE_SRC = os.path.join(ROOT, "paged_kv_cache_14_gb300", "csrc", "pa_decode.cu")
 
 
@@ -202,7 +206,7 @@ def measured_peak_tensor() -> tuple[float, str]:
         return 1900.0, "fallback"
 
 
-def profiled_traffic(summary: str = PROFILE_SUMMARY) -> float | None:
+def profiled_traffic(summary: str) -> float | None:
     """DRAM bytes per decode launch from a committed ncu summary, if the
     decode source has not changed since it was captured."""
     try:
@@ -513,7 +517,7 @@ def native_arm(args) -> None:
                                      "paged decode (plan + main + split-KV merge)"), "bound": "hbm",
                           "achieved": round(dec_gbs, 2), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                           "frac": round(dec_gbs / peak, 4),
-                          "traffic": profiled_traffic(PROFILE_SUMMARY_FP8 if fp8 else PROFILE_SUMMARY),
+                          "traffic": profiled_traffic(profile_summary(args.config, fp8)),
                           "algorithmic_bytes": dec_bytes["total"], "ms_per_launch": round(dec_mean, 5)}
                          if st.is_decode else
                          {"kernel": "chunked prefill call (tcgen05 chunk tiles + decode rows)", "bound": "tensor",
