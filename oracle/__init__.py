@@ -22,5 +22,6 @@ from .paged_attention import (  # noqa: F401
     slot_for,
     slot_mapping,
     softmax_attention,
+    swap_blocks,
     to_f64,
 )

@@ -23,6 +23,9 @@ definition states. The sources are four web pages on PagedAttention:
      section "Physical Block Mapping and Kernel Invocation" (the attention
      equation and the block index / offset equation), section "The KV-Cache
      Bottleneck" (KV bytes per sequence).
+[P5'] the same page, section "Preemption Mechanics: Swapping vs.
+     Recomputation" (blocks of a preempted sequence swapped to a pinned host
+     pool and back); [P3] "Preemption & eviction".
 [P1] "Tech Radar: vLLM v1 Production Engine Architecture & Distributed KV
      Cache Optimization", section 2, subsection "Mathematical Modeling of
      PagedAttention v3 Memory Bounds" (block count, block bytes, internal
@@ -132,6 +135,18 @@ def copy_blocks(k_cache, v_cache, pairs) -> None:
     for src, dst in np.asarray(pairs).reshape(-1, 2):
         k_cache[int(dst)] = k_cache[int(src)]
         v_cache[int(dst)] = v_cache[int(src)]
+
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, pairs) -> None:
+    """Swap preemption ([P5] "Preemption Mechanics: Swapping vs.
+    Recomputation": a preempted sequence's blocks move to a host pool and
+    back; [P3] "Preemption & eviction"): for every (src, dst) pair the whole
+    K and V block dst_pool[dst] <- src_pool[src] (src_v / dst_v may be None
+    for a single pool)."""
+    for src, dst in np.asarray(pairs).reshape(-1, 2):
+        dst_k[int(dst)] = src_k[int(src)]
+        if src_v is not None:
+            dst_v[int(dst)] = src_v[int(src)]
 
 
 # ---------------------------------------------------------------------------

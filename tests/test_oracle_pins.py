@@ -402,10 +402,36 @@ def pin_sizing_examples():
         oracle.kv_bytes_per_sequence(80, 8, 128, 8192, 1)
 
 
+def pin_swap_roundtrip():
+    """Swap a sequence's blocks out to a host pool and back into other device
+    blocks: the blocks come back bit for bit and the sequence's attention
+    (with its table pointing at the new blocks) equals the attention before
+    the swap."""
+    rng = np.random.default_rng(31)
+    lens = np.array([40, 70])
+    q, _, _, kc, vc, tables = random_case(31, lens, B=16, hq=4, hkv=2, d=16, extra_blocks=12)
+    before = oracle.decode(q, kc, vc, tables, lens, 0.3, 16)
+    used = tables[1][: -(-int(lens[1]) // 16)]
+    free = np.setdiff1d(np.arange(kc.shape[0]), np.concatenate([tables[0][: -(-int(lens[0]) // 16)], used]))
+    host_k = np.zeros((len(used),) + kc.shape[1:])
+    host_v = np.zeros_like(host_k)
+    oracle.swap_blocks(kc, vc, host_k, host_v, [(int(b), i) for i, b in enumerate(used)])
+    saved_k, saved_v = kc[used].copy(), vc[used].copy()
+    kc[used] = np.nan                      # the device blocks are reused meanwhile
+    vc[used] = np.nan
+    new = rng.choice(free, size=len(used), replace=False)
+    oracle.swap_blocks(host_k, host_v, kc, vc, [(i, int(b)) for i, b in enumerate(new)])
+    assert np.array_equal(kc[new], saved_k, equal_nan=True) and np.array_equal(vc[new], saved_v, equal_nan=True)
+    t2 = tables.copy()
+    t2[1][: len(used)] = new
+    after = oracle.decode(q, kc, vc, t2, lens, 0.3, 16)
+    assert np.array_equal(before[1], after[1])
+
+
 ALL_PINS = [
     pin_decode_vs_sdpa, pin_prefill_vs_sdpa, pin_worked_example, pin_slots_match_layout,
     pin_reshape_and_cache_roundtrip, pin_copy_blocks, pin_permutation_invariance,
-    pin_prefix_sharing, pin_closed_forms, pin_split_merge, pin_sizing_examples,
+    pin_prefix_sharing, pin_closed_forms, pin_split_merge, pin_sizing_examples, pin_swap_roundtrip,
 ]
 
 
@@ -516,10 +542,28 @@ def _mut_fragmentation_floor(monkeypatch):
     monkeypatch.setattr(oracle, "num_blocks_for", lambda S, B: S // B)
 
 
+def _mut_swap_k_only(monkeypatch):
+    def bad(sk, sv, dk, dv, pairs):
+        for s_, d in np.asarray(pairs).reshape(-1, 2):
+            dk[int(d)] = sk[int(s_)]
+    monkeypatch.setattr(opa, "swap_blocks", bad)
+    monkeypatch.setattr(oracle, "swap_blocks", bad)
+
+
+def _mut_swap_reversed(monkeypatch):
+    def bad(sk, sv, dk, dv, pairs):
+        for s_, d in np.asarray(pairs).reshape(-1, 2):
+            dk[int(s_) % dk.shape[0]] = sk[int(d) % sk.shape[0]]
+            dv[int(s_) % dv.shape[0]] = sv[int(d) % sv.shape[0]]
+    monkeypatch.setattr(opa, "swap_blocks", bad)
+    monkeypatch.setattr(oracle, "swap_blocks", bad)
+
+
 MUTATIONS = [
     _mut_offset, _mut_swap_block_offset_in_gather, _mut_gqa, _mut_no_scale, _mut_k_for_v,
     _mut_softmax_no_norm, _mut_prefill_off_by_one, _mut_merge_sign, _mut_copy_k_only,
-    _mut_cache_write_offset0, _mut_slot_uses_logical_block, _mut_fragmentation_floor,
+    _mut_cache_write_offset0, _mut_slot_uses_logical_block, _mut_fragmentation_floor, _mut_swap_k_only,
+    _mut_swap_reversed,
 ]
 
 
