@@ -137,6 +137,36 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst_pairs, i
                    int32_t num_blocks, int64_t block_bytes, void* stream);
 
 /*
+ * pa_swap_blocks — swap preemption ("Inside vLLM: Anatomy of a
+ * High-Throughput LLM Inference System (2025)", section "Preemption
+ * Mechanics: Swapping vs. Recomputation"; "03 - PagedAttention & the vLLM V1
+ * Architecture", section "Preemption & eviction": a preempted sequence's
+ * blocks are written out to a host pool and later brought back, possibly
+ * into other physical blocks). For every pair, the whole block
+ * dst_pool[dst] <- src_pool[src] of the K pool and, if given, the V pool.
+ *   src_k, src_v : source pools ([src_num_blocks] blocks of block_bytes)
+ *   dst_k, dst_v : destination pools ([dst_num_blocks] blocks)
+ *                  Each pool is device memory, managed memory or pinned
+ *                  (page-locked: cudaHostAlloc / cudaHostRegister) host
+ *                  memory; the kernel reads and writes host memory directly
+ *                  (over NVLink-C2C on Grace-Blackwell). Pageable host memory
+ *                  returns PA_ERR_ARG. src_v and dst_v are both NULL (one
+ *                  pool, e.g. the scales of an e4m3 cache) or both given.
+ *   src_dst_pairs : HOST int64 [num_pairs][2] (src, dst), validated before
+ *                  any launch: src in [0, src_num_blocks), dst in
+ *                  [0, dst_num_blocks) else PA_ERR_BLOCK_OOB; no dst repeated
+ *                  and, when src and dst are the same pool, no dst equal to a
+ *                  src, else PA_ERR_ALIAS. Passed to the kernel by value.
+ *   block_bytes  : bytes of one block of one pool, a multiple of 4
+ *                  (PA_ERR_UNSUPPORTED otherwise); 16-byte vectors are used
+ *                  when it is a multiple of 16 and the pools are aligned.
+ * Bit-exact. num_pairs == 0 is a no-op.
+ */
+int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v, const int64_t* src_dst_pairs,
+                   int32_t num_pairs, int32_t src_num_blocks, int32_t dst_num_blocks, int64_t block_bytes,
+                   void* stream);
+
+/*
  * Split-KV partitioning of decode. A sequence of L keys is cut into
  * ceil(L / partition_size) partitions; each is reduced to (m, l, o~)
  * partials (running max, sum of exp(s - m), unnormalised output) in the

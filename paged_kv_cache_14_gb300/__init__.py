@@ -29,6 +29,7 @@ from ._binding import (  # noqa: F401
     pa_reshape_and_cache_fp8,
     pa_slot_mapping,
     pa_strerror,
+    pa_swap_blocks,
     pa_version,
 )
 from .builder import LIB_PATH, build  # noqa: F401

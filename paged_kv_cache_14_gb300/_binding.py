@@ -27,7 +27,7 @@ EXPORTS = (
     "pa_copy_blocks", "pa_decode_partition_size", "pa_decode_workspace_size", "pa_decode",
     "pa_chunked_prefill_workspace_size", "pa_chunked_prefill", "pa_decode_shared_prefix_workspace_size",
     "pa_decode_shared_prefix", "pa_decode_noalloc_scratch_limit", "pa_decode_noalloc",
-    "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8", "pa_decode_fp8",
+    "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8", "pa_decode_fp8", "pa_swap_blocks",
 )
 
 _i32, _i64, _f32, _vp, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
@@ -74,6 +74,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "pa_reshape_and_cache_fp8": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                                     ctypes.c_int, _vp]),
         "pa_copy_blocks_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp]),
+        "pa_swap_blocks": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp]),
         "pa_decode_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                          _i32, _f32, _vp, _i32, _vp, _sz, ctypes.c_int, _vp]),
     }
@@ -338,3 +339,30 @@ def pa_decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         float(scale), _cuda(out, "out", dt), int(partition_size), ws_ptr, ws_bytes, _DT[dt], _stream(stream))
     _check(rc, "pa_decode_fp8")
     return out
+
+
+def _pool_ptr(t: torch.Tensor | None, name: str) -> int | None:
+    """Pointer of a pool for pa_swap_blocks: a contiguous CUDA tensor or a
+    pinned CPU tensor."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or t.is_pinned()):
+        raise TypeError(f"{name} must be a CUDA tensor or a pinned CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def pa_swap_blocks(src_k: torch.Tensor, src_v: torch.Tensor | None, dst_k: torch.Tensor,
+                   dst_v: torch.Tensor | None, src_dst_pairs, stream=None) -> None:
+    """Whole blocks dst[dst] <- src[src] between two pools (CUDA or pinned CPU
+    tensors, leading dimension = blocks). src_dst_pairs: HOST int64 [n, 2]."""
+    pairs = np.ascontiguousarray(np.asarray(src_dst_pairs, dtype=np.int64).reshape(-1, 2))
+    if src_k.dtype != dst_k.dtype or src_k.shape[1:] != dst_k.shape[1:]:
+        raise ValueError("source and destination pools differ in block layout")
+    block_bytes = src_k[0].numel() * src_k.element_size()
+    rc = load().pa_swap_blocks(
+        _pool_ptr(src_k, "src_k"), _pool_ptr(src_v, "src_v"), _pool_ptr(dst_k, "dst_k"), _pool_ptr(dst_v, "dst_v"),
+        pairs.ctypes.data_as(ctypes.c_void_p), pairs.shape[0], src_k.shape[0], dst_k.shape[0], block_bytes,
+        _stream(stream))
+    _check(rc, "pa_swap_blocks")

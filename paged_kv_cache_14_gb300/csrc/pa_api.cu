@@ -409,6 +409,53 @@ int pa_copy_blocks_fp8(void* k_cache, void* v_cache, float* kv_scales, const int
                             static_cast<cudaStream_t>(stream));
 }
 
+// A pointer the GPU can dereference for this pool (device, managed or pinned
+// host memory), or nullptr if it cannot (pageable host memory).
+static const void* device_usable(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of the query
+    return nullptr;
+  }
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged: return p;
+    case cudaMemoryTypeHost: return a.devicePointer;
+    default: return nullptr;
+  }
+}
+
+int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v, const int64_t* src_dst_pairs,
+                   int32_t num_pairs, int32_t src_num_blocks, int32_t dst_num_blocks, int64_t block_bytes,
+                   void* stream) {
+  if (num_pairs < 0 || src_num_blocks < 1 || dst_num_blocks < 1 || block_bytes <= 0) return PA_ERR_ARG;
+  if (block_bytes % 4 != 0) return PA_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PA_OK;
+  if (!src_k || !dst_k || !src_dst_pairs || (src_v == nullptr) != (dst_v == nullptr)) return PA_ERR_ARG;
+  const bool same_pool = src_k == dst_k;
+  std::vector<int32_t> src(num_pairs), dst(num_pairs);
+  std::unordered_set<int64_t> dsts;
+  dsts.reserve(num_pairs * 2);
+  for (int32_t i = 0; i < num_pairs; ++i) {
+    const int64_t s = src_dst_pairs[2 * i], d = src_dst_pairs[2 * i + 1];
+    if (s < 0 || s >= src_num_blocks || d < 0 || d >= dst_num_blocks) return PA_ERR_BLOCK_OOB;
+    if (!dsts.insert(d).second) return PA_ERR_ALIAS;
+    src[i] = (int32_t)s;
+    dst[i] = (int32_t)d;
+  }
+  if (same_pool)
+    for (int32_t i = 0; i < num_pairs; ++i)
+      if (dsts.count(src[i])) return PA_ERR_ALIAS;
+  const void* sk = device_usable(src_k);
+  const void* dk = device_usable(dst_k);
+  const void* sv = src_v ? device_usable(src_v) : nullptr;
+  const void* dv = dst_v ? device_usable(dst_v) : nullptr;
+  if (!sk || !dk || (src_v && (!sv || !dv))) return PA_ERR_ARG;
+  const int vec16 = block_bytes % 16 == 0 && aligned16(sk) && aligned16(dk) && (!sv || (aligned16(sv) && aligned16(dv)));
+  return launch_swap_blocks(sk, sv, const_cast<void*>(dk), const_cast<void*>(dv), src.data(), dst.data(), num_pairs,
+                            block_bytes, vec16, static_cast<cudaStream_t>(stream));
+}
+
 size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                               int32_t head_dim, int32_t block_size, int32_t max_seq_len,
                                               int32_t partition_size, int32_t num_groups) {

@@ -259,6 +259,39 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint8_t* __restrict__ 
   for (; i < n; i += 256) dst[i] = src[i];
 }
 
+// Swap preemption ("Inside vLLM...", section "Preemption Mechanics: Swapping
+// vs. Recomputation"): whole blocks between two pools, either of which may be
+// device memory or pinned host memory (the GPU reaches the latter directly,
+// over NVLink-C2C on a Grace-Blackwell node). grid = (num_pairs, pools): y
+// selects the K or the V pool; one CTA per block, four independent loads in
+// flight per thread so remote host memory latency is covered.
+__global__ void __launch_bounds__(256) swap_blocks_kernel(const uint8_t* __restrict__ src_k,
+                                                          const uint8_t* __restrict__ src_v,
+                                                          uint8_t* __restrict__ dst_k, uint8_t* __restrict__ dst_v,
+                                                          const __grid_constant__ CopyPairs pairs,
+                                                          int64_t block_bytes, int vec16) {
+  const uint8_t* sp = (blockIdx.y == 0 ? src_k : src_v) + (int64_t)pairs.src[blockIdx.x] * block_bytes;
+  uint8_t* dp = (blockIdx.y == 0 ? dst_k : dst_v) + (int64_t)pairs.dst[blockIdx.x] * block_bytes;
+  if (vec16) {
+    const int4* src = reinterpret_cast<const int4*>(sp);
+    int4* dst = reinterpret_cast<int4*>(dp);
+    const int64_t n = block_bytes >> 4;
+    int64_t i = threadIdx.x;
+    for (; i + 3 * 256 < n; i += 4 * 256) {
+      int4 a = src[i], b = src[i + 256], c = src[i + 512], d = src[i + 768];
+      dst[i] = a;
+      dst[i + 256] = b;
+      dst[i + 512] = c;
+      dst[i + 768] = d;
+    }
+    for (; i < n; i += 256) dst[i] = src[i];
+  } else {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(sp);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(dp);
+    for (int64_t i = threadIdx.x; i < (block_bytes >> 2); i += 256) dst[i] = src[i];
+  }
+}
+
 static int grid_for(int64_t work, int per_block) {
   int64_t g = (work + per_block - 1) / per_block;
   if (g < 1) g = 1;
@@ -297,6 +330,24 @@ int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const i
     }
     copy_blocks_kernel<<<dim3(n, 2), 256, 0, stream>>>(static_cast<uint8_t*>(k_cache),
                                                        static_cast<uint8_t*>(v_cache), pairs, block_bytes);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+int launch_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v, const int32_t* src,
+                       const int32_t* dst, int32_t num_pairs, int64_t block_bytes, int vec16, cudaStream_t stream) {
+  const int pools = src_v ? 2 : 1;
+  for (int32_t base = 0; base < num_pairs; base += kCopyPairsPerLaunch) {
+    const int32_t n = num_pairs - base < kCopyPairsPerLaunch ? num_pairs - base : kCopyPairsPerLaunch;
+    CopyPairs pairs;
+    for (int32_t i = 0; i < n; ++i) {
+      pairs.src[i] = src[base + i];
+      pairs.dst[i] = dst[base + i];
+    }
+    swap_blocks_kernel<<<dim3(n, pools), 256, 0, stream>>>(
+        static_cast<const uint8_t*>(src_k), static_cast<const uint8_t*>(src_v), static_cast<uint8_t*>(dst_k),
+        static_cast<uint8_t*>(dst_v), pairs, block_bytes, vec16);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;

@@ -161,6 +161,9 @@ int launch_reshape_and_cache_fp8(const void* k, const void* v, const int64_t* sl
                                  uint8_t* k_cache, uint8_t* v_cache, float* kv_scales, int32_t num_blocks,
                                  int32_t block_size, int32_t num_kv_heads, int32_t head_dim, pa_dtype dt,
                                  int* status, cudaStream_t stream);
+// Whole blocks between two pools (device or pinned host memory; device-usable pointers).
+int launch_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v, const int32_t* src,
+                       const int32_t* dst, int32_t num_pairs, int64_t block_bytes, int vec16, cudaStream_t stream);
 // The (K, V) scales of whole blocks, dst <- src.
 int launch_copy_scales(float* kv_scales, const int32_t* src, const int32_t* dst, int32_t num_pairs,
                        int32_t num_kv_heads, cudaStream_t stream);

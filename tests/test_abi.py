@@ -172,3 +172,19 @@ def test_fp8_host_checks(lib):
     assert cp8([(1, 10)]) == -7
     assert cp8([(1, 2)], sc=None) == -1
     assert cp8([]) == 0
+
+
+def test_swap_host_checks(lib):
+    def call(pairs, **o):
+        arr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+        a = dict(sk=0x1000, sv=0x2000, dk=0x3000, dv=0x4000, ns=10, nd=6, bb=4096)
+        a.update(o)
+        return lib.pa_swap_blocks(a["sk"], a["sv"], a["dk"], a["dv"], arr.ctypes.data_as(ctypes.c_void_p),
+                                  arr.shape[0], a["ns"], a["nd"], a["bb"], None)
+    assert call([(9, 5)], bb=4098) == -10        # block bytes not a multiple of 4
+    assert call([(10, 0)]) == -7                 # src outside its pool
+    assert call([(0, 6)]) == -7                  # dst outside its pool
+    assert call([(1, 2), (3, 2)]) == -6          # dst repeated
+    assert call([(1, 2), (2, 3)], dk=0x1000, dv=0x2000, nd=10) == -6   # same pool: dst 2 is a src
+    assert call([(1, 2)], sv=None) == -1         # one V pool without the other
+    assert call([]) == 0
