@@ -14,17 +14,18 @@
 // tile, KV head) listed by a plan kernel, longest first:
 //   warp 0  producer: TMA of the 128 query rows (3-D tensor map over
 //           [tokens][heads][head_dim], 128-byte swizzle), then for every
-//           64-token KV tile the four 16-token sub-tiles of K and V through
-//           the block table into a 2-stage ring;
-//   warp 1  owns the tensor memory (256 columns: S = 128x64 fp32 at column 0,
-//           O = 128x128 fp32 at column 128) and one lane issues the MMAs:
-//           S = Q K^T (K-major operands), then O += P V (P K-major from
-//           shared memory, V MN-major);
+//           64-token KV tile the four 16-token sub-tiles of K and of V
+//           through the block table, into separate 2-stage K and V rings;
+//   warp 1  owns the tensor memory (256 columns: two S buffers of 128x64
+//           fp32 at columns 0 and 64, O = 128x128 fp32 at column 128) and
+//           one lane issues the MMAs: S = Q K^T (K-major operands from
+//           shared memory), then O += P V with P read from tensor memory
+//           and V an MN-major shared-memory operand;
 //   warps 2-5  softmax: thread i owns row i (tensor-memory lane i): it loads
 //           its S row, applies the causal mask, keeps the running max and sum
-//           in registers, writes P (16-bit) into the swizzled P tile,
-//           rescales its O row in tensor memory when the max moved, and at
-//           the end normalises O and stores it.
+//           in registers, writes P (16-bit) back over its S row, rescales its
+//           O row in tensor memory when the max moved, and at the end
+//           normalises O and stores it.
 // Every mbarrier wait is time-bounded: on a timeout the kernel records
 // PA_ERR_TIMEOUT, lets outstanding copies and MMAs finish (bounded) and
 // returns; no wait can spin forever.
@@ -46,23 +47,27 @@ constexpr int kThreads = 192;  // producer, MMA, 4 softmax warps
 constexpr int kQHalf = kM * 128;           // one 64-column half of Q: 128 rows x 128 B
 constexpr int kQBytes = 2 * kQHalf;        // 32 KB
 constexpr int kKVHalf = kN * 128;          // 64 rows x 128 B
-constexpr int kKBytes = 2 * kKVHalf;       // 16 KB
-constexpr int kStageBytes = 2 * kKBytes;   // K + V: 32 KB
-constexpr int kPBytes = kM * 128;          // 128 rows x 64 keys x 2 B
+constexpr int kKBytes = 2 * kKVHalf;       // one K (or V) tile: 16 KB
+constexpr int NK = 2;                      // K stages
+constexpr int NV = 2;                      // V stages
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kQBytes;
+constexpr int kOffK = kOffQ + kQBytes;
+constexpr int kOffV = kOffK + NK * kKBytes;
+constexpr int kOffBar = kOffV + NV * kKBytes;
+// bars: q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2], o_done[2]
+constexpr int kBarQ = 0;
+constexpr int kBarKFull = 1;
+constexpr int kBarKEmpty = kBarKFull + NK;
+constexpr int kBarVFull = kBarKEmpty + NK;
+constexpr int kBarVEmpty = kBarVFull + NV;
+constexpr int kBarSFull = kBarVEmpty + NV;
+constexpr int kBarPFull = kBarSFull + 2;
+constexpr int kBarODone = kBarPFull + 2;
+constexpr int kNumBars = kBarODone + 2;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, item, abort
+constexpr int kSmem = kOffMisc + 64;
 constexpr int kTmemCols = 256;
-// Layout past the K/V ring of NS stages.
-template <int NS>
-struct Layout {
-  static constexpr int kOffP = kOffKV + NS * kStageBytes;
-  static constexpr int kOffBar = kOffP + kPBytes;
-  // bars: q_full, kv_full[NS], kv_empty[NS], s_full[2], s_free[2], p_full, o_done
-  static constexpr int kNumBars = 1 + 2 * NS + 6;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, item, abort
-  static constexpr int kSmem = kOffMisc + 64;
-};
-constexpr int kColS = 0;  // two S buffers: columns 0..63 and 64..127 (tile g uses buffer g & 1)
+constexpr int kColS = 0;  // two S buffers: columns 0..63 and 64..127 (tile g uses buffer g & 1); P(g) over its first 32
 constexpr int kColO = 128;
 }  // namespace pf
 
@@ -132,27 +137,38 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
 // PREFIX = true: prefix pass of shared-prefix decode (rows = group members x
 // GQA heads, each row masked to its own verified prefix, fp32 partial
 // (m, l, o~) written to slot 0 of the member's partials).
-template <typename T, int BS, bool PREFIX, int NS>
-__global__ void __launch_bounds__(pf::kThreads, NS <= 2 ? 2 : 1)
+//
+// Pipeline of one item (tile g = tile_base + j):
+//   producer:  K(g) into K stage g % NK (after S(g - NK) freed it), V(g) into
+//              V stage g % NV (after PV(g - NV) freed it);
+//   MMA:       S(g) into S buffer g & 1 two tiles ahead; after P(g) is ready,
+//              PV(g) with P read from tensor memory (the A operand), then
+//              S(g + 2) into the same buffer. The tensor pipe executes one
+//              thread's MMAs in issue order, so S(g + 2) cannot overwrite
+//              P(g) before PV(g) has read it;
+//   softmax:   reads S(g), writes P(g) (16-bit) over the first 32 columns of
+//              the same buffer, and only waits for PV(g - 1) when it must
+//              rescale O (the running max grew past the lazy threshold).
+// Barriers with more than one phase in flight are doubled per buffer parity
+// (s_full, p_full, o_done), so no parity wait can alias an older phase.
+template <typename T, int BS, bool PREFIX>
+__global__ void __launch_bounds__(pf::kThreads, 2)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
   using namespace pf;
-  using Lay = Layout<NS>;
-  constexpr int kOffP = Lay::kOffP;
-  constexpr int kOffBar = Lay::kOffBar;
-  constexpr int kOffMisc = Lay::kOffMisc;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   constexpr uint32_t kIdescS = idesc_f16(kM, kN, kBf16, false);  // S = Q K^T
   constexpr uint32_t kIdescO = idesc_f16(kM, kD, kBf16, true);   // O += P V (V MN-major)
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  const uint32_t b_q = smem_u32(&bars[0]);
-  const uint32_t b_kvfull0 = smem_u32(&bars[1]);        // + 8 * stage
-  const uint32_t b_kvempty0 = smem_u32(&bars[1 + NS]);  // + 8 * stage
-  const uint32_t b_sfull0 = smem_u32(&bars[1 + 2 * NS]);  // + 8 * buffer
-  const uint32_t b_sfree0 = smem_u32(&bars[3 + 2 * NS]);  // + 8 * buffer
-  const uint32_t b_pfull = smem_u32(&bars[5 + 2 * NS]);
-  const uint32_t b_odone = smem_u32(&bars[6 + 2 * NS]);
+  const uint32_t b_q = smem_u32(&bars[kBarQ]);
+  const uint32_t b_kfull0 = smem_u32(&bars[kBarKFull]);    // + 8 * stage
+  const uint32_t b_kempty0 = smem_u32(&bars[kBarKEmpty]);  // + 8 * stage
+  const uint32_t b_vfull0 = smem_u32(&bars[kBarVFull]);    // + 8 * stage
+  const uint32_t b_vempty0 = smem_u32(&bars[kBarVEmpty]);  // + 8 * stage
+  const uint32_t b_sfull0 = smem_u32(&bars[kBarSFull]);    // + 8 * buffer
+  const uint32_t b_pfull0 = smem_u32(&bars[kBarPFull]);    // + 8 * buffer
+  const uint32_t b_odone0 = smem_u32(&bars[kBarODone]);    // + 8 * (tile & 1)
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(&misc[2]);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -161,16 +177,19 @@ __global__ void __launch_bounds__(pf::kThreads, NS <= 2 ? 2 : 1)
   if (threadIdx.x == 0) {
     if ((sbase & 1023u) != 0) record_error(p.status, PA_ERR_ALIGN);
     mbar_init(b_q, 1);
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(b_kvfull0 + 8 * i, 1);
-      mbar_init(b_kvempty0 + 8 * i, 1);
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(b_kfull0 + 8 * i, 1);
+      mbar_init(b_kempty0 + 8 * i, 1);
     }
-    mbar_init(b_sfull0, 1);
-    mbar_init(b_sfull0 + 8, 1);
-    mbar_init(b_sfree0, 4);
-    mbar_init(b_sfree0 + 8, 4);
-    mbar_init(b_pfull, 4);
-    mbar_init(b_odone, 1);
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(b_vfull0 + 8 * i, 1);
+      mbar_init(b_vempty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_sfull0 + 8 * i, 1);
+      mbar_init(b_pfull0 + 8 * i, 4);
+      mbar_init(b_odone0 + 8 * i, 1);
+    }
     abort_flag[0] = (sbase & 1023u) != 0;
     fence_barrier_init();
   }
@@ -224,6 +243,7 @@ __global__ void __launch_bounds__(pf::kThreads, NS <= 2 ? 2 : 1)
     if (warp == 0) {
       // =========================== producer ===========================
       bool bad = false;
+      int k_issued = 0, v_issued = 0;  // tiles of this item whose K / V copies were issued
       if (lane == 0) {
         mbar_arrive_expect_tx(b_q, kQBytes);
         tma_load_3d(sbase + kOffQ, &qmap, 0, kvh * G, q_z, b_q);
@@ -232,7 +252,6 @@ __global__ void __launch_bounds__(pf::kThreads, NS <= 2 ? 2 : 1)
       const int32_t* bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
       for (int j = 0; j < ntiles; ++j) {
         const int g = tile_base + j;
-        const int s = g % NS;
         // Lanes 0..3: physical block of the tile's 16-token sub-tile `lane`.
         int id = 0;
         if (lane < 4) {
@@ -249,20 +268,33 @@ __global__ void __launch_bounds__(pf::kThreads, NS <= 2 ? 2 : 1)
 #pragma unroll
         for (int u = 0; u < 4; ++u) ids[u] = __shfl_sync(0xffffffffu, id, u);
         if (lane == 0) {
-          if (g >= NS && !mbar_wait(b_kvempty0 + 8 * s, ((g / NS) & 1) ^ 1, p.status)) {
+          const int sk = g % NK, sv = g % NV;
+          if (g >= NK && !mbar_wait(b_kempty0 + 8 * sk, ((g / NK) & 1) ^ 1, p.status)) {
             bad = true;
           } else {
-            const uint32_t fb = b_kvfull0 + 8 * s;
-            mbar_arrive_expect_tx(fb, kStageBytes);
-            const uint32_t kdst = sbase + kOffKV + s * kStageBytes;
+            const uint32_t fb = b_kfull0 + 8 * sk;
+            mbar_arrive_expect_tx(fb, kKBytes);
+            const uint32_t kdst = sbase + kOffK + sk * kKBytes;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int row = (ids[u] * p.num_kv_heads + kvh) * BS + ((j * kN + u * 16) % BS);
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                tma_load_2d(kdst + h * kKVHalf + u * 2048, &kmap, h * 64, row, fb);
-                tma_load_2d(kdst + kKBytes + h * kKVHalf + u * 2048, &vmap, h * 64, row, fb);
+              for (int h = 0; h < 2; ++h) tma_load_2d(kdst + h * kKVHalf + u * 2048, &kmap, h * 64, row, fb);
+            }
+            k_issued = j + 1;
+            if (g >= NV && !mbar_wait(b_vempty0 + 8 * sv, ((g / NV) & 1) ^ 1, p.status)) {
+              bad = true;
+            } else {
+              const uint32_t fv = b_vfull0 + 8 * sv;
+              mbar_arrive_expect_tx(fv, kKBytes);
+              const uint32_t vdst = sbase + kOffV + sv * kKBytes;
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int row = (ids[u] * p.num_kv_heads + kvh) * BS + ((j * kN + u * 16) % BS);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) tma_load_2d(vdst + h * kKVHalf + u * 2048, &vmap, h * 64, row, fv);
               }
+              v_issued = j + 1;
             }
           }
         }
@@ -272,8 +304,10 @@ __global__ void __launch_bounds__(pf::kThreads, NS <= 2 ? 2 : 1)
           // Let the copies already issued land before the CTA moves on.
           if (lane == 0) {
             mbar_wait(b_q, it & 1, nullptr);
-            for (int jj = max(0, j - NS); jj < j; ++jj)
-              mbar_wait(b_kvfull0 + 8 * ((tile_base + jj) % NS), ((tile_base + jj) / NS) & 1, nullptr);
+            for (int jj = max(0, k_issued - NK); jj < k_issued; ++jj)
+              mbar_wait(b_kfull0 + 8 * ((tile_base + jj) % NK), ((tile_base + jj) / NK) & 1, nullptr);
+            for (int jj = max(0, v_issued - NV); jj < v_issued; ++jj)
+              mbar_wait(b_vfull0 + 8 * ((tile_base + jj) % NV), ((tile_base + jj) / NV) & 1, nullptr);
           }
           break;
         }
@@ -283,45 +317,43 @@ __global__ void __launch_bounds__(pf::kThreads, NS <= 2 ? 2 : 1)
       if (lane == 0) {
         bool bad = !mbar_wait(b_q, it & 1, p.status);
         uint32_t last_bar = 0, last_phase = 0;  // the last commit: it covers every MMA issued before it
-        // S for tile g goes to TMEM buffer g & 1; S of the next tile is issued
-        // before waiting for this tile's P, so the tensor core computes it
-        // while the softmax warps work.
         auto issue_s = [&](int g) -> bool {
-          const int st = g % NS;  // K/V stage
+          const int sk = g % NK;  // K stage
           const int sb = g & 1;   // S buffer
-          if (!mbar_wait(b_kvfull0 + 8 * st, (g / NS) & 1, p.status)) return false;
-          if (g >= 2 && !mbar_wait(b_sfree0 + 8 * sb, ((g >> 1) & 1) ^ 1, p.status)) return false;
+          if (!mbar_wait(b_kfull0 + 8 * sk, (g / NK) & 1, p.status)) return false;
           tc_fence_after();
-          const uint32_t kst = sbase + kOffKV + st * kStageBytes;
+          const uint32_t kst = sbase + kOffK + sk * kKBytes;
 #pragma unroll
           for (int k = 0; k < kD / 16; ++k) {
             const uint64_t ad = sdesc_sw128(sbase + kOffQ + (k >> 2) * kQHalf + (k & 3) * 32, 16, 1024);
             const uint64_t bd = sdesc_sw128(kst + (k >> 2) * kKVHalf + (k & 3) * 32, 16, 1024);
             tc_mma_f16(tmem + kColS + sb * kN, ad, bd, kIdescS, k > 0);
           }
+          tc_commit(b_kempty0 + 8 * sk);
           tc_commit(b_sfull0 + 8 * sb);
           last_bar = b_sfull0 + 8 * sb;
           last_phase = (g >> 1) & 1;
           return true;
         };
         if (!bad && ntiles > 0) bad = !issue_s(tile_base);
+        if (!bad && ntiles > 1) bad = !issue_s(tile_base + 1);
         for (int j = 0; j < ntiles && !bad; ++j) {
           const int g = tile_base + j;
-          const int s = g % NS;
-          if (j + 1 < ntiles && !issue_s(g + 1)) { bad = true; break; }
-          if (!mbar_wait(b_pfull, g & 1, p.status)) { bad = true; break; }
+          const int sb = g & 1, sv = g % NV;
+          if (!mbar_wait(b_pfull0 + 8 * sb, (g >> 1) & 1, p.status)) { bad = true; break; }
+          if (!mbar_wait(b_vfull0 + 8 * sv, (g / NV) & 1, p.status)) { bad = true; break; }
           tc_fence_after();
-          const uint32_t kst = sbase + kOffKV + s * kStageBytes;
+          const uint32_t vst = sbase + kOffV + sv * kKBytes;
 #pragma unroll
           for (int k = 0; k < kN / 16; ++k) {
-            const uint64_t ad = sdesc_sw128(sbase + kOffP + k * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(kst + kKBytes + k * 2048, kKVHalf, 1024);
-            tc_mma_f16(tmem + kColO, ad, bd, kIdescO, (j > 0 || k > 0) ? 1u : 0u);
+            const uint64_t bd = sdesc_sw128(vst + k * 2048, kKVHalf, 1024);
+            tc_mma_f16_ta(tmem + kColO, tmem + kColS + sb * kN + k * 8, bd, kIdescO, (j > 0 || k > 0) ? 1u : 0u);
           }
-          tc_commit(b_odone);
-          tc_commit(b_kvempty0 + 8 * s);
-          last_bar = b_odone;
-          last_phase = g & 1;
+          tc_commit(b_vempty0 + 8 * sv);
+          tc_commit(b_odone0 + 8 * sb);
+          last_bar = b_odone0 + 8 * sb;
+          last_phase = (g >> 1) & 1;
+          if (j + 2 < ntiles && !issue_s(g + 2)) { bad = true; break; }
         }
         if (bad) {
           abort_flag[0] = 1;
@@ -355,9 +387,6 @@ __global__ void __launch_bounds__(pf::kThreads, NS <= 2 ? 2 : 1)
         tmem_ld32(tmem + tl + kColS + sb * kN, sr[0]);
         tmem_ld32(tmem + tl + kColS + sb * kN + 32, sr[1]);
         tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_sfree0 + 8 * sb);
         const int k0 = j * kN;
         // Raw-score row max (scale > 0 keeps the order); the causal / prefix
         // mask is skipped when the whole tile is visible to every row of the warp.
@@ -403,30 +432,24 @@ __global__ void __launch_bounds__(pf::kThreads, NS <= 2 ? 2 : 1)
             pk[h * 16 + c / 2] = MmaOp<T>::pack(a, b);
           }
         l = l * alpha + rs;
-        // PV of the previous tile must be done before P and O are touched.
-        if (j > 0 && !mbar_wait(b_odone, (g - 1) & 1, p.status)) { bad = true; break; }
-        tc_fence_after();
-        const int s = g % NS;
         if (k0 + kN > kv_len) {
           // Keys past the sequence end carry p = 0, but their V slots may
-          // hold any bits (NaN included): zero those V rows.
-          if (!mbar_wait(b_kvfull0 + 8 * s, (g / NS) & 1, p.status)) { bad = true; break; }
-          uint8_t* vst = smem + kOffKV + s * kStageBytes + kKBytes;
+          // hold any bits (NaN included): zero those V rows before PV reads them.
+          const int sv = g % NV;
+          if (!mbar_wait(b_vfull0 + 8 * sv, (g / NV) & 1, p.status)) { bad = true; break; }
+          uint8_t* vst = smem + kOffV + sv * kKBytes;
           const int first = max(kv_len - k0, 0);
           for (int idx = threadIdx.x - 64; idx < (kN - first) * 16; idx += 128) {
             const int r = first + idx / 16, c = idx % 16;  // row, 16-byte chunk over both halves
             *reinterpret_cast<int4*>(vst + (c >> 3) * kKVHalf + r * 128 + (c & 7) * 16) = make_int4(0, 0, 0, 0);
           }
+          fence_async_shared();
         }
-        // P row (64 keys, 16-bit) into the 128-byte-swizzled K-major P tile.
-        uint8_t* prow = smem + kOffP + row * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        fence_async_shared();
-        // Rescale the O row when the running max moved (warp-uniform).
+        // Rescale the O row when the running max moved (warp-uniform); PV of
+        // the previous tile must have finished accumulating into O first.
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          if (!mbar_wait(b_odone0 + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1, p.status)) { bad = true; break; }
+          tc_fence_after();
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t orow[32];
@@ -436,13 +459,17 @@ __global__ void __launch_bounds__(pf::kThreads, NS <= 2 ? 2 : 1)
             for (int c = 0; c < 32; ++c) orow[c] = __float_as_uint(__uint_as_float(orow[c]) * alpha);
             tmem_st32(tmem + tl + kColO + cc * 32, orow);
           }
-          tmem_st_wait();
         }
+        // P (64 keys, 16-bit pairs) over the first 32 columns of this tile's
+        // S buffer: the A operand of PV.
+        tmem_st32(tmem + tl + kColS + sb * kN, pk);
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(b_pfull);
+        if (lane == 0) mbar_arrive(b_pfull0 + 8 * sb);
       }
-      if (!bad && mbar_wait(b_odone, (tile_base + ntiles - 1) & 1, p.status)) {
+      const int gl = tile_base + ntiles - 1;
+      if (!bad && mbar_wait(b_odone0 + 8 * (gl & 1), (gl >> 1) & 1, p.status)) {
         tc_fence_after();
         if constexpr (!PREFIX) {
           const float inv = 1.f / l;
@@ -500,20 +527,16 @@ __global__ void __launch_bounds__(pf::kThreads, NS <= 2 ? 2 : 1)
 template <typename T, int BS, bool PREFIX>
 static int launch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                  const PrefillParams& p, int ctas, cudaStream_t stream) {
-  // Chunked prefill: 2 stages, two CTAs per SM. Prefix pass (few items, one
-  // CTA per SM): 4 stages to keep more K/V in flight per CTA.
-  constexpr int NS = PREFIX ? 4 : 2;
-  constexpr int kSmemBytes = pf::Layout<NS>::kSmem;
-  auto kern = prefill_tc_kernel<T, BS, PREFIX, NS>;
+  auto kern = prefill_tc_kernel<T, BS, PREFIX>;
   static bool attr_set[64] = {};  // one flag per device for this instantiation
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pf::kSmem) != cudaSuccess)
       return PA_ERR_CUDA;
     attr_set[dev] = true;
   }
-  kern<<<ctas, pf::kThreads, kSmemBytes, stream>>>(qmap, kmap, vmap, p);
+  kern<<<ctas, pf::kThreads, pf::kSmem, stream>>>(qmap, kmap, vmap, p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
