@@ -66,13 +66,7 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t codes, uint32_t& lo, ui
       : "r"(codes));
 }
 
-// 2^x with the hardware approximation (inputs here are <= 0 or -inf; the
-// result's relative error is a few ulp, results below 2^-126 flush to 0).
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
+
 
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

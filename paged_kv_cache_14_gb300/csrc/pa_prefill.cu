@@ -392,22 +392,19 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
         // mask is skipped when the whole tile is visible to every row of the warp.
         const bool full_vis = __all_sync(0xffffffffu, k0 + kN - 1 <= lim);
         float mx = -CUDART_INF_F;
-        if (full_vis) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(sr[h][c]));
-        } else {
+        if (!full_vis) {
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
               const int key = k0 + h * 32 + c;
-              const float v = key <= lim ? __uint_as_float(sr[h][c]) : -CUDART_INF_F;
-              sr[h][c] = __float_as_uint(v);
-              mx = fmaxf(mx, v);
+              if (key > lim) sr[h][c] = __float_as_uint(-CUDART_INF_F);
             }
         }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) mx = fmax3(mx, __uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1]));
         // Exponentials are taken against m (raw units). It only moves up when
         // the row max exceeds it by more than 2^8 in probability (then O and l
         // are rescaled); below that, p <= 256 stays exact enough in fp32 and
@@ -416,22 +413,28 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
         if (m == -CUDART_INF_F) {
           m = mx;  // first keys of this row (still -inf for a row without keys)
         } else if ((mx - m) * sl2 > 8.f) {
-          alpha = exp2f((m - mx) * sl2);
+          alpha = fast_exp2((m - mx) * sl2);
           m = mx;
         }
         const float neg = m == -CUDART_INF_F ? 0.f : -m * sl2;
-        float rs = 0.f;
+        // p = 2^(s * scale * log2(e) - m * scale * log2(e)), two keys per
+        // paired FMA; the row sum accumulates in pairs.
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), negx2 = f2_pack(neg, neg);
+        uint64_t rs2 = f2_pack(0.f, 0.f);
         uint32_t pk[32];
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            const float a = exp2f(fmaf(__uint_as_float(sr[h][c]), sl2, neg));
-            const float b = exp2f(fmaf(__uint_as_float(sr[h][c + 1]), sl2, neg));
-            rs += a + b;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1])), sl2x2, negx2), x0, x1);
+            const float a = fast_exp2(x0), b = fast_exp2(x1);
+            rs2 = f2_add(rs2, f2_pack(a, b));
             pk[h * 16 + c / 2] = MmaOp<T>::pack(a, b);
           }
-        l = l * alpha + rs;
+        float rs0, rs1;
+        f2_unpack(rs2, rs0, rs1);
+        l = l * alpha + (rs0 + rs1);
         if (k0 + kN > kv_len) {
           // Keys past the sequence end carry p = 0, but their V slots may
           // hold any bits (NaN included): zero those V rows before PV reads them.
