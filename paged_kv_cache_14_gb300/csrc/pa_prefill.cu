@@ -42,11 +42,16 @@ namespace pa {
 namespace pf {
 constexpr int kM = 128;        // packed rows per tile (tensor-memory lanes)
 constexpr int kD = 128;        // head_dim
-constexpr int kN = 64;         // keys per KV tile
+#ifndef PA_PREFILL_KN
+#define PA_PREFILL_KN 64
+#endif
+constexpr int kN = PA_PREFILL_KN;  // keys per KV tile (64: two CTAs per SM; 128: one)
+constexpr int kSubTiles = kN / 16;  // 16-token sub-tiles per KV tile
+constexpr int kCtasPerSm = kN == 64 ? 2 : 1;
 constexpr int kThreads = 192;  // producer, MMA, 4 softmax warps
 constexpr int kQHalf = kM * 128;           // one 64-column half of Q: 128 rows x 128 B
 constexpr int kQBytes = 2 * kQHalf;        // 32 KB
-constexpr int kKVHalf = kN * 128;          // 64 rows x 128 B
+constexpr int kKVHalf = kN * 128;          // kN rows x 128 B
 constexpr int kKBytes = 2 * kKVHalf;       // one K (or V) tile: 16 KB
 constexpr int NK = 2;                      // K stages
 constexpr int NV = 2;                      // V stages
@@ -66,9 +71,9 @@ constexpr int kBarODone = kBarPFull + 2;
 constexpr int kNumBars = kBarODone + 2;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, item, abort
 constexpr int kSmem = kOffMisc + 64;
-constexpr int kTmemCols = 256;
-constexpr int kColS = 0;  // two S buffers: columns 0..63 and 64..127 (tile g uses buffer g & 1); P(g) over its first 32
-constexpr int kColO = 128;
+constexpr int kColS = 0;        // two S buffers of kN columns (tile g uses buffer g & 1); P(g) over its first kN/2
+constexpr int kColO = 2 * kN;   // O: 128 columns
+constexpr int kTmemCols = kN == 64 ? 256 : 512;
 }  // namespace pf
 
 // Plan: list (sequence, row tile) pairs of every chunk with q_len > 1,
@@ -152,7 +157,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
 // Barriers with more than one phase in flight are doubled per buffer parity
 // (s_full, p_full, o_done), so no parity wait can alias an older phase.
 template <typename T, int BS, bool PREFIX>
-__global__ void __launch_bounds__(pf::kThreads, 2)
+__global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
   using namespace pf;
@@ -252,9 +257,9 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
       const int32_t* bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
       for (int j = 0; j < ntiles; ++j) {
         const int g = tile_base + j;
-        // Lanes 0..3: physical block of the tile's 16-token sub-tile `lane`.
+        // Lanes 0..kSubTiles-1: physical block of the tile's 16-token sub-tile `lane`.
         int id = 0;
-        if (lane < 4) {
+        if (lane < kSubTiles) {
           const int bi = (j * kN + lane * 16) / BS;
           if (bi < nblk_seq) {
             id = bt[bi];
@@ -264,9 +269,9 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
             }
           }
         }
-        int ids[4];
+        int ids[kSubTiles];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) ids[u] = __shfl_sync(0xffffffffu, id, u);
+        for (int u = 0; u < kSubTiles; ++u) ids[u] = __shfl_sync(0xffffffffu, id, u);
         if (lane == 0) {
           const int sk = g % NK, sv = g % NV;
           if (g >= NK && !mbar_wait(b_kempty0 + 8 * sk, ((g / NK) & 1) ^ 1, p.status)) {
@@ -276,7 +281,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
             mbar_arrive_expect_tx(fb, kKBytes);
             const uint32_t kdst = sbase + kOffK + sk * kKBytes;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kSubTiles; ++u) {
               const int row = (ids[u] * p.num_kv_heads + kvh) * BS + ((j * kN + u * 16) % BS);
 #pragma unroll
               for (int h = 0; h < 2; ++h) tma_load_2d(kdst + h * kKVHalf + u * 2048, &kmap, h * 64, row, fb);
@@ -289,7 +294,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
               mbar_arrive_expect_tx(fv, kKBytes);
               const uint32_t vdst = sbase + kOffV + sv * kKBytes;
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
+              for (int u = 0; u < kSubTiles; ++u) {
                 const int row = (ids[u] * p.num_kv_heads + kvh) * BS + ((j * kN + u * 16) % BS);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) tma_load_2d(vdst + h * kKVHalf + u * 2048, &vmap, h * 64, row, fv);
@@ -383,9 +388,9 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
         const int sb = g & 1;  // S buffer of this tile
         if (!mbar_wait(b_sfull0 + 8 * sb, (g >> 1) & 1, p.status)) { bad = true; break; }
         tc_fence_after();
-        uint32_t sr[2][32];
-        tmem_ld32(tmem + tl + kColS + sb * kN, sr[0]);
-        tmem_ld32(tmem + tl + kColS + sb * kN + 32, sr[1]);
+        uint32_t sr[kN / 32][32];
+#pragma unroll
+        for (int h = 0; h < kN / 32; ++h) tmem_ld32(tmem + tl + kColS + sb * kN + h * 32, sr[h]);
         tmem_ld_wait();
         const int k0 = j * kN;
         // Raw-score row max (scale > 0 keeps the order); the causal / prefix
@@ -394,7 +399,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
         float mx = -CUDART_INF_F;
         if (!full_vis) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
+          for (int h = 0; h < kN / 32; ++h)
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
               const int key = k0 + h * 32 + c;
@@ -402,7 +407,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
             }
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < kN / 32; ++h)
 #pragma unroll
           for (int c = 0; c < 32; c += 2) mx = fmax3(mx, __uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1]));
         // Exponentials are taken against m (raw units). It only moves up when
@@ -421,9 +426,9 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
         // paired FMA; the row sum accumulates in pairs.
         const uint64_t sl2x2 = f2_pack(sl2, sl2), negx2 = f2_pack(neg, neg);
         uint64_t rs2 = f2_pack(0.f, 0.f);
-        uint32_t pk[32];
+        uint32_t pk[kN / 2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < kN / 32; ++h)
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             float x0, x1;
@@ -463,9 +468,11 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
             tmem_st32(tmem + tl + kColO + cc * 32, orow);
           }
         }
-        // P (64 keys, 16-bit pairs) over the first 32 columns of this tile's
-        // S buffer: the A operand of PV.
-        tmem_st32(tmem + tl + kColS + sb * kN, pk);
+        // P (kN keys, 16-bit pairs) over the first kN/2 columns of this
+        // tile's S buffer: the A operand of PV.
+#pragma unroll
+        for (int h = 0; h < kN / 64; ++h)
+          tmem_st32(tmem + tl + kColS + sb * kN + h * 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + h * 32));
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -576,7 +583,7 @@ int launch_prefill(const PrefillParams& p0, const void* k_cache, const void* v_c
   prefill_plan_kernel<<<1, 1024, 0, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   const int64_t upper = (int64_t)(p.total_q > 0 ? p.total_q : 1) * p.num_kv_heads;
-  const int64_t resident = 2LL * num_sms_current_device();
+  const int64_t resident = (int64_t)pf::kCtasPerSm * num_sms_current_device();
   const int ctas = (int)(upper < resident ? upper : resident);
   return dispatch_prefill_kernel<false>(qmap, kmap, vmap, p, ctas, dt, stream);
 }
@@ -600,7 +607,7 @@ int launch_prefix_pass(const PrefillParams& p0, const void* k_cache, const void*
   rc = make_kv_tensor_map(&vmap, v_cache, rows, pf::kD, dt, 16);
   if (rc != PA_OK) return rc;
   const int64_t upper = (int64_t)p.num_seqs * p.num_kv_heads;
-  const int64_t resident = num_sms_current_device();
+  const int64_t resident = (int64_t)pf::kCtasPerSm * num_sms_current_device();
   const int ctas = (int)(upper < resident ? upper : resident);
   return dispatch_prefill_kernel<true>(qmap, kmap, vmap, p, ctas, dt, stream);
 }
