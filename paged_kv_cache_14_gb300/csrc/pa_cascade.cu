@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(1024) cascade_prep_kernel(const DecodeParams p
                                                             int32_t members_per_tile, int32_t* prefix_out,
                                                             int32_t* group_ref, int32_t* group_of_seq,
                                                             int32_t* work, int32_t* pairs, int32_t* pair_keys) {
+  pdl_trigger();  // the prefix pass may start its set-up now; it waits for this kernel
   __shared__ int count;
   const int N = p.num_seqs, B = p.block_size;
   const int tid = threadIdx.x, nt = blockDim.x;

@@ -96,6 +96,7 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
 
 template <typename T>
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeParams p) {
+  pdl_trigger();  // the main kernel may start its set-up now; it waits for this plan
   decode_plan_body<T>(p);
 }
 
@@ -187,6 +188,8 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
   for (int i = threadIdx.x; i < C::kSlots * C::kQBytes / 16; i += blockDim.x)
     reinterpret_cast<int4*>(smem + C::kQ)[i] = make_int4(0, 0, 0, 0);
   __syncthreads();
+  pdl_wait();  // the work list (and any prefix partials) of the previous kernel
+  pdl_trigger();
   const uint32_t ring0 = smem_u32(smem + C::kRing);
 
   if (warp == C::kConsumers) {
@@ -858,6 +861,8 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
 // ---------------------------------------------------------------------------
 template <int VEC>
 __global__ void __launch_bounds__(128) decode_simt_kernel(const DecodeParams p) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int D = VEC * 32;
   constexpr int ROWS = 8;
   constexpr int NW = 4;
@@ -986,6 +991,8 @@ __global__ void __launch_bounds__(128) decode_simt_kernel(const DecodeParams p) 
 // partitions with coalesced 16-byte loads.
 template <typename T>
 __global__ void __launch_bounds__(256) splitkv_merge_kernel(const DecodeParams p) {
+  pdl_wait();  // every partial of the decode kernel
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x * 8 + warp;
   const int seq = blockIdx.y;
@@ -1033,13 +1040,14 @@ __global__ void __launch_bounds__(256) splitkv_merge_kernel(const DecodeParams p
 static int launch_merge(const DecodeParams& p, pa_dtype dt, cudaStream_t stream) {
   if (p.max_parts <= 1) return PA_OK;
   const dim3 grid((p.num_q_heads + 7) / 8, p.num_seqs);
+  cudaError_t e;
   if (dt == PA_F32)
-    splitkv_merge_kernel<float><<<grid, 256, 0, stream>>>(p);
+    e = launch_dependent(splitkv_merge_kernel<float>, grid, dim3(256), 0, stream, p);
   else if (dt == PA_BF16)
-    splitkv_merge_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(p);
+    e = launch_dependent(splitkv_merge_kernel<__nv_bfloat16>, grid, dim3(256), 0, stream, p);
   else
-    splitkv_merge_kernel<__half><<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    e = launch_dependent(splitkv_merge_kernel<__half>, grid, dim3(256), 0, stream, p);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 template <typename T, int D, int BS, int NT, bool KV8>
@@ -1075,8 +1083,8 @@ static int launch_tc(const DecodeParams& p, cudaStream_t stream) {
   const int64_t upper = (int64_t)p.num_seqs * p.max_parts * p.num_kv_heads * p.row_groups;
   const int64_t resident = (NT == 1 ? 2LL : 1LL) * num_sms_current_device();
   const int ctas = (int)(upper < resident ? upper : resident);
-  kern<<<ctas, C::kThreads, C::kSmem, stream>>>(kmap, vmap, p);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_dependent(kern, dim3(ctas), dim3(C::kThreads), C::kSmem, stream, kmap, vmap, p) != cudaSuccess)
+    return PA_ERR_CUDA;
   return launch_merge(p, dt, stream);
 }
 
@@ -1084,8 +1092,7 @@ template <int VEC>
 static int launch_simt(const DecodeParams& p, cudaStream_t stream) {
   decode_plan_kernel<float><<<1, 1024, 0, stream>>>(p);
   dim3 grid(p.max_parts, p.num_kv_heads * p.row_groups, p.num_seqs);
-  decode_simt_kernel<VEC><<<grid, 128, 0, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_dependent(decode_simt_kernel<VEC>, grid, dim3(128), 0, stream, p) != cudaSuccess) return PA_ERR_CUDA;
   return launch_merge(p, PA_F32, stream);
 }
 

@@ -80,6 +80,7 @@ constexpr int kTmemCols = kN == 64 ? 256 : 512;
 // ordered by decreasing number of KV tiles (longest items first), and reset
 // the item counter. One CTA of 1024 threads.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams p) {
+  pdl_trigger();  // the chunk kernel may start its set-up now; it waits for this plan
   constexpr int kBins = 2048;
   __shared__ int hist[kBins];
   __shared__ int total;
@@ -205,6 +206,8 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();  // the work list of the plan / preparation kernel
+  pdl_trigger();
   const uint32_t tmem = misc[0];
   const int G = 1 << p.gshift;
   const int pp = kM >> p.gshift;
@@ -546,8 +549,9 @@ static int launch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& kma
       return PA_ERR_CUDA;
     attr_set[dev] = true;
   }
-  kern<<<ctas, pf::kThreads, pf::kSmem, stream>>>(qmap, kmap, vmap, p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return launch_dependent(kern, dim3(ctas), dim3(pf::kThreads), pf::kSmem, stream, qmap, kmap, vmap, p) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
 }
 
 template <bool PREFIX>
