@@ -188,7 +188,14 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
   for (int i = threadIdx.x; i < C::kSlots * C::kQBytes / 16; i += blockDim.x)
     reinterpret_cast<int4*>(smem + C::kQ)[i] = make_int4(0, 0, 0, 0);
   __syncthreads();
-  pdl_wait();  // the work list (and any prefix partials) of the previous kernel
+  // Plain decode waits here for its plan kernel. Shared-prefix decode reads
+  // a work list built by the preparation kernel two launches back (complete
+  // before this launch: the prefix pass in between waited for it before
+  // letting this kernel start), so it streams its suffix at once, overlapping
+  // the prefix pass, and waits for that pass only before reading a prefix
+  // partial and before it exits (so the merge kernel sees both).
+  const bool overlap = p.planned && p.prefix;
+  if (!overlap) pdl_wait();
   pdl_trigger();
   const uint32_t ring0 = smem_u32(smem + C::kRing);
 
@@ -373,6 +380,7 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
       if (off >= fail_n || ((fail_mask >> off) & 1u)) last -= C::kStages;
       if (last >= 0) mbar_wait(smem_u32(&full[sl]), (last / C::kStages) & 1, nullptr);
     }
+    pdl_wait();
     return;
   }
 
@@ -829,8 +837,9 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
         acc.w += v.w;
       }
       if (mt.out_mode == kOutWithPrefix) {
-        // Merge with the prefix pass's partial (written by an earlier
+        // Merge with the prefix pass's partial (written by the previous
         // launch on this stream): M' = max(M, m0), weights 2^(M - M'), 2^(m0 - M').
+        pdl_wait();
         const int64_t b0 = ((int64_t)mt.seq * p.num_q_heads + mt.h0 + h) * p.max_parts;
         const float2 ml0 = __ldcg(reinterpret_cast<const float2*>(p.part_ml + b0 * 2));
         const float4 o0 = __ldcg(reinterpret_cast<const float4*>(p.part_o + b0 * D + d4));
@@ -852,6 +861,7 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
     }
     named_barrier_sync(1, C::kConsumers * 32);
   }
+  pdl_wait();
 }
 
 // ---------------------------------------------------------------------------
