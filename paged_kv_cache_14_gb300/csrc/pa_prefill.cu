@@ -53,7 +53,7 @@ constexpr int kQHalf = kM * 128;           // one 64-column half of Q: 128 rows 
 constexpr int kQBytes = 2 * kQHalf;        // 32 KB
 constexpr int kKVHalf = kN * 128;          // kN rows x 128 B
 constexpr int kKBytes = 2 * kKVHalf;       // one K (or V) tile: 16 KB
-constexpr int NK = 2;                      // K stages
+constexpr int NK = 3;                      // K stages
 constexpr int NV = 2;                      // V stages
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;
@@ -250,6 +250,12 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
 
     if (warp == 0) {
       // =========================== producer ===========================
+      // Copies are issued in the order the MMA stream frees their stages:
+      // S(g) completes before PV(g-1), which completes before S(g+1), so at
+      // step t the producer issues K(t) (stage freed by S(t - NK)) and then
+      // V(t - 2) (stage freed by PV(t - 4)): every wait is for a later event
+      // than the one before, and each tile's K is in flight for about two
+      // tiles of MMA and softmax time before S needs it.
       bool bad = false;
       int k_issued = 0, v_issued = 0;  // tiles of this item whose K / V copies were issued
       if (lane == 0) {
@@ -258,9 +264,11 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
         tma_load_3d(sbase + kOffQ + kQHalf, &qmap, 64, kvh * G, q_z, b_q);
       }
       const int32_t* bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
-      for (int j = 0; j < ntiles; ++j) {
-        const int g = tile_base + j;
-        // Lanes 0..kSubTiles-1: physical block of the tile's 16-token sub-tile `lane`.
+      // Lane u < kSubTiles owns 16-token sub-tile u of every tile: it loads
+      // the sub-tile's physical block and issues its copies (lane 0 first
+      // waits for the stage and posts the stage's byte count), so a tile's
+      // copies leave in one warp instruction per tensor.
+      auto sub_id = [&](int j) -> int {
         int id = 0;
         if (lane < kSubTiles) {
           const int bi = (j * kN + lane * 16) / BS;
@@ -272,52 +280,57 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
             }
           }
         }
-        int ids[kSubTiles];
+        return id;
+      };
+      constexpr int kLag = 2;  // V(t - kLag) is issued at step t
+      int idh[kLag + 1];       // this lane's sub-tile block of tiles t, t-1, t-2
+      for (int t = 0; t < ntiles + kLag && !bad; ++t) {
 #pragma unroll
-        for (int u = 0; u < kSubTiles; ++u) ids[u] = __shfl_sync(0xffffffffu, id, u);
-        if (lane == 0) {
-          const int sk = g % NK, sv = g % NV;
-          if (g >= NK && !mbar_wait(b_kempty0 + 8 * sk, ((g / NK) & 1) ^ 1, p.status)) {
-            bad = true;
-          } else {
-            const uint32_t fb = b_kfull0 + 8 * sk;
-            mbar_arrive_expect_tx(fb, kKBytes);
-            const uint32_t kdst = sbase + kOffK + sk * kKBytes;
-#pragma unroll
-            for (int u = 0; u < kSubTiles; ++u) {
-              const int row = (ids[u] * p.num_kv_heads + kvh) * BS + ((j * kN + u * 16) % BS);
-#pragma unroll
-              for (int h = 0; h < 2; ++h) tma_load_2d(kdst + h * kKVHalf + u * 2048, &kmap, h * 64, row, fb);
-            }
-            k_issued = j + 1;
-            if (g >= NV && !mbar_wait(b_vempty0 + 8 * sv, ((g / NV) & 1) ^ 1, p.status)) {
-              bad = true;
-            } else {
-              const uint32_t fv = b_vfull0 + 8 * sv;
-              mbar_arrive_expect_tx(fv, kKBytes);
-              const uint32_t vdst = sbase + kOffV + sv * kKBytes;
-#pragma unroll
-              for (int u = 0; u < kSubTiles; ++u) {
-                const int row = (ids[u] * p.num_kv_heads + kvh) * BS + ((j * kN + u * 16) % BS);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) tma_load_2d(vdst + h * kKVHalf + u * 2048, &vmap, h * 64, row, fv);
-              }
-              v_issued = j + 1;
-            }
-          }
-        }
-        bad = __shfl_sync(0xffffffffu, bad, 0);
-        if (bad) {
-          abort_flag[0] = 1;
-          // Let the copies already issued land before the CTA moves on.
+        for (int hh = kLag; hh > 0; --hh) idh[hh] = idh[hh - 1];
+        if (t < ntiles) idh[0] = sub_id(t);
+        if (t < ntiles) {
+          const int g = tile_base + t, sk = g % NK;
           if (lane == 0) {
-            mbar_wait(b_q, it & 1, nullptr);
-            for (int jj = max(0, k_issued - NK); jj < k_issued; ++jj)
-              mbar_wait(b_kfull0 + 8 * ((tile_base + jj) % NK), ((tile_base + jj) / NK) & 1, nullptr);
-            for (int jj = max(0, v_issued - NV); jj < v_issued; ++jj)
-              mbar_wait(b_vfull0 + 8 * ((tile_base + jj) % NV), ((tile_base + jj) / NV) & 1, nullptr);
+            if (g >= NK && !mbar_wait(b_kempty0 + 8 * sk, ((g / NK) & 1) ^ 1, p.status)) bad = true;
+            else mbar_arrive_expect_tx(b_kfull0 + 8 * sk, kKBytes);
           }
-          break;
+          bad = __shfl_sync(0xffffffffu, bad, 0);
+          if (bad) break;
+          if (lane < kSubTiles) {
+            const uint32_t kdst = sbase + kOffK + sk * kKBytes + lane * 2048;
+            const int row = (idh[0] * p.num_kv_heads + kvh) * BS + ((t * kN + lane * 16) % BS);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) tma_load_2d(kdst + h * kKVHalf, &kmap, h * 64, row, b_kfull0 + 8 * sk);
+          }
+          k_issued = t + 1;
+        }
+        const int tv = t - kLag;
+        if (tv >= 0 && tv < ntiles) {
+          const int g = tile_base + tv, sv = g % NV;
+          if (lane == 0) {
+            if (g >= NV && !mbar_wait(b_vempty0 + 8 * sv, ((g / NV) & 1) ^ 1, p.status)) bad = true;
+            else mbar_arrive_expect_tx(b_vfull0 + 8 * sv, kKBytes);
+          }
+          bad = __shfl_sync(0xffffffffu, bad, 0);
+          if (bad) break;
+          if (lane < kSubTiles) {
+            const uint32_t vdst = sbase + kOffV + sv * kKBytes + lane * 2048;
+            const int row = (idh[kLag] * p.num_kv_heads + kvh) * BS + ((tv * kN + lane * 16) % BS);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) tma_load_2d(vdst + h * kKVHalf, &vmap, h * 64, row, b_vfull0 + 8 * sv);
+          }
+          v_issued = tv + 1;
+        }
+      }
+      if (bad) {
+        abort_flag[0] = 1;
+        // Let the copies already issued land before the CTA moves on.
+        if (lane == 0) {
+          mbar_wait(b_q, it & 1, nullptr);
+          for (int jj = max(0, k_issued - NK); jj < k_issued; ++jj)
+            mbar_wait(b_kfull0 + 8 * ((tile_base + jj) % NK), ((tile_base + jj) / NK) & 1, nullptr);
+          for (int jj = max(0, v_issued - NV); jj < v_issued; ++jj)
+            mbar_wait(b_vfull0 + 8 * ((tile_base + jj) % NV), ((tile_base + jj) / NV) & 1, nullptr);
         }
       }
     } else if (warp == 1) {

@@ -39,3 +39,30 @@ def test_step_replays_from_cuda_graph(lib, kind):
     st.run()
     assert lib.pa_get_status() == 0
     assert torch.equal(replayed, st.out)
+
+
+@pytest.mark.parametrize("batch", [1, 2, 8, 64])
+def test_decode_graph_per_batch_bucket(lib, batch):
+    """One captured decode step per batch-size bucket, replayed on new inputs
+    (new q and new K/V of the appended token): equal to eager calls."""
+    from paged_kv_cache_14_gb300.step import step_from_host
+    rng = np.random.default_rng(batch)
+    lens = rng.integers(1, 3000, size=batch)
+    b = build_batch(name="bucket", seed=100 + batch, dtype="bf16", block_size=16, num_q_heads=32, num_kv_heads=8,
+                    head_dim=128, q_lens=np.ones(batch, np.int32), kv_lens=lens)
+    st = step_from_host(b)
+    st.run()
+    assert lib.pa_get_status() == 0
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st.run()
+    gen = torch.Generator().manual_seed(batch)
+    for _ in range(2):
+        st.q.copy_(torch.randn(st.q.shape, generator=gen).to(st.q.dtype).cuda())
+        st.k_new.copy_(torch.randn(st.k_new.shape, generator=gen).to(st.k_new.dtype).cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        replayed = st.out.clone()
+        st.run()
+        assert lib.pa_get_status() == 0
+        assert torch.equal(replayed, st.out)
