@@ -53,8 +53,8 @@ constexpr int kQHalf = kM * 128;           // one 64-column half of Q: 128 rows 
 constexpr int kQBytes = 2 * kQHalf;        // 32 KB
 constexpr int kKVHalf = kN * 128;          // kN rows x 128 B
 constexpr int kKBytes = 2 * kKVHalf;       // one K (or V) tile: 16 KB
-constexpr int NK = 3;                      // K stages
-constexpr int NV = 2;                      // V stages
+constexpr int NK = 2;                      // K stages
+constexpr int NV = 3;                      // V stages
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;
 constexpr int kOffV = kOffK + NK * kKBytes;
@@ -251,11 +251,12 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
     if (warp == 0) {
       // =========================== producer ===========================
       // Copies are issued in the order the MMA stream frees their stages:
-      // S(g) completes before PV(g-1), which completes before S(g+1), so at
+      // S(x + 1) completes before PV(x), which completes before S(x + 2). At
       // step t the producer issues K(t) (stage freed by S(t - NK)) and then
-      // V(t - 2) (stage freed by PV(t - 4)): every wait is for a later event
-      // than the one before, and each tile's K is in flight for about two
-      // tiles of MMA and softmax time before S needs it.
+      // V(t - kLag) (stage freed by PV(t - kLag - NV)); kLag = NK - NV + 1
+      // makes every wait one for a later event than the one before. With
+      // three V stages each V tile is requested about two tiles before PV
+      // needs it, each K tile about one and a half tiles before S.
       bool bad = false;
       int k_issued = 0, v_issued = 0;  // tiles of this item whose K / V copies were issued
       if (lane == 0) {
@@ -264,14 +265,17 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
         tma_load_3d(sbase + kOffQ + kQHalf, &qmap, 64, kvh * G, q_z, b_q);
       }
       const int32_t* bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
-      // Lane u < kSubTiles owns 16-token sub-tile u of every tile: it loads
-      // the sub-tile's physical block and issues its copies (lane 0 first
-      // waits for the stage and posts the stage's byte count), so a tile's
-      // copies leave in one warp instruction per tensor.
-      auto sub_id = [&](int j) -> int {
+      // Block ids are loaded 32 sub-tiles (kTB tiles) at a time, one per
+      // lane, a batch ahead of use, so no copy waits on a table load. Lane
+      // u < kSubTiles then owns sub-tile u of every tile: it picks its id
+      // from the batch with a shuffle and issues that sub-tile's copies
+      // (lane 0 first waits for the stage and posts its byte count).
+      constexpr int kTB = 32 / kSubTiles;
+      auto load_batch = [&](int b0) -> int {
+        const int j = b0 + lane / kSubTiles, u = lane % kSubTiles;
         int id = 0;
-        if (lane < kSubTiles) {
-          const int bi = (j * kN + lane * 16) / BS;
+        if (j < ntiles) {
+          const int bi = (j * kN + u * 16) / BS;
           if (bi < nblk_seq) {
             id = bt[bi];
             if (id < 0 || id >= p.num_blocks) {
@@ -282,14 +286,21 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
         }
         return id;
       };
-      constexpr int kLag = 2;  // V(t - kLag) is issued at step t
-      int idh[kLag + 1];       // this lane's sub-tile block of tiles t, t-1, t-2
+      constexpr int kLag = NK - NV + 1;  // V(t - kLag) is issued at step t
+      static_assert(kLag >= 0 && kLag < 32 / kSubTiles, "V lag must stay within the previous id batch");
+      int b_start = 0;
+      int id_cur = load_batch(0), id_next = load_batch(kTB), id_prev = 0;
+      const int su = lane % kSubTiles;
       for (int t = 0; t < ntiles + kLag && !bad; ++t) {
-#pragma unroll
-        for (int hh = kLag; hh > 0; --hh) idh[hh] = idh[hh - 1];
-        if (t < ntiles) idh[0] = sub_id(t);
+        if (t == b_start + kTB) {
+          id_prev = id_cur;
+          id_cur = id_next;
+          b_start += kTB;
+          id_next = load_batch(b_start + kTB);
+        }
         if (t < ntiles) {
           const int g = tile_base + t, sk = g % NK;
+          const int idk = __shfl_sync(0xffffffffu, id_cur, (t - b_start) * kSubTiles + su);
           if (lane == 0) {
             if (g >= NK && !mbar_wait(b_kempty0 + 8 * sk, ((g / NK) & 1) ^ 1, p.status)) bad = true;
             else mbar_arrive_expect_tx(b_kfull0 + 8 * sk, kKBytes);
@@ -298,7 +309,7 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
           if (bad) break;
           if (lane < kSubTiles) {
             const uint32_t kdst = sbase + kOffK + sk * kKBytes + lane * 2048;
-            const int row = (idh[0] * p.num_kv_heads + kvh) * BS + ((t * kN + lane * 16) % BS);
+            const int row = (idk * p.num_kv_heads + kvh) * BS + ((t * kN + lane * 16) % BS);
 #pragma unroll
             for (int h = 0; h < 2; ++h) tma_load_2d(kdst + h * kKVHalf, &kmap, h * 64, row, b_kfull0 + 8 * sk);
           }
@@ -307,6 +318,12 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
         const int tv = t - kLag;
         if (tv >= 0 && tv < ntiles) {
           const int g = tile_base + tv, sv = g % NV;
+          // Tile tv is in the current batch or the previous one.
+          const int in_cur = tv >= b_start;
+          const int src = (in_cur ? tv - b_start : tv - (b_start - kTB)) * kSubTiles + su;
+          const int a_cur = __shfl_sync(0xffffffffu, id_cur, src);
+          const int a_prev = __shfl_sync(0xffffffffu, id_prev, src);
+          const int idv = in_cur ? a_cur : a_prev;
           if (lane == 0) {
             if (g >= NV && !mbar_wait(b_vempty0 + 8 * sv, ((g / NV) & 1) ^ 1, p.status)) bad = true;
             else mbar_arrive_expect_tx(b_vfull0 + 8 * sv, kKBytes);
@@ -315,7 +332,7 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
           if (bad) break;
           if (lane < kSubTiles) {
             const uint32_t vdst = sbase + kOffV + sv * kKBytes + lane * 2048;
-            const int row = (idh[kLag] * p.num_kv_heads + kvh) * BS + ((tv * kN + lane * 16) % BS);
+            const int row = (idv * p.num_kv_heads + kvh) * BS + ((tv * kN + lane * 16) % BS);
 #pragma unroll
             for (int h = 0; h < 2; ++h) tma_load_2d(vdst + h * kKVHalf, &vmap, h * 64, row, b_vfull0 + 8 * sv);
           }
