@@ -47,14 +47,18 @@ constexpr int kD = 128;        // head_dim
 #endif
 constexpr int kN = PA_PREFILL_KN;  // keys per KV tile (64: two CTAs per SM; 128: one)
 constexpr int kSubTiles = kN / 16;  // 16-token sub-tiles per KV tile
-constexpr int kCtasPerSm = kN == 64 ? 2 : 1;
+constexpr int kCtasPerSm = 2;
+// 64-key tiles: two S buffers (S of tile g+2 is computed while the softmax
+// works on g), 2 K and 3 V stages. 128-key tiles: one S buffer and one stage
+// each, which keeps 256 tensor-memory columns and two CTAs per SM.
+constexpr int kSBuf = kN == 64 ? 2 : 1;
 constexpr int kThreads = 192;  // producer, MMA, 4 softmax warps
 constexpr int kQHalf = kM * 128;           // one 64-column half of Q: 128 rows x 128 B
 constexpr int kQBytes = 2 * kQHalf;        // 32 KB
 constexpr int kKVHalf = kN * 128;          // kN rows x 128 B
 constexpr int kKBytes = 2 * kKVHalf;       // one K (or V) tile: 16 KB
-constexpr int NK = 2;                      // K stages
-constexpr int NV = 3;                      // V stages
+constexpr int NK = kN == 64 ? 2 : 1;       // K stages
+constexpr int NV = kN == 64 ? 3 : 1;       // V stages
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;
 constexpr int kOffV = kOffK + NK * kKBytes;
@@ -71,9 +75,9 @@ constexpr int kBarODone = kBarPFull + 2;
 constexpr int kNumBars = kBarODone + 2;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, item, abort
 constexpr int kSmem = kOffMisc + 64;
-constexpr int kColS = 0;        // two S buffers of kN columns (tile g uses buffer g & 1); P(g) over its first kN/2
-constexpr int kColO = 2 * kN;   // O: 128 columns
-constexpr int kTmemCols = kN == 64 ? 256 : 512;
+constexpr int kColS = 0;           // kSBuf S buffers of kN columns (tile g uses buffer g % kSBuf); P over the first kN/2
+constexpr int kColO = kSBuf * kN;  // O: 128 columns
+constexpr int kTmemCols = 256;
 }  // namespace pf
 
 // Plan: list (sequence, row tile) pairs of every chunk with q_len > 1,
@@ -250,13 +254,13 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
 
     if (warp == 0) {
       // =========================== producer ===========================
-      // Copies are issued in the order the MMA stream frees their stages:
-      // S(x + 1) completes before PV(x), which completes before S(x + 2). At
-      // step t the producer issues K(t) (stage freed by S(t - NK)) and then
-      // V(t - kLag) (stage freed by PV(t - kLag - NV)); kLag = NK - NV + 1
-      // makes every wait one for a later event than the one before. With
-      // three V stages each V tile is requested about two tiles before PV
-      // needs it, each K tile about one and a half tiles before S.
+      // Copies are issued in the order the MMA stream frees their stages.
+      // With two S buffers S(x + 1) completes before PV(x), which completes
+      // before S(x + 2): at step t the producer issues K(t) (stage freed by
+      // S(t - NK)) and then V(t - kLag) (freed by PV(t - kLag - NV)), with
+      // kLag = NK - NV + 1. With one S buffer S(x) < PV(x) < S(x + 1): it
+      // issues V(t - 1) (freed by PV(t - 2)) and then K(t) (freed by S(t - 1)).
+      // Either way every wait is for a later event than the one before.
       bool bad = false;
       int k_issued = 0, v_issued = 0;  // tiles of this item whose K / V copies were issued
       if (lane == 0) {
@@ -286,7 +290,7 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
         }
         return id;
       };
-      constexpr int kLag = NK - NV + 1;  // V(t - kLag) is issued at step t
+      constexpr int kLag = kSBuf == 2 ? NK - NV + 1 : 1;  // V(t - kLag) is issued at step t
       static_assert(kLag >= 0 && kLag < 32 / kSubTiles, "V lag must stay within the previous id batch");
       int b_start = 0;
       int id_cur = load_batch(0), id_next = load_batch(kTB), id_prev = 0;
@@ -298,45 +302,56 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
           b_start += kTB;
           id_next = load_batch(b_start + kTB);
         }
-        if (t < ntiles) {
-          const int g = tile_base + t, sk = g % NK;
-          const int idk = __shfl_sync(0xffffffffu, id_cur, (t - b_start) * kSubTiles + su);
-          if (lane == 0) {
-            if (g >= NK && !mbar_wait(b_kempty0 + 8 * sk, ((g / NK) & 1) ^ 1, p.status)) bad = true;
-            else mbar_arrive_expect_tx(b_kfull0 + 8 * sk, kKBytes);
-          }
-          bad = __shfl_sync(0xffffffffu, bad, 0);
-          if (bad) break;
-          if (lane < kSubTiles) {
-            const uint32_t kdst = sbase + kOffK + sk * kKBytes + lane * 2048;
-            const int row = (idk * p.num_kv_heads + kvh) * BS + ((t * kN + lane * 16) % BS);
+        auto issue_k = [&]() {
+          if (t < ntiles) {
+            const int g = tile_base + t, sk = g % NK;
+            const int idk = __shfl_sync(0xffffffffu, id_cur, (t - b_start) * kSubTiles + su);
+            if (lane == 0) {
+              if (g >= NK && !mbar_wait(b_kempty0 + 8 * sk, ((g / NK) & 1) ^ 1, p.status)) bad = true;
+              else mbar_arrive_expect_tx(b_kfull0 + 8 * sk, kKBytes);
+            }
+            bad = __shfl_sync(0xffffffffu, bad, 0);
+            if (bad) return;
+            if (lane < kSubTiles) {
+              const uint32_t kdst = sbase + kOffK + sk * kKBytes + lane * 2048;
+              const int row = (idk * p.num_kv_heads + kvh) * BS + ((t * kN + lane * 16) % BS);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) tma_load_2d(kdst + h * kKVHalf, &kmap, h * 64, row, b_kfull0 + 8 * sk);
+              for (int h = 0; h < 2; ++h) tma_load_2d(kdst + h * kKVHalf, &kmap, h * 64, row, b_kfull0 + 8 * sk);
+            }
+            k_issued = t + 1;
           }
-          k_issued = t + 1;
-        }
-        const int tv = t - kLag;
-        if (tv >= 0 && tv < ntiles) {
-          const int g = tile_base + tv, sv = g % NV;
-          // Tile tv is in the current batch or the previous one.
-          const int in_cur = tv >= b_start;
-          const int src = (in_cur ? tv - b_start : tv - (b_start - kTB)) * kSubTiles + su;
-          const int a_cur = __shfl_sync(0xffffffffu, id_cur, src);
-          const int a_prev = __shfl_sync(0xffffffffu, id_prev, src);
-          const int idv = in_cur ? a_cur : a_prev;
-          if (lane == 0) {
-            if (g >= NV && !mbar_wait(b_vempty0 + 8 * sv, ((g / NV) & 1) ^ 1, p.status)) bad = true;
-            else mbar_arrive_expect_tx(b_vfull0 + 8 * sv, kKBytes);
-          }
-          bad = __shfl_sync(0xffffffffu, bad, 0);
-          if (bad) break;
-          if (lane < kSubTiles) {
-            const uint32_t vdst = sbase + kOffV + sv * kKBytes + lane * 2048;
-            const int row = (idv * p.num_kv_heads + kvh) * BS + ((tv * kN + lane * 16) % BS);
+        };
+        auto issue_v = [&]() {
+          const int tv = t - kLag;
+          if (tv >= 0 && tv < ntiles) {
+            const int g = tile_base + tv, sv = g % NV;
+            // Tile tv is in the current batch or the previous one.
+            const int in_cur = tv >= b_start;
+            const int src = (in_cur ? tv - b_start : tv - (b_start - kTB)) * kSubTiles + su;
+            const int a_cur = __shfl_sync(0xffffffffu, id_cur, src);
+            const int a_prev = __shfl_sync(0xffffffffu, id_prev, src);
+            const int idv = in_cur ? a_cur : a_prev;
+            if (lane == 0) {
+              if (g >= NV && !mbar_wait(b_vempty0 + 8 * sv, ((g / NV) & 1) ^ 1, p.status)) bad = true;
+              else mbar_arrive_expect_tx(b_vfull0 + 8 * sv, kKBytes);
+            }
+            bad = __shfl_sync(0xffffffffu, bad, 0);
+            if (bad) return;
+            if (lane < kSubTiles) {
+              const uint32_t vdst = sbase + kOffV + sv * kKBytes + lane * 2048;
+              const int row = (idv * p.num_kv_heads + kvh) * BS + ((tv * kN + lane * 16) % BS);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) tma_load_2d(vdst + h * kKVHalf, &vmap, h * 64, row, b_vfull0 + 8 * sv);
+              for (int h = 0; h < 2; ++h) tma_load_2d(vdst + h * kKVHalf, &vmap, h * 64, row, b_vfull0 + 8 * sv);
+            }
+            v_issued = tv + 1;
           }
-          v_issued = tv + 1;
+        };
+        if constexpr (kSBuf == 1) {
+          issue_v();
+          if (!bad) issue_k();
+        } else {
+          issue_k();
+          if (!bad) issue_v();
         }
       }
       if (bad) {
@@ -356,8 +371,8 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
         bool bad = !mbar_wait(b_q, it & 1, p.status);
         uint32_t last_bar = 0, last_phase = 0;  // the last commit: it covers every MMA issued before it
         auto issue_s = [&](int g) -> bool {
-          const int sk = g % NK;  // K stage
-          const int sb = g & 1;   // S buffer
+          const int sk = g % NK;     // K stage
+          const int sb = g % kSBuf;  // S buffer
           if (!mbar_wait(b_kfull0 + 8 * sk, (g / NK) & 1, p.status)) return false;
           tc_fence_after();
           const uint32_t kst = sbase + kOffK + sk * kKBytes;
@@ -370,15 +385,14 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
           tc_commit(b_kempty0 + 8 * sk);
           tc_commit(b_sfull0 + 8 * sb);
           last_bar = b_sfull0 + 8 * sb;
-          last_phase = (g >> 1) & 1;
+          last_phase = (g / kSBuf) & 1;
           return true;
         };
-        if (!bad && ntiles > 0) bad = !issue_s(tile_base);
-        if (!bad && ntiles > 1) bad = !issue_s(tile_base + 1);
+        for (int i = 0; i < kSBuf && i < ntiles && !bad; ++i) bad = !issue_s(tile_base + i);
         for (int j = 0; j < ntiles && !bad; ++j) {
           const int g = tile_base + j;
-          const int sb = g & 1, sv = g % NV;
-          if (!mbar_wait(b_pfull0 + 8 * sb, (g >> 1) & 1, p.status)) { bad = true; break; }
+          const int sb = g % kSBuf, sv = g % NV;
+          if (!mbar_wait(b_pfull0 + 8 * sb, (g / kSBuf) & 1, p.status)) { bad = true; break; }
           if (!mbar_wait(b_vfull0 + 8 * sv, (g / NV) & 1, p.status)) { bad = true; break; }
           tc_fence_after();
           const uint32_t vst = sbase + kOffV + sv * kKBytes;
@@ -390,8 +404,8 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
           tc_commit(b_vempty0 + 8 * sv);
           tc_commit(b_odone0 + 8 * sb);
           last_bar = b_odone0 + 8 * sb;
-          last_phase = (g >> 1) & 1;
-          if (j + 2 < ntiles && !issue_s(g + 2)) { bad = true; break; }
+          last_phase = (g / kSBuf) & 1;
+          if (j + kSBuf < ntiles && !issue_s(g + kSBuf)) { bad = true; break; }
         }
         if (bad) {
           abort_flag[0] = 1;
@@ -418,8 +432,8 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
       bool bad = false;
       for (int j = 0; j < ntiles; ++j) {
         const int g = tile_base + j;
-        const int sb = g & 1;  // S buffer of this tile
-        if (!mbar_wait(b_sfull0 + 8 * sb, (g >> 1) & 1, p.status)) { bad = true; break; }
+        const int sb = g % kSBuf;  // S buffer of this tile
+        if (!mbar_wait(b_sfull0 + 8 * sb, (g / kSBuf) & 1, p.status)) { bad = true; break; }
         tc_fence_after();
         uint32_t sr[kN / 32][32];
 #pragma unroll
@@ -489,7 +503,7 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
         // Rescale the O row when the running max moved (warp-uniform); PV of
         // the previous tile must have finished accumulating into O first.
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          if (!mbar_wait(b_odone0 + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1, p.status)) { bad = true; break; }
+          if (!mbar_wait(b_odone0 + 8 * ((g - 1) % kSBuf), ((g - 1) / kSBuf) & 1, p.status)) { bad = true; break; }
           tc_fence_after();
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
@@ -512,7 +526,7 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
         if (lane == 0) mbar_arrive(b_pfull0 + 8 * sb);
       }
       const int gl = tile_base + ntiles - 1;
-      if (!bad && mbar_wait(b_odone0 + 8 * (gl & 1), (gl >> 1) & 1, p.status)) {
+      if (!bad && mbar_wait(b_odone0 + 8 * (gl % kSBuf), (gl / kSBuf) & 1, p.status)) {
         tc_fence_after();
         if constexpr (!PREFIX) {
           const float inv = 1.f / l;
