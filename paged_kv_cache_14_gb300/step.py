@@ -71,6 +71,24 @@ class PagedStep:
         if kv_scales is not None and (self.shared_prefix or not self.is_decode):
             raise ValueError("the e4m3 cache is supported by plain decode only")
 
+    # Per-step inputs a serving loop refreshes (attribute names).
+    INPUTS = ("q", "k_new", "v_new", "block_tables", "kv_lens", "new_seq_ids", "new_positions",
+              "group_starts", "prefix_lens", "cu_q_lens", "ctx_lens")
+
+    def twin(self) -> "PagedStep":
+        """A step over the same KV pools (and scales) with its own input,
+        output, slot-mapping and workspace buffers (same shapes)."""
+        t = PagedStep.__new__(PagedStep)
+        t.__dict__.update(self.__dict__)
+        for name in self.INPUTS:
+            v = getattr(self, name, None)
+            if isinstance(v, torch.Tensor):
+                setattr(t, name, v.clone())
+        t.slot_mapping = torch.empty_like(self.slot_mapping)
+        t.out = torch.empty_like(self.out)
+        t.workspace = torch.empty_like(self.workspace)
+        return t
+
     @property
     def launches(self) -> int:
         """Kernel launches of one step (the library's own kernels)."""
@@ -160,3 +178,51 @@ def step_from_host(batch, device="cuda", partition_size: int = 0, shared_prefix:
         group_starts=dev(batch.group_starts, torch.int32) if shared_prefix else None,
         prefix_lens=dev(batch.prefix_lens, torch.int32) if shared_prefix else None,
     )
+
+
+class HostPipeline:
+    """Steps fed from the host with the transfers overlapped with compute.
+
+    A serving loop that receives every step's inputs in (pinned) host memory
+    and wants the attention output back on the host submits steps here. Two
+    device buffer sets (a step and its twin over the same KV pools) alternate:
+    step i's inputs are copied in on a copy stream while step i-1 computes,
+    and its output is copied out on a second copy stream while step i+1
+    computes. Events order every buffer's reuse; the steps themselves run in
+    submission order on the compute stream, so the cache updates keep their
+    order.
+    """
+
+    def __init__(self, step: PagedStep, compute_stream: torch.cuda.Stream | None = None):
+        self.steps = (step, step.twin())
+        self.compute = compute_stream or torch.cuda.current_stream()
+        self.h2d = torch.cuda.Stream()
+        self.d2h = torch.cuda.Stream()
+        self.ev_in = [torch.cuda.Event(), torch.cuda.Event()]     # inputs of buffer k copied in
+        self.ev_done = [torch.cuda.Event(), torch.cuda.Event()]   # step on buffer k computed
+        self.ev_out = [torch.cuda.Event(), torch.cuda.Event()]    # output of buffer k copied out
+        self.n = 0
+
+    def submit(self, host_inputs: dict, host_out: torch.Tensor) -> None:
+        """Enqueue one step: host_inputs maps PagedStep input names to pinned
+        host tensors; host_out (pinned) receives the step's output."""
+        k = self.n & 1
+        st = self.steps[k]
+        self.h2d.wait_event(self.ev_done[k])          # buffer k's previous step has read its inputs
+        with torch.cuda.stream(self.h2d):
+            for name, t in host_inputs.items():
+                getattr(st, name).copy_(t, non_blocking=True)
+        self.ev_in[k].record(self.h2d)
+        self.compute.wait_event(self.ev_in[k])
+        self.compute.wait_event(self.ev_out[k])      # buffer k's previous output has been copied out
+        st.run(stream=self.compute)
+        self.ev_done[k].record(self.compute)
+        self.d2h.wait_event(self.ev_done[k])
+        with torch.cuda.stream(self.d2h):
+            host_out.copy_(st.out, non_blocking=True)
+        self.ev_out[k].record(self.d2h)
+        self.n += 1
+
+    def drain(self) -> None:
+        """Make the compute stream wait for every submitted copy."""
+        self.compute.wait_stream(self.d2h)

@@ -66,3 +66,28 @@ def test_decode_graph_per_batch_bucket(lib, batch):
         st.run()
         assert lib.pa_get_status() == 0
         assert torch.equal(replayed, st.out)
+
+
+def test_host_pipeline_matches_eager(lib):
+    """Steps fed from pinned host memory through HostPipeline (copies on
+    their own streams, two buffer sets) give the outputs of eager steps."""
+    from paged_kv_cache_14_gb300.step import HostPipeline, step_from_host
+    lens = [5, 64, 300, 700, 1300, 2100, 31, 900]
+    b = build_batch(name="pipe", seed=93, dtype="bf16", block_size=16, num_q_heads=64, num_kv_heads=8,
+                    head_dim=128, q_lens=np.ones(8, np.int32), kv_lens=lens, share_group=4,
+                    share_prefix_tokens=256, cow_per_seq=True)
+    st = step_from_host(b, shared_prefix=True)
+    gen = torch.Generator().manual_seed(3)
+    qs = [torch.randn(st.q.shape, generator=gen).to(st.q.dtype).pin_memory() for _ in range(4)]
+    outs = [torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory() for _ in range(4)]
+    pipe = HostPipeline(st)
+    for q, o in zip(qs, outs):
+        pipe.submit({"q": q}, o)
+    pipe.drain()
+    torch.cuda.synchronize()
+    assert lib.pa_get_status() == 0
+    for q, o in zip(qs, outs):
+        st.q.copy_(q)
+        st.run()
+        torch.cuda.synchronize()
+        assert torch.equal(o, st.out.cpu())
