@@ -503,7 +503,7 @@ int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_ca
   dp.prefix = prefix;
   decode_set_rows(dp, dtype);
   // 1. Verify the hints, list the prefix pass's work and the suffix decode's.
-  rc = launch_cascade_prep(dp, dtype, group_starts, prefix_lens, num_groups, 128 / g, prefix, group_ref,
+  rc = launch_cascade_prep(dp, dtype, group_starts, prefix_lens, num_groups, kPrefillRowsPerItem / g, prefix, group_ref,
                            group_of_seq, pwork, ppairs, pkeys, s);
   dp.planned = 1;
   if (rc != PA_OK) return rc;

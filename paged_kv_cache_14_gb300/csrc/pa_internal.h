@@ -77,6 +77,10 @@ inline DecodeWorkspace decode_workspace_layout(int64_t num_seqs, int64_t num_q_h
   return w;
 }
 
+// Packed (position, GQA head) rows per work item of the tcgen05 prefill
+// kernel (chunks and the shared-prefix pass).
+constexpr int kPrefillRowsPerItem = 256;
+
 struct PrefillParams {
   const void* q;
   void* out;

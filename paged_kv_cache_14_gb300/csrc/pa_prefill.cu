@@ -5,27 +5,32 @@
 // phase (same page, "The Prefill Phase (Compute-Bound)").
 //
 // Tiles. A chunk of q_len query rows of a sequence with ctx prior tokens is
-// cut into M = 128-row tiles of packed (query position, GQA head) rows: all G
-// query heads that share one KV head are consecutive rows, so every K/V tile
-// is read once per KV head and feeds a full 128-row MMA. Row r of the chunk
-// sits at position ctx + r and attends to keys 0 .. ctx + r.
+// cut into work items of 256 packed (query position, GQA head) rows, two
+// Q tiles of 128: all G query heads that share one KV head are consecutive
+// rows, so every K/V tile is read once per KV head and item and feeds two
+// full 128-row MMAs. Row r of the chunk sits at position ctx + r and attends
+// to keys 0 .. ctx + r.
 //
-// One persistent CTA (192 threads, two per SM) loops over work items (chunk
-// tile, KV head) listed by a plan kernel, longest first:
-//   warp 0  producer: TMA of the 128 query rows (3-D tensor map over
+// One persistent CTA per SM (320 threads) loops over work items (chunk
+// rows, KV head) listed by a plan kernel, longest first:
+//   warp 0  producer: TMA of the two Q tiles (3-D tensor map over
 //           [tokens][heads][head_dim], 128-byte swizzle), then for every
-//           64-token KV tile the four 16-token sub-tiles of K and of V
-//           through the block table, into separate 2-stage K and V rings;
-//   warp 1  owns the tensor memory (256 columns: two S buffers of 128x64
-//           fp32 at columns 0 and 64, O = 128x128 fp32 at column 128) and
-//           one lane issues the MMAs: S = Q K^T (K-major operands from
-//           shared memory), then O += P V with P read from tensor memory
-//           and V an MN-major shared-memory operand;
-//   warps 2-5  softmax: thread i owns row i (tensor-memory lane i): it loads
-//           its S row, applies the causal mask, keeps the running max and sum
-//           in registers, writes P (16-bit) back over its S row, rescales its
-//           O row in tensor memory when the max moved, and at the end
-//           normalises O and stores it.
+//           128-token KV tile the eight 16-token sub-tiles of K and of V
+//           through the block table, into separate K and V rings;
+//   warp 1  owns the tensor memory (all 512 columns: per Q tile an S tile
+//           of 128x128 fp32 and O = 128x128 fp32) and one lane issues the
+//           MMAs: S = Q K^T (K-major operands from shared memory), then
+//           O += P V with P read from tensor memory and V an MN-major
+//           shared-memory operand;
+//   warps 2-5, 6-9  softmax of Q tile 0, 1: thread i of a warpgroup owns
+//           row i (tensor-memory lane i): it loads its S row, applies the
+//           causal mask, keeps the running max and sum in registers, writes P
+//           (16-bit) back over its S row, rescales its O row in tensor memory
+//           when the max moved, and at the end normalises O and stores it.
+// While one warpgroup computes its softmax the tensor pipe runs the other
+// Q tile's MMAs. Per SM and KV tile the MMAs read 192 KB of shared memory
+// and the copies write 64 KB, against 2048 tensor-pipe cycles at
+// 8192 flop per cycle.
 // Every mbarrier wait is time-bounded: on a timeout the kernel records
 // PA_ERR_TIMEOUT, lets outstanding copies and MMAs finish (bounded) and
 // returns; no wait can spin forever.
@@ -40,44 +45,50 @@
 namespace pa {
 
 namespace pf {
-constexpr int kM = 128;        // packed rows per tile (tensor-memory lanes)
-constexpr int kD = 128;        // head_dim
-#ifndef PA_PREFILL_KN
-#define PA_PREFILL_KN 64
-#endif
-constexpr int kN = PA_PREFILL_KN;  // keys per KV tile (64: two CTAs per SM; 128: one)
+constexpr int kM = 128;          // rows per Q tile (tensor-memory lanes)
+constexpr int kQT = 2;           // Q tiles per work item, one softmax warpgroup each
+constexpr int kRows = kM * kQT;  // packed rows per work item
+constexpr int kD = 128;          // head_dim
+constexpr int kN = 128;          // keys per KV tile
 constexpr int kSubTiles = kN / 16;  // 16-token sub-tiles per KV tile
-constexpr int kCtasPerSm = 2;
-// 64-key tiles: two S buffers (S of tile g+2 is computed while the softmax
-// works on g), 2 K and 3 V stages. 128-key tiles: one S buffer and one stage
-// each, which keeps 256 tensor-memory columns and two CTAs per SM.
-constexpr int kSBuf = kN == 64 ? 2 : 1;
-constexpr int kThreads = 192;  // producer, MMA, 4 softmax warps
-constexpr int kQHalf = kM * 128;           // one 64-column half of Q: 128 rows x 128 B
-constexpr int kQBytes = 2 * kQHalf;        // 32 KB
-constexpr int kKVHalf = kN * 128;          // kN rows x 128 B
-constexpr int kKBytes = 2 * kKVHalf;       // one K (or V) tile: 16 KB
-constexpr int NK = kN == 64 ? 2 : 1;       // K stages
-constexpr int NV = kN == 64 ? 3 : 1;       // V stages
+constexpr int kThreads = 64 + kQT * 128;  // producer, MMA, one softmax warpgroup per Q tile
+constexpr int kSoftmaxWarp0 = 2;           // first softmax warp
+constexpr int kQHalf = kM * 128;          // one 64-column half of a Q tile: 128 rows x 128 B
+constexpr int kQBytes = 2 * kQHalf;       // one Q tile: 32 KB
+constexpr int kKVHalf = kN * 128;         // kN rows x 128 B
+constexpr int kKBytes = 2 * kKVHalf;      // one K (or V) tile: 32 KB
+#ifndef PA_PREFILL_NV
+#define PA_PREFILL_NV 2
+#endif
+constexpr int NK = 2;               // K stages
+constexpr int NV = PA_PREFILL_NV;   // V stages (2 or 3)
+constexpr int kVLead = NV - NK;     // V(t + kVLead) is issued right after K(t)
+static_assert(kVLead == 0 || kVLead == 1, "two K stages, two or three V stages");
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQBytes;
+constexpr int kOffK = kOffQ + kQT * kQBytes;
 constexpr int kOffV = kOffK + NK * kKBytes;
 constexpr int kOffBar = kOffV + NV * kKBytes;
-// bars: q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], s_full[2], p_full[2], o_done[2]
+// bars: q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], then per Q
+// tile s_full, p_full, o_done
 constexpr int kBarQ = 0;
 constexpr int kBarKFull = 1;
 constexpr int kBarKEmpty = kBarKFull + NK;
 constexpr int kBarVFull = kBarKEmpty + NK;
 constexpr int kBarVEmpty = kBarVFull + NV;
 constexpr int kBarSFull = kBarVEmpty + NV;
-constexpr int kBarPFull = kBarSFull + 2;
-constexpr int kBarODone = kBarPFull + 2;
-constexpr int kNumBars = kBarODone + 2;
+constexpr int kBarPFull = kBarSFull + kQT;
+constexpr int kBarODone = kBarPFull + kQT;
+constexpr int kNumBars = kBarODone + kQT;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, item, abort
 constexpr int kSmem = kOffMisc + 64;
-constexpr int kColS = 0;           // kSBuf S buffers of kN columns (tile g uses buffer g % kSBuf); P over the first kN/2
-constexpr int kColO = kSBuf * kN;  // O: 128 columns
-constexpr int kTmemCols = 256;
+static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
+// Tensor memory, per Q tile t: S (kN fp32 columns; P, 16-bit pairs, over its
+// first kN/2) at t * 256, O (128 fp32 columns) at t * 256 + 128.
+constexpr int kTmemCols = 512;
+constexpr int kCtasPerSm = 1;
+__host__ __device__ constexpr int col_s(int t) { return t * 256; }
+__host__ __device__ constexpr int col_o(int t) { return t * 256 + kN; }
+static_assert(kRows == kPrefillRowsPerItem, "work list granularity shared with the shared-prefix preparation");
 }  // namespace pf
 
 // Plan: list (sequence, row tile) pairs of every chunk with q_len > 1,
@@ -88,7 +99,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
   constexpr int kBins = 2048;
   __shared__ int hist[kBins];
   __shared__ int total;
-  const int pp = pf::kM >> p.gshift;  // query positions per tile
+  const int pp = pf::kRows >> p.gshift;  // query positions per work item
   for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
   if (threadIdx.x == 0) total = 0;
   __syncthreads();
@@ -148,21 +159,25 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
 // GQA heads, each row masked to its own verified prefix, fp32 partial
 // (m, l, o~) written to slot 0 of the member's partials).
 //
-// Pipeline of one item (tile g = tile_base + j):
-//   producer:  K(g) into K stage g % NK (after S(g - NK) freed it), V(g) into
-//              V stage g % NV (after PV(g - NV) freed it);
-//   MMA:       S(g) into S buffer g & 1 two tiles ahead; after P(g) is ready,
-//              PV(g) with P read from tensor memory (the A operand), then
-//              S(g + 2) into the same buffer. The tensor pipe executes one
-//              thread's MMAs in issue order, so S(g + 2) cannot overwrite
-//              P(g) before PV(g) has read it;
-//   softmax:   reads S(g), writes P(g) (16-bit) over the first 32 columns of
-//              the same buffer, and only waits for PV(g - 1) when it must
-//              rescale O (the running max grew past the lazy threshold).
-// Barriers with more than one phase in flight are doubled per buffer parity
-// (s_full, p_full, o_done), so no parity wait can alias an older phase.
+// Pipeline of one item (KV tile g = tile_base + j, Q tiles 0 and 1):
+//   producer:  K(g) into K stage g % NK once S1(g - NK) freed it, then V
+//              into its stage once PV1 of the tile NV back freed it (the
+//              stages free in the order K(g), V(g), K(g + 1), ...);
+//   MMA:       S0(g), S1(g), then per tile PV0(g), S0(g + 1), PV1(g),
+//              S1(g + 1). The tensor pipe executes one thread's MMAs in issue
+//              order, so S_t(g + 1) cannot overwrite P_t(g) before PV_t(g)
+//              has read it, and the commit that reports S_t(g + 1) also
+//              covers PV_t(g): a softmax warpgroup that sees S_t ready may
+//              rescale its O at once. The issue order also keeps the two Q
+//              tiles half a step apart, so one tile's softmax overlaps the
+//              other tile's MMAs;
+//   softmax t: reads S_t(g), writes P_t(g) (16-bit) over the first kN/2
+//              columns of S_t, signals p_full[t].
+// Every barrier completes once per KV tile (s_full, p_full, stages) or once
+// per item (q_full, o_done), those of Q tile 1 only on items whose second
+// tile has rows, and is waited on in phase order.
 template <typename T, int BS, bool PREFIX>
-__global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
+__global__ void __launch_bounds__(pf::kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
   using namespace pf;
@@ -176,9 +191,9 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
   const uint32_t b_kempty0 = smem_u32(&bars[kBarKEmpty]);  // + 8 * stage
   const uint32_t b_vfull0 = smem_u32(&bars[kBarVFull]);    // + 8 * stage
   const uint32_t b_vempty0 = smem_u32(&bars[kBarVEmpty]);  // + 8 * stage
-  const uint32_t b_sfull0 = smem_u32(&bars[kBarSFull]);    // + 8 * buffer
-  const uint32_t b_pfull0 = smem_u32(&bars[kBarPFull]);    // + 8 * buffer
-  const uint32_t b_odone0 = smem_u32(&bars[kBarODone]);    // + 8 * (tile & 1)
+  const uint32_t b_sfull0 = smem_u32(&bars[kBarSFull]);    // + 8 * Q tile
+  const uint32_t b_pfull0 = smem_u32(&bars[kBarPFull]);    // + 8 * Q tile
+  const uint32_t b_odone0 = smem_u32(&bars[kBarODone]);    // + 8 * Q tile
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(&misc[2]);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -195,9 +210,9 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
       mbar_init(b_vfull0 + 8 * i, 1);
       mbar_init(b_vempty0 + 8 * i, 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kQT; ++i) {
       mbar_init(b_sfull0 + 8 * i, 1);
-      mbar_init(b_pfull0 + 8 * i, 4);
+      mbar_init(b_pfull0 + 8 * i, 4);  // one arrival per softmax warp
       mbar_init(b_odone0 + 8 * i, 1);
     }
     abort_flag[0] = (sbase & 1023u) != 0;
@@ -214,10 +229,13 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
   pdl_trigger();
   const uint32_t tmem = misc[0];
   const int G = 1 << p.gshift;
-  const int pp = kM >> p.gshift;
+  const int pp = kM >> p.gshift;  // query positions (or group members) per Q tile
   const int total = p.work[1];
 
   int tile_base = 0;  // KV tiles processed by this CTA before the current item
+  // The barriers of Q tile 1 (s_full, p_full, o_done) only complete on items
+  // whose second tile has rows: their phases count those items and tiles.
+  int tile_base1 = 0, items1 = 0;
   for (int it = 0;; ++it) {
     if (threadIdx.x == 0) misc[1] = abort_flag[0] ? 0x7fffffff : atomicAdd(&p.work[0], 1);
     __syncthreads();
@@ -227,23 +245,24 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
     const int pr = p.pairs[pi];
     const int kvh = item - pi * p.num_kv_heads;
     const int mt = pr & 0xffff;
-    // Tile geometry. Chunk: rows are query positions pos_lo.. of sequence
-    // `seq`; prefix pass: rows are members m_lo.. of group `grp`, keys are
-    // the group's shared prefix read through the reference member's table.
+    // Item geometry (kQT * pp positions from pos_lo). Chunk: rows are query
+    // positions of sequence `seq`; prefix pass: rows are members of group
+    // `grp`, keys are the group's shared prefix read through the reference
+    // member's table.
     int seq, q_z, q0 = 0, ql = 0, ctx = 0, kv_len, keys, grp = 0, s0 = 0, m_hi = 0;
-    const int pos_lo = mt * pp;
+    const int pos_lo = mt * kQT * pp;
     if constexpr (!PREFIX) {
       seq = pr >> 16;
       q0 = p.cu_q_lens[seq];
       ql = p.cu_q_lens[seq + 1] - q0;
       ctx = p.ctx_lens[seq];
       kv_len = ctx + ql;
-      keys = ctx + min(pos_lo + pp, ql);  // keys the tile's last row needs
+      keys = ctx + min(pos_lo + kQT * pp, ql);  // keys the item's last row needs
       q_z = q0 + pos_lo;
     } else {
       grp = pr >> 16;
       s0 = p.group_starts[grp];
-      m_hi = min(pos_lo + pp, p.group_starts[grp + 1] - s0);
+      m_hi = min(pos_lo + kQT * pp, p.group_starts[grp + 1] - s0);
       seq = p.group_ref[grp];
       keys = p.pair_keys[pi];
       kv_len = keys;
@@ -251,29 +270,28 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
     }
     const int ntiles = (keys + kN - 1) / kN;
     const int nblk_seq = (kv_len + BS - 1) / BS;
+    // Q tiles with at least one row (the second is empty when the chunk or
+    // group ends within the first): an empty tile gets no MMAs.
+    const int nq = (PREFIX ? m_hi : ql) - pos_lo > pp ? 2 : 1;
 
     if (warp == 0) {
       // =========================== producer ===========================
-      // Copies are issued in the order the MMA stream frees their stages.
-      // With two S buffers S(x + 1) completes before PV(x), which completes
-      // before S(x + 2): at step t the producer issues K(t) (stage freed by
-      // S(t - NK)) and then V(t - kLag) (freed by PV(t - kLag - NV)), with
-      // kLag = NK - NV + 1. With one S buffer S(x) < PV(x) < S(x + 1): it
-      // issues V(t - 1) (freed by PV(t - 2)) and then K(t) (freed by S(t - 1)).
-      // Either way every wait is for a later event than the one before.
       bool bad = false;
       int k_issued = 0, v_issued = 0;  // tiles of this item whose K / V copies were issued
       if (lane == 0) {
-        mbar_arrive_expect_tx(b_q, kQBytes);
-        tma_load_3d(sbase + kOffQ, &qmap, 0, kvh * G, q_z, b_q);
-        tma_load_3d(sbase + kOffQ + kQHalf, &qmap, 64, kvh * G, q_z, b_q);
+        mbar_arrive_expect_tx(b_q, kQT * kQBytes);
+#pragma unroll
+        for (int t = 0; t < kQT; ++t)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tma_load_3d(sbase + kOffQ + t * kQBytes + h * kQHalf, &qmap, h * 64, kvh * G, q_z + t * pp, b_q);
       }
       const int32_t* bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
       // Block ids are loaded 32 sub-tiles (kTB tiles) at a time, one per
       // lane, a batch ahead of use, so no copy waits on a table load. Lane
-      // u < kSubTiles then owns sub-tile u of every tile: it picks its id
-      // from the batch with a shuffle and issues that sub-tile's copies
-      // (lane 0 first waits for the stage and posts its byte count).
+      // u < kSubTiles owns sub-tile u of every tile: it picks its id from the
+      // batch with a shuffle and issues that sub-tile's copies (lane 0 first
+      // waits for the stage and posts its byte count).
       constexpr int kTB = 32 / kSubTiles;
       auto load_batch = [&](int b0) -> int {
         const int j = b0 + lane / kSubTiles, u = lane % kSubTiles;
@@ -290,69 +308,49 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
         }
         return id;
       };
-      constexpr int kLag = kSBuf == 2 ? NK - NV + 1 : 1;  // V(t - kLag) is issued at step t
-      static_assert(kLag >= 0 && kLag < 32 / kSubTiles, "V lag must stay within the previous id batch");
       int b_start = 0;
-      int id_cur = load_batch(0), id_next = load_batch(kTB), id_prev = 0;
+      int id_cur = load_batch(0), id_next = load_batch(kTB);
       const int su = lane % kSubTiles;
-      for (int t = 0; t < ntiles + kLag && !bad; ++t) {
+      // Block id of sub-tile su of tile x (x in the current or the next batch).
+      auto id_of = [&](int x) -> int {
+        const bool nxt = x >= b_start + kTB;
+        const int src = ((x - b_start) % kTB) * kSubTiles + su;
+        const int a = __shfl_sync(0xffffffffu, id_cur, src);
+        const int b = __shfl_sync(0xffffffffu, id_next, src);
+        return nxt ? b : a;
+      };
+      // One tile of K or V: wait for its stage, post the bytes, issue the
+      // kSubTiles x 2 boxes.
+      auto issue = [&](int x, bool is_v) {
+        const int g = tile_base + x;
+        const int ns = is_v ? NV : NK;
+        const int st = g % ns;
+        const uint32_t b_full = (is_v ? b_vfull0 : b_kfull0) + 8 * st;
+        const uint32_t b_empty = (is_v ? b_vempty0 : b_kempty0) + 8 * st;
+        const int id = id_of(x);
+        if (lane == 0) {
+          if (g >= ns && !mbar_wait(b_empty, ((g / ns) & 1) ^ 1, p.status)) bad = true;
+          else mbar_arrive_expect_tx(b_full, kKBytes);
+        }
+        bad = __shfl_sync(0xffffffffu, bad, 0);
+        if (bad) return;
+        if (lane < kSubTiles) {
+          const uint32_t dst = sbase + (is_v ? kOffV : kOffK) + st * kKBytes + lane * 2048;
+          const int row = (id * p.num_kv_heads + kvh) * BS + ((x * kN + lane * 16) % BS);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) tma_load_2d(dst + h * kKVHalf, is_v ? &vmap : &kmap, h * 64, row, b_full);
+        }
+        if (is_v) v_issued = x + 1;
+        else k_issued = x + 1;
+      };
+      for (int t = -kVLead; t < ntiles && !bad; ++t) {
         if (t == b_start + kTB) {
-          id_prev = id_cur;
           id_cur = id_next;
           b_start += kTB;
           id_next = load_batch(b_start + kTB);
         }
-        auto issue_k = [&]() {
-          if (t < ntiles) {
-            const int g = tile_base + t, sk = g % NK;
-            const int idk = __shfl_sync(0xffffffffu, id_cur, (t - b_start) * kSubTiles + su);
-            if (lane == 0) {
-              if (g >= NK && !mbar_wait(b_kempty0 + 8 * sk, ((g / NK) & 1) ^ 1, p.status)) bad = true;
-              else mbar_arrive_expect_tx(b_kfull0 + 8 * sk, kKBytes);
-            }
-            bad = __shfl_sync(0xffffffffu, bad, 0);
-            if (bad) return;
-            if (lane < kSubTiles) {
-              const uint32_t kdst = sbase + kOffK + sk * kKBytes + lane * 2048;
-              const int row = (idk * p.num_kv_heads + kvh) * BS + ((t * kN + lane * 16) % BS);
-#pragma unroll
-              for (int h = 0; h < 2; ++h) tma_load_2d(kdst + h * kKVHalf, &kmap, h * 64, row, b_kfull0 + 8 * sk);
-            }
-            k_issued = t + 1;
-          }
-        };
-        auto issue_v = [&]() {
-          const int tv = t - kLag;
-          if (tv >= 0 && tv < ntiles) {
-            const int g = tile_base + tv, sv = g % NV;
-            // Tile tv is in the current batch or the previous one.
-            const int in_cur = tv >= b_start;
-            const int src = (in_cur ? tv - b_start : tv - (b_start - kTB)) * kSubTiles + su;
-            const int a_cur = __shfl_sync(0xffffffffu, id_cur, src);
-            const int a_prev = __shfl_sync(0xffffffffu, id_prev, src);
-            const int idv = in_cur ? a_cur : a_prev;
-            if (lane == 0) {
-              if (g >= NV && !mbar_wait(b_vempty0 + 8 * sv, ((g / NV) & 1) ^ 1, p.status)) bad = true;
-              else mbar_arrive_expect_tx(b_vfull0 + 8 * sv, kKBytes);
-            }
-            bad = __shfl_sync(0xffffffffu, bad, 0);
-            if (bad) return;
-            if (lane < kSubTiles) {
-              const uint32_t vdst = sbase + kOffV + sv * kKBytes + lane * 2048;
-              const int row = (idv * p.num_kv_heads + kvh) * BS + ((tv * kN + lane * 16) % BS);
-#pragma unroll
-              for (int h = 0; h < 2; ++h) tma_load_2d(vdst + h * kKVHalf, &vmap, h * 64, row, b_vfull0 + 8 * sv);
-            }
-            v_issued = tv + 1;
-          }
-        };
-        if constexpr (kSBuf == 1) {
-          issue_v();
-          if (!bad) issue_k();
-        } else {
-          issue_k();
-          if (!bad) issue_v();
-        }
+        if (t >= 0) issue(t, false);
+        if (!bad && t + kVLead < ntiles) issue(t + kVLead, true);
       }
       if (bad) {
         abort_flag[0] = 1;
@@ -370,42 +368,74 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
       if (lane == 0) {
         bool bad = !mbar_wait(b_q, it & 1, p.status);
         uint32_t last_bar = 0, last_phase = 0;  // the last commit: it covers every MMA issued before it
-        auto issue_s = [&](int g) -> bool {
-          const int sk = g % NK;     // K stage
-          const int sb = g % kSBuf;  // S buffer
-          if (!mbar_wait(b_kfull0 + 8 * sk, (g / NK) & 1, p.status)) return false;
-          tc_fence_after();
-          const uint32_t kst = sbase + kOffK + sk * kKBytes;
+        // Shared-memory descriptors differ only in the start-address field
+        // (address >> 4, 14 bits; every operand lies below 256 KB), so each is
+        // a base descriptor plus a constant: no per-MMA descriptor assembly.
+        const uint64_t dq = sdesc_sw128(sbase + kOffQ, 16, 1024);
+        const uint64_t dk = sdesc_sw128(sbase + kOffK, 16, 1024);
+        const uint64_t dv = sdesc_sw128(sbase + kOffV, kKVHalf, 1024);
+        // S_t(g) = Q_t K(g)^T into S_t (phase ph of s_full[t]).
+        auto issue_s = [&](int t, int g, int ph) {
+          const uint64_t ka = dk + (uint64_t)((g % NK) * (kKBytes >> 4));
+          const uint64_t qa = dq + (uint64_t)(t * (kQBytes >> 4));
 #pragma unroll
-          for (int k = 0; k < kD / 16; ++k) {
-            const uint64_t ad = sdesc_sw128(sbase + kOffQ + (k >> 2) * kQHalf + (k & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(kst + (k >> 2) * kKVHalf + (k & 3) * 32, 16, 1024);
-            tc_mma_f16(tmem + kColS + sb * kN, ad, bd, kIdescS, k > 0);
-          }
-          tc_commit(b_kempty0 + 8 * sk);
-          tc_commit(b_sfull0 + 8 * sb);
-          last_bar = b_sfull0 + 8 * sb;
-          last_phase = (g / kSBuf) & 1;
+          for (int k = 0; k < kD / 16; ++k)
+            tc_mma_f16(tmem + col_s(t), qa + (((k >> 2) * kQHalf + (k & 3) * 32) >> 4),
+                       ka + (((k >> 2) * kKVHalf + (k & 3) * 32) >> 4), kIdescS, k > 0);
+          tc_commit(b_sfull0 + 8 * t);
+          last_bar = b_sfull0 + 8 * t;
+          last_phase = ph & 1;
+        };
+        // O_t += P_t(g) V(g), P_t read from tensor memory, once the softmax
+        // has written P_t(g) (phase ph of p_full[t]).
+        auto issue_pv = [&](int t, int g, int ph, bool acc) -> bool {
+          if (!mbar_wait(b_pfull0 + 8 * t, ph & 1, p.status)) return false;
+          tc_fence_after();
+          const uint64_t va = dv + (uint64_t)((g % NV) * (kKBytes >> 4));
+#pragma unroll
+          for (int k = 0; k < kN / 16; ++k)
+            tc_mma_f16_ta(tmem + col_o(t), tmem + col_s(t) + k * 8, va + ((k * 2048) >> 4), kIdescO,
+                          (acc || k > 0) ? 1u : 0u);
           return true;
         };
-        for (int i = 0; i < kSBuf && i < ntiles && !bad; ++i) bad = !issue_s(tile_base + i);
-        for (int j = 0; j < ntiles && !bad; ++j) {
-          const int g = tile_base + j;
-          const int sb = g % kSBuf, sv = g % NV;
-          if (!mbar_wait(b_pfull0 + 8 * sb, (g / kSBuf) & 1, p.status)) { bad = true; break; }
-          if (!mbar_wait(b_vfull0 + 8 * sv, (g / NV) & 1, p.status)) { bad = true; break; }
+        auto wait_k = [&](int g) -> bool {
+          if (!mbar_wait(b_kfull0 + 8 * (g % NK), (g / NK) & 1, p.status)) return false;
           tc_fence_after();
-          const uint32_t vst = sbase + kOffV + sv * kKBytes;
-#pragma unroll
-          for (int k = 0; k < kN / 16; ++k) {
-            const uint64_t bd = sdesc_sw128(vst + k * 2048, kKVHalf, 1024);
-            tc_mma_f16_ta(tmem + kColO, tmem + kColS + sb * kN + k * 8, bd, kIdescO, (j > 0 || k > 0) ? 1u : 0u);
+          return true;
+        };
+        if (!bad && ntiles > 0) {
+          if (!wait_k(tile_base)) {
+            bad = true;
+          } else {
+            issue_s(0, tile_base, tile_base);
+            if (nq == 2) issue_s(1, tile_base, tile_base1);
+            tc_commit(b_kempty0 + 8 * (tile_base % NK));
           }
-          tc_commit(b_vempty0 + 8 * sv);
-          tc_commit(b_odone0 + 8 * sb);
-          last_bar = b_odone0 + 8 * sb;
-          last_phase = (g / kSBuf) & 1;
-          if (j + kSBuf < ntiles && !issue_s(g + kSBuf)) { bad = true; break; }
+        }
+        for (int j = 0; j < ntiles && !bad; ++j) {
+          const int g = tile_base + j, g1 = tile_base1 + j;  // phases of Q tile 0 / 1
+          const bool more = j + 1 < ntiles;
+          if (!mbar_wait(b_vfull0 + 8 * (g % NV), (g / NV) & 1, p.status)) { bad = true; break; }
+          if (!issue_pv(0, g, g, j > 0)) { bad = true; break; }
+          if (!more) {
+            tc_commit(b_odone0);
+            last_bar = b_odone0;
+            last_phase = it & 1;
+          } else {
+            if (!wait_k(g + 1)) { bad = true; break; }
+            issue_s(0, g + 1, g + 1);
+          }
+          if (nq == 2 && !issue_pv(1, g, g1, j > 0)) { bad = true; break; }
+          tc_commit(b_vempty0 + 8 * (g % NV));
+          if (nq == 2 && !more) {
+            tc_commit(b_odone0 + 8);
+            last_bar = b_odone0 + 8;
+            last_phase = items1 & 1;
+          }
+          if (more) {
+            if (nq == 2) issue_s(1, g + 1, g1 + 1);
+            tc_commit(b_kempty0 + 8 * ((g + 1) % NK));
+          }
         }
         if (bad) {
           abort_flag[0] = 1;
@@ -416,10 +446,13 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
       __syncwarp();
     } else {
       // =========================== softmax ===========================
+      const int t = (warp - kSoftmaxWarp0) >> 2;  // Q tile of this warpgroup
       const int q = warp & 3;             // tensor-memory lane quarter of this warp
-      const int row = q * 32 + lane;      // packed row owned by this thread
+      const int row = q * 32 + lane;      // packed row of Q tile t owned by this thread
       const uint32_t tl = (uint32_t)(q * 32) << 16;
-      const int pos = pos_lo + (row >> p.gshift);  // query position (chunk) or group member (prefix)
+      const uint32_t ts = tmem + tl + col_s(t), to = tmem + tl + col_o(t);
+      const uint32_t b_sfull = b_sfull0 + 8 * t, b_pfull = b_pfull0 + 8 * t, b_odone = b_odone0 + 8 * t;
+      const int pos = pos_lo + t * pp + (row >> p.gshift);  // query position (chunk) or group member (prefix)
       const int head = row & (G - 1);
       int lim;  // last key this row may see (-1: none)
       if constexpr (!PREFIX) {
@@ -430,20 +463,20 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
       const float sl2 = p.scale_log2;
       float m = -CUDART_INF_F, l = 0.f;
       bool bad = false;
-      for (int j = 0; j < ntiles; ++j) {
+      const bool live = t < nq;  // warpgroup 0 always: it also zeroes V rows past the keys
+      const int ph0 = t == 0 ? tile_base : tile_base1;  // phase base of this tile's s_full / p_full
+      for (int j = 0; j < ntiles && live; ++j) {
         const int g = tile_base + j;
-        const int sb = g % kSBuf;  // S buffer of this tile
-        if (!mbar_wait(b_sfull0 + 8 * sb, (g / kSBuf) & 1, p.status)) { bad = true; break; }
+        if (!mbar_wait(b_sfull, (ph0 + j) & 1, p.status)) { bad = true; break; }
         tc_fence_after();
         uint32_t sr[kN / 32][32];
 #pragma unroll
-        for (int h = 0; h < kN / 32; ++h) tmem_ld32(tmem + tl + kColS + sb * kN + h * 32, sr[h]);
+        for (int h = 0; h < kN / 32; ++h) tmem_ld32(ts + h * 32, sr[h]);
         tmem_ld_wait();
         const int k0 = j * kN;
         // Raw-score row max (scale > 0 keeps the order); the causal / prefix
         // mask is skipped when the whole tile is visible to every row of the warp.
         const bool full_vis = __all_sync(0xffffffffu, k0 + kN - 1 <= lim);
-        float mx = -CUDART_INF_F;
         if (!full_vis) {
 #pragma unroll
           for (int h = 0; h < kN / 32; ++h)
@@ -453,6 +486,7 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
               if (key > lim) sr[h][c] = __float_as_uint(-CUDART_INF_F);
             }
         }
+        float mx = -CUDART_INF_F;
 #pragma unroll
         for (int h = 0; h < kN / 32; ++h)
 #pragma unroll
@@ -468,74 +502,79 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
           alpha = fast_exp2((m - mx) * sl2);
           m = mx;
         }
-        const float neg = m == -CUDART_INF_F ? 0.f : -m * sl2;
-        // p = 2^(s * scale * log2(e) - m * scale * log2(e)), two keys per
-        // paired FMA; the row sum accumulates in pairs.
-        const uint64_t sl2x2 = f2_pack(sl2, sl2), negx2 = f2_pack(neg, neg);
-        uint64_t rs2 = f2_pack(0.f, 0.f);
-        uint32_t pk[kN / 2];
-#pragma unroll
-        for (int h = 0; h < kN / 32; ++h)
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1])), sl2x2, negx2), x0, x1);
-            const float a = fast_exp2(x0), b = fast_exp2(x1);
-            rs2 = f2_add(rs2, f2_pack(a, b));
-            pk[h * 16 + c / 2] = MmaOp<T>::pack(a, b);
-          }
-        float rs0, rs1;
-        f2_unpack(rs2, rs0, rs1);
-        l = l * alpha + (rs0 + rs1);
-        if (k0 + kN > kv_len) {
+        if (t == 0 && k0 + kN > kv_len) {
           // Keys past the sequence end carry p = 0, but their V slots may
-          // hold any bits (NaN included): zero those V rows before PV reads them.
+          // hold any bits (NaN included): zero those V rows before PV reads
+          // them (warpgroup 0 does it before its p_full; PV1 is issued
+          // after PV0, which waits for that).
           const int sv = g % NV;
           if (!mbar_wait(b_vfull0 + 8 * sv, (g / NV) & 1, p.status)) { bad = true; break; }
           uint8_t* vst = smem + kOffV + sv * kKBytes;
           const int first = max(kv_len - k0, 0);
-          for (int idx = threadIdx.x - 64; idx < (kN - first) * 16; idx += 128) {
+          for (int idx = threadIdx.x - 32 * kSoftmaxWarp0 - 128 * t; idx < (kN - first) * 16; idx += 128) {
             const int r = first + idx / 16, c = idx % 16;  // row, 16-byte chunk over both halves
             *reinterpret_cast<int4*>(vst + (c >> 3) * kKVHalf + r * 128 + (c & 7) * 16) = make_int4(0, 0, 0, 0);
           }
           fence_async_shared();
         }
-        // Rescale the O row when the running max moved (warp-uniform); PV of
-        // the previous tile must have finished accumulating into O first.
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          if (!mbar_wait(b_odone0 + 8 * ((g - 1) % kSBuf), ((g - 1) / kSBuf) & 1, p.status)) { bad = true; break; }
-          tc_fence_after();
+        const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+        const float neg = m == -CUDART_INF_F ? 0.f : -m * sl2;
+        // p = 2^(s * scale * log2(e) - m * scale * log2(e)), two keys per
+        // paired FMA; the row sum accumulates in pairs. P goes to tensor
+        // memory 64 keys (32 columns) at a time.
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), negx2 = f2_pack(neg, neg);
+        uint64_t rs2 = f2_pack(0.f, 0.f);
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t orow[32];
-            tmem_ld32(tmem + tl + kColO + cc * 32, orow);
-            tmem_ld_wait();
+        for (int hh = 0; hh < kN / 64; ++hh) {
+          uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) orow[c] = __float_as_uint(__uint_as_float(orow[c]) * alpha);
-            tmem_st32(tmem + tl + kColO + cc * 32, orow);
+          for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const int h = hh * 2 + h2;
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1])), sl2x2, negx2), x0,
+                        x1);
+              const float a = fast_exp2(x0), b = fast_exp2(x1);
+              rs2 = f2_add(rs2, f2_pack(a, b));
+              pk[h2 * 16 + c / 2] = MmaOp<T>::pack(a, b);
+            }
+          if (hh == 0 && rescale) {
+            // Rescale the O row when the running max moved (warp-uniform),
+            // before PV of this tile accumulates (here, once half of the
+            // scores are dead, to keep registers free). PV_t of the previous
+            // tile has completed: its commit preceded S_t(g)'s.
+#pragma unroll 1
+            for (int cc = 0; cc < kD / 16; ++cc) {
+              uint32_t orow[16];
+              tmem_ld16(to + cc * 16, orow);
+              tmem_ld_wait();
+#pragma unroll
+              for (int c = 0; c < 16; ++c) orow[c] = __float_as_uint(__uint_as_float(orow[c]) * alpha);
+              tmem_st16(to + cc * 16, orow);
+            }
           }
+          tmem_st32(ts + hh * 32, pk);
         }
-        // P (kN keys, 16-bit pairs) over the first kN/2 columns of this
-        // tile's S buffer: the A operand of PV.
-#pragma unroll
-        for (int h = 0; h < kN / 64; ++h)
-          tmem_st32(tmem + tl + kColS + sb * kN + h * 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + h * 32));
+        float rs0, rs1;
+        f2_unpack(rs2, rs0, rs1);
+        l = l * alpha + (rs0 + rs1);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(b_pfull0 + 8 * sb);
+        if (lane == 0) mbar_arrive(b_pfull);
       }
-      const int gl = tile_base + ntiles - 1;
-      if (!bad && mbar_wait(b_odone0 + 8 * (gl % kSBuf), (gl / kSBuf) & 1, p.status)) {
+      if (!live) {
+      } else if (!bad && mbar_wait(b_odone, (t == 0 ? it : items1) & 1, p.status)) {
         tc_fence_after();
         if constexpr (!PREFIX) {
           const float inv = 1.f / l;
           T* orow = static_cast<T*>(p.out) + ((int64_t)(q0 + pos) * p.num_q_heads + kvh * G + head) * kD;
           const bool valid = pos < ql;
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < kD / 32; ++cc) {
             uint32_t ov[32];
-            tmem_ld32(tmem + tl + kColO + cc * 32, ov);
+            tmem_ld32(to + cc * 32, ov);
             tmem_ld_wait();
             if (valid) {
 #pragma unroll
@@ -552,9 +591,9 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
           const bool valid = lim >= 0;
           const int64_t base = ((int64_t)(s0 + pos) * p.num_q_heads + kvh * G + head) * p.max_parts;
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < kD / 32; ++cc) {
             uint32_t ov[32];
-            tmem_ld32(tmem + tl + kColO + cc * 32, ov);
+            tmem_ld32(to + cc * 32, ov);
             tmem_ld_wait();
             if (valid) {
 #pragma unroll
@@ -573,6 +612,10 @@ __global__ void __launch_bounds__(pf::kThreads, pf::kCtasPerSm)
       tc_fence_before();
     }
     tile_base += ntiles;
+    if (nq == 2) {
+      tile_base1 += ntiles;
+      ++items1;
+    }
     __syncthreads();
     if (abort_flag[0]) break;
   }
