@@ -320,6 +320,7 @@ static int decode_prepare(const void* q, const void* k_cache, const void* v_cach
   p.pairs = reinterpret_cast<int32_t*>(ws + wl->pairs);
   p.part_o = max_parts > 1 ? reinterpret_cast<float*>(ws + wl->part_o) : nullptr;
   p.part_ml = max_parts > 1 ? reinterpret_cast<float*>(ws + wl->part_ml) : nullptr;
+  p.merge_list = max_parts > 1 ? reinterpret_cast<int4*>(ws + wl->merge) : nullptr;
   p.prefix = nullptr;
   p.slot0 = extra_slots;
   p.status = st;

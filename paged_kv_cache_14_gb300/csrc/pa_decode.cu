@@ -996,60 +996,80 @@ __global__ void __launch_bounds__(128) decode_simt_kernel(const DecodeParams p) 
 
 // Split-KV merge: out = sum_p 2^(m_p - M) o~_p / sum_p 2^(m_p - M) l_p with
 // M = max_p m_p (scores are kept in log2 units). One warp per (sequence,
-// query head), eight heads per CTA: lanes reduce the partitions' (m, l)
-// pairs, then each lane accumulates four head_dim columns over the
-// partitions with coalesced 16-byte loads.
+// query head), eight heads per work unit, over the sequences the plan listed
+// (those with more than one partition), on a fixed grid. Each lane reads
+// every partition's (m, l) and its own four head_dim columns of every
+// partial, all loads in flight together (up to eight partitions), then
+// accumulates in partition order.
 template <typename T>
 __global__ void __launch_bounds__(256) splitkv_merge_kernel(const DecodeParams p) {
-  pdl_wait();  // every partial of the decode kernel
+  pdl_wait();  // every partial of the decode kernel, and the plan's list
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x * 8 + warp;
-  const int seq = blockIdx.y;
-  if (h >= p.num_q_heads) return;
-  int qrow, len;
-  if (!decode_row(p, seq, qrow, len) || !len_ok(p, len)) return;
-  const int pfx = p.prefix ? p.prefix[seq] : 0;
-  const int ns = (len - pfx + p.partition - 1) / p.partition;  // suffix partitions
-  if (ns <= 1) return;  // written by the decode kernel (alone, or merged with the prefix partial)
-  const int first = pfx > 0 ? 0 : p.slot0;                      // slot 0 holds the prefix pass
-  const int n = p.slot0 + ns - first;
-  const int64_t base = ((int64_t)seq * p.num_q_heads + h) * p.max_parts + first;
-  const float* ml = p.part_ml + base * 2;
-  float M = -CUDART_INF_F;
-  for (int i = lane; i < n; i += 32) M = fmaxf(M, __ldcg(ml + 2 * i));
+  const int hgroups = (p.num_q_heads + 7) / 8;
+  // The first unit's list entry is read together with the count (the
+  // grid never exceeds num_seqs x hgroups, so the index is in range).
+  int4 e = p.merge_list[blockIdx.x / hgroups];
+  const int units = p.work[2] * hgroups;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    if (u != (int)blockIdx.x) e = p.merge_list[u / hgroups];
+    const int h = (u - (u / hgroups) * hgroups) * 8 + warp;
+    if (h >= p.num_q_heads) continue;
+    const int seq = e.x, qrow = e.y, first = e.z, n = e.w;
+    const int64_t base = ((int64_t)seq * p.num_q_heads + h) * p.max_parts + first;
+    const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + base;
+    const int D = p.head_dim;
+    T* out = static_cast<T*>(p.out) + ((int64_t)qrow * p.num_q_heads + h) * D;
+    for (int c0 = 0; c0 < D; c0 += 128) {
+      const int d4 = c0 + lane * 4;
+      const bool col = d4 < D;
+      const float* src = p.part_o + base * D + d4;
+      float M = -CUDART_INF_F, L = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      auto add = [&](float2 mv, float4 ov) {
+        const float w = mv.x == -CUDART_INF_F ? 0.f : exp2f(mv.x - M);
+        L += w * mv.y;
+        acc.x = fmaf(w, ov.x, acc.x);
+        acc.y = fmaf(w, ov.y, acc.y);
+        acc.z = fmaf(w, ov.z, acc.z);
+        acc.w = fmaf(w, ov.w, acc.w);
+      };
+      if (n <= 8) {
+        float2 mv[8];
+        float4 ov[8];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float L = 0.f;
-  for (int i = lane; i < n; i += 32) {
-    const float2 v = __ldcg(reinterpret_cast<const float2*>(ml + 2 * i));
-    L += v.x == -CUDART_INF_F ? 0.f : exp2f(v.x - M) * v.y;
-  }
+        for (int i = 0; i < 8; ++i) {
+          mv[i] = make_float2(-CUDART_INF_F, 0.f);
+          ov[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (i < n) {
+            mv[i] = __ldcg(ml + i);
+            if (col) ov[i] = __ldcg(reinterpret_cast<const float4*>(src + (int64_t)i * D));
+          }
+        }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  const float invL = 1.f / L;
-  const int D = p.head_dim;
-  T* out = static_cast<T*>(p.out) + ((int64_t)qrow * p.num_q_heads + h) * D;
-  for (int d4 = lane * 4; d4 < D; d4 += 128) {
-    const float* src = p.part_o + base * D + d4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int i = 0; i < n; ++i) {
-      const float mi = __ldcg(ml + 2 * i);
-      const float w = mi == -CUDART_INF_F ? 0.f : exp2f(mi - M);
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (int64_t)i * D));
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+        for (int i = 0; i < 8; ++i) M = fmaxf(M, mv[i].x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i < n) add(mv[i], ov[i]);
+      } else {
+        for (int i = 0; i < n; ++i) M = fmaxf(M, __ldcg(ml + i).x);
+        for (int i = 0; i < n; ++i)
+          add(__ldcg(ml + i), col ? __ldcg(reinterpret_cast<const float4*>(src + (int64_t)i * D))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f));
+      }
+      const float invL = 1.f / L;
+      if (col) store4(out + d4, make_float4(acc.x * invL, acc.y * invL, acc.z * invL, acc.w * invL));
     }
-    store4(out + d4, make_float4(acc.x * invL, acc.y * invL, acc.z * invL, acc.w * invL));
   }
 }
 
 static int launch_merge(const DecodeParams& p, pa_dtype dt, cudaStream_t stream) {
   if (p.max_parts <= 1) return PA_OK;
-  const dim3 grid((p.num_q_heads + 7) / 8, p.num_seqs);
+  // A fixed grid (one wave of 256-thread CTAs) over however many sequences
+  // the plan listed.
+  const int64_t units = (int64_t)p.num_seqs * ((p.num_q_heads + 7) / 8);
+  const int64_t cap = 4LL * num_sms_current_device();
+  const dim3 grid((unsigned)(units < cap ? units : cap));
   cudaError_t e;
   if (dt == PA_F32)
     e = launch_dependent(splitkv_merge_kernel<float>, grid, dim3(256), 0, stream, p);

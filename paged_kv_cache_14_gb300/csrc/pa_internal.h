@@ -40,7 +40,10 @@ struct DecodeParams {
   float scale_log2;      // scale * log2(e)
   float* part_o;         // [num_seqs][num_q_heads][max_parts][head_dim]
   float* part_ml;        // [num_seqs][num_q_heads][max_parts][2] (m, l)
-  int32_t* work;         // [0] next work item, [1] number of work items (written by the plan kernel)
+  // [num_seqs] x {sequence, output row, first partial slot, slots}: the
+  // sequences with more than one split-KV partition (written by the plan).
+  int4* merge_list;
+  int32_t* work;         // [0] next work item, [1] number of work items, [2] sequences to merge (plan)
   int32_t* pairs;        // [num_seqs * max_parts] (seq << 16 | partition), in work order
   // Shared-prefix (cascade) decode: tokens [0, prefix[i]) of sequence i were
   // attended by the prefix pass, whose partial sits in slot 0; the suffix
@@ -61,7 +64,7 @@ void decode_set_rows(DecodeParams& p, pa_dtype dt);
 // Split-KV workspace layout shared by the size query and the launch. Every
 // region starts on a 256-byte boundary.
 struct DecodeWorkspace {
-  size_t work, pairs, part_o, part_ml, total;
+  size_t work, pairs, part_o, part_ml, merge, total;
 };
 inline DecodeWorkspace decode_workspace_layout(int64_t num_seqs, int64_t num_q_heads, int64_t head_dim,
                                                int64_t max_parts) {
@@ -73,7 +76,8 @@ inline DecodeWorkspace decode_workspace_layout(int64_t num_seqs, int64_t num_q_h
   const size_t po = max_parts > 1 ? (size_t)num_seqs * num_q_heads * max_parts * head_dim * 4 : 0;
   w.part_ml = up(w.part_o + po);
   const size_t pm = max_parts > 1 ? (size_t)num_seqs * num_q_heads * max_parts * 2 * 4 : 0;
-  w.total = up(w.part_ml + pm);
+  w.merge = up(w.part_ml + pm);
+  w.total = up(w.merge + (max_parts > 1 ? (size_t)num_seqs * 16 : 0));
   return w;
 }
 

@@ -697,8 +697,16 @@ int launch_prefix_pass(const PrefillParams& p0, const void* k_cache, const void*
   if (rc != PA_OK) return rc;
   rc = make_kv_tensor_map(&vmap, v_cache, rows, pf::kD, dt, 16);
   if (rc != PA_OK) return rc;
+  // The suffix decode runs beside this pass and cannot share an SM with it
+  // (shared memory), so the pass takes only a fraction of the SMs: it is
+  // bound by the latency of its shared-prefix reads, not by SM count, and
+  // the decode keeps the rest streaming from the start.
+#ifndef PA_PREFIX_SM_DIV
+#define PA_PREFIX_SM_DIV 4
+#endif
   const int64_t upper = (int64_t)p.num_seqs * p.num_kv_heads;
-  const int64_t resident = (int64_t)pf::kCtasPerSm * num_sms_current_device();
+  int64_t resident = (int64_t)pf::kCtasPerSm * num_sms_current_device() / PA_PREFIX_SM_DIV;
+  if (resident < 1) resident = 1;
   const int ctas = (int)(upper < resident ? upper : resident);
   return dispatch_prefill_kernel<true>(qmap, kmap, vmap, p, ctas, dt, stream);
 }

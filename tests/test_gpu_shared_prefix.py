@@ -94,3 +94,21 @@ def test_llama3_70b_prefix_config_shared_prefix(lib):
     pick = sorted(set([int(order[0]), int(order[-1]), 0, 15, 16]) | set(rng.choice(256, 10, replace=False).tolist()))
     ref = oracle_decode(b, kr, vr, seqs=pick)
     assert_attention_close(to_f64(out)[pick], ref[pick], "bf16", "shared-prefix vs oracle, full size")
+
+
+@pytest.mark.parametrize("n", [5000, 17000], ids=["staged_large", "unstaged"])
+def test_shared_prefix_many_sequences(lib, n):
+    # The preparation kernel keeps its per-sequence state in shared memory up
+    # to a size cap (5000 sequences: above the 48 KB default, so the opt-in
+    # size is used) and works on the workspace arrays beyond it (17000).
+    rng = np.random.default_rng(n)
+    lens = rng.integers(33, 97, size=n).astype(np.int32)
+    b = build_batch(name="cascade_many", seed=91, dtype="bf16", block_size=16, num_q_heads=8, num_kv_heads=1,
+                    head_dim=128, q_lens=np.ones(n, np.int32), kv_lens=lens, share_group=8,
+                    share_prefix_tokens=32, cow_per_seq=False)
+    assert (b.prefix_lens > 0).all()
+    st = _device_step(lib, b)
+    plain = to_f64(st.out)
+    out = to_f64(_shared(lib, st, b))
+    assert lib.pa_get_status() == 0
+    assert_attention_close(out, plain, "bf16", f"{n} sequences: shared-prefix vs pa_decode")
