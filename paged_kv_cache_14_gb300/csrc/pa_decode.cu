@@ -274,15 +274,15 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
                       static_cast<const T*>(p.q) + ((int64_t)qrow * p.num_q_heads + h0) * D, nrows * D * 2, fb);
       }
       const int32_t* bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq + t_begin / BS;
-      for (int ub = 0; ub < nsub_pad && !bad; ub += 32) {
-        // Lane k holds the physical blocks of the sub-tiles of stage ub + k
-        // (-1: padding) and, for an e4m3 cache, those blocks' (K, V) scales.
-        int id[C::kSubTiles];
-        float2 bsc[C::kSubTiles];
+      // Lane k holds the physical blocks of the sub-tiles of stage ub + k of
+      // a batch of 32 stages (-1: padding) and, for an e4m3 cache, those
+      // blocks' (K, V) scales. Loads run ahead of use: at the start of batch
+      // ub the scales of batch ub + 32 and the ids of batch ub + 64 are
+      // requested, so no batch waits on a table or scale load.
+      auto load_ids = [&](int ub, int (&id)[C::kSubTiles]) {
 #pragma unroll
         for (int h = 0; h < C::kSubTiles; ++h) {
           id[h] = -1;
-          bsc[h] = make_float2(0.f, 0.f);
           const int sub = (ub + lane) * C::kSubTiles + h;
           if (sub < nsub16) {
             id[h] = bt[sub / kSubPerBlock];
@@ -290,12 +290,29 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
               record_error(p.status, PA_ERR_BLOCK_OOB);
               id[h] = -1;
             }
-            if constexpr (KV8) {
-              if (id[h] >= 0)
-                bsc[h] = __ldg(reinterpret_cast<const float2*>(p.kv_scales) + (int64_t)id[h] * p.num_kv_heads + kvh);
-            }
           }
         }
+      };
+      auto load_scales = [&](const int (&id)[C::kSubTiles], float2 (&sc)[C::kSubTiles]) {
+#pragma unroll
+        for (int h = 0; h < C::kSubTiles; ++h) {
+          sc[h] = make_float2(0.f, 0.f);
+          if constexpr (KV8) {
+            if (id[h] >= 0)
+              sc[h] = __ldg(reinterpret_cast<const float2*>(p.kv_scales) + (int64_t)id[h] * p.num_kv_heads + kvh);
+          }
+        }
+      };
+      int id[C::kSubTiles], id_next[C::kSubTiles];
+      float2 bsc[C::kSubTiles];
+      load_ids(0, id);
+      load_scales(id, bsc);
+      load_ids(32, id_next);
+      for (int ub = 0; ub < nsub_pad && !bad; ub += 32) {
+        int id_after[C::kSubTiles];
+        float2 bsc_next[C::kSubTiles];
+        load_scales(id_next, bsc_next);
+        load_ids(ub + 64, id_after);
         const int cnt = min(32, nsub_pad - ub);
         // Issue the batch in groups of up to kStages stages, one lane per
         // stage: each lane waits for its own ring slot (all distinct within
@@ -365,6 +382,12 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
             decode_row(p, next_pr >> 16, next_qrow, next_len);
             next_pfx = p.prefix ? p.prefix[next_pr >> 16] : 0;
           }
+        }
+#pragma unroll
+        for (int h = 0; h < C::kSubTiles; ++h) {
+          id[h] = id_next[h];
+          bsc[h] = bsc_next[h];
+          id_next[h] = id_after[h];
         }
       }
       if (bad) break;
