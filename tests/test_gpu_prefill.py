@@ -30,6 +30,8 @@ CASES = [
     ("f16", 16, 32, 8, [31, 2, 1, 1], [15, 16, 0, 700]),  # group 4
     ("bf16", 32, 32, 2, [40, 3], [128, 1]),          # group 16: 8 positions per tile
     ("f16", 32, 64, 8, [512], [1000]),               # a long chunk over a long context
+    ("bf16", 16, 64, 2, [9, 4, 13], [30, 0, 100]),   # group 32: 4 positions per Q tile
+    ("f16", 16, 128, 1, [3, 2, 5, 1], [7, 40, 0, 9]),  # group 128: one position per Q tile
 ]
 
 
@@ -90,3 +92,19 @@ def test_mixed_prefill_config_sampled(lib):
     cu = b.cu_q_lens
     sel = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in dec] + [cu[i] + np.array(rows[i]) for i in chunks])
     assert_attention_close(out[sel], ref[sel], "f16", "mixed_prefill_fp16")
+
+
+def test_prefill_many_items_mixed_q_tiles(lib):
+    # A work item is 256 packed rows in two Q tiles (16 positions each at
+    # group 8). A 48-row chunk gives one item with both tiles and one whose
+    # second tile is empty. With 24 such chunks x 8 KV heads (384 items)
+    # every CTA runs several items of both kinds in turn, which exercises
+    # the second tile's own barrier phases.
+    rng = np.random.default_rng(404)
+    qls = [48] * 24 + [17, 33]
+    ctxs = rng.integers(0, 600, size=len(qls)).tolist()
+    b = build_batch(name="pf_many", seed=404, dtype="bf16", block_size=16, num_q_heads=64, num_kv_heads=8,
+                    head_dim=128, q_lens=qls, kv_lens=[c + q for c, q in zip(ctxs, qls)])
+    _, out = run_step(lib, b)
+    kc, vc, _ = oracle_caches_after_step(b)
+    assert_attention_close(out, oracle_prefill(b, kc, vc), "bf16", "many items, mixed Q tiles")

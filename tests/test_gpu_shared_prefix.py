@@ -112,3 +112,34 @@ def test_shared_prefix_many_sequences(lib, n):
     out = to_f64(_shared(lib, st, b))
     assert lib.pa_get_status() == 0
     assert_attention_close(out, plain, "bf16", f"{n} sequences: shared-prefix vs pa_decode")
+
+
+def test_shared_prefix_many_groups_mixed_q_tiles(lib):
+    # Groups of 20 members (at group 8: two Q tiles, the second with 4
+    # members) alternate with groups of 10 (one Q tile). 48 groups x 8 KV
+    # heads give 384 prefix-pass items, more than that pass has CTAs, so
+    # each CTA runs both kinds in turn.
+    sizes = [20, 10] * 24
+    lens, starts = [], [0]
+    rng = np.random.default_rng(505)
+    for g in sizes:
+        lens += rng.integers(130, 400, size=g).tolist()
+        starts.append(starts[-1] + g)
+    b = build_batch(name="cascade_mixed", seed=505, dtype="bf16", block_size=16, num_q_heads=64, num_kv_heads=8,
+                    head_dim=128, q_lens=np.ones(len(lens), np.int32), kv_lens=lens, share_group=1,
+                    share_prefix_tokens=0, cow_per_seq=False)
+    st = _device_step(lib, b)
+    gs = np.array(starts, np.int32)
+    pl = np.full(len(lens), 128, np.int32)  # hint: the first 8 blocks are shared
+    # Make every group share its first 8 blocks: point each member's first
+    # table entries at the group's first member's blocks, then compare
+    # against plain decode on the same tables.
+    bt = st.block_tables.clone()
+    for gi in range(len(sizes)):
+        s0, s1 = starts[gi], starts[gi + 1]
+        bt[s0 + 1:s1, :8] = bt[s0, :8]
+    st.block_tables.copy_(bt)
+    plain = to_f64(lib.pa_decode(st.q, st.k_cache, st.v_cache, st.block_tables, st.kv_lens, st.max_seq_len, b.scale))
+    out = to_f64(_shared(lib, st, b, group_starts=gs, prefix_lens=pl))
+    assert lib.pa_get_status() == 0
+    assert_attention_close(out, plain, "bf16", "mixed group sizes: shared-prefix vs pa_decode")
