@@ -403,22 +403,29 @@ def native_arm(args) -> None:
     if status != 0:
         raise RuntimeError(f"device status after warm-up: {pa.pa_strerror(status)}")
 
-    # Timed region: K steps; CUDA events bracket the whole region and, on the
-    # same stream, each decode launch (main + merge kernels).
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # Timed region: K whole steps (PagedStep.run: one call for a
+    # shared-prefix step, whose prefix check runs beside the cache side),
+    # bracketed by CUDA events on the launching stream.
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier()
         start.record(stream)
         for i in range(args.steps):
-            st.prepare()
-            ev[i][0].record(stream)
-            st.attend()
-            ev[i][1].record(stream)
+            st.run()
         stop.record(stream)
         barrier()
         clocks = clk.summary()
     ms_total = start.elapsed_time(stop)
+    # The attention call alone (the roofline entry): K more steps run as
+    # cache side + attention call, with events around each attention call.
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        st.prepare()
+        ev[i][0].record(stream)
+        st.attend()
+        ev[i][1].record(stream)
+    barrier()
     dec_ms = [a.elapsed_time(b) for a, b in ev]
     status = pa.pa_get_status()
     if status != 0:
@@ -502,8 +509,9 @@ def native_arm(args) -> None:
                 "kv_cache": ("e4m3 codes + fp32 (K, V) scale per (block, KV head); q/out " + batch.dtype)
                 if fp8 else batch.dtype,
                 "step": ("copy_blocks_fp8 + slot_mapping + reshape_and_cache_fp8 + pa_decode_fp8" if fp8 else
+                         "pa_decode_step_shared_prefix (copy_blocks + slot_mapping + reshape_and_cache + "
+                         "pa_decode_shared_prefix in one call)" if st.shared_prefix else
                          "copy_blocks + slot_mapping + reshape_and_cache + " + (
-                             "pa_decode_shared_prefix" if st.shared_prefix else
                              "pa_decode" if st.is_decode else "pa_chunked_prefill")),
                 "step_bytes": step_bytes, "decode_bytes": dec_bytes,
                 "l2": "inputs larger than L2 (KV pools %.2f GB vs 129 MB L2); no flush" % (

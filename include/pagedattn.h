@@ -250,8 +250,8 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
  *                  record PA_ERR_ARG and disable every hint.
  *   workspace    : pa_decode_shared_prefix_workspace_size() bytes.
  * Other arguments as pa_decode. fp16/bf16, head_dim 128, GQA group a power
- * of two up to 128 (up to 128/group members per tensor-core tile; larger
- * groups take several tiles), scale > 0.
+ * of two up to 128 (up to 256/group members per tensor-core work item, in
+ * two tiles; larger groups take several items), scale > 0.
  */
 size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                               int32_t head_dim, int32_t block_size, int32_t max_seq_len,
@@ -262,6 +262,43 @@ int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_ca
                             int32_t num_groups, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                             int32_t block_size, int32_t num_blocks, float scale, void* out, int32_t partition_size,
                             void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream);
+
+/*
+ * pa_decode_step_shared_prefix — one decode step of a prefix-sharing batch
+ * in a single call: the same work and results as, in this order,
+ *   pa_copy_blocks(k_cache, v_cache, cow_pairs, num_cow_pairs, ...),
+ *   pa_slot_mapping(block_tables, ..., new_seq_ids, new_positions,
+ *                   num_new_tokens, ..., slot_mapping),
+ *   pa_reshape_and_cache(k_new, v_new, slot_mapping, num_new_tokens, ...),
+ *   pa_decode_shared_prefix(q, k_cache, v_cache, block_tables, ...)
+ * (a serving step: copy-on-write of shared blocks about to be written,
+ * "High-Throughput Local LLM Infrastructure...", section 1.2; slots and the
+ * cache write of the step's new tokens, section 1.2 and "Inside vLLM...",
+ * "PagedAttention"; then the attention of the new query tokens).
+ * Because every kernel of the step is this library's, the call launches the
+ * shared-prefix check first and runs the copies, slots and cache write beside
+ * it (it reads only block_tables, seq_lens, group_starts and prefix_lens,
+ * which they do not write); the attention kernels start once the cache write
+ * has completed.
+ *   cow_pairs      : int64 [num_cow_pairs][2] HOST (src, dst) block ids, as
+ *                    pa_copy_blocks (may be NULL when num_cow_pairs == 0)
+ *   new_seq_ids, new_positions : int32 [num_new_tokens] device, as
+ *                    pa_slot_mapping
+ *   k_new, v_new   : [num_new_tokens][num_kv_heads][head_dim] device, dtype
+ *   slot_mapping   : int64 [num_new_tokens] device, written
+ * Other arguments as pa_decode_shared_prefix. Every host check of the four
+ * calls runs before the first launch: a rejected call launches nothing.
+ * fp16/bf16 only (PA_ERR_DTYPE otherwise). Errors as the four calls.
+ */
+int pa_decode_step_shared_prefix(const int64_t* cow_pairs, int32_t num_cow_pairs, const int32_t* new_seq_ids,
+                                 const int32_t* new_positions, const void* k_new, const void* v_new,
+                                 int64_t num_new_tokens, int64_t* slot_mapping, const void* q, void* k_cache,
+                                 void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                                 const int32_t* group_starts, const int32_t* prefix_lens, int32_t num_groups,
+                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 int32_t num_blocks, float scale, void* out, int32_t partition_size, void* workspace,
+                                 size_t workspace_bytes, pa_dtype dtype, void* stream);
 
 /*
  * pa_decode_noalloc — pa_decode for callers that cannot allocate device

@@ -217,14 +217,15 @@ int pa_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mappi
                                   num_kv_heads, (int32_t)row_bytes, st, static_cast<cudaStream_t>(stream));
 }
 
-int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst_pairs, int32_t num_pairs,
-                   int32_t num_blocks, int64_t block_bytes, void* stream) {
-  if (num_pairs < 0 || num_blocks < 1 || block_bytes <= 0) return PA_ERR_ARG;
-  if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
-  if (num_pairs == 0) return PA_OK;
-  if (!k_cache || !v_cache || !src_dst_pairs) return PA_ERR_ARG;
-  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
-  std::vector<int32_t> src(num_pairs), dst(num_pairs);
+}  // extern "C"
+
+namespace pa {
+// Host check of copy-on-write pairs: every block in range, no destination
+// repeated or also a source. On success src / dst hold the pairs.
+static int check_copy_pairs(const int64_t* src_dst_pairs, int32_t num_pairs, int32_t num_blocks,
+                            std::vector<int32_t>& src, std::vector<int32_t>& dst) {
+  src.resize(num_pairs);
+  dst.resize(num_pairs);
   std::unordered_set<int64_t> dsts;
   dsts.reserve(num_pairs * 2);
   for (int32_t i = 0; i < num_pairs; ++i) {
@@ -236,6 +237,22 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst_pairs, i
   }
   for (int32_t i = 0; i < num_pairs; ++i)
     if (dsts.count(src[i])) return PA_ERR_ALIAS;
+  return PA_OK;
+}
+}  // namespace pa
+
+extern "C" {
+
+int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst_pairs, int32_t num_pairs,
+                   int32_t num_blocks, int64_t block_bytes, void* stream) {
+  if (num_pairs < 0 || num_blocks < 1 || block_bytes <= 0) return PA_ERR_ARG;
+  if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !src_dst_pairs) return PA_ERR_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+  std::vector<int32_t> src, dst;
+  const int rc = check_copy_pairs(src_dst_pairs, num_pairs, num_blocks, src, dst);
+  if (rc != PA_OK) return rc;
   return launch_copy_blocks(k_cache, v_cache, src.data(), dst.data(), num_pairs, block_bytes,
                             static_cast<cudaStream_t>(stream));
 }
@@ -468,14 +485,19 @@ size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_he
          cascade_workspace_layout(num_seqs, num_groups).total;
 }
 
-int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+}  // extern "C"
+
+namespace pa {
+template <typename Between>
+static int shared_prefix_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                             int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
                             int32_t max_seq_len, const int32_t* group_starts, const int32_t* prefix_lens,
                             int32_t num_groups, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                             int32_t block_size, int32_t num_blocks, float scale, void* out, int32_t partition_size,
-                            void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
+                            void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream,
+                            Between&& between) {
   if (num_seqs < 0 || num_groups < 0) return PA_ERR_ARG;
-  if (num_seqs == 0) return PA_OK;
+  if (num_seqs == 0) return between(false);
   if (num_groups < 1 || num_groups > num_seqs || !group_starts || !prefix_lens) return PA_ERR_ARG;
   if (dtype == PA_F32) return PA_ERR_DTYPE;
   if (!(scale > 0.f)) return PA_ERR_ARG;  // the prefix pass needs scale > 0
@@ -508,6 +530,10 @@ int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_ca
                            group_of_seq, pwork, ppairs, pkeys, s);
   dp.planned = 1;
   if (rc != PA_OK) return rc;
+  // Whatever the caller launches here runs beside the check: it must not
+  // write what the check reads (tables, lengths, hints, groups).
+  rc = between(true);
+  if (rc != PA_OK) return rc;
   // 2. Prefix pass (tcgen05): every group's shared blocks once for all its
   //    members, partials into slot 0.
   PrefillParams pp{};
@@ -538,6 +564,79 @@ int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_ca
   if (rc != PA_OK) return rc;
   // 3. Suffix decode (split-KV over the private keys) and the merge.
   return launch_decode(dp, dtype, s);
+}
+
+}  // namespace pa
+
+extern "C" {
+
+int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                            int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                            int32_t max_seq_len, const int32_t* group_starts, const int32_t* prefix_lens,
+                            int32_t num_groups, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t num_blocks, float scale, void* out, int32_t partition_size,
+                            void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
+  return shared_prefix_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                              group_starts, prefix_lens, num_groups, num_q_heads, num_kv_heads, head_dim, block_size,
+                              num_blocks, scale, out, partition_size, workspace, workspace_bytes, dtype, stream,
+                              [](bool) { return PA_OK; });
+}
+
+int pa_decode_step_shared_prefix(const int64_t* cow_pairs, int32_t num_cow_pairs, const int32_t* new_seq_ids,
+                                 const int32_t* new_positions, const void* k_new, const void* v_new,
+                                 int64_t num_new_tokens, int64_t* slot_mapping, const void* q, void* k_cache,
+                                 void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                                 const int32_t* group_starts, const int32_t* prefix_lens, int32_t num_groups,
+                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 int32_t num_blocks, float scale, void* out, int32_t partition_size, void* workspace,
+                                 size_t workspace_bytes, pa_dtype dtype, void* stream) {
+  // Host checks of the cache side, as the separate calls make them; the
+  // decode's own checks run inside shared_prefix_decode before any launch,
+  // so a rejected call launches nothing.
+  if (num_cow_pairs < 0 || num_new_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 1 ||
+      max_blocks_per_seq < 1 || num_seqs < 0)
+    return PA_ERR_ARG;
+  if (block_size != 16 && block_size != 32) return PA_ERR_BLOCKSIZE;
+  const int eb = elem_bytes(dtype);
+  if (!eb || dtype == PA_F32) return PA_ERR_DTYPE;
+  const int64_t row_bytes = (int64_t)head_dim * eb;
+  if (row_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+  if (!k_cache || !v_cache) return PA_ERR_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+  std::vector<int32_t> src, dst;
+  if (num_cow_pairs > 0) {
+    if (!cow_pairs) return PA_ERR_ARG;
+    const int rc = check_copy_pairs(cow_pairs, num_cow_pairs, num_blocks, src, dst);
+    if (rc != PA_OK) return rc;
+  }
+  if (num_new_tokens > 0) {
+    if (!new_seq_ids || !new_positions || !k_new || !v_new || !slot_mapping || !block_tables) return PA_ERR_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return PA_ERR_ALIGN;
+  }
+  int* st = device_status_ptr();
+  if (!st) return PA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t block_bytes = (int64_t)num_kv_heads * block_size * row_bytes;
+  // The cache side, launched after the prefix check: copy-on-write copies,
+  // slots, cache write. Chained (programmatic dependents) when it runs
+  // beside the check; none of them writes what the check reads.
+  auto cache_side = [&](bool chained) -> int {
+    int rc = PA_OK;
+    if (num_cow_pairs > 0)
+      rc = launch_copy_blocks(k_cache, v_cache, src.data(), dst.data(), num_cow_pairs, block_bytes, s, chained);
+    if (rc == PA_OK && num_new_tokens > 0)
+      rc = launch_slot_mapping(block_tables, max_blocks_per_seq, num_seqs, new_seq_ids, new_positions,
+                               num_new_tokens, block_size, num_blocks, slot_mapping, st, s, chained);
+    if (rc == PA_OK && num_new_tokens > 0)
+      rc = launch_reshape_and_cache(k_new, v_new, slot_mapping, num_new_tokens, k_cache, v_cache, num_blocks,
+                                    block_size, num_kv_heads, (int32_t)row_bytes, st, s, chained);
+    return rc;
+  };
+  return shared_prefix_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                              group_starts, prefix_lens, num_groups, num_q_heads, num_kv_heads, head_dim, block_size,
+                              num_blocks, scale, out, partition_size, workspace, workspace_bytes, dtype, stream,
+                              cache_side);
 }
 
 size_t pa_chunked_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,

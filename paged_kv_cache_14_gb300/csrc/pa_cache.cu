@@ -1,6 +1,13 @@
 // Cache-side kernels: slot derivation, the paged KV write (reshape_and_cache)
 // and whole-block copy-on-write copies. All three are bandwidth-trivial,
 // bit-exact moves of 16-byte vectors.
+//
+// In a chained step (launched as programmatic dependents, see
+// launch_dependent) slot derivation and block copies read nothing their
+// predecessor writes: they let their successor start at once and wait for
+// the predecessor only before exiting, so each one's completion still
+// implies every earlier kernel's. The cache write reads the slots, so it
+// waits first. Launched the ordinary way these calls are no-ops.
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -18,6 +25,7 @@ __global__ void slot_mapping_kernel(const int32_t* __restrict__ block_tables, in
                                     int32_t num_seqs, const int32_t* __restrict__ seq_ids,
                                     const int32_t* __restrict__ positions, int64_t num_tokens, int32_t block_size,
                                     int32_t num_blocks, int64_t* __restrict__ slot_mapping, int* status) {
+  pdl_trigger();
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < num_tokens;
        t += (int64_t)gridDim.x * blockDim.x) {
     const int32_t s = seq_ids[t];
@@ -30,6 +38,7 @@ __global__ void slot_mapping_kernel(const int32_t* __restrict__ block_tables, in
     if (slot < 0) record_error(status, PA_ERR_BLOCK_OOB);
     slot_mapping[t] = slot;
   }
+  pdl_wait();
 }
 
 // One warp per (token, KV head) row of row_bytes bytes; lanes move 16-byte
@@ -39,6 +48,8 @@ __global__ void reshape_and_cache_kernel(const uint8_t* __restrict__ k, const ui
                                          uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
                                          int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
                                          int32_t row_bytes, int* status) {
+  pdl_wait();  // the slots (and, in a chained step, every earlier kernel)
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t total_rows = num_tokens * num_kv_heads;
@@ -243,6 +254,7 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint8_t* __restrict__ 
                                                           uint8_t* __restrict__ v_cache,
                                                           const __grid_constant__ CopyPairs pairs,
                                                           int64_t block_bytes) {
+  pdl_trigger();
   uint8_t* pool = blockIdx.y == 0 ? k_cache : v_cache;
   const int4* src = reinterpret_cast<const int4*>(pool + (int64_t)pairs.src[blockIdx.x] * block_bytes);
   int4* dst = reinterpret_cast<int4*>(pool + (int64_t)pairs.dst[blockIdx.x] * block_bytes);
@@ -257,6 +269,7 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint8_t* __restrict__ 
     dst[i + 768] = d;
   }
   for (; i < n; i += 256) dst[i] = src[i];
+  pdl_wait();
 }
 
 // Swap preemption ("Inside vLLM...", section "Preemption Mechanics: Swapping
@@ -301,26 +314,42 @@ static int grid_for(int64_t work, int per_block) {
 
 int launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t num_seqs,
                         const int32_t* seq_ids, const int32_t* positions, int64_t num_tokens, int32_t block_size,
-                        int32_t num_blocks, int64_t* slot_mapping, int* status, cudaStream_t stream) {
-  slot_mapping_kernel<<<grid_for(num_tokens, 256), 256, 0, stream>>>(
-      block_tables, max_blocks_per_seq, num_seqs, seq_ids, positions, num_tokens, block_size, num_blocks,
-      slot_mapping, status);
+                        int32_t num_blocks, int64_t* slot_mapping, int* status, cudaStream_t stream,
+                        bool chained) {
+  const dim3 grid(grid_for(num_tokens, 256));
+  if (chained)
+    return launch_dependent(slot_mapping_kernel, grid, dim3(256), 0, stream, block_tables, max_blocks_per_seq,
+                            num_seqs, seq_ids, positions, num_tokens, block_size, num_blocks, slot_mapping,
+                            status) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+  slot_mapping_kernel<<<grid, 256, 0, stream>>>(block_tables, max_blocks_per_seq, num_seqs, seq_ids, positions,
+                                                num_tokens, block_size, num_blocks, slot_mapping, status);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 int launch_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
                              void* k_cache, void* v_cache, int32_t num_blocks, int32_t block_size,
-                             int32_t num_kv_heads, int32_t row_bytes, int* status, cudaStream_t stream) {
+                             int32_t num_kv_heads, int32_t row_bytes, int* status, cudaStream_t stream,
+                             bool chained) {
   const int64_t rows = num_tokens * num_kv_heads;
-  reshape_and_cache_kernel<<<grid_for(rows, 8), 256, 0, stream>>>(
-      static_cast<const uint8_t*>(k), static_cast<const uint8_t*>(v), slot_mapping, num_tokens,
-      static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), num_blocks, block_size, num_kv_heads,
-      row_bytes, status);
+  const dim3 grid(grid_for(rows, 8));
+  const uint8_t* kp = static_cast<const uint8_t*>(k);
+  const uint8_t* vp = static_cast<const uint8_t*>(v);
+  uint8_t* kc = static_cast<uint8_t*>(k_cache);
+  uint8_t* vc = static_cast<uint8_t*>(v_cache);
+  if (chained)
+    return launch_dependent(reshape_and_cache_kernel, grid, dim3(256), 0, stream, kp, vp, slot_mapping, num_tokens,
+                            kc, vc, num_blocks, block_size, num_kv_heads, row_bytes, status) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+  reshape_and_cache_kernel<<<grid, 256, 0, stream>>>(kp, vp, slot_mapping, num_tokens, kc, vc, num_blocks,
+                                                     block_size, num_kv_heads, row_bytes, status);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int32_t num_pairs,
-                       int64_t block_bytes, cudaStream_t stream) {
+                       int64_t block_bytes, cudaStream_t stream, bool chained) {
   for (int32_t base = 0; base < num_pairs; base += kCopyPairsPerLaunch) {
     const int32_t n = num_pairs - base < kCopyPairsPerLaunch ? num_pairs - base : kCopyPairsPerLaunch;
     CopyPairs pairs;
@@ -328,8 +357,15 @@ int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const i
       pairs.src[i] = src[base + i];
       pairs.dst[i] = dst[base + i];
     }
-    copy_blocks_kernel<<<dim3(n, 2), 256, 0, stream>>>(static_cast<uint8_t*>(k_cache),
-                                                       static_cast<uint8_t*>(v_cache), pairs, block_bytes);
+    uint8_t* kc = static_cast<uint8_t*>(k_cache);
+    uint8_t* vc = static_cast<uint8_t*>(v_cache);
+    if (chained) {
+      if (launch_dependent(copy_blocks_kernel, dim3(n, 2), dim3(256), 0, stream, kc, vc, pairs, block_bytes) !=
+          cudaSuccess)
+        return PA_ERR_CUDA;
+      continue;
+    }
+    copy_blocks_kernel<<<dim3(n, 2), 256, 0, stream>>>(kc, vc, pairs, block_bytes);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;

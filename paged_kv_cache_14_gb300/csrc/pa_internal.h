@@ -157,12 +157,16 @@ int make_2d_tensor_map(CUtensorMap* map, const void* base, int64_t rows, int32_t
 
 int launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t num_seqs,
                         const int32_t* seq_ids, const int32_t* positions, int64_t num_tokens, int32_t block_size,
-                        int32_t num_blocks, int64_t* slot_mapping, int* status, cudaStream_t stream);
+                        int32_t num_blocks, int64_t* slot_mapping, int* status, cudaStream_t stream,
+                        bool chained = false);
 int launch_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
                              void* k_cache, void* v_cache, int32_t num_blocks, int32_t block_size,
-                             int32_t num_kv_heads, int32_t row_bytes, int* status, cudaStream_t stream);
+                             int32_t num_kv_heads, int32_t row_bytes, int* status, cudaStream_t stream,
+                             bool chained = false);
+// chained = true: launched as programmatic dependents of the previous kernel
+// (a step whose kernels are all this library's, see launch_dependent).
 int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst, int32_t num_pairs,
-                       int64_t block_bytes, cudaStream_t stream);
+                       int64_t block_bytes, cudaStream_t stream, bool chained = false);
 // e4m3 cache write: per (run of consecutive tokens in one block, KV head,
 // pool) one warp computes the block's new scale and encodes the rows.
 int launch_reshape_and_cache_fp8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,

@@ -108,6 +108,16 @@ class PagedStep:
         return n
 
     def run(self, stream=None) -> torch.Tensor:
+        if self.shared_prefix and self.kv_scales is None:
+            # One call: the shared-prefix check runs beside the copies,
+            # slots and cache write (same results as prepare() + attend()).
+            pa.pa_decode_step_shared_prefix(self.cow_pairs, self.new_seq_ids, self.new_positions, self.k_new,
+                                            self.v_new, self.slot_mapping, self.q, self.k_cache, self.v_cache,
+                                            self.block_tables, self.kv_lens, self.max_seq_len, self.group_starts,
+                                            self.prefix_lens, self.scale, out=self.out,
+                                            partition_size=self.partition_size, workspace=self.workspace,
+                                            stream=stream)
+            return self.out
         self.prepare(stream)
         self.attend(stream)
         return self.out

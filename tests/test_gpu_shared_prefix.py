@@ -143,3 +143,51 @@ def test_shared_prefix_many_groups_mixed_q_tiles(lib):
     out = to_f64(_shared(lib, st, b, group_starts=gs, prefix_lens=pl))
     assert lib.pa_get_status() == 0
     assert_attention_close(out, plain, "bf16", "mixed group sizes: shared-prefix vs pa_decode")
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[3]], ids=["grp4", "grp37"])
+def test_step_in_one_call_matches_separate_calls(lib, case):
+    # pa_decode_step_shared_prefix runs the prefix check beside the
+    # copy-on-write copies, slots and cache write; the result must be the
+    # four separate calls' to the bit: output, both pools and the slots.
+    from paged_kv_cache_14_gb300.step import step_from_host
+    dtype, B, hq, hkv, lens, grp, pref = case
+    b = build_batch(name="cascade_step", seed=606, dtype=dtype, block_size=B, num_q_heads=hq, num_kv_heads=hkv,
+                    head_dim=128, q_lens=np.ones(len(lens), np.int32), kv_lens=lens, share_group=grp,
+                    share_prefix_tokens=pref, cow_per_seq=True)
+    assert len(b.cow_pairs) > 0
+    sep = step_from_host(b, shared_prefix=True)
+    sep.prepare()
+    sep.attend()
+    one = step_from_host(b, shared_prefix=True)
+    one.run()
+    torch.cuda.synchronize()
+    assert lib.pa_get_status() == 0
+    assert torch.equal(one.slot_mapping, sep.slot_mapping)
+    assert torch.equal(one.k_cache, sep.k_cache) and torch.equal(one.v_cache, sep.v_cache)
+    assert torch.equal(one.out, sep.out)
+    kc, vc, _ = oracle_caches_after_step(b)
+    assert_attention_close(to_f64(one.out), oracle_decode(b, kc, vc), dtype, "one-call step vs oracle")
+
+
+def test_step_in_one_call_rejects_before_launching(lib):
+    # A bad copy-on-write pair is caught on the host: nothing is launched,
+    # so the pools and the output are untouched.
+    from paged_kv_cache_14_gb300.step import step_from_host
+    dtype, B, hq, hkv, lens, grp, pref = CASES[0]
+    b = build_batch(name="cascade_step_bad", seed=607, dtype=dtype, block_size=B, num_q_heads=hq,
+                    num_kv_heads=hkv, head_dim=128, q_lens=np.ones(len(lens), np.int32), kv_lens=lens,
+                    share_group=grp, share_prefix_tokens=pref, cow_per_seq=True)
+    st = step_from_host(b, shared_prefix=True)
+    k0, v0 = st.k_cache.clone(), st.v_cache.clone()
+    st.out.fill_(7)
+    bad = np.asarray(st.cow_pairs).copy()
+    bad[0, 1] = st.k_cache.shape[0]  # destination out of range
+    with pytest.raises(lib.PagedAttnError):
+        lib.pa_decode_step_shared_prefix(bad, st.new_seq_ids, st.new_positions, st.k_new, st.v_new,
+                                         st.slot_mapping, st.q, st.k_cache, st.v_cache, st.block_tables,
+                                         st.kv_lens, st.max_seq_len, st.group_starts, st.prefix_lens, b.scale,
+                                         out=st.out, workspace=st.workspace)
+    torch.cuda.synchronize()
+    assert torch.equal(st.k_cache, k0) and torch.equal(st.v_cache, v0)
+    assert bool((st.out == 7).all())
