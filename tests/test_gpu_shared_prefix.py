@@ -191,3 +191,24 @@ def test_step_in_one_call_rejects_before_launching(lib):
     torch.cuda.synchronize()
     assert torch.equal(st.k_cache, k0) and torch.equal(st.v_cache, v0)
     assert bool((st.out == 7).all())
+
+
+def test_shared_prefix_long_prefix_mismatch_past_64_blocks(lib):
+    # Hints of 96 shared blocks: the table check compares 64 entries per pass,
+    # so a member whose block 80 differs from the reference's must still be
+    # caught (its hint dropped). Compared against plain decode on the same
+    # tables.
+    lens = [1700, 1800, 1650, 2000, 1900, 1750]
+    b = build_batch(name="cascade_long", seed=808, dtype="bf16", block_size=16, num_q_heads=64, num_kv_heads=8,
+                    head_dim=128, q_lens=np.ones(len(lens), np.int32), kv_lens=lens, share_group=3,
+                    share_prefix_tokens=1536, cow_per_seq=False)
+    st = _device_step(lib, b)
+    bt = st.block_tables.clone()
+    bt[1, 80] = bt[1, 100]  # member 1 of group 0 now reads a private block at position 80
+    bt[4, 95] = bt[4, 99]   # member 1 of group 1: the last shared entry
+    st.block_tables.copy_(bt)
+    plain = to_f64(lib.pa_decode(st.q, st.k_cache, st.v_cache, st.block_tables, st.kv_lens, st.max_seq_len,
+                                 b.scale))
+    out = to_f64(_shared(lib, st, b))
+    assert lib.pa_get_status() == 0
+    assert_attention_close(out, plain, "bf16", "mismatch past the first 64 shared blocks")
