@@ -511,6 +511,8 @@ def native_arm(args) -> None:
                 "step": ("copy_blocks_fp8 + slot_mapping + reshape_and_cache_fp8 + pa_decode_fp8" if fp8 else
                          "pa_decode_step_shared_prefix (copy_blocks + slot_mapping + reshape_and_cache + "
                          "pa_decode_shared_prefix in one call)" if st.shared_prefix else
+                         "pa_decode_step (copy_blocks + slot_mapping + reshape_and_cache + pa_decode in one call)"
+                         if st.is_decode and st.q.dtype != torch.float32 else
                          "copy_blocks + slot_mapping + reshape_and_cache + " + (
                              "pa_decode" if st.is_decode else "pa_chunked_prefill")),
                 "step_bytes": step_bytes, "decode_bytes": dec_bytes,

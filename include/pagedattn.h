@@ -264,6 +264,25 @@ int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_ca
                             void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream);
 
 /*
+ * pa_decode_step — one decode step in a single call: the same work and
+ * results as pa_copy_blocks, pa_slot_mapping, pa_reshape_and_cache and
+ * pa_decode, in that order. The decode plan (it reads only block_tables
+ * and seq_lens, which the other three do not write) is launched first and
+ * the copies, slots and cache write run beside it; the decode kernel starts
+ * once the cache write has completed. Arguments as pa_decode_step_shared_prefix
+ * without the sharing groups; the workspace is pa_decode_workspace_size()
+ * bytes. fp16/bf16 only (PA_ERR_DTYPE otherwise). Every host check runs
+ * before the first launch.
+ */
+int pa_decode_step(const int64_t* cow_pairs, int32_t num_cow_pairs, const int32_t* new_seq_ids,
+                   const int32_t* new_positions, const void* k_new, const void* v_new, int64_t num_new_tokens,
+                   int64_t* slot_mapping, const void* q, void* k_cache, void* v_cache, const int32_t* block_tables,
+                   int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                   int32_t num_blocks, float scale, void* out, int32_t partition_size, void* workspace,
+                   size_t workspace_bytes, pa_dtype dtype, void* stream);
+
+/*
  * pa_decode_step_shared_prefix — one decode step of a prefix-sharing batch
  * in a single call: the same work and results as, in this order,
  *   pa_copy_blocks(k_cache, v_cache, cow_pairs, num_cow_pairs, ...),

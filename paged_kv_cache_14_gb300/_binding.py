@@ -28,7 +28,7 @@ EXPORTS = (
     "pa_chunked_prefill_workspace_size", "pa_chunked_prefill", "pa_decode_shared_prefix_workspace_size",
     "pa_decode_shared_prefix", "pa_decode_noalloc_scratch_limit", "pa_decode_noalloc",
     "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8", "pa_decode_fp8", "pa_swap_blocks",
-    "pa_decode_step_shared_prefix",
+    "pa_decode_step_shared_prefix", "pa_decode_step",
 )
 
 _i32, _i64, _f32, _vp, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
@@ -76,6 +76,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                                     ctypes.c_int, _vp]),
         "pa_copy_blocks_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp]),
         "pa_swap_blocks": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp]),
+        "pa_decode_step": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _i32, _vp,
+                                          _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _i32, _vp, _sz,
+                                          ctypes.c_int, _vp]),
         "pa_decode_step_shared_prefix": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp,
                                                         _vp, _i32, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _i32,
                                                         _i32, _i32, _i32, _f32, _vp, _i32, _vp, _sz, ctypes.c_int,
@@ -268,6 +271,37 @@ def pa_decode_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
         hq, hkv, D, B, P, float(scale), _cuda(out, "out", dt), int(partition_size), ws_ptr, ws_bytes, _DT[dt],
         _stream(stream))
     _check(rc, "pa_decode_shared_prefix")
+    return out
+
+
+def pa_decode_step(cow_pairs, new_seq_ids: torch.Tensor, new_positions: torch.Tensor, k_new: torch.Tensor,
+                   v_new: torch.Tensor, slot_mapping: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                   v_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                   scale: float, out: torch.Tensor | None = None, partition_size: int = 0,
+                   workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One decode step in one call: pa_copy_blocks(cow_pairs), pa_slot_mapping,
+    pa_reshape_and_cache, pa_decode. cow_pairs: HOST int64 [n, 2]."""
+    pairs = np.ascontiguousarray(np.asarray(cow_pairs, dtype=np.int64).reshape(-1, 2))
+    N, hq, D = q.shape
+    P, hkv, B, _ = k_cache.shape
+    dt = q.dtype
+    T = new_seq_ids.shape[0]
+    if out is None:
+        out = torch.empty_like(q)
+    need = pa_decode_workspace_size(N, hq, hkv, D, B, max_seq_len, partition_size)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load().pa_decode_step(
+        pairs.ctypes.data_as(ctypes.c_void_p) if pairs.shape[0] else None, pairs.shape[0],
+        _cuda(new_seq_ids, "new_seq_ids", torch.int32), _cuda(new_positions, "new_positions", torch.int32),
+        _cuda(k_new, "k_new", dt), _cuda(v_new, "v_new", dt), T, _cuda(slot_mapping, "slot_mapping", torch.int64),
+        _cuda(q, "q", dt), _cuda(k_cache, "k_cache", dt), _cuda(v_cache, "v_cache", dt),
+        _cuda(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _cuda(seq_lens, "seq_lens", torch.int32), N, int(max_seq_len), hq, hkv, D, B, P, float(scale),
+        _cuda(out, "out", dt), int(partition_size), ws_ptr, ws_bytes, _DT[dt], _stream(stream))
+    _check(rc, "pa_decode_step")
     return out
 
 

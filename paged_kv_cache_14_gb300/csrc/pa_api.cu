@@ -239,6 +239,73 @@ static int check_copy_pairs(const int64_t* src_dst_pairs, int32_t num_pairs, int
     if (dsts.count(src[i])) return PA_ERR_ALIAS;
   return PA_OK;
 }
+
+// The cache side of a one-call decode step: copy-on-write copies, slots and
+// the cache write of the step's new tokens. check() makes every host check
+// of pa_copy_blocks, pa_slot_mapping and pa_reshape_and_cache before
+// anything is launched; launch() issues the kernels, as programmatic
+// dependents of the previous kernel when chained.
+struct StepCacheSide {
+  const int64_t* cow_pairs;
+  int32_t num_cow_pairs;
+  const int32_t* new_seq_ids;
+  const int32_t* new_positions;
+  const void* k_new;
+  const void* v_new;
+  int64_t num_new_tokens;
+  int64_t* slot_mapping;
+  void* k_cache;
+  void* v_cache;
+  const int32_t* block_tables;
+  int32_t max_blocks_per_seq;
+  int32_t num_seqs;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t block_size;
+  int32_t num_blocks;
+  pa_dtype dtype;
+  std::vector<int32_t> src, dst;
+  int64_t row_bytes = 0;
+  int* status = nullptr;
+
+  int check() {
+    if (num_cow_pairs < 0 || num_new_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 1 ||
+        max_blocks_per_seq < 1 || num_seqs < 0)
+      return PA_ERR_ARG;
+    if (block_size != 16 && block_size != 32) return PA_ERR_BLOCKSIZE;
+    const int eb = elem_bytes(dtype);
+    if (!eb || dtype == PA_F32) return PA_ERR_DTYPE;
+    row_bytes = (int64_t)head_dim * eb;
+    if (row_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (!k_cache || !v_cache) return PA_ERR_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+    if (num_cow_pairs > 0) {
+      if (!cow_pairs) return PA_ERR_ARG;
+      const int rc = check_copy_pairs(cow_pairs, num_cow_pairs, num_blocks, src, dst);
+      if (rc != PA_OK) return rc;
+    }
+    if (num_new_tokens > 0) {
+      if (!new_seq_ids || !new_positions || !k_new || !v_new || !slot_mapping || !block_tables) return PA_ERR_ARG;
+      if (!aligned16(k_new) || !aligned16(v_new)) return PA_ERR_ALIGN;
+    }
+    status = device_status_ptr();
+    return status ? PA_OK : PA_ERR_CUDA;
+  }
+
+  int launch(cudaStream_t s, bool chained) {
+    int rc = PA_OK;
+    if (num_cow_pairs > 0)
+      rc = launch_copy_blocks(k_cache, v_cache, src.data(), dst.data(), num_cow_pairs,
+                              (int64_t)num_kv_heads * block_size * row_bytes, s, chained);
+    if (rc == PA_OK && num_new_tokens > 0)
+      rc = launch_slot_mapping(block_tables, max_blocks_per_seq, num_seqs, new_seq_ids, new_positions,
+                               num_new_tokens, block_size, num_blocks, slot_mapping, status, s, chained);
+    if (rc == PA_OK && num_new_tokens > 0)
+      rc = launch_reshape_and_cache(k_new, v_new, slot_mapping, num_new_tokens, k_cache, v_cache, num_blocks,
+                                    block_size, num_kv_heads, (int32_t)row_bytes, status, s, chained);
+    return rc;
+  }
+};
 }  // namespace pa
 
 extern "C" {
@@ -594,49 +661,51 @@ int pa_decode_step_shared_prefix(const int64_t* cow_pairs, int32_t num_cow_pairs
   // Host checks of the cache side, as the separate calls make them; the
   // decode's own checks run inside shared_prefix_decode before any launch,
   // so a rejected call launches nothing.
-  if (num_cow_pairs < 0 || num_new_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 1 ||
-      max_blocks_per_seq < 1 || num_seqs < 0)
-    return PA_ERR_ARG;
-  if (block_size != 16 && block_size != 32) return PA_ERR_BLOCKSIZE;
-  const int eb = elem_bytes(dtype);
-  if (!eb || dtype == PA_F32) return PA_ERR_DTYPE;
-  const int64_t row_bytes = (int64_t)head_dim * eb;
-  if (row_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
-  if (!k_cache || !v_cache) return PA_ERR_ARG;
-  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
-  std::vector<int32_t> src, dst;
-  if (num_cow_pairs > 0) {
-    if (!cow_pairs) return PA_ERR_ARG;
-    const int rc = check_copy_pairs(cow_pairs, num_cow_pairs, num_blocks, src, dst);
-    if (rc != PA_OK) return rc;
-  }
-  if (num_new_tokens > 0) {
-    if (!new_seq_ids || !new_positions || !k_new || !v_new || !slot_mapping || !block_tables) return PA_ERR_ARG;
-    if (!aligned16(k_new) || !aligned16(v_new)) return PA_ERR_ALIGN;
-  }
-  int* st = device_status_ptr();
-  if (!st) return PA_ERR_CUDA;
+  StepCacheSide cs{cow_pairs,    num_cow_pairs, new_seq_ids,        new_positions, k_new,      v_new,
+                   num_new_tokens, slot_mapping, k_cache,           v_cache,       block_tables, max_blocks_per_seq,
+                   num_seqs,     num_kv_heads,  head_dim,           block_size,    num_blocks, dtype};
+  int rc = cs.check();
+  if (rc != PA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int64_t block_bytes = (int64_t)num_kv_heads * block_size * row_bytes;
-  // The cache side, launched after the prefix check: copy-on-write copies,
-  // slots, cache write. Chained (programmatic dependents) when it runs
-  // beside the check; none of them writes what the check reads.
-  auto cache_side = [&](bool chained) -> int {
-    int rc = PA_OK;
-    if (num_cow_pairs > 0)
-      rc = launch_copy_blocks(k_cache, v_cache, src.data(), dst.data(), num_cow_pairs, block_bytes, s, chained);
-    if (rc == PA_OK && num_new_tokens > 0)
-      rc = launch_slot_mapping(block_tables, max_blocks_per_seq, num_seqs, new_seq_ids, new_positions,
-                               num_new_tokens, block_size, num_blocks, slot_mapping, st, s, chained);
-    if (rc == PA_OK && num_new_tokens > 0)
-      rc = launch_reshape_and_cache(k_new, v_new, slot_mapping, num_new_tokens, k_cache, v_cache, num_blocks,
-                                    block_size, num_kv_heads, (int32_t)row_bytes, st, s, chained);
-    return rc;
-  };
+  // The cache side runs after the prefix check is launched, chained
+  // (programmatic dependents) when it runs beside it; none of its kernels
+  // writes what the check reads.
+  auto cache_side = [&](bool chained) -> int { return cs.launch(s, chained); };
   return shared_prefix_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
                               group_starts, prefix_lens, num_groups, num_q_heads, num_kv_heads, head_dim, block_size,
                               num_blocks, scale, out, partition_size, workspace, workspace_bytes, dtype, stream,
                               cache_side);
+}
+
+int pa_decode_step(const int64_t* cow_pairs, int32_t num_cow_pairs, const int32_t* new_seq_ids,
+                   const int32_t* new_positions, const void* k_new, const void* v_new, int64_t num_new_tokens,
+                   int64_t* slot_mapping, const void* q, void* k_cache, void* v_cache, const int32_t* block_tables,
+                   int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                   int32_t num_blocks, float scale, void* out, int32_t partition_size, void* workspace,
+                   size_t workspace_bytes, pa_dtype dtype, void* stream) {
+  StepCacheSide cs{cow_pairs,    num_cow_pairs, new_seq_ids,        new_positions, k_new,      v_new,
+                   num_new_tokens, slot_mapping, k_cache,           v_cache,       block_tables, max_blocks_per_seq,
+                   num_seqs,     num_kv_heads,  head_dim,           block_size,    num_blocks, dtype};
+  int rc = cs.check();
+  if (rc != PA_OK) return rc;
+  DecodeParams p;
+  DecodeWorkspace wl;
+  rc = decode_prepare(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
+                      max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out,
+                      partition_size, 0, workspace, workspace_bytes, dtype, &p, &wl);
+  if (rc != PA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (num_seqs == 0) return cs.launch(s, false);
+  // The plan reads only the tables and lengths, which the cache side does
+  // not write: it goes first and the cache side runs beside it, chained; the
+  // decode kernel waits for the cache write (hence for all of them).
+  rc = launch_decode_plan(p, dtype, s);
+  if (rc != PA_OK) return rc;
+  rc = cs.launch(s, true);
+  if (rc != PA_OK) return rc;
+  p.planned = 1;
+  return launch_decode(p, dtype, s);
 }
 
 size_t pa_chunked_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,

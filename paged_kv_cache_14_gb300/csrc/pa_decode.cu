@@ -1204,4 +1204,16 @@ int launch_decode(const DecodeParams& p0, pa_dtype dt, cudaStream_t stream) {
   return dt == PA_BF16 ? launch_tc_dispatch<__nv_bfloat16>(p, stream) : launch_tc_dispatch<__half>(p, stream);
 }
 
+int launch_decode_plan(const DecodeParams& p0, pa_dtype dt, cudaStream_t stream) {
+  DecodeParams p = p0;
+  decode_set_rows(p, dt);
+  if (dt == PA_BF16)
+    decode_plan_kernel<__nv_bfloat16><<<1, 1024, 0, stream>>>(p);
+  else if (dt == PA_F16)
+    decode_plan_kernel<__half><<<1, 1024, 0, stream>>>(p);
+  else
+    return PA_ERR_DTYPE;
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 }  // namespace pa

@@ -182,6 +182,10 @@ int launch_copy_scales(float* kv_scales, const int32_t* src, const int32_t* dst,
 
 // Decode: split-KV main pass (+ merge pass when max_parts > 1).
 int launch_decode(const DecodeParams& p, pa_dtype dt, cudaStream_t stream);
+// The decode plan alone (fp16/bf16), for a step that launches other kernels
+// between the plan and the decode: launch_decode then runs with
+// planned = 1 and its first kernel waits for the ones before it.
+int launch_decode_plan(const DecodeParams& p, pa_dtype dt, cudaStream_t stream);
 // Prefill chunks (q_len > 1) on the tensor-core path.
 int launch_prefill(const PrefillParams& p, const void* k_cache, const void* v_cache, pa_dtype dt,
                    cudaStream_t stream);

@@ -118,6 +118,13 @@ class PagedStep:
                                             partition_size=self.partition_size, workspace=self.workspace,
                                             stream=stream)
             return self.out
+        if self.is_decode and self.kv_scales is None and self.q.dtype != torch.float32:
+            # One call: the decode plan runs beside the cache side.
+            pa.pa_decode_step(self.cow_pairs, self.new_seq_ids, self.new_positions, self.k_new, self.v_new,
+                              self.slot_mapping, self.q, self.k_cache, self.v_cache, self.block_tables,
+                              self.kv_lens, self.max_seq_len, self.scale, out=self.out,
+                              partition_size=self.partition_size, workspace=self.workspace, stream=stream)
+            return self.out
         self.prepare(stream)
         self.attend(stream)
         return self.out
