@@ -74,3 +74,46 @@ def test_decode_step_8b_config_matches_separate_calls(lib):
     assert lib.pa_get_status() == 0
     assert torch.equal(one.out, sep.out)
     assert torch.equal(one.k_cache, sep.k_cache) and torch.equal(one.v_cache, sep.v_cache)
+
+
+def test_one_call_steps_with_empty_parts(lib):
+    # No copy-on-write pairs and no new tokens: the one-call steps are the
+    # plain attention calls; an empty batch still runs its cache side.
+    from paged_kv_cache_14_gb300.step import step_from_host
+    lens = [5, 64, 300, 700, 1300, 2100, 31, 900]
+    b = build_batch(name="step_empty", seed=720, dtype="bf16", block_size=16, num_q_heads=64, num_kv_heads=8,
+                    head_dim=128, q_lens=np.ones(len(lens), np.int32), kv_lens=lens, share_group=4,
+                    share_prefix_tokens=256, cow_per_seq=False)
+    for shared in (False, True):
+        st = step_from_host(b, shared_prefix=shared)
+        st.prepare()
+        st.attend()
+        ref = st.out.clone()
+        e32 = torch.empty(0, dtype=torch.int32, device="cuda")
+        e64 = torch.empty(0, dtype=torch.int64, device="cuda")
+        ekv = torch.empty((0,) + tuple(st.k_new.shape[1:]), dtype=st.k_new.dtype, device="cuda")
+        st.out.zero_()
+        if shared:
+            lib.pa_decode_step_shared_prefix(np.zeros((0, 2), np.int64), e32, e32, ekv, ekv, e64, st.q, st.k_cache,
+                                             st.v_cache, st.block_tables, st.kv_lens, st.max_seq_len,
+                                             st.group_starts, st.prefix_lens, b.scale, out=st.out,
+                                             workspace=st.workspace)
+        else:
+            lib.pa_decode_step(np.zeros((0, 2), np.int64), e32, e32, ekv, ekv, e64, st.q, st.k_cache, st.v_cache,
+                               st.block_tables, st.kv_lens, st.max_seq_len, b.scale, out=st.out,
+                               workspace=st.workspace)
+        torch.cuda.synchronize()
+        assert lib.pa_get_status() == 0
+        assert torch.equal(st.out, ref)
+    # An empty batch with new tokens: only the cache side runs (slots of
+    # sequences outside the batch are -1, so nothing is written).
+    st = step_from_host(b)
+    k0 = st.k_cache.clone()
+    eq = torch.empty((0,) + tuple(st.q.shape[1:]), dtype=st.q.dtype, device="cuda")
+    lib.pa_decode_step(np.zeros((0, 2), np.int64), st.new_seq_ids, st.new_positions, st.k_new, st.v_new,
+                       st.slot_mapping, eq, st.k_cache, st.v_cache, st.block_tables, st.kv_lens[:0],
+                       st.max_seq_len, b.scale, out=torch.empty_like(eq))
+    torch.cuda.synchronize()
+    assert bool((st.slot_mapping == -1).all())
+    assert torch.equal(st.k_cache, k0)
+    lib.pa_get_status()  # clears the slot errors recorded for tokens outside the batch
