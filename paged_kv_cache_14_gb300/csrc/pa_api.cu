@@ -147,79 +147,6 @@ static int32_t auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t num
   return part;
 }
 
-}  // namespace pa
-
-using namespace pa;
-
-extern "C" {
-
-const char* pa_strerror(int s) {
-  switch (s) {
-    case PA_OK: return "PA_OK";
-    case PA_ERR_ARG: return "PA_ERR_ARG: invalid argument";
-    case PA_ERR_DTYPE: return "PA_ERR_DTYPE: dtype not supported here";
-    case PA_ERR_HEADS: return "PA_ERR_HEADS: num_q_heads is not a multiple of num_kv_heads";
-    case PA_ERR_BLOCKSIZE: return "PA_ERR_BLOCKSIZE: block_size must be 16 or 32";
-    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing or too small";
-    case PA_ERR_ALIAS: return "PA_ERR_ALIAS: copy_blocks destination repeated or also a source";
-    case PA_ERR_BLOCK_OOB: return "PA_ERR_BLOCK_OOB: block id or slot outside the pool";
-    case PA_ERR_SEQLEN: return "PA_ERR_SEQLEN: sequence length out of range";
-    case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA runtime error";
-    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: shape not supported";
-    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: a bounded device wait ran out";
-    case PA_ERR_ALIGN: return "PA_ERR_ALIGN: pointer not 16-byte aligned";
-    case PA_ERR_SCRATCH: return "PA_ERR_SCRATCH: the call needs more than pa_decode_noalloc's fixed scratch";
-  }
-  return "unknown status";
-}
-
-int pa_version(void) { return 100; }
-
-int pa_get_status(void* stream) {
-  int* p = device_status_ptr();
-  if (!p) return PA_ERR_CUDA;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
-  int v = 0;
-  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
-  const int zero = 0;
-  if (v != 0 && cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return PA_ERR_CUDA;
-  return v;
-}
-
-int pa_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t num_seqs,
-                    const int32_t* seq_ids, const int32_t* positions, int64_t num_tokens, int32_t block_size,
-                    int32_t num_blocks, int64_t* slot_mapping, void* stream) {
-  if (num_tokens < 0 || num_seqs < 0 || max_blocks_per_seq < 1 || num_blocks < 1) return PA_ERR_ARG;
-  if (block_size != 16 && block_size != 32) return PA_ERR_BLOCKSIZE;
-  if (num_tokens == 0) return PA_OK;
-  if (!block_tables || !seq_ids || !positions || !slot_mapping) return PA_ERR_ARG;
-  int* st = device_status_ptr();
-  if (!st) return PA_ERR_CUDA;
-  return launch_slot_mapping(block_tables, max_blocks_per_seq, num_seqs, seq_ids, positions, num_tokens, block_size,
-                             num_blocks, slot_mapping, st, static_cast<cudaStream_t>(stream));
-}
-
-int pa_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
-                         void* k_cache, void* v_cache, int32_t num_blocks, int32_t block_size,
-                         int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype, void* stream) {
-  if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 1) return PA_ERR_ARG;
-  if (block_size != 16 && block_size != 32) return PA_ERR_BLOCKSIZE;
-  const int eb = elem_bytes(dtype);
-  if (!eb) return PA_ERR_DTYPE;
-  const int64_t row_bytes = (int64_t)head_dim * eb;
-  if (row_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
-  if (num_tokens == 0) return PA_OK;
-  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_ARG;
-  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
-  int* st = device_status_ptr();
-  if (!st) return PA_ERR_CUDA;
-  return launch_reshape_and_cache(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, block_size,
-                                  num_kv_heads, (int32_t)row_bytes, st, static_cast<cudaStream_t>(stream));
-}
-
-}  // extern "C"
-
-namespace pa {
 // Host check of copy-on-write pairs: every block in range, no destination
 // repeated or also a source. On success src / dst hold the pairs.
 static int check_copy_pairs(const int64_t* src_dst_pairs, int32_t num_pairs, int32_t num_blocks,
@@ -306,45 +233,6 @@ struct StepCacheSide {
     return rc;
   }
 };
-}  // namespace pa
-
-extern "C" {
-
-int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst_pairs, int32_t num_pairs,
-                   int32_t num_blocks, int64_t block_bytes, void* stream) {
-  if (num_pairs < 0 || num_blocks < 1 || block_bytes <= 0) return PA_ERR_ARG;
-  if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
-  if (num_pairs == 0) return PA_OK;
-  if (!k_cache || !v_cache || !src_dst_pairs) return PA_ERR_ARG;
-  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
-  std::vector<int32_t> src, dst;
-  const int rc = check_copy_pairs(src_dst_pairs, num_pairs, num_blocks, src, dst);
-  if (rc != PA_OK) return rc;
-  return launch_copy_blocks(k_cache, v_cache, src.data(), dst.data(), num_pairs, block_bytes,
-                            static_cast<cudaStream_t>(stream));
-}
-
-int32_t pa_decode_partition_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t block_size,
-                                 int32_t max_seq_len, int32_t partition_size) {
-  if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || max_seq_len < 0) return PA_ERR_ARG;
-  if (num_q_heads % num_kv_heads) return PA_ERR_HEADS;
-  if (block_size != 16 && block_size != 32) return PA_ERR_BLOCKSIZE;
-  if (partition_size < 0) return PA_ERR_ARG;
-  if (partition_size > 0) {
-    if (partition_size % block_size || partition_size > kMaxPartition) return PA_ERR_ARG;
-    return partition_size;
-  }
-  return auto_partition(num_seqs, num_q_heads, num_kv_heads, max_seq_len < 1 ? 1 : max_seq_len);
-}
-
-size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                int32_t block_size, int32_t max_seq_len, int32_t partition_size) {
-  const int32_t part =
-      pa_decode_partition_size(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, partition_size);
-  if (part <= 0 || head_dim < 1 || num_seqs < 1) return 0;
-  const int64_t max_parts = ((max_seq_len < 1 ? 1 : max_seq_len) + part - 1) / part;
-  return decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_parts).total;
-}
 
 // Checks and parameter block of a decode launch. extra_slots = 1 reserves a
 // partial slot per (sequence, head) for the prefix pass of shared-prefix
@@ -425,6 +313,190 @@ static int decode_common(const void* q, const void* k_cache, const void* v_cache
                                 partition_size, 0, workspace, workspace_bytes, dtype, &p, &wl);
   if (rc != PA_OK || num_seqs == 0) return rc;
   return launch_decode(p, dtype, stream);
+}
+
+template <typename Between>
+static int shared_prefix_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                            int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                            int32_t max_seq_len, const int32_t* group_starts, const int32_t* prefix_lens,
+                            int32_t num_groups, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t num_blocks, float scale, void* out, int32_t partition_size,
+                            void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream,
+                            Between&& between) {
+  if (num_seqs < 0 || num_groups < 0) return PA_ERR_ARG;
+  if (num_seqs == 0) return between(false);
+  if (num_groups < 1 || num_groups > num_seqs || !group_starts || !prefix_lens) return PA_ERR_ARG;
+  if (dtype == PA_F32) return PA_ERR_DTYPE;
+  if (!(scale > 0.f)) return PA_ERR_ARG;  // the prefix pass needs scale > 0
+  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads) return PA_ERR_HEADS;
+  const int32_t g = num_q_heads / num_kv_heads;
+  if (g > 128 || (g & (g - 1))) return PA_ERR_UNSUPPORTED;
+  const size_t need = pa_decode_shared_prefix_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                            block_size, max_seq_len, partition_size, num_groups);
+  if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+  DecodeParams dp;
+  DecodeWorkspace wl;
+  int rc = decode_prepare(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
+                          max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out,
+                          partition_size, 1, workspace, workspace_bytes, dtype, &dp, &wl);
+  if (rc != PA_OK) return rc;
+  const CascadeWorkspace cw = cascade_workspace_layout(num_seqs, num_groups);
+  uint8_t* cbase = static_cast<uint8_t*>(workspace) + wl.total;
+  int32_t* prefix = reinterpret_cast<int32_t*>(cbase + cw.prefix);
+  int32_t* group_ref = reinterpret_cast<int32_t*>(cbase + cw.group_ref);
+  int32_t* group_of_seq = reinterpret_cast<int32_t*>(cbase + cw.group_of);
+  int32_t* pwork = reinterpret_cast<int32_t*>(cbase + cw.work);
+  int32_t* ppairs = reinterpret_cast<int32_t*>(cbase + cw.pairs);
+  int32_t* pkeys = reinterpret_cast<int32_t*>(cbase + cw.pair_keys);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  dp.prefix = prefix;
+  decode_set_rows(dp, dtype);
+  // 1. Verify the hints, list the prefix pass's work and the suffix decode's.
+  rc = launch_cascade_prep(dp, dtype, group_starts, prefix_lens, num_groups, kPrefillRowsPerItem / g, prefix, group_ref,
+                           group_of_seq, pwork, ppairs, pkeys, s);
+  dp.planned = 1;
+  if (rc != PA_OK) return rc;
+  // Whatever the caller launches here runs beside the check: it must not
+  // write what the check reads (tables, lengths, hints, groups).
+  rc = between(true);
+  if (rc != PA_OK) return rc;
+  // 2. Prefix pass (tcgen05): every group's shared blocks once for all its
+  //    members, partials into slot 0.
+  PrefillParams pp{};
+  pp.q = q;
+  pp.out = out;
+  pp.block_tables = block_tables;
+  pp.max_blocks_per_seq = max_blocks_per_seq;
+  pp.num_seqs = num_seqs;
+  pp.num_q_heads = num_q_heads;
+  pp.num_kv_heads = num_kv_heads;
+  pp.head_dim = head_dim;
+  pp.block_size = block_size;
+  pp.num_blocks = num_blocks;
+  pp.group = g;
+  pp.total_q = num_seqs;
+  pp.scale_log2 = dp.scale_log2;
+  pp.work = pwork;
+  pp.pairs = ppairs;
+  pp.group_starts = group_starts;
+  pp.prefix = prefix;
+  pp.group_ref = group_ref;
+  pp.pair_keys = pkeys;
+  pp.part_o = dp.part_o;
+  pp.part_ml = dp.part_ml;
+  pp.max_parts = dp.max_parts;
+  pp.status = dp.status;
+  rc = launch_prefix_pass(pp, k_cache, v_cache, dtype, s);
+  if (rc != PA_OK) return rc;
+  // 3. Suffix decode (split-KV over the private keys) and the merge.
+  return launch_decode(dp, dtype, s);
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* pa_strerror(int s) {
+  switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_ARG: return "PA_ERR_ARG: invalid argument";
+    case PA_ERR_DTYPE: return "PA_ERR_DTYPE: dtype not supported here";
+    case PA_ERR_HEADS: return "PA_ERR_HEADS: num_q_heads is not a multiple of num_kv_heads";
+    case PA_ERR_BLOCKSIZE: return "PA_ERR_BLOCKSIZE: block_size must be 16 or 32";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing or too small";
+    case PA_ERR_ALIAS: return "PA_ERR_ALIAS: copy_blocks destination repeated or also a source";
+    case PA_ERR_BLOCK_OOB: return "PA_ERR_BLOCK_OOB: block id or slot outside the pool";
+    case PA_ERR_SEQLEN: return "PA_ERR_SEQLEN: sequence length out of range";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA runtime error";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: shape not supported";
+    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: a bounded device wait ran out";
+    case PA_ERR_ALIGN: return "PA_ERR_ALIGN: pointer not 16-byte aligned";
+    case PA_ERR_SCRATCH: return "PA_ERR_SCRATCH: the call needs more than pa_decode_noalloc's fixed scratch";
+  }
+  return "unknown status";
+}
+
+int pa_version(void) { return 100; }
+
+int pa_get_status(void* stream) {
+  int* p = device_status_ptr();
+  if (!p) return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  const int zero = 0;
+  if (v != 0 && cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return PA_ERR_CUDA;
+  return v;
+}
+
+int pa_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t num_seqs,
+                    const int32_t* seq_ids, const int32_t* positions, int64_t num_tokens, int32_t block_size,
+                    int32_t num_blocks, int64_t* slot_mapping, void* stream) {
+  if (num_tokens < 0 || num_seqs < 0 || max_blocks_per_seq < 1 || num_blocks < 1) return PA_ERR_ARG;
+  if (block_size != 16 && block_size != 32) return PA_ERR_BLOCKSIZE;
+  if (num_tokens == 0) return PA_OK;
+  if (!block_tables || !seq_ids || !positions || !slot_mapping) return PA_ERR_ARG;
+  int* st = device_status_ptr();
+  if (!st) return PA_ERR_CUDA;
+  return launch_slot_mapping(block_tables, max_blocks_per_seq, num_seqs, seq_ids, positions, num_tokens, block_size,
+                             num_blocks, slot_mapping, st, static_cast<cudaStream_t>(stream));
+}
+
+int pa_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                         void* k_cache, void* v_cache, int32_t num_blocks, int32_t block_size,
+                         int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype, void* stream) {
+  if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 1) return PA_ERR_ARG;
+  if (block_size != 16 && block_size != 32) return PA_ERR_BLOCKSIZE;
+  const int eb = elem_bytes(dtype);
+  if (!eb) return PA_ERR_DTYPE;
+  const int64_t row_bytes = (int64_t)head_dim * eb;
+  if (row_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+  int* st = device_status_ptr();
+  if (!st) return PA_ERR_CUDA;
+  return launch_reshape_and_cache(k, v, slot_mapping, num_tokens, k_cache, v_cache, num_blocks, block_size,
+                                  num_kv_heads, (int32_t)row_bytes, st, static_cast<cudaStream_t>(stream));
+}
+
+int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst_pairs, int32_t num_pairs,
+                   int32_t num_blocks, int64_t block_bytes, void* stream) {
+  if (num_pairs < 0 || num_blocks < 1 || block_bytes <= 0) return PA_ERR_ARG;
+  if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !src_dst_pairs) return PA_ERR_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_ALIGN;
+  std::vector<int32_t> src, dst;
+  const int rc = check_copy_pairs(src_dst_pairs, num_pairs, num_blocks, src, dst);
+  if (rc != PA_OK) return rc;
+  return launch_copy_blocks(k_cache, v_cache, src.data(), dst.data(), num_pairs, block_bytes,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int32_t pa_decode_partition_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t block_size,
+                                 int32_t max_seq_len, int32_t partition_size) {
+  if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || max_seq_len < 0) return PA_ERR_ARG;
+  if (num_q_heads % num_kv_heads) return PA_ERR_HEADS;
+  if (block_size != 16 && block_size != 32) return PA_ERR_BLOCKSIZE;
+  if (partition_size < 0) return PA_ERR_ARG;
+  if (partition_size > 0) {
+    if (partition_size % block_size || partition_size > kMaxPartition) return PA_ERR_ARG;
+    return partition_size;
+  }
+  return auto_partition(num_seqs, num_q_heads, num_kv_heads, max_seq_len < 1 ? 1 : max_seq_len);
+}
+
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                int32_t block_size, int32_t max_seq_len, int32_t partition_size) {
+  const int32_t part =
+      pa_decode_partition_size(num_seqs, num_q_heads, num_kv_heads, block_size, max_seq_len, partition_size);
+  if (part <= 0 || head_dim < 1 || num_seqs < 1) return 0;
+  const int64_t max_parts = ((max_seq_len < 1 ? 1 : max_seq_len) + part - 1) / part;
+  return decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_parts).total;
 }
 
 int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -551,91 +623,6 @@ size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_he
   return decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_parts).total +
          cascade_workspace_layout(num_seqs, num_groups).total;
 }
-
-}  // extern "C"
-
-namespace pa {
-template <typename Between>
-static int shared_prefix_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
-                            int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
-                            int32_t max_seq_len, const int32_t* group_starts, const int32_t* prefix_lens,
-                            int32_t num_groups, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                            int32_t block_size, int32_t num_blocks, float scale, void* out, int32_t partition_size,
-                            void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream,
-                            Between&& between) {
-  if (num_seqs < 0 || num_groups < 0) return PA_ERR_ARG;
-  if (num_seqs == 0) return between(false);
-  if (num_groups < 1 || num_groups > num_seqs || !group_starts || !prefix_lens) return PA_ERR_ARG;
-  if (dtype == PA_F32) return PA_ERR_DTYPE;
-  if (!(scale > 0.f)) return PA_ERR_ARG;  // the prefix pass needs scale > 0
-  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
-  if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads) return PA_ERR_HEADS;
-  const int32_t g = num_q_heads / num_kv_heads;
-  if (g > 128 || (g & (g - 1))) return PA_ERR_UNSUPPORTED;
-  const size_t need = pa_decode_shared_prefix_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                                            block_size, max_seq_len, partition_size, num_groups);
-  if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
-  DecodeParams dp;
-  DecodeWorkspace wl;
-  int rc = decode_prepare(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, nullptr, num_seqs,
-                          max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out,
-                          partition_size, 1, workspace, workspace_bytes, dtype, &dp, &wl);
-  if (rc != PA_OK) return rc;
-  const CascadeWorkspace cw = cascade_workspace_layout(num_seqs, num_groups);
-  uint8_t* cbase = static_cast<uint8_t*>(workspace) + wl.total;
-  int32_t* prefix = reinterpret_cast<int32_t*>(cbase + cw.prefix);
-  int32_t* group_ref = reinterpret_cast<int32_t*>(cbase + cw.group_ref);
-  int32_t* group_of_seq = reinterpret_cast<int32_t*>(cbase + cw.group_of);
-  int32_t* pwork = reinterpret_cast<int32_t*>(cbase + cw.work);
-  int32_t* ppairs = reinterpret_cast<int32_t*>(cbase + cw.pairs);
-  int32_t* pkeys = reinterpret_cast<int32_t*>(cbase + cw.pair_keys);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  dp.prefix = prefix;
-  decode_set_rows(dp, dtype);
-  // 1. Verify the hints, list the prefix pass's work and the suffix decode's.
-  rc = launch_cascade_prep(dp, dtype, group_starts, prefix_lens, num_groups, kPrefillRowsPerItem / g, prefix, group_ref,
-                           group_of_seq, pwork, ppairs, pkeys, s);
-  dp.planned = 1;
-  if (rc != PA_OK) return rc;
-  // Whatever the caller launches here runs beside the check: it must not
-  // write what the check reads (tables, lengths, hints, groups).
-  rc = between(true);
-  if (rc != PA_OK) return rc;
-  // 2. Prefix pass (tcgen05): every group's shared blocks once for all its
-  //    members, partials into slot 0.
-  PrefillParams pp{};
-  pp.q = q;
-  pp.out = out;
-  pp.block_tables = block_tables;
-  pp.max_blocks_per_seq = max_blocks_per_seq;
-  pp.num_seqs = num_seqs;
-  pp.num_q_heads = num_q_heads;
-  pp.num_kv_heads = num_kv_heads;
-  pp.head_dim = head_dim;
-  pp.block_size = block_size;
-  pp.num_blocks = num_blocks;
-  pp.group = g;
-  pp.total_q = num_seqs;
-  pp.scale_log2 = dp.scale_log2;
-  pp.work = pwork;
-  pp.pairs = ppairs;
-  pp.group_starts = group_starts;
-  pp.prefix = prefix;
-  pp.group_ref = group_ref;
-  pp.pair_keys = pkeys;
-  pp.part_o = dp.part_o;
-  pp.part_ml = dp.part_ml;
-  pp.max_parts = dp.max_parts;
-  pp.status = dp.status;
-  rc = launch_prefix_pass(pp, k_cache, v_cache, dtype, s);
-  if (rc != PA_OK) return rc;
-  // 3. Suffix decode (split-KV over the private keys) and the merge.
-  return launch_decode(dp, dtype, s);
-}
-
-}  // namespace pa
-
-extern "C" {
 
 int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
                             int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
