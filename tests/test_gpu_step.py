@@ -117,3 +117,26 @@ def test_one_call_steps_with_empty_parts(lib):
     assert bool((st.slot_mapping == -1).all())
     assert torch.equal(st.k_cache, k0)
     lib.pa_get_status()  # clears the slot errors recorded for tokens outside the batch
+
+
+@pytest.mark.parametrize("shared", [False, True], ids=["plain", "shared_prefix"])
+def test_one_call_step_with_more_than_1024_cow_pairs(lib, shared):
+    # 1100 copy-on-write pairs take two chained copy launches (1024 pairs
+    # per launch); the cache write must still see both complete.
+    from paged_kv_cache_14_gb300.step import step_from_host
+    rng = np.random.default_rng(730)
+    n = 1100
+    lens = rng.integers(20, 60, size=n).astype(np.int32)
+    b = build_batch(name="step_cow_many", seed=730, dtype="bf16", block_size=16, num_q_heads=16, num_kv_heads=2,
+                    head_dim=128, q_lens=np.ones(n, np.int32), kv_lens=lens, share_group=2,
+                    share_prefix_tokens=16, cow_per_seq=True)
+    assert len(b.cow_pairs) > 1024
+    sep = step_from_host(b, shared_prefix=shared)
+    sep.prepare()
+    sep.attend()
+    one = step_from_host(b, shared_prefix=shared)
+    one.run()
+    torch.cuda.synchronize()
+    assert lib.pa_get_status() == 0
+    assert torch.equal(one.k_cache, sep.k_cache) and torch.equal(one.v_cache, sep.v_cache)
+    assert torch.equal(one.out, sep.out)
