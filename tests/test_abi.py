@@ -188,3 +188,33 @@ def test_swap_host_checks(lib):
     assert call([(1, 2), (2, 3)], dk=0x1000, dv=0x2000, nd=10) == -6   # same pool: dst 2 is a src
     assert call([(1, 2)], sv=None) == -1         # one V pool without the other
     assert call([]) == 0
+
+
+@pytest.mark.parametrize("entry", ["pa_decode_step", "pa_decode_step_shared_prefix"])
+def test_one_call_step_host_checks(lib, entry):
+    # The cache side's checks run before anything touches the GPU.
+    fn = getattr(lib, entry)
+
+    def call(pairs=((3, 4),), **o):
+        arr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+        a = dict(n_pairs=arr.shape[0], ids=0x1000, pos=0x2000, kn=0x3000, vn=0x4000, T=4, slots=0x5000,
+                 q=0x6000, kc=0x10000, vc=0x20000, bt=0x7000, mb=8, lens=0x8000, N=2, maxlen=100, hq=8, hkv=2,
+                 D=128, B=16, P=10, dtype=2)
+        a.update(o)
+        head = [arr.ctypes.data_as(ctypes.c_void_p) if arr.shape[0] else None, a["n_pairs"], a["ids"], a["pos"],
+                a["kn"], a["vn"], a["T"], a["slots"], a["q"], a["kc"], a["vc"], a["bt"], a["mb"], a["lens"], a["N"],
+                a["maxlen"]]
+        if entry == "pa_decode_step_shared_prefix":
+            head += [0x9000, 0xA000, 1]  # group_starts, prefix_lens, num_groups
+        tail = [a["hq"], a["hkv"], a["D"], a["B"], a["P"], 0.1, 0xB000, 0, 0xC000, 1 << 20, a["dtype"], None]
+        return fn(*head, *tail)
+    assert call(B=8) == -4                         # block size
+    assert call(dtype=0) == -2                     # fp32: not a one-call step
+    assert call(kc=0) == -1                        # missing pool
+    assert call(kc=0x10008) == -12                 # pool not 16-byte aligned
+    assert call(pairs=[(3, 10)]) == -7             # destination outside the pool
+    assert call(pairs=[(3, 4), (5, 4)]) == -6      # destination repeated
+    assert call(pairs=[(3, 4), (4, 5)]) == -6      # destination also a source
+    assert call(ids=0) == -1                       # new tokens without their ids
+    assert call(kn=0x3004) == -12                  # new K not 16-byte aligned
+    assert call(T=-1) == -1                        # negative token count
