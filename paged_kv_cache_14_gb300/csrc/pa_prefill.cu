@@ -91,7 +91,7 @@ __host__ __device__ constexpr int col_o(int t) { return t * 256 + kN; }
 static_assert(kRows == kPrefillRowsPerItem, "work list granularity shared with the shared-prefix preparation");
 }  // namespace pf
 
-// Plan: list (sequence, row tile) pairs of every chunk with q_len > 1,
+// Plan: list (sequence, 256-row item) pairs of every chunk with q_len > 1,
 // ordered by decreasing number of KV tiles (longest items first), and reset
 // the item counter. One CTA of 1024 threads.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams p) {
