@@ -445,6 +445,15 @@ int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const
                   int32_t block_size, int32_t num_blocks, float scale, void* out, int32_t partition_size,
                   void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream);
 
+/*
+ * pa_selftest_bounded_wait — exercises the failure path every kernel relies
+ * on: one warp waits on an mbarrier that nothing completes; the wait gives up
+ * after limit_ns nanoseconds of device time (1 us .. 1 s, else PA_ERR_ARG),
+ * records PA_ERR_TIMEOUT in the status word read by pa_get_status, and the
+ * kernel returns, leaving the context usable. Nothing faults or traps.
+ */
+int pa_selftest_bounded_wait(int64_t limit_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     pa_decode_partition_size,
     pa_decode_shared_prefix,
     pa_decode_step,
+    pa_selftest_bounded_wait,
     pa_decode_step_shared_prefix,
     pa_decode_shared_prefix_workspace_size,
     pa_decode_workspace_size,

@@ -28,7 +28,7 @@ EXPORTS = (
     "pa_chunked_prefill_workspace_size", "pa_chunked_prefill", "pa_decode_shared_prefix_workspace_size",
     "pa_decode_shared_prefix", "pa_decode_noalloc_scratch_limit", "pa_decode_noalloc",
     "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8", "pa_decode_fp8", "pa_swap_blocks",
-    "pa_decode_step_shared_prefix", "pa_decode_step",
+    "pa_decode_step_shared_prefix", "pa_decode_step", "pa_selftest_bounded_wait",
 )
 
 _i32, _i64, _f32, _vp, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
@@ -76,6 +76,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                                     ctypes.c_int, _vp]),
         "pa_copy_blocks_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp]),
         "pa_swap_blocks": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp]),
+        "pa_selftest_bounded_wait": (ctypes.c_int, [_i64, _vp]),
         "pa_decode_step": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _i32, _vp,
                                           _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _i32, _vp, _sz,
                                           ctypes.c_int, _vp]),
@@ -340,6 +341,12 @@ def pa_decode_step_shared_prefix(cow_pairs, new_seq_ids: torch.Tensor, new_posit
         _stream(stream))
     _check(rc, "pa_decode_step_shared_prefix")
     return out
+
+
+def pa_selftest_bounded_wait(limit_ns: int, stream=None) -> None:
+    """Launch a wait that nothing completes: it gives up after limit_ns and
+    records PA_ERR_TIMEOUT (read it with pa_get_status)."""
+    _check(load().pa_selftest_bounded_wait(int(limit_ns), _stream(stream)), "pa_selftest_bounded_wait")
 
 
 def pa_decode_noalloc_scratch_limit() -> int:

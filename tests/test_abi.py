@@ -218,3 +218,8 @@ def test_one_call_step_host_checks(lib, entry):
     assert call(ids=0) == -1                       # new tokens without their ids
     assert call(kn=0x3004) == -12                  # new K not 16-byte aligned
     assert call(T=-1) == -1                        # negative token count
+
+
+def test_selftest_wait_limit_checked(lib):
+    assert lib.pa_selftest_bounded_wait(10, None) == -1              # below 1 us
+    assert lib.pa_selftest_bounded_wait(2_000_000_000, None) == -1   # above 1 s
