@@ -5,6 +5,8 @@
 #include <algorithm>
 #include <cmath>
 #include <mutex>
+#include <set>
+#include <utility>
 #include <unordered_set>
 #include <vector>
 
@@ -63,6 +65,19 @@ int num_sms_current_device() {
     g_num_sms[dev] = n;
   }
   return g_num_sms[dev];
+}
+
+int set_max_dynamic_smem(const void* kernel, int bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done.count({kernel, dev})) return PA_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return PA_ERR_CUDA;
+  done.insert({kernel, dev});
+  return PA_OK;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

@@ -165,19 +165,9 @@ int launch_cascade_prep(const DecodeParams& dp, pa_dtype dt, const int32_t* grou
   const size_t smem = cascade_prep_smem(dp.num_seqs, num_groups);
   const int staged = smem <= kCascadePrepSmemMax && !dp.cu_q_lens;
   auto kern = dt == PA_BF16 ? cascade_prep_kernel<__nv_bfloat16> : cascade_prep_kernel<__half>;
-  if (staged && smem > 48 * 1024) {
-    static bool attr_set[2][64] = {};  // per instantiation and device
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const int k = dt == PA_BF16 ? 1 : 0;
-    if (dev < 0 || dev >= 64) return PA_ERR_CUDA;
-    if (!attr_set[k][dev]) {
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCascadePrepSmemMax) !=
-          cudaSuccess)
-        return PA_ERR_CUDA;
-      attr_set[k][dev] = true;
-    }
-  }
+  if (staged && smem > 48 * 1024 &&
+      set_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)kCascadePrepSmemMax) != PA_OK)
+    return PA_ERR_CUDA;
   kern<<<1, 1024, staged ? smem : 0, stream>>>(dp, group_starts, prefix_in, num_groups, members_per_tile, staged,
                                                prefix_out, group_ref, group_of_seq, work, pairs, pair_keys);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;

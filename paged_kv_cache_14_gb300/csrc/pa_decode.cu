@@ -1121,14 +1121,7 @@ static int launch_tc(const DecodeParams& p, cudaStream_t stream) {
   }
   if (rc != PA_OK) return rc;
   auto kern = decode_tc_kernel<T, D, BS, NT, KV8>;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
-      return PA_ERR_CUDA;
-    attr_set[dev] = true;
-  }
+  if (set_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)C::kSmem) != PA_OK) return PA_ERR_CUDA;
   if (!p.planned) {
     decode_plan_kernel<T><<<1, 1024, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;

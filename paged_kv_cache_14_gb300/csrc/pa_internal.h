@@ -141,6 +141,9 @@ inline CascadeWorkspace cascade_workspace_layout(int64_t num_seqs, int64_t num_g
 // Returns the device status word of the current device (nullptr on error).
 int* device_status_ptr();
 int num_sms_current_device();
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device); thread-safe. PA_OK or PA_ERR_CUDA.
+int set_max_dynamic_smem(const void* kernel, int bytes);
 
 // Encode a 2-D tensor map over a KV pool seen as [num_blocks*num_kv_heads*block_size rows][head_dim],
 // box = [box_rows rows][64 elements] with 128-byte swizzle (16-bit dtypes only).

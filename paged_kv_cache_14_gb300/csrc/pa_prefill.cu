@@ -628,14 +628,7 @@ template <typename T, int BS, bool PREFIX>
 static int launch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                  const PrefillParams& p, int ctas, cudaStream_t stream) {
   auto kern = prefill_tc_kernel<T, BS, PREFIX>;
-  static bool attr_set[64] = {};  // one flag per device for this instantiation
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pf::kSmem) != cudaSuccess)
-      return PA_ERR_CUDA;
-    attr_set[dev] = true;
-  }
+  if (set_max_dynamic_smem(reinterpret_cast<const void*>(kern), pf::kSmem) != PA_OK) return PA_ERR_CUDA;
   return launch_dependent(kern, dim3(ctas), dim3(pf::kThreads), pf::kSmem, stream, qmap, kmap, vmap, p) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
