@@ -53,3 +53,19 @@ def test_single_rank_is_identity():
     import bench
     assert bench.reduce_max_over_ranks([3.0, 4.0], 1) == [3.0, 4.0]
     assert bench.weak_scaling_value(1, 1e9, 1.0) == pytest.approx(1000.0)
+
+
+def test_profiled_traffic_only_for_the_profiled_source(tmp_path):
+    # The bench reports a kernel's DRAM traffic from a committed ncu summary
+    # only while the decode source is the one that summary was taken on.
+    import hashlib
+
+    import bench
+    sha = hashlib.sha256(open(bench.DECODE_SRC, "rb").read()).hexdigest()
+    good = tmp_path / "good.md"
+    good.write_text(f"decode_source_sha256: {sha}\ntraffic_bytes_per_launch: 123456\n")
+    assert bench.profiled_traffic(str(good)) == 123456.0
+    stale = tmp_path / "stale.md"
+    stale.write_text("decode_source_sha256: " + "0" * 64 + "\ntraffic_bytes_per_launch: 123456\n")
+    assert bench.profiled_traffic(str(stale)) is None
+    assert bench.profiled_traffic(str(tmp_path / "missing.md")) is None
