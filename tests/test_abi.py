@@ -223,3 +223,20 @@ def test_one_call_step_host_checks(lib, entry):
 def test_selftest_wait_limit_checked(lib):
     assert lib.pa_selftest_bounded_wait(10, None) == -1              # below 1 us
     assert lib.pa_selftest_bounded_wait(2_000_000_000, None) == -1   # above 1 s
+
+
+def test_binding_refuses_host_tensors_and_wrong_dtypes(lib):
+    # The binding only marshals arguments: it never computes on the CPU and
+    # never converts. Host tensors or a mismatched dtype raise before any call.
+    import torch
+    q = torch.zeros(2, 8, 128, dtype=torch.bfloat16)
+    kc = torch.zeros(4, 2, 16, 128, dtype=torch.bfloat16)
+    bt = torch.zeros(2, 4, dtype=torch.int32)
+    lens = torch.ones(2, dtype=torch.int32)
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        pa.pa_decode(q, kc, kc, bt, lens, 16, 0.1, out=torch.zeros_like(q), workspace=torch.zeros(1 << 20,
+                     dtype=torch.uint8))
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        pa.pa_copy_blocks(kc, kc, [(0, 1)])
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        pa.pa_slot_mapping(bt, torch.zeros(2, dtype=torch.int32), torch.zeros(2, dtype=torch.int32), 16, 4)
