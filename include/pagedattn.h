@@ -76,7 +76,9 @@ int pa_version(void);
 /*
  * pa_get_status — synchronise `stream`, return the first device-side error
  * recorded since the last call (PA_OK if none), and clear it. The status
- * word is per device and shared by all streams.
+ * word is per device and shared by all streams. Its device address is looked
+ * up once per device and cached for the life of the process, so the library
+ * must not be used across a cudaDeviceReset.
  */
 int pa_get_status(void* stream);
 
@@ -326,17 +328,23 @@ int pa_decode_step_shared_prefix(const int64_t* cow_pairs, int32_t num_cow_pairs
  * start-up because it synchronises the device, or code that must not create
  * allocations while a stream is being captured). The pages describe no such
  * call; it exists for these callers only.
- * Same arguments and results as pa_decode, without workspace arguments: the
- * split-KV scratch is a fixed device array of
- * pa_decode_noalloc_scratch_limit() bytes (64 MiB) inside the library, which
- * every GPU that loads the library holds until the process exits. The call
- * allocates nothing. A call whose pa_decode_workspace_size() exceeds the
- * limit returns PA_ERR_SCRATCH before launching anything.
+ * Same arguments, checks and results as pa_decode, without workspace
+ * arguments: the split-KV scratch is a fixed device array of
+ * pa_decode_noalloc_scratch_limit() bytes (64 MiB) inside the library, held
+ * on a device until the process exits once the library's code is loaded
+ * there. The call itself calls no cudaMalloc, cudaFree or allocating
+ * library routine. A call whose pa_decode_workspace_size() exceeds the limit
+ * returns PA_ERR_SCRATCH before launching anything.
  * The first call on a device looks up the array's device address (with that
- * device current) and caches it; make that first call during set-up, before
- * any stream capture. All calls share the one array and it keeps the last
- * call's contents (nothing in it needs to start at zero): two calls whose
- * executions overlap on the device, on different streams, race on it.
+ * device current) and caches it. Under CUDA's default lazy module loading
+ * that lookup is what loads the library's module on the device, so the first
+ * call makes a one-time 64 MiB device reservation and may synchronise: make
+ * it during set-up, before any stream capture and before the point after
+ * which the caller may not allocate. All calls share the one array and it
+ * keeps the last call's contents (nothing in it needs to start at zero): two
+ * calls whose executions overlap on the device, on different streams, race
+ * on it. The cached address is that of the device's primary context: do not
+ * use the library across a cudaDeviceReset.
  */
 size_t pa_decode_noalloc_scratch_limit(void);
 int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,

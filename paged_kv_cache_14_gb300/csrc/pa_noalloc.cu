@@ -26,7 +26,11 @@ std::mutex g_noalloc_mu;
 void* g_noalloc_addr[kMaxDev] = {};
 
 // Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached. nullptr on failure.
+// device (with that device current) and cached. nullptr on failure. The
+// lookup is also what loads this file's module on a device under lazy module
+// loading, so it is the moment the 64 MiB array is reserved there. The cached
+// address belongs to the device's primary context: after a cudaDeviceReset it
+// is stale, and the library must not be used across one.
 void* noalloc_scratch_address() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
@@ -49,7 +53,8 @@ extern "C" int pa_decode_noalloc(const void* q, const void* k_cache, const void*
                                  int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale, void* out,
                                  int32_t partition_size, pa_dtype dtype, void* stream) {
-  if (num_seqs == 0) return PA_OK;
+  // An empty or malformed call needs no scratch (size 0) and gets pa_decode's
+  // own argument checks and result.
   const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                                max_seq_len, partition_size);
   if (need > pa::kNoAllocScratchBytes) return PA_ERR_SCRATCH;
