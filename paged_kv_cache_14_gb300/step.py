@@ -107,6 +107,31 @@ class PagedStep:
             n += 2  # prefill plan, prefill chunks
         return n
 
+    @property
+    def step_calls(self) -> str:
+        """The library calls one run() makes."""
+        if self.shared_prefix and self.kv_scales is None:
+            return ("pa_decode_step_shared_prefix (copy_blocks + slot_mapping + reshape_and_cache + "
+                    "pa_decode_shared_prefix in one call)")
+        if self.is_decode and self.kv_scales is None and self.q.dtype != torch.float32:
+            return "pa_decode_step (copy_blocks + slot_mapping + reshape_and_cache + pa_decode in one call)"
+        if self.kv_scales is not None:
+            return "pa_copy_blocks_fp8 + pa_slot_mapping + pa_reshape_and_cache_fp8 + pa_decode_fp8"
+        return "pa_copy_blocks + pa_slot_mapping + pa_reshape_and_cache + " + (
+            "pa_decode" if self.is_decode else "pa_chunked_prefill")
+
+    @property
+    def attention_kernels(self) -> str:
+        """What the step's attention call (attend()) runs on the device."""
+        if self.kv_scales is not None:
+            return "pa_decode_fp8: plan + persistent e4m3 decode + split-KV merge"
+        if self.shared_prefix:
+            return ("pa_decode_shared_prefix: prefix check + tcgen05 prefix pass + split-KV suffix decode "
+                    "+ merge")
+        if self.is_decode:
+            return "pa_decode: plan + persistent decode + split-KV merge"
+        return "pa_chunked_prefill: decode rows (plan + decode + merge) and tcgen05 chunk kernel (plan + main)"
+
     def run(self, stream=None) -> torch.Tensor:
         if self.shared_prefix and self.kv_scales is None:
             # One call: the shared-prefix check runs beside the copies,

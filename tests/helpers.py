@@ -9,6 +9,9 @@ Cache writes, block copies and slot mappings must be bit-exact.
 """
 from __future__ import annotations
 
+import dataclasses
+import functools
+
 import numpy as np
 import torch
 
@@ -60,3 +63,24 @@ def oracle_prefill(batch, kc, vc, seqs=None, rows=None):
 
 def to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu", torch.float64).numpy()
+
+
+def oracle_step(batch, **replace):
+    """Oracle output of a whole step on `batch` (copy-on-write copies, the
+    cache write of the new tokens, then decode or chunked prefill), with any
+    of the batch's fields (q, k_new, v_new, block_tables, ...) replaced by
+    host arrays: what a replayed or pipelined step must produce."""
+    if replace:
+        batch = dataclasses.replace(batch, **replace)
+    kc, vc, _ = oracle_caches_after_step(batch)
+    if batch.is_decode:
+        return oracle_decode(batch, kc, vc)
+    return oracle_prefill(batch, kc, vc)
+
+
+@functools.lru_cache(maxsize=2)
+def full_config(name: str):
+    """A named full-size workload, generated once per test session (the
+    generator takes tens of seconds). Callers must not modify it."""
+    from workloads import make_config
+    return make_config(name)

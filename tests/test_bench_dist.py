@@ -56,16 +56,41 @@ def test_single_rank_is_identity():
 
 
 def test_profiled_traffic_only_for_the_profiled_source(tmp_path):
-    # The bench reports a kernel's DRAM traffic from a committed ncu summary
-    # only while the decode source is the one that summary was taken on.
-    import hashlib
-
+    # The bench reports an attention call's DRAM traffic from a committed ncu
+    # summary only while the library's CUDA sources are the ones that summary
+    # was taken on.
     import bench
-    sha = hashlib.sha256(open(bench.DECODE_SRC, "rb").read()).hexdigest()
+    sha = bench.source_sha256()
     good = tmp_path / "good.md"
-    good.write_text(f"decode_source_sha256: {sha}\ntraffic_bytes_per_launch: 123456\n")
-    assert bench.profiled_traffic(str(good)) == 123456.0
+    good.write_text(f"source_sha256: {sha}\ncall_dram_bytes: 123456\nkernel_dram_bytes: 1000\n"
+                    "dominant_kernel: decode_tc_kernel\n")
+    assert bench.profiled_traffic(str(good)) == {"call": 123456.0, "kernel": 1000.0,
+                                                 "kernel_name": "decode_tc_kernel"}
     stale = tmp_path / "stale.md"
-    stale.write_text("decode_source_sha256: " + "0" * 64 + "\ntraffic_bytes_per_launch: 123456\n")
+    stale.write_text("source_sha256: " + "0" * 64 + "\ncall_dram_bytes: 123456\n")
     assert bench.profiled_traffic(str(stale)) is None
     assert bench.profiled_traffic(str(tmp_path / "missing.md")) is None
+
+
+def test_clock_samples_are_taken_from_the_timed_window():
+    import bench
+    clk = bench.ClockSampler(0)
+    line = "{sm}, 2070, Active, {hw}, Not Active, Not Active, Not Active"
+    clk.samples = [(1.0, line.format(sm=1000, hw="Not Active")),   # before the window
+                   (2.0, line.format(sm=2070, hw="Not Active")),
+                   (2.5, line.format(sm=2060, hw="Not Active")),
+                   (3.0, line.format(sm=2050, hw="Not Active")),
+                   (9.0, line.format(sm=900, hw="Active")),         # after the window
+                   (9.5, "garbage")]
+    s = clk.summary(2.0, 3.0)
+    assert s == {"sm_mhz": 2060.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3}
+    whole = clk.summary()
+    assert whole["samples"] == 5 and whole["reasons"] == ["hw_slowdown"]
+    assert bench.ClockSampler(0).summary(0, 1)["samples"] == 0
+
+
+def test_timed_block_count():
+    import bench
+    assert bench.timed_block_count(6.3, 1000.0) == 159     # 20 steps of 0.315 ms: about 1 s
+    assert bench.timed_block_count(500.0, 1000.0) == 3      # at least three blocks
+    assert bench.timed_block_count(0.01, 1000.0) == 1000    # at most a thousand

@@ -6,8 +6,8 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import assert_attention_close, oracle_caches_after_step, oracle_prefill, to_f64
-from workloads import build_batch, make_config
+from helpers import assert_attention_close, full_config, oracle_caches_after_step, oracle_prefill, oracle_step, to_f64
+from workloads import build_batch
 
 pytestmark = pytest.mark.gpu
 
@@ -70,11 +70,12 @@ def test_prefill_repeat_is_deterministic(lib):
     c = st.run().clone()
     assert lib.pa_get_status() == 0
     assert torch.equal(a, c)
+    assert_attention_close(to_f64(a), oracle_step(b), "bf16", "repeated prefill vs oracle")
 
 
 @pytest.mark.slow
 def test_mixed_prefill_config_sampled(lib):
-    b = make_config("mixed_prefill_fp16")
+    b = full_config("mixed_prefill_fp16")
     st, out = run_step(lib, b)
     assert np.all(np.isfinite(out))
     kr, vr, slots = oracle_caches_after_step(b)

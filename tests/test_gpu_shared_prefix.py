@@ -8,8 +8,10 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import assert_attention_close, oracle_caches_after_step, oracle_decode, to_f64
-from workloads import build_batch, make_config
+import oracle
+
+from helpers import assert_attention_close, full_config, oracle_caches_after_step, oracle_decode, to_f64
+from workloads import build_batch
 
 pytestmark = pytest.mark.gpu
 
@@ -82,18 +84,31 @@ def test_shared_prefix_bad_hints_still_correct(lib):
 
 @pytest.mark.slow
 def test_llama3_70b_prefix_config_shared_prefix(lib):
-    b = make_config("llama3_70b_prefix_bf16")
-    st = _device_step(lib, b)
-    plain = st.out.clone()
-    out = _shared(lib, st, b)
+    """The full 70B prefix-sharing batch through the one-call shared-prefix
+    step, the launch configuration the bench times: the blocks the step
+    touched equal the oracle's bit for bit and every sequence's output is
+    compared with the oracle (and with plain decode)."""
+    from paged_kv_cache_14_gb300.step import step_from_host
+    b = full_config("llama3_70b_prefix_bf16")
+    st = step_from_host(b, shared_prefix=True)
+    st.run()
     assert lib.pa_get_status() == 0
-    assert_attention_close(to_f64(out), to_f64(plain), "bf16", "shared-prefix vs pa_decode, full size")
+    out = to_f64(st.out)
+    kr, vr, slots = oracle_caches_after_step(b)
+    touched = torch.from_numpy(np.unique(np.concatenate([b.cow_pairs[:, 1], slots // b.block_size])))
+    assert torch.equal(st.k_cache.cpu()[touched].view(torch.int16), kr[touched].view(torch.int16))
+    assert torch.equal(st.v_cache.cpu()[touched].view(torch.int16), vr[touched].view(torch.int16))
+    assert_attention_close(out, oracle_decode(b, kr, vr), "bf16", "shared-prefix step vs oracle, every sequence")
+    plain = lib.pa_decode(st.q, st.k_cache, st.v_cache, st.block_tables, st.kv_lens, st.max_seq_len, b.scale)
+    assert lib.pa_get_status() == 0
+    assert_attention_close(out, to_f64(plain), "bf16", "shared-prefix vs pa_decode, full size")
+
+
+def _oracle_rows(b, block_tables, pick):
+    """Oracle rows of the sequences in `pick` after the batch's step, on the
+    given (possibly edited) block tables."""
     kr, vr, _ = oracle_caches_after_step(b)
-    rng = np.random.default_rng(12)
-    order = np.argsort(b.kv_lens)
-    pick = sorted(set([int(order[0]), int(order[-1]), 0, 15, 16]) | set(rng.choice(256, 10, replace=False).tolist()))
-    ref = oracle_decode(b, kr, vr, seqs=pick)
-    assert_attention_close(to_f64(out)[pick], ref[pick], "bf16", "shared-prefix vs oracle, full size")
+    return oracle.decode(b.q, kr, vr, block_tables, b.kv_lens, b.scale, b.block_size, seqs=pick)
 
 
 @pytest.mark.parametrize("n", [5000, 17000], ids=["staged_large", "unstaged"])
@@ -112,6 +127,15 @@ def test_shared_prefix_many_sequences(lib, n):
     out = to_f64(_shared(lib, st, b))
     assert lib.pa_get_status() == 0
     assert_attention_close(out, plain, "bf16", f"{n} sequences: shared-prefix vs pa_decode")
+    # Against the oracle: every member of the first, a middle and the last
+    # groups, plus 400 sequences drawn at random.
+    gs = b.group_starts
+    mid = len(gs) // 2
+    pick = set(range(gs[0], gs[1])) | set(range(gs[mid], gs[mid + 1])) | set(range(gs[-2], gs[-1]))
+    pick |= set(np.random.default_rng(n + 1).choice(n, 400, replace=False).tolist())
+    pick = sorted(int(i) for i in pick)
+    ref = _oracle_rows(b, b.block_tables, pick)
+    assert_attention_close(out[pick], ref[pick], "bf16", f"{n} sequences: shared-prefix vs oracle")
 
 
 def test_shared_prefix_many_groups_mixed_q_tiles(lib):
@@ -143,6 +167,8 @@ def test_shared_prefix_many_groups_mixed_q_tiles(lib):
     out = to_f64(_shared(lib, st, b, group_starts=gs, prefix_lens=pl))
     assert lib.pa_get_status() == 0
     assert_attention_close(out, plain, "bf16", "mixed group sizes: shared-prefix vs pa_decode")
+    ref = _oracle_rows(b, bt.cpu().numpy(), list(range(len(lens))))
+    assert_attention_close(out, ref, "bf16", "mixed group sizes: shared-prefix vs oracle")
 
 
 @pytest.mark.parametrize("case", [CASES[0], CASES[3]], ids=["grp4", "grp37"])
@@ -212,3 +238,5 @@ def test_shared_prefix_long_prefix_mismatch_past_64_blocks(lib):
     out = to_f64(_shared(lib, st, b))
     assert lib.pa_get_status() == 0
     assert_attention_close(out, plain, "bf16", "mismatch past the first 64 shared blocks")
+    ref = _oracle_rows(b, bt.cpu().numpy(), list(range(len(lens))))
+    assert_attention_close(out, ref, "bf16", "mismatch past the first 64 shared blocks vs oracle")

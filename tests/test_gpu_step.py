@@ -8,8 +8,8 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import assert_attention_close, oracle_caches_after_step, oracle_decode, to_f64
-from workloads import build_batch, make_config
+from helpers import assert_attention_close, full_config, oracle_caches_after_step, oracle_decode, oracle_step, to_f64
+from workloads import build_batch
 
 pytestmark = pytest.mark.gpu
 
@@ -64,7 +64,7 @@ def test_decode_step_rejects_before_launching(lib):
 
 def test_decode_step_8b_config_matches_separate_calls(lib):
     from paged_kv_cache_14_gb300.step import step_from_host
-    b = make_config("llama3_8b_bf16")
+    b = full_config("llama3_8b_bf16")
     sep = step_from_host(b)
     sep.prepare()
     sep.attend()
@@ -74,6 +74,7 @@ def test_decode_step_8b_config_matches_separate_calls(lib):
     assert lib.pa_get_status() == 0
     assert torch.equal(one.out, sep.out)
     assert torch.equal(one.k_cache, sep.k_cache) and torch.equal(one.v_cache, sep.v_cache)
+    assert_attention_close(to_f64(one.out), oracle_step(b), "bf16", "8B one-call step vs oracle, every sequence")
 
 
 def test_one_call_steps_with_empty_parts(lib):
@@ -105,6 +106,7 @@ def test_one_call_steps_with_empty_parts(lib):
         torch.cuda.synchronize()
         assert lib.pa_get_status() == 0
         assert torch.equal(st.out, ref)
+        assert_attention_close(to_f64(st.out), oracle_step(b), "bf16", f"empty parts (shared={shared}) vs oracle")
     # An empty batch with new tokens: only the cache side runs (slots of
     # sequences outside the batch are -1, so nothing is written).
     st = step_from_host(b)
@@ -140,3 +142,4 @@ def test_one_call_step_with_more_than_1024_cow_pairs(lib, shared):
     assert lib.pa_get_status() == 0
     assert torch.equal(one.k_cache, sep.k_cache) and torch.equal(one.v_cache, sep.v_cache)
     assert torch.equal(one.out, sep.out)
+    assert_attention_close(to_f64(one.out), oracle_step(b), "bf16", "1100 CoW pairs: one-call step vs oracle")
