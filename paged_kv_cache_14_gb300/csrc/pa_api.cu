@@ -20,6 +20,17 @@ namespace pa {
 
 namespace {
 constexpr int kMaxDevices = 64;
+// Decode-row KV bytes one SM streams in the time it runs one (item, KV tile)
+// unit of the chunk kernel (see mixed_plan_kernel); it sets how a mixed batch
+// splits the SMs. On GB300 a unit takes about 1.6 us and the decode kernel
+// streams about 90-100 GB/s per SM when only a few SMs run it. A sweep of the
+// mixed 70B-shaped batch (8 chunks of 512 rows, 96 decode rows) gave the
+// call 1.27 / 1.01 / 0.98 / 0.935 / 0.99 / 1.00 ms at 40K / 80K / 120K /
+// 160K / 240K / 400K bytes, and 1.03 ms with all SMs to the chunks.
+#ifndef PA_DECODE_BYTES_PER_CHUNK_TILE
+#define PA_DECODE_BYTES_PER_CHUNK_TILE 160000.0f
+#endif
+constexpr float kDecodeBytesPerChunkTile = PA_DECODE_BYTES_PER_CHUNK_TILE;
 std::mutex g_mu;
 int* g_status_ptr[kMaxDevices] = {};
 int g_num_sms[kMaxDevices] = {};
@@ -745,11 +756,16 @@ int pa_chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_lens,
     return PA_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // Decode rows (q_len == 1): the split-KV decode path, key count ctx + 1.
-  int rc = decode_common(q, k_cache, v_cache, block_tables, max_blocks_per_seq, ctx_lens, cu_q_lens, num_seqs,
-                         max_kv_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out, 0,
-                         workspace, dec_ws, dtype, s);
-  if (rc != PA_OK || max_q_len <= 1) return rc;
-  // Chunks (q_len > 1): tcgen05 tiles.
+  DecodeParams dp;
+  DecodeWorkspace wl;
+  int rc = decode_prepare(q, k_cache, v_cache, block_tables, max_blocks_per_seq, ctx_lens, cu_q_lens, num_seqs,
+                          max_kv_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out, 0, 0,
+                          workspace, dec_ws, dtype, &dp, &wl);
+  if (rc != PA_OK) return rc;
+  if (max_q_len <= 1) return launch_decode(dp, dtype, s);
+  // Chunks (q_len > 1): tcgen05 tiles. One plan lists the chunk items and
+  // the decode rows' partitions and splits the SMs between them; the chunk
+  // kernel runs on its share and the decode kernel beside it on the rest.
   PrefillParams p{};
   p.q = q;
   p.out = out;
@@ -771,8 +787,14 @@ int pa_chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_lens,
   uint8_t* pw = static_cast<uint8_t*>(workspace) + dec_ws;
   p.work = reinterpret_cast<int32_t*>(pw);
   p.pairs = reinterpret_cast<int32_t*>(pw + 16);
-  p.status = device_status_ptr();
-  return launch_prefill(p, k_cache, v_cache, dtype, s);
+  p.status = dp.status;
+  p.decode_token_bytes = 2 * num_kv_heads * head_dim * elem_bytes(dtype);
+  p.decode_bytes_per_tile = kDecodeBytesPerChunkTile;
+  rc = launch_prefill(p, k_cache, v_cache, dtype, s, &dp);
+  if (rc != PA_OK) return rc;
+  dp.planned = 1;
+  dp.beside = 1;
+  return launch_decode(dp, dtype, s);
 }
 
 }  // extern "C"

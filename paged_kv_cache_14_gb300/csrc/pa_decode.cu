@@ -194,9 +194,13 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
   // letting this kernel start), so it streams its suffix at once, overlapping
   // the prefix pass, and waits for that pass only before reading a prefix
   // partial and before it exits (so the merge kernel sees both).
-  const bool overlap = p.planned && p.prefix;
+  // The decode rows of a mixed batch (beside) likewise stream at once,
+  // beside the chunk kernel, and wait for it before exiting; they let the
+  // merge kernel launch only as they exit, so its CTAs take no SM that a
+  // decode CTA could use once a chunk CTA leaves.
+  const bool overlap = p.planned && (p.prefix || p.beside);
   if (!overlap) pdl_wait();
-  pdl_trigger();
+  if (!p.beside) pdl_trigger();
   const uint32_t ring0 = smem_u32(smem + C::kRing);
 
   if (warp == C::kConsumers) {

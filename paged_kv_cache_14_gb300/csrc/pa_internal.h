@@ -51,6 +51,11 @@ struct DecodeParams {
   const int32_t* prefix;
   int32_t slot0;
   int32_t planned;       // the work list is already built (by the shared-prefix preparation)
+  // The decode rows of a mixed batch: launched behind the chunk kernel,
+  // which waited for the plan that built this work list before letting this
+  // kernel start; the decode streams at once, beside it, and waits for it
+  // only before exiting.
+  int32_t beside;
   // e4m3 KV cache: (K, V) scale per (block, KV head), float32
   // [num_blocks][num_kv_heads][2]; nullptr when the pools hold q's dtype.
   const float* kv_scales;
@@ -104,8 +109,14 @@ struct PrefillParams {
   int32_t total_q;   // rows of q / out
   int32_t gshift;    // log2(group)
   float scale_log2;
-  int32_t* work;     // [0] next work item, [1] number of work items
+  int32_t* work;     // [0] next work item, [1] number of work items, [2] CTAs that run items (chunks)
   int32_t* pairs;    // (seq << 16 | row tile), longest first; prefix pass: (group << 16 | member tile)
+  int32_t ctas;      // grid of the chunk kernel
+  int32_t num_sms;
+  // Mixed batches: KV bytes of one decode-row token (K and V, all KV heads)
+  // and the SM-time of one chunk (item, KV tile) unit in decode KV bytes.
+  int32_t decode_token_bytes;
+  float decode_bytes_per_tile;
   // Prefix pass of shared-prefix decode (null for chunked prefill): rows are
   // (group member, GQA head); keys are the group's shared blocks, read
   // through the table of the member with the longest verified prefix; the
@@ -189,9 +200,12 @@ int launch_decode(const DecodeParams& p, pa_dtype dt, cudaStream_t stream);
 // between the plan and the decode: launch_decode then runs with
 // planned = 1 and its first kernel waits for the ones before it.
 int launch_decode_plan(const DecodeParams& p, pa_dtype dt, cudaStream_t stream);
-// Prefill chunks (q_len > 1) on the tensor-core path.
+// Prefill chunks (q_len > 1) on the tensor-core path. With `beside` (the
+// decode rows of the same batch), the plan also builds their work list and
+// splits the SMs; the caller then launches the decode (planned, beside)
+// right after.
 int launch_prefill(const PrefillParams& p, const void* k_cache, const void* v_cache, pa_dtype dt,
-                   cudaStream_t stream);
+                   cudaStream_t stream, const DecodeParams* beside = nullptr);
 // Prefix pass of shared-prefix decode on the same tensor-core kernel.
 int launch_prefix_pass(const PrefillParams& p, const void* k_cache, const void* v_cache, pa_dtype dt,
                        cudaStream_t stream);

@@ -40,6 +40,7 @@
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
+#include "pa_plan.cuh"
 #include "pa_tcgen05.cuh"
 
 namespace pa {
@@ -93,12 +94,13 @@ static_assert(kRows == kPrefillRowsPerItem, "work list granularity shared with t
 
 // Plan: list (sequence, 256-row item) pairs of every chunk with q_len > 1,
 // ordered by decreasing number of KV tiles (longest items first), and reset
-// the item counter. One CTA of 1024 threads.
-__global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams p) {
-  pdl_trigger();  // the chunk kernel may start its set-up now; it waits for this plan
+// the item counter. Run by the 1024 threads of one CTA. Returns (to every
+// thread) the number of (item, KV tile) units the chunk kernel will run.
+__device__ __forceinline__ int64_t prefill_plan_body(const PrefillParams& p) {
   constexpr int kBins = 2048;
   __shared__ int hist[kBins];
   __shared__ int total;
+  __shared__ int scratch[33];
   const int pp = pf::kRows >> p.gshift;  // query positions per work item
   for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
   if (threadIdx.x == 0) total = 0;
@@ -111,6 +113,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
     const int t = (keys + pf::kN - 1) / pf::kN;
     return min(t, kBins - 1);
   };
+  int my_tiles = 0;
   for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) {
     const int ql = p.cu_q_lens[s + 1] - p.cu_q_lens[s];
     if (ql <= 1) continue;
@@ -120,13 +123,17 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
       continue;
     }
     const int nm = (ql + pp - 1) / pp;
-    for (int mt = 0; mt < nm; ++mt) atomicAdd(&hist[tiles_of(s, mt)], 1);
+    for (int mt = 0; mt < nm; ++mt) {
+      const int t = tiles_of(s, mt);
+      my_tiles += t;
+      atomicAdd(&hist[t], 1);
+    }
   }
-  __syncthreads();
+  int all_tiles;
+  block_exclusive_scan_1024(my_tiles, scratch, &all_tiles);
   {
     // Exclusive scan from the longest bin down: thread t owns bins
     // kBins-1-2t and kBins-2-2t.
-    __shared__ int scratch[33];
     const int b0 = kBins - 1 - 2 * threadIdx.x, b1 = b0 - 1;
     const int c0 = hist[b0], c1 = hist[b1];
     int tot;
@@ -151,6 +158,53 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams 
   if (threadIdx.x == 0) {
     p.work[0] = 0;
     p.work[1] = total * p.num_kv_heads;
+  }
+  return (int64_t)all_tiles * p.num_kv_heads;
+}
+
+// Plan of a batch of chunks only: every CTA of the chunk kernel runs items.
+__global__ void __launch_bounds__(1024) prefill_plan_kernel(const PrefillParams p) {
+  pdl_trigger();  // the chunk kernel may start its set-up now; it waits for this plan
+  prefill_plan_body(p);
+  if (threadIdx.x == 0) p.work[2] = p.ctas;
+}
+
+// Plan of a mixed batch (chunks and decode rows): the chunk list, the decode
+// rows' work list (the decode kernel runs beside the chunk kernel and reads
+// it without waiting: every chunk CTA lets the decode kernel start only
+// after waiting for this plan), and the split of the SMs. The chunk kernel
+// is bound by its tensor work, the decode rows by their KV reads, so the
+// chunk kernel gets a share of the SMs in proportion to its estimated time
+// on one SM: (item, KV tile) units at the measured per-SM rate against the
+// decode rows' KV bytes at the measured per-SM streaming rate, expressed as
+// decode_bytes_per_tile (KV bytes one SM streams in the time it runs one
+// unit). Its surplus CTAs exit at once and the decode kernel takes their
+// SMs; decode CTAs also take the SMs of chunk CTAs that run out of items.
+template <typename T>
+__global__ void __launch_bounds__(1024) mixed_plan_kernel(const PrefillParams p, const DecodeParams dp) {
+  pdl_trigger();
+  __shared__ int scratch2[33];
+  const int64_t chunk_units = prefill_plan_body(p);
+  __syncthreads();
+  decode_plan_body<T>(dp);
+  int64_t my_tokens = 0;
+  for (int s = threadIdx.x; s < dp.num_seqs; s += blockDim.x) {
+    int qrow, len;
+    if (decode_row(dp, s, qrow, len) && len_ok(dp, len)) my_tokens += len;
+  }
+  // Tokens of one thread stay below 2^31 (at most num_seqs / 1024 rows of
+  // at most 2^31 / 64 tokens each): the block sum is taken in units of 64.
+  int total64;
+  block_exclusive_scan_1024((int)((my_tokens + 63) >> 6), scratch2, &total64);
+  if (threadIdx.x == 0) {
+    const double decode_units = (double)total64 * 64.0 * p.decode_token_bytes / p.decode_bytes_per_tile;
+    int n = p.ctas;
+    if (chunk_units > 0 && decode_units > 0.0) {
+      const double share = (double)chunk_units / ((double)chunk_units + decode_units);
+      n = (int)lrint(share * p.num_sms);
+      n = max(1, min(n, p.ctas));
+    }
+    p.work[2] = n;
   }
 }
 
@@ -228,6 +282,14 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   pdl_wait();  // the work list of the plan / preparation kernel
   pdl_trigger();
   const uint32_t tmem = misc[0];
+  if constexpr (!PREFIX) {
+    // CTAs beyond the plan's share of the SMs leave them to the decode rows
+    // of a mixed batch at once.
+    if ((int)blockIdx.x >= p.work[2]) {
+      if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+      return;
+    }
+  }
   const int G = 1 << p.gshift;
   const int pp = kM >> p.gshift;  // query positions (or group members) per Q tile
   const int total = p.work[1];
@@ -646,7 +708,7 @@ static int dispatch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& k
 }
 
 int launch_prefill(const PrefillParams& p0, const void* k_cache, const void* v_cache, pa_dtype dt,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, const DecodeParams* beside) {
   PrefillParams p = p0;
   if (p.head_dim != pf::kD) return PA_ERR_UNSUPPORTED;
   if (p.group < 1 || p.group > pf::kM || (p.group & (p.group - 1))) return PA_ERR_UNSUPPORTED;
@@ -664,11 +726,22 @@ int launch_prefill(const PrefillParams& p0, const void* k_cache, const void* v_c
     rc = make_kv_tensor_map(&vmap, v_cache, rows, pf::kD, dt, 16);
     if (rc != PA_OK) return rc;
   }
-  prefill_plan_kernel<<<1, 1024, 0, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   const int64_t upper = (int64_t)(p.total_q > 0 ? p.total_q : 1) * p.num_kv_heads;
-  const int64_t resident = (int64_t)pf::kCtasPerSm * num_sms_current_device();
+  p.num_sms = num_sms_current_device();
+  const int64_t resident = (int64_t)pf::kCtasPerSm * p.num_sms;
   const int ctas = (int)(upper < resident ? upper : resident);
+  p.ctas = ctas;
+  if (beside) {
+    DecodeParams dp = *beside;
+    decode_set_rows(dp, dt);
+    if (dt == PA_BF16)
+      mixed_plan_kernel<__nv_bfloat16><<<1, 1024, 0, stream>>>(p, dp);
+    else
+      mixed_plan_kernel<__half><<<1, 1024, 0, stream>>>(p, dp);
+  } else {
+    prefill_plan_kernel<<<1, 1024, 0, stream>>>(p);
+  }
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   return dispatch_prefill_kernel<false>(qmap, kmap, vmap, p, ctas, dt, stream);
 }
 
