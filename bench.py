@@ -60,6 +60,7 @@ PER_CONFIG = (
     ("llama3_8b_bf16", "e4m3"),
     ("llama3_70b_prefix_bf16", "e4m3"),
     ("long_splitkv_bf16", "e4m3"),
+    ("mixed_prefill_fp16", "e4m3"),
 )
 
 
@@ -259,9 +260,10 @@ def source_sha256() -> str:
 
 def profile_summary(config: str, kv_cache: str = "native") -> str:
     """The committed ncu summary of the attention call on this workload."""
+    kind = "prefill" if config.startswith("mixed_prefill") else "decode"
     if kv_cache == "e4m3":
-        return os.path.join(PROFILES, f"decode_e4m3_{config}.md")
-    if config.startswith("mixed_prefill"):
+        return os.path.join(PROFILES, f"{kind}_e4m3_{config}.md")
+    if kind == "prefill":
         return os.path.join(PROFILES, f"prefill_{config}.md")
     return os.path.join(PROFILES, f"decode_{config}.md")
 
@@ -569,8 +571,12 @@ def chunk_only_entry(pa, torch, st, batch, timer, calls: int) -> dict:
     max_q = int(ql.max())
 
     def call():
-        pa.pa_chunked_prefill(q, cuq, st.k_cache, st.v_cache, tables, ctx, max_q, st.max_seq_len, batch.scale,
-                              out=out, workspace=ws)
+        if st.kv_scales is not None:
+            pa.pa_chunked_prefill_fp8(q, cuq, st.k_cache, st.v_cache, st.kv_scales, tables, ctx, max_q,
+                                      st.max_seq_len, batch.scale, out=out, workspace=ws)
+        else:
+            pa.pa_chunked_prefill(q, cuq, st.k_cache, st.v_cache, tables, ctx, max_q, st.max_seq_len, batch.scale,
+                                  out=out, workspace=ws)
     for _ in range(3):
         call()
     ms = timer.each(lambda: None, call, calls)
@@ -591,7 +597,7 @@ def per_config_entry(pa, torch, batch, kv_cache: str, timer, steps: int, warmup:
     fp8 = kv_cache == "e4m3"
     pool = e4m3_pool(batch.meta["seed"], batch.num_blocks, batch.num_kv_heads, batch.block_size,
                      batch.head_dim) if fp8 else None
-    shared = batch.is_decode and batch.prefix_lens is not None and bool(batch.prefix_lens.any()) and not fp8
+    shared = batch.is_decode and batch.prefix_lens is not None and bool(batch.prefix_lens.any())
     st = step_from_host(batch, shared_prefix=shared, fp8_pool=pool)
     kv_es = 1 if fp8 else None
     for _ in range(warmup):
@@ -633,8 +639,6 @@ def native_arm(args) -> None:
     fp8 = args.kv_cache == "e4m3"
     shared = batch.is_decode and (args.decode == "shared_prefix" or (
         args.decode == "auto" and batch.prefix_lens is not None and bool(batch.prefix_lens.any())))
-    if fp8 and shared:
-        shared = False  # the e4m3 cache runs plain decode
     pool = e4m3_pool(batch.meta["seed"], batch.num_blocks, batch.num_kv_heads, batch.block_size,
                      batch.head_dim) if fp8 else None
     st = step_from_host(batch, partition_size=args.partition, shared_prefix=shared, fp8_pool=pool)

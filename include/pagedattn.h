@@ -454,6 +454,54 @@ int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const
                   void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream);
 
 /*
+ * pa_decode_shared_prefix_fp8 — pa_decode_shared_prefix over the e4m3 pools:
+ * the attention of pa_decode_fp8 (every stored value is the e4m3 code times
+ * its (block, KV head) scale), computed as pa_decode_shared_prefix computes
+ * it: each group's shared blocks once per KV head for all its members in the
+ * tcgen05 tensor-core pass, the private suffixes in the split-KV decode, the
+ * two merged with log-sum-exp weights. FP8 block-quantised caching is the
+ * page's pairing for serving many concurrent 70B-class sequences ("Tech
+ * Radar: vLLM v1 Production Engine Architecture...", section 2, item 3;
+ * "High-Throughput Local LLM Infrastructure...", section 6, Q5); prefix
+ * sharing is section 1.2 of the latter, "Reference Counting &
+ * Copy-on-Write".
+ *   k_cache, v_cache, kv_scales : the e4m3 pools and scales, as for
+ *                  pa_decode_fp8 (kv_scales 16-byte aligned, else PA_ERR_ALIGN;
+ *                  NULL with num_seqs > 0: PA_ERR_ARG)
+ * Other arguments, hints, checks and errors as pa_decode_shared_prefix; the
+ * workspace is pa_decode_shared_prefix_workspace_size() bytes. q/out fp16
+ * or bf16, head_dim 128, GQA group a power of two up to 128, scale > 0.
+ * The codes are widened to fp16 exactly (a bf16 query row is moved into fp16
+ * by a power of two); scores, softmax and accumulation are fp32.
+ */
+int pa_decode_shared_prefix_fp8(const void* q, const void* k_cache, const void* v_cache, const float* kv_scales,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                int32_t num_seqs, int32_t max_seq_len, const int32_t* group_starts,
+                                const int32_t* prefix_lens, int32_t num_groups, int32_t num_q_heads,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                float scale, void* out, int32_t partition_size, void* workspace,
+                                size_t workspace_bytes, pa_dtype dtype, void* stream);
+
+/*
+ * pa_chunked_prefill_fp8 — pa_chunked_prefill over the e4m3 pools (chunked
+ * prefill mixed with decode rows, "Tech Radar...", section 3 "Dynamic
+ * Chunked Prefill", over the FP8 block-quantised cache of section 2, item
+ * 3): the attention of pa_chunked_prefill on the dequantised values. Decode
+ * rows go through the e4m3 decode kernel, chunks through the tcgen05 kernel
+ * with the codes widened to fp16 in shared memory. Arguments as
+ * pa_chunked_prefill plus kv_scales (as pa_decode_fp8); the workspace is
+ * pa_chunked_prefill_workspace_size() bytes. q/out fp16 or bf16 (else
+ * PA_ERR_DTYPE), head_dim 128 (else PA_ERR_UNSUPPORTED); chunks need a
+ * power-of-two GQA group up to 128 and scale > 0.
+ */
+int pa_chunked_prefill_fp8(const void* q, int32_t total_q, const int32_t* cu_q_lens, const void* k_cache,
+                           const void* v_cache, const float* kv_scales, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* ctx_lens, int32_t num_seqs, int32_t max_q_len,
+                           int32_t max_kv_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, int32_t num_blocks, float scale, void* out, void* workspace,
+                           size_t workspace_bytes, pa_dtype dtype, void* stream);
+
+/*
  * pa_selftest_bounded_wait — exercises the failure path every kernel relies
  * on: one warp waits on an mbarrier that nothing completes; the wait gives up
  * after limit_ns nanoseconds of device time (1 us .. 1 s, else PA_ERR_ARG),

@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     exported_symbols,
     load,
     pa_chunked_prefill,
+    pa_chunked_prefill_fp8,
     pa_chunked_prefill_workspace_size,
     pa_copy_blocks,
     pa_copy_blocks_fp8,
@@ -22,6 +23,7 @@ from ._binding import (  # noqa: F401
     pa_decode_noalloc_scratch_limit,
     pa_decode_partition_size,
     pa_decode_shared_prefix,
+    pa_decode_shared_prefix_fp8,
     pa_decode_step,
     pa_selftest_bounded_wait,
     pa_decode_step_shared_prefix,

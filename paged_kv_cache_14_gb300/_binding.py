@@ -28,7 +28,8 @@ EXPORTS = (
     "pa_chunked_prefill_workspace_size", "pa_chunked_prefill", "pa_decode_shared_prefix_workspace_size",
     "pa_decode_shared_prefix", "pa_decode_noalloc_scratch_limit", "pa_decode_noalloc",
     "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8", "pa_decode_fp8", "pa_swap_blocks",
-    "pa_decode_step_shared_prefix", "pa_decode_step", "pa_selftest_bounded_wait",
+    "pa_decode_step_shared_prefix", "pa_decode_step", "pa_selftest_bounded_wait", "pa_decode_shared_prefix_fp8",
+    "pa_chunked_prefill_fp8",
 )
 
 _i32, _i64, _f32, _vp, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
@@ -86,6 +87,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                                         _vp]),
         "pa_decode_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                          _i32, _f32, _vp, _i32, _vp, _sz, ctypes.c_int, _vp]),
+        "pa_decode_shared_prefix_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _vp, _vp,
+                                                       _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _i32, _vp,
+                                                       _sz, ctypes.c_int, _vp]),
+        "pa_chunked_prefill_fp8": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
+                                                  _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _sz, ctypes.c_int,
+                                                  _vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -421,6 +428,58 @@ def pa_decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         block_tables.shape[1], _cuda(seq_lens, "seq_lens", torch.int32), N, int(max_seq_len), hq, hkv, D, B, P,
         float(scale), _cuda(out, "out", dt), int(partition_size), ws_ptr, ws_bytes, _DT[dt], _stream(stream))
     _check(rc, "pa_decode_fp8")
+    return out
+
+
+def pa_decode_shared_prefix_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                kv_scales: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                                max_seq_len: int, group_starts: torch.Tensor, prefix_lens: torch.Tensor, scale: float,
+                                out: torch.Tensor | None = None, partition_size: int = 0,
+                                workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    N, hq, D = q.shape
+    P, hkv, B, _ = k_cache.shape
+    G = group_starts.shape[0] - 1
+    dt = q.dtype
+    if out is None:
+        out = torch.empty_like(q)
+    need = pa_decode_shared_prefix_workspace_size(N, hq, hkv, D, B, max_seq_len, partition_size, G)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load().pa_decode_shared_prefix_fp8(
+        _cuda(q, "q", dt), _cuda(k_cache, "k_cache", torch.uint8), _cuda(v_cache, "v_cache", torch.uint8),
+        _cuda(kv_scales, "kv_scales", torch.float32), _cuda(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _cuda(seq_lens, "seq_lens", torch.int32), N, int(max_seq_len),
+        _cuda(group_starts, "group_starts", torch.int32), _cuda(prefix_lens, "prefix_lens", torch.int32), G,
+        hq, hkv, D, B, P, float(scale), _cuda(out, "out", dt), int(partition_size), ws_ptr, ws_bytes, _DT[dt],
+        _stream(stream))
+    _check(rc, "pa_decode_shared_prefix_fp8")
+    return out
+
+
+def pa_chunked_prefill_fp8(q: torch.Tensor, cu_q_lens: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           kv_scales: torch.Tensor, block_tables: torch.Tensor, ctx_lens: torch.Tensor,
+                           max_q_len: int, max_kv_len: int, scale: float, out: torch.Tensor | None = None,
+                           workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    T, hq, D = q.shape
+    P, hkv, B, _ = k_cache.shape
+    n = ctx_lens.shape[0]
+    dt = q.dtype
+    if out is None:
+        out = torch.empty_like(q)
+    need = pa_chunked_prefill_workspace_size(n, hq, hkv, D, B, T, max_kv_len)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load().pa_chunked_prefill_fp8(
+        _cuda(q, "q", dt), T, _cuda(cu_q_lens, "cu_q_lens", torch.int32), _cuda(k_cache, "k_cache", torch.uint8),
+        _cuda(v_cache, "v_cache", torch.uint8), _cuda(kv_scales, "kv_scales", torch.float32),
+        _cuda(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _cuda(ctx_lens, "ctx_lens", torch.int32), n, int(max_q_len), int(max_kv_len), hq, hkv, D, B, P,
+        float(scale), _cuda(out, "out", dt), ws_ptr, ws_bytes, _DT[dt], _stream(stream))
+    _check(rc, "pa_chunked_prefill_fp8")
     return out
 
 

@@ -348,7 +348,7 @@ static int shared_prefix_decode(const void* q, const void* k_cache, const void* 
                             int32_t num_groups, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                             int32_t block_size, int32_t num_blocks, float scale, void* out, int32_t partition_size,
                             void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream,
-                            Between&& between) {
+                            const float* kv_scales, Between&& between) {
   if (num_seqs < 0 || num_groups < 0) return PA_ERR_ARG;
   if (num_seqs == 0) return between(false);
   if (num_groups < 1 || num_groups > num_seqs || !group_starts || !prefix_lens) return PA_ERR_ARG;
@@ -367,6 +367,8 @@ static int shared_prefix_decode(const void* q, const void* k_cache, const void* 
                           max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out,
                           partition_size, 1, workspace, workspace_bytes, dtype, &dp, &wl);
   if (rc != PA_OK) return rc;
+  if (kv_scales && !aligned16(kv_scales)) return PA_ERR_ALIGN;
+  dp.kv_scales = kv_scales;  // e4m3 cache (nullptr: the pools hold q's dtype)
   const CascadeWorkspace cw = cascade_workspace_layout(num_seqs, num_groups);
   uint8_t* cbase = static_cast<uint8_t*>(workspace) + wl.total;
   int32_t* prefix = reinterpret_cast<int32_t*>(cbase + cw.prefix);
@@ -413,6 +415,7 @@ static int shared_prefix_decode(const void* q, const void* k_cache, const void* 
   pp.part_ml = dp.part_ml;
   pp.max_parts = dp.max_parts;
   pp.status = dp.status;
+  pp.kv_scales = kv_scales;
   rc = launch_prefix_pass(pp, k_cache, v_cache, dtype, s);
   if (rc != PA_OK) return rc;
   // 3. Suffix decode (split-KV over the private keys) and the merge.
@@ -659,7 +662,21 @@ int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_ca
   return shared_prefix_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
                               group_starts, prefix_lens, num_groups, num_q_heads, num_kv_heads, head_dim, block_size,
                               num_blocks, scale, out, partition_size, workspace, workspace_bytes, dtype, stream,
-                              [](bool) { return PA_OK; });
+                              nullptr, [](bool) { return PA_OK; });
+}
+
+int pa_decode_shared_prefix_fp8(const void* q, const void* k_cache, const void* v_cache, const float* kv_scales,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                int32_t num_seqs, int32_t max_seq_len, const int32_t* group_starts,
+                                const int32_t* prefix_lens, int32_t num_groups, int32_t num_q_heads,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                float scale, void* out, int32_t partition_size, void* workspace,
+                                size_t workspace_bytes, pa_dtype dtype, void* stream) {
+  if (num_seqs > 0 && !kv_scales) return PA_ERR_ARG;
+  return shared_prefix_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                              group_starts, prefix_lens, num_groups, num_q_heads, num_kv_heads, head_dim, block_size,
+                              num_blocks, scale, out, partition_size, workspace, workspace_bytes, dtype, stream,
+                              kv_scales, [](bool) { return PA_OK; });
 }
 
 int pa_decode_step_shared_prefix(const int64_t* cow_pairs, int32_t num_cow_pairs, const int32_t* new_seq_ids,
@@ -687,7 +704,7 @@ int pa_decode_step_shared_prefix(const int64_t* cow_pairs, int32_t num_cow_pairs
   return shared_prefix_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
                               group_starts, prefix_lens, num_groups, num_q_heads, num_kv_heads, head_dim, block_size,
                               num_blocks, scale, out, partition_size, workspace, workspace_bytes, dtype, stream,
-                              cache_side);
+                              nullptr, cache_side);
 }
 
 int pa_decode_step(const int64_t* cow_pairs, int32_t num_cow_pairs, const int32_t* new_seq_ids,
@@ -730,12 +747,17 @@ size_t pa_chunked_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads, 
   return dec + (((size_t)16 + (size_t)(total_q > 0 ? total_q : 0) * 4 + 255) & ~size_t(255));
 }
 
-int pa_chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_lens, const void* k_cache,
-                       const void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
-                       const int32_t* ctx_lens, int32_t num_seqs, int32_t max_q_len, int32_t max_kv_len,
-                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                       int32_t num_blocks, float scale, void* out, void* workspace, size_t workspace_bytes,
-                       pa_dtype dtype, void* stream) {
+}  // extern "C"
+
+namespace pa {
+// Mixed batch (chunks and decode rows) over 16-bit pools, or over e4m3 pools
+// when kv_scales is given.
+static int chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_lens, const void* k_cache,
+                           const void* v_cache, const float* kv_scales, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* ctx_lens, int32_t num_seqs, int32_t max_q_len,
+                           int32_t max_kv_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, int32_t num_blocks, float scale, void* out, void* workspace,
+                           size_t workspace_bytes, pa_dtype dtype, void* stream) {
   if (num_seqs < 0 || max_q_len < 0 || max_kv_len < 0 || total_q < 0) return PA_ERR_ARG;
   if (num_seqs == 0 || max_q_len == 0 || total_q == 0) return PA_OK;
   if (!cu_q_lens || !ctx_lens) return PA_ERR_ARG;
@@ -762,6 +784,10 @@ int pa_chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_lens,
                           max_kv_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out, 0, 0,
                           workspace, dec_ws, dtype, &dp, &wl);
   if (rc != PA_OK) return rc;
+  if (kv_scales) {
+    if (!aligned16(kv_scales)) return PA_ERR_ALIGN;
+    dp.kv_scales = kv_scales;
+  }
   if (max_q_len <= 1) return launch_decode(dp, dtype, s);
   // Chunks (q_len > 1): tcgen05 tiles. One plan lists the chunk items and
   // the decode rows' partitions and splits the SMs between them; the chunk
@@ -790,11 +816,40 @@ int pa_chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_lens,
   p.status = dp.status;
   p.decode_token_bytes = 2 * num_kv_heads * head_dim * elem_bytes(dtype);
   p.decode_bytes_per_tile = kDecodeBytesPerChunkTile;
+  p.kv_scales = kv_scales;
   rc = launch_prefill(p, k_cache, v_cache, dtype, s, &dp);
   if (rc != PA_OK) return rc;
   dp.planned = 1;
   dp.beside = 1;
   return launch_decode(dp, dtype, s);
+}
+}  // namespace pa
+
+extern "C" {
+
+int pa_chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_lens, const void* k_cache,
+                       const void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* ctx_lens, int32_t num_seqs, int32_t max_q_len, int32_t max_kv_len,
+                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                       int32_t num_blocks, float scale, void* out, void* workspace, size_t workspace_bytes,
+                       pa_dtype dtype, void* stream) {
+  return chunked_prefill(q, total_q, cu_q_lens, k_cache, v_cache, nullptr, block_tables, max_blocks_per_seq,
+                         ctx_lens, num_seqs, max_q_len, max_kv_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                         num_blocks, scale, out, workspace, workspace_bytes, dtype, stream);
+}
+
+int pa_chunked_prefill_fp8(const void* q, int32_t total_q, const int32_t* cu_q_lens, const void* k_cache,
+                           const void* v_cache, const float* kv_scales, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* ctx_lens, int32_t num_seqs, int32_t max_q_len,
+                           int32_t max_kv_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, int32_t num_blocks, float scale, void* out, void* workspace,
+                           size_t workspace_bytes, pa_dtype dtype, void* stream) {
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (num_seqs > 0 && total_q > 0 && !kv_scales) return PA_ERR_ARG;
+  return chunked_prefill(q, total_q, cu_q_lens, k_cache, v_cache, kv_scales, block_tables, max_blocks_per_seq,
+                         ctx_lens, num_seqs, max_q_len, max_kv_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                         num_blocks, scale, out, workspace, workspace_bytes, dtype, stream);
 }
 
 }  // extern "C"

@@ -55,16 +55,6 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
   return d;
 }
 
-// Four e4m3 codes (byte 0 first) to two fp16 pairs: lo <- bytes 0, 1 and
-// hi <- bytes 2, 3 (low half first); exact.
-__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t codes, uint32_t& lo, uint32_t& hi) {
-  asm("{\n\t.reg .b16 a, b;\n\t"
-      "mov.b32 {a, b}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(codes));
-}
 
 
 

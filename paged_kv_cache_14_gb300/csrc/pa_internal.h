@@ -117,6 +117,9 @@ struct PrefillParams {
   // and the SM-time of one chunk (item, KV tile) unit in decode KV bytes.
   int32_t decode_token_bytes;
   float decode_bytes_per_tile;
+  // e4m3 cache: (K, V) scale per (block, KV head), float32
+  // [num_blocks][num_kv_heads][2]; nullptr when the pools hold q's dtype.
+  const float* kv_scales;
   // Prefix pass of shared-prefix decode (null for chunked prefill): rows are
   // (group member, GQA head); keys are the group's shared blocks, read
   // through the table of the member with the longest verified prefix; the

@@ -79,9 +79,22 @@ constexpr int kBarVEmpty = kBarVFull + NV;
 constexpr int kBarSFull = kBarVEmpty + NV;
 constexpr int kBarPFull = kBarSFull + kQT;
 constexpr int kBarODone = kBarPFull + kQT;
-constexpr int kNumBars = kBarODone + kQT;
+// e4m3 cache only: codes of K / V landed in a stage (TMA), Q tiles moved
+// into fp16 (converter warps).
+constexpr int kBarKCode = kBarODone + kQT;
+constexpr int kBarVCode = kBarKCode + NK;
+constexpr int kBarQConv = kBarVCode + NV;
+constexpr int kNumBars = kBarQConv + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, item, abort
-constexpr int kSmem = kOffMisc + 64;
+constexpr int kOffQExp = kOffMisc + 64;           // e4m3: per-row exponent of the fp16 Q rows [kQT][kM]
+constexpr int kSmem = kOffQExp + kQT * kM * 4;
+// e4m3 cache: one more warp widens the codes of each K / V stage (TMA puts
+// them in the upper half of the stage) into the 16-bit stage layout, and
+// moves a bf16 Q tile into fp16.
+constexpr int kConvWarp0 = kSoftmaxWarp0 + 4 * kQT;
+constexpr int kConvWarps = 1;
+template <bool KV8>
+__host__ __device__ constexpr int threads() { return kThreads + (KV8 ? 32 * kConvWarps : 0); }
 static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
 // Tensor memory, per Q tile t: S (kN fp32 columns; P, 16-bit pairs, over its
 // first kN/2) at t * 256, O (128 fp32 columns) at t * 256 + 128.
@@ -230,12 +243,24 @@ __global__ void __launch_bounds__(1024) mixed_plan_kernel(const PrefillParams p,
 // Every barrier completes once per KV tile (s_full, p_full, stages) or once
 // per item (q_full, o_done), those of Q tile 1 only on items whose second
 // tile has rows, and is waited on in phase order.
-template <typename T, int BS, bool PREFIX>
-__global__ void __launch_bounds__(pf::kThreads, 1)
+//
+// KV8 (e4m3 cache, kv_scales given): the producer loads each 16-token
+// sub-tile's codes into the upper half of its 16-bit stage; two converter
+// warps widen them (exactly) to fp16 in the stage's swizzled layout and
+// complete k_full / v_full. The MMAs run in fp16: a bf16 Q tile is moved into
+// fp16 in place once per item, each row by its own power of two. The softmax
+// multiplies a score by the K scale of its key's block (and the Q row's power
+// of two) before the max, and weights P by the V scale of the key's block
+// times 2^kap, kap the largest exponent keeping every weight of the item
+// seen so far below 2^7 (P stays below 2^15 in fp16); O is rescaled exactly
+// when kap drops and divided by 2^kap at the end. The row sum takes p alone.
+template <typename T, int BS, bool PREFIX, bool KV8>
+__global__ void __launch_bounds__(pf::threads<KV8>(), 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
   using namespace pf;
-  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value && !KV8;  // the MMA's 16-bit type
+  using MT = typename std::conditional<KV8, __half, T>::type;             // P's 16-bit type
   constexpr uint32_t kIdescS = idesc_f16(kM, kN, kBf16, false);  // S = Q K^T
   constexpr uint32_t kIdescO = idesc_f16(kM, kD, kBf16, true);   // O += P V (V MN-major)
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -256,14 +281,19 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   if (threadIdx.x == 0) {
     if ((sbase & 1023u) != 0) record_error(p.status, PA_ERR_ALIGN);
     mbar_init(b_q, 1);
+    // A K / V stage is complete once its copies landed or, with an e4m3
+    // cache, once both converter warps widened it.
     for (int i = 0; i < NK; ++i) {
-      mbar_init(b_kfull0 + 8 * i, 1);
+      mbar_init(b_kfull0 + 8 * i, KV8 ? kConvWarps : 1);
       mbar_init(b_kempty0 + 8 * i, 1);
+      mbar_init(smem_u32(&bars[kBarKCode + i]), 1);
     }
     for (int i = 0; i < NV; ++i) {
-      mbar_init(b_vfull0 + 8 * i, 1);
+      mbar_init(b_vfull0 + 8 * i, KV8 ? kConvWarps : 1);
       mbar_init(b_vempty0 + 8 * i, 1);
+      mbar_init(smem_u32(&bars[kBarVCode + i]), 1);
     }
+    mbar_init(smem_u32(&bars[kBarQConv]), kConvWarps);
     for (int i = 0; i < kQT; ++i) {
       mbar_init(b_sfull0 + 8 * i, 1);
       mbar_init(b_pfull0 + 8 * i, 4);  // one arrival per softmax warp
@@ -387,20 +417,29 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const int g = tile_base + x;
         const int ns = is_v ? NV : NK;
         const int st = g % ns;
-        const uint32_t b_full = (is_v ? b_vfull0 : b_kfull0) + 8 * st;
+        // e4m3: the copies complete the stage's code barrier; the converter
+        // warps complete its full barrier.
+        const uint32_t b_full = KV8 ? smem_u32(&bars[(is_v ? kBarVCode : kBarKCode) + st])
+                                    : (is_v ? b_vfull0 : b_kfull0) + 8 * st;
         const uint32_t b_empty = (is_v ? b_vempty0 : b_kempty0) + 8 * st;
         const int id = id_of(x);
         if (lane == 0) {
           if (g >= ns && !mbar_wait(b_empty, ((g / ns) & 1) ^ 1, p.status)) bad = true;
-          else mbar_arrive_expect_tx(b_full, kKBytes);
+          else mbar_arrive_expect_tx(b_full, KV8 ? kKVHalf : kKBytes);
         }
         bad = __shfl_sync(0xffffffffu, bad, 0);
         if (bad) return;
         if (lane < kSubTiles) {
-          const uint32_t dst = sbase + (is_v ? kOffV : kOffK) + st * kKBytes + lane * 2048;
           const int row = (id * p.num_kv_heads + kvh) * BS + ((x * kN + lane * 16) % BS);
+          if constexpr (KV8) {
+            // 16 tokens x 128 one-byte codes (2 KB) into the stage's upper half.
+            const uint32_t dst = sbase + (is_v ? kOffV : kOffK) + st * kKBytes + kKVHalf + lane * 2048;
+            tma_load_2d(dst, is_v ? &vmap : &kmap, 0, row, b_full);
+          } else {
+            const uint32_t dst = sbase + (is_v ? kOffV : kOffK) + st * kKBytes + lane * 2048;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) tma_load_2d(dst + h * kKVHalf, is_v ? &vmap : &kmap, h * 64, row, b_full);
+            for (int h = 0; h < 2; ++h) tma_load_2d(dst + h * kKVHalf, is_v ? &vmap : &kmap, h * 64, row, b_full);
+          }
         }
         if (is_v) v_issued = x + 1;
         else k_issued = x + 1;
@@ -419,16 +458,19 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         // Let the copies already issued land before the CTA moves on.
         if (lane == 0) {
           mbar_wait(b_q, it & 1, nullptr);
+          const uint32_t kb0 = KV8 ? smem_u32(&bars[kBarKCode]) : b_kfull0;
+          const uint32_t vb0 = KV8 ? smem_u32(&bars[kBarVCode]) : b_vfull0;
           for (int jj = max(0, k_issued - NK); jj < k_issued; ++jj)
-            mbar_wait(b_kfull0 + 8 * ((tile_base + jj) % NK), ((tile_base + jj) / NK) & 1, nullptr);
+            mbar_wait(kb0 + 8 * ((tile_base + jj) % NK), ((tile_base + jj) / NK) & 1, nullptr);
           for (int jj = max(0, v_issued - NV); jj < v_issued; ++jj)
-            mbar_wait(b_vfull0 + 8 * ((tile_base + jj) % NV), ((tile_base + jj) / NV) & 1, nullptr);
+            mbar_wait(vb0 + 8 * ((tile_base + jj) % NV), ((tile_base + jj) / NV) & 1, nullptr);
         }
       }
     } else if (warp == 1) {
       // ============================= MMA =============================
       if (lane == 0) {
-        bool bad = !mbar_wait(b_q, it & 1, p.status);
+        // e4m3: the converter warps complete q_conv once the Q tiles are in fp16.
+        bool bad = !mbar_wait(KV8 ? smem_u32(&bars[kBarQConv]) : b_q, it & 1, p.status);
         uint32_t last_bar = 0, last_phase = 0;  // the last commit: it covers every MMA issued before it
         // Shared-memory descriptors differ only in the start-address field
         // (address >> 4, 14 bits; every operand lies below 256 KB), so each is
@@ -506,6 +548,92 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         }
       }
       __syncwarp();
+    } else if (KV8 && warp >= kConvWarp0) {
+      // ========================== converters ==========================
+      if constexpr (KV8) {
+        const int ct = threadIdx.x - 32 * kConvWarp0;  // lane of the converter warp(s)
+        bool bad = !mbar_wait(b_q, it & 1, p.status);
+        if (!bad && std::is_same<T, __nv_bfloat16>::value) {
+          // bf16 Q rows into fp16 in place: x * 2^-e, e from the row's
+          // largest magnitude (amax * 2^-e in [2^14, 2^15)), so every element
+          // within 2^24 of the row's largest is an exact fp16 normal value.
+          int* qexp = reinterpret_cast<int*>(smem + kOffQExp);
+          for (int rr = ct; rr < nq * kM; rr += 32 * kConvWarps) {
+            const int t = rr / kM, r = rr % kM;
+            uint8_t* rb = smem + kOffQ + t * kQBytes + r * 128;
+            auto chunk = [&](int c) -> uint4* {  // 16-byte chunk c (8 elements) of the row
+              return reinterpret_cast<uint4*>(rb + (c >> 3) * kQHalf + (((c & 7) ^ (r & 7)) << 4));
+            };
+            float amax = 0.f;
+#pragma unroll 4
+            for (int c = 0; c < 16; ++c) {
+              const uint4 raw = *chunk(c);
+              const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                amax = fmax3(amax, fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+            }
+            int ex = 0;
+            frexpf(amax, &ex);
+            const int sh = amax > 0.f ? ex - 15 : 0;
+            const float mul = ldexpf(1.f, -sh);
+#pragma unroll 4
+            for (int c = 0; c < 16; ++c) {
+              const uint4 raw = *chunk(c);
+              uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                w[i] = MmaOp<__half>::pack(__uint_as_float(w[i] << 16) * mul, __uint_as_float(w[i] & 0xffff0000u) * mul);
+              *chunk(c) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            qexp[t * kM + r] = sh;
+          }
+        }
+        fence_async_shared();  // the MMAs read Q through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars[kBarQConv]));
+        // K then V of every tile: wait for its codes, widen them in place,
+        // one row per lane at a time. The codes of a row sit exactly where
+        // the widened upper half (head_dim 64..127) of that same row goes, so
+        // reading the whole row before writing it is all the ordering needed.
+        for (int j = 0; j < ntiles && !bad; ++j) {
+          const int g = tile_base + j;
+#pragma unroll 1
+          for (int kv = 0; kv < 2; ++kv) {
+            const int ns = kv ? NV : NK, st = g % ns;
+            if (!mbar_wait(smem_u32(&bars[(kv ? kBarVCode : kBarKCode) + st]), (g / ns) & 1, p.status)) {
+              bad = true;
+              break;
+            }
+            uint8_t* base = smem + (kv ? kOffV : kOffK) + st * kKBytes;
+#pragma unroll 2
+            for (int r = ct; r < kN; r += 32 * kConvWarps) {
+              uint4 cr[8];
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                cr[c] = *reinterpret_cast<const uint4*>(base + kKVHalf + r * 128 + ((c ^ (r & 7)) << 4));
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                // Codes of head_dim 16c .. 16c + 15 -> two 16-byte chunks of
+                // 16-bit values in half c / 4 of the row.
+                uint32_t o[8];
+                e4m3x4_to_f16x4(cr[c].x, o[0], o[1]);
+                e4m3x4_to_f16x4(cr[c].y, o[2], o[3]);
+                e4m3x4_to_f16x4(cr[c].z, o[4], o[5]);
+                e4m3x4_to_f16x4(cr[c].w, o[6], o[7]);
+                uint8_t* rb = base + (c >> 2) * kKVHalf + r * 128;
+                const int cc = 2 * (c & 3);
+                *reinterpret_cast<uint4*>(rb + ((cc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4*>(rb + (((cc + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+              }
+            }
+            fence_async_shared();  // the MMAs read the stage through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive((kv ? b_vfull0 : b_kfull0) + 8 * st);
+          }
+        }
+        if (bad) abort_flag[0] = 1;
+      }
     } else {
       // =========================== softmax ===========================
       const int t = (warp - kSoftmaxWarp0) >> 2;  // Q tile of this warpgroup
@@ -522,101 +650,219 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       } else {
         lim = pos < m_hi ? p.prefix[s0 + pos] - 1 : -1;
       }
-      const float sl2 = p.scale_log2;
+      // e4m3: scores are scaled to log2 units before the max (sl2 then 1).
+      const float sl2 = KV8 ? 1.f : p.scale_log2;
       float m = -CUDART_INF_F, l = 0.f;
       bool bad = false;
       const bool live = t < nq;  // warpgroup 0 always: it also zeroes V rows past the keys
       const int ph0 = t == 0 ? tile_base : tile_base1;  // phase base of this tile's s_full / p_full
-      for (int j = 0; j < ntiles && live; ++j) {
+      // e4m3: rf = log2(e) * scale * 2^(this row's Q exponent); kap / pw =
+      // 2^kap weight the V scales (see the kernel comment).
+      float rf = p.scale_log2;
+      constexpr int kKapUnset = 1 << 20;
+      int kap = kKapUnset;
+      float pw = 1.f;
+      const int32_t* btab = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
+      auto load_scales = [&](int jj) -> float2 {
+        float2 r = make_float2(0.f, 0.f);
+        if constexpr (KV8) {
+          if (lane < kSubTiles && jj < ntiles) {
+            const int bi = (jj * kN + lane * 16) / BS;
+            if (bi < nblk_seq) {
+              const int id = btab[bi];
+              if (id >= 0 && id < p.num_blocks)
+                r = __ldg(reinterpret_cast<const float2*>(p.kv_scales) + (int64_t)id * p.num_kv_heads + kvh);
+            }
+          }
+        }
+        return r;
+      };
+      if constexpr (KV8) {
+        if (live) {
+          if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+            if (!mbar_wait(smem_u32(&bars[kBarQConv]), it & 1, p.status)) bad = true;
+            rf = ldexpf(p.scale_log2, reinterpret_cast<const int*>(smem + kOffQExp)[t * kM + row]);
+          }
+        }
+      }
+      for (int j = 0; j < ntiles && live && !bad; ++j) {
         const int g = tile_base + j;
+        // e4m3: lane u < kSubTiles holds the (K, V) scale of sub-tile u;
+        // every thread takes sub-tile u's score factor s_K(u) * rf and V
+        // weight s_V(u) * 2^kap from it with a shuffle where it needs them.
+        float2 csc = make_float2(0.f, 0.f);
+        float kap_r = 1.f;    // e4m3: 2^(new kap - old kap) when kap dropped
+        if constexpr (KV8) {
+          // Requested before the wait for S, which covers their latency.
+          csc = load_scales(j);
+          float vmax = lane < kSubTiles ? csc.y : 0.f;
+          vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
+          vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
+          vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 4));
+          vmax = __shfl_sync(0xffffffffu, vmax, 0);  // lanes 0..7 hold the max: the same in every lane
+          if (vmax > 0.f) {
+            // vmax in [2^(ex-1), 2^ex) (a subnormal counts as ex = -126):
+            // kap = 7 - ex keeps vmax * 2^kap below 2^7.
+            const int ex = (int)((__float_as_uint(vmax) >> 23) & 0xffu) - 126;
+            const int kmax = min(7 - ex, 127);
+            if (kmax < kap) {
+              if (kap != kKapUnset) kap_r = __uint_as_float((uint32_t)(max(kmax - kap, -126) + 127) << 23);
+              kap = kmax;
+              pw = __uint_as_float((uint32_t)(kmax + 127) << 23);
+            }
+          }
+        }
         if (!mbar_wait(b_sfull, (ph0 + j) & 1, p.status)) { bad = true; break; }
         tc_fence_after();
-        uint32_t sr[kN / 32][32];
-#pragma unroll
-        for (int h = 0; h < kN / 32; ++h) tmem_ld32(ts + h * 32, sr[h]);
-        tmem_ld_wait();
         const int k0 = j * kN;
-        // Raw-score row max (scale > 0 keeps the order); the causal / prefix
-        // mask is skipped when the whole tile is visible to every row of the warp.
+        // The causal / prefix mask is skipped when the whole tile is visible
+        // to every row of the warp.
         const bool full_vis = __all_sync(0xffffffffu, k0 + kN - 1 <= lim);
-        if (!full_vis) {
+        // Exponentials are taken against m. It only moves up when the row max
+        // exceeds it by more than 2^8 in probability (then O and l are
+        // rescaled); below that, p <= 256 stays exact enough in fp32 and
+        // representable in the 16-bit P tile, and O / l is unchanged.
+        float alpha = 1.f;
+        auto update_max = [&](float mx) {
+          if (m == -CUDART_INF_F) {
+            m = mx;  // first keys of this row (still -inf for a row without keys)
+          } else if ((mx - m) * sl2 > 8.f) {
+            alpha = fast_exp2((m - mx) * sl2);
+            m = mx;
+          }
+        };
+        // Keys past the sequence end carry p = 0, but their V slots may hold
+        // any bits (NaN included): zero those V rows before PV reads them
+        // (warpgroup 0 does it before its p_full; PV1 is issued after PV0,
+        // which waits for that). False if the wait for V ran out.
+        auto zero_v_tail = [&]() -> bool {
+          if (t == 0 && k0 + kN > kv_len) {
+            const int sv = g % NV;
+            if (!mbar_wait(b_vfull0 + 8 * sv, (g / NV) & 1, p.status)) return false;
+            uint8_t* vst = smem + kOffV + sv * kKBytes;
+            const int first = max(kv_len - k0, 0);
+            for (int idx = threadIdx.x - 32 * kSoftmaxWarp0 - 128 * t; idx < (kN - first) * 16; idx += 128) {
+              const int r = first + idx / 16, c = idx % 16;  // row, 16-byte chunk over both halves
+              *reinterpret_cast<int4*>(vst + (c >> 3) * kKVHalf + r * 128 + (c & 7) * 16) = make_int4(0, 0, 0, 0);
+            }
+            fence_async_shared();
+          }
+          return true;
+        };
+        // Rescale the O row (warp-uniform), before PV of this tile
+        // accumulates. PV_t of the previous tile has completed: its commit
+        // preceded S_t(g)'s.
+        auto rescale_o = [&](float f) {
+#pragma unroll 1
+          for (int cc = 0; cc < kD / 16; ++cc) {
+            uint32_t orow[16];
+            tmem_ld16(to + cc * 16, orow);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 16; ++c) orow[c] = __float_as_uint(__uint_as_float(orow[c]) * f);
+            tmem_st16(to + cc * 16, orow);
+          }
+        };
+        uint64_t rs2 = f2_pack(0.f, 0.f);
+        if constexpr (!KV8) {
+          uint32_t sr[kN / 32][32];
+#pragma unroll
+          for (int h = 0; h < kN / 32; ++h) tmem_ld32(ts + h * 32, sr[h]);
+          tmem_ld_wait();
+          // Raw-score row max (scale > 0 keeps the order).
+          if (!full_vis) {
+#pragma unroll
+            for (int h = 0; h < kN / 32; ++h)
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const int key = k0 + h * 32 + c;
+                if (key > lim) sr[h][c] = __float_as_uint(-CUDART_INF_F);
+              }
+          }
+          float mx = -CUDART_INF_F;
 #pragma unroll
           for (int h = 0; h < kN / 32; ++h)
 #pragma unroll
+            for (int c = 0; c < 32; c += 2) mx = fmax3(mx, __uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1]));
+          update_max(mx);
+          if (!zero_v_tail()) { bad = true; break; }
+          const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+          const float neg = m == -CUDART_INF_F ? 0.f : -m * sl2;
+          // p = 2^(s * scale * log2(e) - m * scale * log2(e)), two keys per
+          // paired FMA; the row sum accumulates in pairs. P goes to tensor
+          // memory 64 keys (32 columns) at a time.
+          const uint64_t sl2x2 = f2_pack(sl2, sl2), negx2 = f2_pack(neg, neg);
+#pragma unroll
+          for (int hh = 0; hh < kN / 64; ++hh) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+              for (int c = 0; c < 32; c += 2) {
+                const int h = hh * 2 + h2;
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1])), sl2x2, negx2),
+                          x0, x1);
+                const float a = fast_exp2(x0), b = fast_exp2(x1);
+                rs2 = f2_add(rs2, f2_pack(a, b));
+                pk[h2 * 16 + c / 2] = MmaOp<T>::pack(a, b);
+              }
+            // (here, once half of the scores are dead, to keep registers free)
+            if (hh == 0 && rescale) rescale_o(alpha);
+            tmem_st32(ts + hh * 32, pk);
+          }
+        } else {
+          // e4m3: two passes over the S row in tensor memory, 32 keys at a
+          // time, so only 32 scores are held in registers. A score is
+          // s * s_K(block) * rf (log2 units). Pass 1: the row max. Pass 2:
+          // p, the row sum, and P = p * s_V(block) * 2^kap over the S columns
+          // already read (P of keys 32h.. goes to columns 16h..).
+          auto scaled = [&](uint32_t (&v)[32], int h) {
+            tmem_ld32(ts + h * 32, v);
+            tmem_ld_wait();
+            const float f0 = __shfl_sync(0xffffffffu, csc.x, 2 * h) * rf;
+            const float f1 = __shfl_sync(0xffffffffu, csc.x, 2 * h + 1) * rf;
+#pragma unroll
             for (int c = 0; c < 32; ++c) {
               const int key = k0 + h * 32 + c;
-              if (key > lim) sr[h][c] = __float_as_uint(-CUDART_INF_F);
+              const float x = __uint_as_float(v[c]) * (c < 16 ? f0 : f1);
+              v[c] = __float_as_uint(!full_vis && key > lim ? -CUDART_INF_F : x);
             }
-        }
-        float mx = -CUDART_INF_F;
+          };
+          float mx = -CUDART_INF_F;
+#pragma unroll 1
+          for (int h = 0; h < kN / 32; ++h) {
+            uint32_t v[32];
+            scaled(v, h);
 #pragma unroll
-        for (int h = 0; h < kN / 32; ++h)
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) mx = fmax3(mx, __uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1]));
-        // Exponentials are taken against m (raw units). It only moves up when
-        // the row max exceeds it by more than 2^8 in probability (then O and l
-        // are rescaled); below that, p <= 256 stays exact enough in fp32 and
-        // representable in the 16-bit P tile, and O / l is unchanged.
-        float alpha = 1.f;
-        if (m == -CUDART_INF_F) {
-          m = mx;  // first keys of this row (still -inf for a row without keys)
-        } else if ((mx - m) * sl2 > 8.f) {
-          alpha = fast_exp2((m - mx) * sl2);
-          m = mx;
-        }
-        if (t == 0 && k0 + kN > kv_len) {
-          // Keys past the sequence end carry p = 0, but their V slots may
-          // hold any bits (NaN included): zero those V rows before PV reads
-          // them (warpgroup 0 does it before its p_full; PV1 is issued
-          // after PV0, which waits for that).
-          const int sv = g % NV;
-          if (!mbar_wait(b_vfull0 + 8 * sv, (g / NV) & 1, p.status)) { bad = true; break; }
-          uint8_t* vst = smem + kOffV + sv * kKBytes;
-          const int first = max(kv_len - k0, 0);
-          for (int idx = threadIdx.x - 32 * kSoftmaxWarp0 - 128 * t; idx < (kN - first) * 16; idx += 128) {
-            const int r = first + idx / 16, c = idx % 16;  // row, 16-byte chunk over both halves
-            *reinterpret_cast<int4*>(vst + (c >> 3) * kKVHalf + r * 128 + (c & 7) * 16) = make_int4(0, 0, 0, 0);
+            for (int c = 0; c < 32; c += 2) mx = fmax3(mx, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
           }
-          fence_async_shared();
-        }
-        const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
-        const float neg = m == -CUDART_INF_F ? 0.f : -m * sl2;
-        // p = 2^(s * scale * log2(e) - m * scale * log2(e)), two keys per
-        // paired FMA; the row sum accumulates in pairs. P goes to tensor
-        // memory 64 keys (32 columns) at a time.
-        const uint64_t sl2x2 = f2_pack(sl2, sl2), negx2 = f2_pack(neg, neg);
-        uint64_t rs2 = f2_pack(0.f, 0.f);
-#pragma unroll
-        for (int hh = 0; hh < kN / 64; ++hh) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2)
+          update_max(mx);
+          if (!zero_v_tail()) { bad = true; break; }
+          // O takes alpha and the drop of kap; l takes alpha alone.
+          const float oalpha = alpha * kap_r;
+          const bool rescale = j > 0 && __any_sync(0xffffffffu, oalpha != 1.f);
+          const float neg = m == -CUDART_INF_F ? 0.f : -m;
+          const uint64_t onex2 = f2_pack(1.f, 1.f), negx2 = f2_pack(neg, neg);
+#pragma unroll 1
+          for (int h = 0; h < kN / 32; ++h) {
+            uint32_t v[32];
+            scaled(v, h);
+            const float fv0 = __shfl_sync(0xffffffffu, csc.y, 2 * h) * pw;
+            const float fv1 = __shfl_sync(0xffffffffu, csc.y, 2 * h + 1) * pw;
+            uint32_t pk[16];
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
-              const int h = hh * 2 + h2;
               float x0, x1;
-              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1])), sl2x2, negx2), x0,
-                        x1);
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), onex2, negx2), x0, x1);
               const float a = fast_exp2(x0), b = fast_exp2(x1);
               rs2 = f2_add(rs2, f2_pack(a, b));
-              pk[h2 * 16 + c / 2] = MmaOp<T>::pack(a, b);
+              const float f = c < 16 ? fv0 : fv1;
+              pk[c / 2] = MmaOp<MT>::pack(a * f, b * f);
             }
-          if (hh == 0 && rescale) {
-            // Rescale the O row when the running max moved (warp-uniform),
-            // before PV of this tile accumulates (here, once half of the
-            // scores are dead, to keep registers free). PV_t of the previous
-            // tile has completed: its commit preceded S_t(g)'s.
-#pragma unroll 1
-            for (int cc = 0; cc < kD / 16; ++cc) {
-              uint32_t orow[16];
-              tmem_ld16(to + cc * 16, orow);
-              tmem_ld_wait();
-#pragma unroll
-              for (int c = 0; c < 16; ++c) orow[c] = __float_as_uint(__uint_as_float(orow[c]) * alpha);
-              tmem_st16(to + cc * 16, orow);
-            }
+            if (h == 1 && rescale) rescale_o(oalpha);
+            tmem_st16(ts + h * 16, pk);
           }
-          tmem_st32(ts + hh * 32, pk);
         }
         float rs0, rs1;
         f2_unpack(rs2, rs0, rs1);
@@ -630,7 +876,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       } else if (!bad && mbar_wait(b_odone, (t == 0 ? it : items1) & 1, p.status)) {
         tc_fence_after();
         if constexpr (!PREFIX) {
-          const float inv = 1.f / l;
+          const float inv = 1.f / (l * pw);  // pw = 2^kap with an e4m3 cache, else 1
           T* orow = static_cast<T*>(p.out) + ((int64_t)(q0 + pos) * p.num_q_heads + kvh * G + head) * kD;
           const bool valid = pos < ql;
 #pragma unroll
@@ -652,6 +898,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           // member's partials.
           const bool valid = lim >= 0;
           const int64_t base = ((int64_t)(s0 + pos) * p.num_q_heads + kvh * G + head) * p.max_parts;
+          const float ipw = 1.f / pw;  // exact: a power of two
 #pragma unroll
           for (int cc = 0; cc < kD / 32; ++cc) {
             uint32_t ov[32];
@@ -661,8 +908,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
 #pragma unroll
               for (int c = 0; c < 32; c += 4)
                 __stcg(reinterpret_cast<float4*>(p.part_o + base * kD + cc * 32 + c),
-                       make_float4(__uint_as_float(ov[c]), __uint_as_float(ov[c + 1]), __uint_as_float(ov[c + 2]),
-                                   __uint_as_float(ov[c + 3])));
+                       make_float4(__uint_as_float(ov[c]) * ipw, __uint_as_float(ov[c + 1]) * ipw,
+                                   __uint_as_float(ov[c + 2]) * ipw, __uint_as_float(ov[c + 3]) * ipw));
             }
           }
           if (valid) __stcg(reinterpret_cast<float2*>(p.part_ml + base * 2), make_float2(m * sl2, l));
@@ -686,25 +933,45 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <typename T, int BS, bool PREFIX>
+template <typename T, int BS, bool PREFIX, bool KV8>
 static int launch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                  const PrefillParams& p, int ctas, cudaStream_t stream) {
-  auto kern = prefill_tc_kernel<T, BS, PREFIX>;
+  auto kern = prefill_tc_kernel<T, BS, PREFIX, KV8>;
   if (set_max_dynamic_smem(reinterpret_cast<const void*>(kern), pf::kSmem) != PA_OK) return PA_ERR_CUDA;
-  return launch_dependent(kern, dim3(ctas), dim3(pf::kThreads), pf::kSmem, stream, qmap, kmap, vmap, p) == cudaSuccess
+  return launch_dependent(kern, dim3(ctas), dim3(pf::threads<KV8>()), pf::kSmem, stream, qmap, kmap, vmap, p) ==
+                 cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
+}
+
+template <bool PREFIX, bool KV8>
+static int dispatch_prefill_bs(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                               const PrefillParams& p, int ctas, pa_dtype dt, cudaStream_t stream) {
+  const bool bf = dt == PA_BF16;
+  if (p.block_size == 16)
+    return bf ? launch_prefill_kernel<__nv_bfloat16, 16, PREFIX, KV8>(qmap, kmap, vmap, p, ctas, stream)
+              : launch_prefill_kernel<__half, 16, PREFIX, KV8>(qmap, kmap, vmap, p, ctas, stream);
+  return bf ? launch_prefill_kernel<__nv_bfloat16, 32, PREFIX, KV8>(qmap, kmap, vmap, p, ctas, stream)
+            : launch_prefill_kernel<__half, 32, PREFIX, KV8>(qmap, kmap, vmap, p, ctas, stream);
 }
 
 template <bool PREFIX>
 static int dispatch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                    const PrefillParams& p, int ctas, pa_dtype dt, cudaStream_t stream) {
-  const bool bf = dt == PA_BF16;
-  if (p.block_size == 16)
-    return bf ? launch_prefill_kernel<__nv_bfloat16, 16, PREFIX>(qmap, kmap, vmap, p, ctas, stream)
-              : launch_prefill_kernel<__half, 16, PREFIX>(qmap, kmap, vmap, p, ctas, stream);
-  return bf ? launch_prefill_kernel<__nv_bfloat16, 32, PREFIX>(qmap, kmap, vmap, p, ctas, stream)
-            : launch_prefill_kernel<__half, 32, PREFIX>(qmap, kmap, vmap, p, ctas, stream);
+  return p.kv_scales ? dispatch_prefill_bs<PREFIX, true>(qmap, kmap, vmap, p, ctas, dt, stream)
+                     : dispatch_prefill_bs<PREFIX, false>(qmap, kmap, vmap, p, ctas, dt, stream);
+}
+
+// Tensor maps of the pools: 16-token sub-tiles of 128 16-bit columns (two
+// 64-column boxes), or of 128 e4m3 codes (one 128-byte box).
+static int make_pool_maps(const PrefillParams& p, const void* k_cache, const void* v_cache, pa_dtype dt,
+                          CUtensorMap* kmap, CUtensorMap* vmap) {
+  const int64_t rows = (int64_t)p.num_blocks * p.num_kv_heads * p.block_size;
+  int rc = p.kv_scales ? make_u8_tensor_map(kmap, k_cache, rows, pf::kD, 16)
+                       : make_kv_tensor_map(kmap, k_cache, rows, pf::kD, dt, 16);
+  if (rc != PA_OK) return rc;
+  return p.kv_scales ? make_u8_tensor_map(vmap, v_cache, rows, pf::kD, 16)
+                     : make_kv_tensor_map(vmap, v_cache, rows, pf::kD, dt, 16);
 }
 
 int launch_prefill(const PrefillParams& p0, const void* k_cache, const void* v_cache, pa_dtype dt,
@@ -720,10 +987,7 @@ int launch_prefill(const PrefillParams& p0, const void* k_cache, const void* v_c
     // q seen as [total_q][num_q_heads][head_dim]; box = 64 columns x G heads x 128/G positions.
     int rc = make_3d_tensor_map(&qmap, p.q, p.total_q, p.num_q_heads, pf::kD, dt, pf::kM / p.group, p.group, 64);
     if (rc != PA_OK) return rc;
-    const int64_t rows = (int64_t)p.num_blocks * p.num_kv_heads * p.block_size;
-    rc = make_kv_tensor_map(&kmap, k_cache, rows, pf::kD, dt, 16);
-    if (rc != PA_OK) return rc;
-    rc = make_kv_tensor_map(&vmap, v_cache, rows, pf::kD, dt, 16);
+    rc = make_pool_maps(p, k_cache, v_cache, dt, &kmap, &vmap);
     if (rc != PA_OK) return rc;
   }
   const int64_t upper = (int64_t)(p.total_q > 0 ? p.total_q : 1) * p.num_kv_heads;
@@ -758,10 +1022,7 @@ int launch_prefix_pass(const PrefillParams& p0, const void* k_cache, const void*
   // consecutive sequences, so a tile is one box of 128/G sequences x G heads.
   int rc = make_3d_tensor_map(&qmap, p.q, p.num_seqs, p.num_q_heads, pf::kD, dt, pf::kM / p.group, p.group, 64);
   if (rc != PA_OK) return rc;
-  const int64_t rows = (int64_t)p.num_blocks * p.num_kv_heads * p.block_size;
-  rc = make_kv_tensor_map(&kmap, k_cache, rows, pf::kD, dt, 16);
-  if (rc != PA_OK) return rc;
-  rc = make_kv_tensor_map(&vmap, v_cache, rows, pf::kD, dt, 16);
+  rc = make_pool_maps(p, k_cache, v_cache, dt, &kmap, &vmap);
   if (rc != PA_OK) return rc;
   // The suffix decode runs beside this pass and cannot share an SM with it
   // (shared memory), so the pass takes only a fraction of the SMs: it is

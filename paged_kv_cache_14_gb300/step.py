@@ -9,7 +9,8 @@ A step is what a serving engine runs per layer per iteration on the KV side:
      new query token (pa_decode_shared_prefix when sequences share prefix
      blocks), pa_chunked_prefill otherwise.
 With an e4m3 cache the same step runs pa_copy_blocks_fp8,
-pa_reshape_and_cache_fp8 and pa_decode_fp8.
+pa_reshape_and_cache_fp8 and pa_decode_fp8 (pa_decode_shared_prefix_fp8,
+pa_chunked_prefill_fp8).
 This module only sequences library calls on one stream and owns the device
 buffers the calls need (slot mapping, output, split-KV workspace), allocated
 once with PyTorch.
@@ -68,8 +69,6 @@ class PagedStep:
                 n, hq, self.num_kv_heads, self.head_dim, self.block_size, self.max_seq_len, self.partition_size,
                 group_starts.shape[0] - 1))
         self.workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
-        if kv_scales is not None and (self.shared_prefix or not self.is_decode):
-            raise ValueError("the e4m3 cache is supported by plain decode only")
 
     # Per-step inputs a serving loop refreshes (attribute names).
     INPUTS = ("q", "k_new", "v_new", "block_tables", "kv_lens", "new_seq_ids", "new_positions",
@@ -100,12 +99,13 @@ class PagedStep:
                                            self.block_size, self.max_seq_len,
                                            self.partition_size if self.is_decode else 0)
         if self.shared_prefix:
-            n += 5  # prefix check, prefix pass, plan, suffix decode, merge
-            return n
-        n += 2 + (1 if -(-self.max_seq_len // part) > 1 else 0)  # plan, main, split-KV merge
+            # prefix check (which also plans the suffixes), prefix pass,
+            # suffix decode, merge (the prefix partial makes it always run)
+            return n + 4
+        merge = 1 if -(-self.max_seq_len // part) > 1 else 0
         if not self.is_decode and self.max_q_len > 1:
-            n += 2  # prefill plan, prefill chunks
-        return n
+            return n + 3 + merge  # one plan for both lists, chunk kernel, decode rows, merge
+        return n + 2 + merge  # plan, decode, split-KV merge
 
     @property
     def step_calls(self) -> str:
@@ -116,13 +116,21 @@ class PagedStep:
         if self.is_decode and self.kv_scales is None and self.q.dtype != torch.float32:
             return "pa_decode_step (copy_blocks + slot_mapping + reshape_and_cache + pa_decode in one call)"
         if self.kv_scales is not None:
-            return "pa_copy_blocks_fp8 + pa_slot_mapping + pa_reshape_and_cache_fp8 + pa_decode_fp8"
+            return "pa_copy_blocks_fp8 + pa_slot_mapping + pa_reshape_and_cache_fp8 + " + (
+                "pa_decode_shared_prefix_fp8" if self.shared_prefix else
+                "pa_decode_fp8" if self.is_decode else "pa_chunked_prefill_fp8")
         return "pa_copy_blocks + pa_slot_mapping + pa_reshape_and_cache + " + (
             "pa_decode" if self.is_decode else "pa_chunked_prefill")
 
     @property
     def attention_kernels(self) -> str:
         """What the step's attention call (attend()) runs on the device."""
+        if self.kv_scales is not None and self.shared_prefix:
+            return ("pa_decode_shared_prefix_fp8: prefix check + tcgen05 prefix pass (codes widened in shared "
+                    "memory) + e4m3 split-KV suffix decode + merge")
+        if self.kv_scales is not None and not self.is_decode:
+            return ("pa_chunked_prefill_fp8: e4m3 decode rows (decode + merge) beside the tcgen05 chunk kernel "
+                    "(codes widened in shared memory), one plan")
         if self.kv_scales is not None:
             return "pa_decode_fp8: plan + persistent e4m3 decode + split-KV merge"
         if self.shared_prefix:
@@ -173,7 +181,16 @@ class PagedStep:
 
     def attend(self, stream=None) -> torch.Tensor:
         """The attention call of the step alone."""
-        if self.kv_scales is not None:
+        if self.kv_scales is not None and self.shared_prefix:
+            pa.pa_decode_shared_prefix_fp8(self.q, self.k_cache, self.v_cache, self.kv_scales, self.block_tables,
+                                           self.kv_lens, self.max_seq_len, self.group_starts, self.prefix_lens,
+                                           self.scale, out=self.out, partition_size=self.partition_size,
+                                           workspace=self.workspace, stream=stream)
+        elif self.kv_scales is not None and not self.is_decode:
+            pa.pa_chunked_prefill_fp8(self.q, self.cu_q_lens, self.k_cache, self.v_cache, self.kv_scales,
+                                      self.block_tables, self.ctx_lens, self.max_q_len, self.max_seq_len, self.scale,
+                                      out=self.out, workspace=self.workspace, stream=stream)
+        elif self.kv_scales is not None:
             pa.pa_decode_fp8(self.q, self.k_cache, self.v_cache, self.kv_scales, self.block_tables, self.kv_lens,
                              self.max_seq_len, self.scale, out=self.out, partition_size=self.partition_size,
                              workspace=self.workspace, stream=stream)
