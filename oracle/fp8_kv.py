@@ -38,11 +38,17 @@ Readings where the pages are silent (each is listed in the design notes):
     it: s_new = fl32(amax / 448), code = e4m3(fl32(x / s)), re-encoded code =
     e4m3(fl32(decode(c) * fl32(s_old / s_new))); a scale of 0 (all rows
     zero) gives code 0;
-  * e5m2 is not built (the same machinery with another format; e4m3 is the
-    one the pages' accuracy note names).
+  * e5m2, the other format [P1] names, follows the same rule with its own
+    codec and largest finite value: OCP FP8 E5M2 (sign bit, 5 exponent bits
+    with bias 15, 2 mantissa bits; exponent field 0 encodes subnormals
+    m * 2^-16; exponent field 31 encodes infinity (m = 0) and NaN (m != 0);
+    the largest finite magnitude is 1.75 * 2^15 = 57344). Encoding rounds to
+    nearest even and saturates at +-57344 (an infinite input included), so
+    a code written by the cache is always finite. The e5m2 functions are
+    separate functions below (suffix _e5m2); the e4m3 ones are unchanged.
 
 Pins: tests/test_oracle_fp8_pins.py checks every function here against
-torch's float8_e4m3fn dtype, the format's closed forms, the rounding error
+torch's float8_e4m3fn / float8_e5m2 dtypes, the format's closed forms, the rounding error
 bound and exact invariants of the scale rule, with planted mistakes that the
 pins must catch. No function is "parity unpinned".
 """
@@ -188,3 +194,117 @@ def copy_blocks_fp8(k_codes, v_codes, scales, pairs) -> None:
         k_codes[int(dst)] = k_codes[int(src)]
         v_codes[int(dst)] = v_codes[int(src)]
         scales[int(dst)] = scales[int(src)]
+
+
+# ---------------------------------------------------------------------------
+# The e5m2 format (OCP 8-bit floating point, E5M2), the other 8-bit format of
+# [P1] item 3, and the same per-block cache rule with its codec.
+# ---------------------------------------------------------------------------
+
+E5M2_MAX = 57344.0
+E5M2_NAN = 0x7F
+
+
+def e5m2_decode(codes) -> np.ndarray:
+    """Value of every code as float64 (exact): (-1)^s * 2^(e-15) * (1 + m/4)
+    for 0 < e < 31, (-1)^s * 2^-14 * (m/4) for e = 0, (-1)^s * infinity for
+    e = 31 with m = 0, NaN for e = 31 with m != 0."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 2) & 0x1F
+    m = c & 0x3
+    normal = np.ldexp(1.0 + m / 4.0, (e - 15).astype(np.int64))
+    sub = np.ldexp(m / 4.0, -14)
+    val = sign * np.where(e > 0, normal, sub)
+    special = np.where(m == 0, sign * np.inf, np.nan)
+    return np.where(e == 31, special, val)
+
+
+def e5m2_encode(x) -> np.ndarray:
+    """Round float32 values to the nearest e5m2 code (ties to even mantissa);
+    magnitudes above 57344 (infinity included) saturate to 57344; NaN gives
+    0x7F. Sign kept (also for zero and for values that round to zero)."""
+    xf = np.asarray(x, dtype=np.float32).astype(np.float64)
+    neg = np.signbit(xf)
+    a = np.minimum(np.abs(xf), E5M2_MAX)
+    a = np.where(np.isnan(xf), 0.0, a)
+    # Binade of a (a in [2^e, 2^(e+1))), floored at the subnormal binade: the
+    # spacing of representable values there is 2^(e-2).
+    _, ex = np.frexp(a)
+    e = np.maximum(ex.astype(np.int64) - 1, -14)
+    quantum = np.ldexp(1.0, e - 2)
+    q = np.rint(a / quantum) * quantum          # a / quantum is exact; rint ties to even
+    _, qe = np.frexp(q)
+    qe = qe.astype(np.int64) - 1
+    is_normal = q >= 2.0 ** -14
+    efield = np.where(is_normal, qe + 15, 0)
+    mfield = np.where(is_normal, np.rint((q / np.ldexp(1.0, qe) - 1.0) * 4.0), np.rint(q / 2.0 ** -16))
+    mag = (efield << 2) | mfield.astype(np.int64)
+    code = np.where(neg, 0x80, 0) | mag
+    code = np.where(np.isnan(xf), E5M2_NAN, code)
+    return code.astype(np.uint8)
+
+
+def write_block_rows_e5m2(codes: np.ndarray, scale: np.float32, offsets, rows) -> np.float32:
+    """write_block_rows with the e5m2 codec: a = largest |x| of the new rows;
+    s_old = 0 if the write touches offset 0, else the stored scale; s_new =
+    max(s_old, fl32(a / 57344)); if s_new > s_old > 0 the codes below the
+    first touched offset are re-encoded with ratio fl32(s_old / s_new); every
+    new row is encoded as e5m2(fl32(x / s_new)) (code 0 when s_new == 0)."""
+    offsets = [int(o) for o in offsets]
+    rows = np.asarray(rows, dtype=np.float32).reshape(len(offsets), -1)
+    o_min = min(offsets)
+    with np.errstate(invalid="ignore"):
+        a = _f32(np.fmax.reduce(np.abs(rows), axis=None)) if rows.size else _f32(0.0)
+    s_old = _f32(0.0) if o_min == 0 else _f32(scale)
+    s_new = _f32(max(s_old, _f32(a / _f32(E5M2_MAX))))
+    if s_new > s_old and s_old > 0 and o_min > 0:
+        r = _f32(s_old / s_new)
+        old = e5m2_decode(codes[:o_min]).astype(np.float32)
+        codes[:o_min] = e5m2_encode((old * r).astype(np.float32))
+    for o, x in zip(offsets, rows):
+        if s_new > 0:
+            codes[o] = e5m2_encode((x / s_new).astype(np.float32))
+        else:
+            codes[o] = 0
+    return s_new
+
+
+def reshape_and_cache_e5m2(k_new, v_new, slots, k_codes, v_codes, scales, block_size: int) -> None:
+    """reshape_and_cache_fp8 into e5m2 pools: one write_block_rows_e5m2 per
+    (block, KV head, pool) over all the call's tokens in that block; slot < 0
+    skips a token."""
+    k_new = np.asarray(k_new, dtype=np.float32)
+    v_new = np.asarray(v_new, dtype=np.float32)
+    by_block: dict[int, list[tuple[int, int]]] = {}
+    for t, slot in enumerate(np.asarray(slots)):
+        slot = int(slot)
+        if slot < 0:
+            continue
+        by_block.setdefault(slot // block_size, []).append((slot % block_size, t))
+    hkv = k_codes.shape[1]
+    for blk, items in by_block.items():
+        offs = [o for o, _ in items]
+        toks = [t for _, t in items]
+        for h in range(hkv):
+            scales[blk, h, 0] = write_block_rows_e5m2(k_codes[blk, h], scales[blk, h, 0], offs, k_new[toks, h])
+            scales[blk, h, 1] = write_block_rows_e5m2(v_codes[blk, h], scales[blk, h, 1], offs, v_new[toks, h])
+
+
+def quantize_fresh_blocks_e5m2(values) -> tuple[np.ndarray, np.ndarray]:
+    """quantize_fresh_blocks with the e5m2 codec: s = fl32(amax / 57344) per
+    (block, KV head), code = e5m2(fl32(x / s))."""
+    x = np.asarray(values, dtype=np.float32)
+    with np.errstate(invalid="ignore"):
+        a = np.fmax.reduce(np.abs(x), axis=(2, 3)).astype(np.float32)
+    s = (a / np.float32(E5M2_MAX)).astype(np.float32)
+    safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+    codes = e5m2_encode((x / safe[:, :, None, None]).astype(np.float32))
+    codes = np.where(s[:, :, None, None] > 0, codes, np.uint8(0)).astype(np.uint8)
+    return codes, s
+
+
+def dequantize_e5m2(codes, scale_kv) -> np.ndarray:
+    """Stored values of an e5m2 pool as float64 [P, Hkv, B, D]: decode(code)
+    times the (block, KV head) scale (exact in float64)."""
+    return e5m2_decode(codes) * np.asarray(scale_kv, dtype=np.float64)[:, :, None, None]
