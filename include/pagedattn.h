@@ -502,6 +502,58 @@ int pa_chunked_prefill_fp8(const void* q, int32_t total_q, const int32_t* cu_q_l
                            size_t workspace_bytes, pa_dtype dtype, void* stream);
 
 /*
+ * e5m2 KV cache: the other 8-bit format the page names for block-quantised
+ * caching ("Tech Radar: vLLM v1 Production Engine Architecture...", section
+ * 2, "Hopper TMA Warp Specialization & FP8 Kernel Integration", item 3:
+ * e4m3 or e5m2). Same pools, scales, scale rule and errors as the e4m3 calls
+ * above, with the OCP FP8 E5M2 codec in place of e4m3:
+ *   k_cache, v_cache : uint8 pools [num_blocks][num_kv_heads][block_size][head_dim]
+ *                      of e5m2 codes (sign, 5 exponent bits with bias 15, 2
+ *                      mantissa bits; exponent field 31 holds infinities and
+ *                      NaNs; largest finite 57344)
+ *   kv_scales        : float32 [num_blocks][num_kv_heads][2], as above
+ * The cache write's scale is s_new = max(s_old, fl32(a / 57344)) and every
+ * code is e5m2(fl32(x / s)) (round to nearest even, saturating at +-57344,
+ * so the cache only ever writes finite codes); re-encoding on scale growth
+ * as for e4m3. The attention calls widen every code to fp16 exactly (an
+ * e5m2 code is the upper byte of the fp16 of the same value). Codes past a
+ * sequence's end may hold any bits, infinities and NaNs included.
+ * pa_copy_blocks_fp8 copies e5m2 pools and their scales unchanged (it moves
+ * bytes and scales, whatever the format).
+ */
+
+/* pa_reshape_and_cache_e5m2 — pa_reshape_and_cache_fp8 writing e5m2 codes. */
+int pa_reshape_and_cache_e5m2(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                              void* k_cache, void* v_cache, float* kv_scales, int32_t num_blocks, int32_t block_size,
+                              int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype, void* stream);
+
+/* pa_decode_e5m2 — pa_decode_fp8 over e5m2 pools (same arguments). */
+int pa_decode_e5m2(const void* q, const void* k_cache, const void* v_cache, const float* kv_scales,
+                   const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                   int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                   int32_t block_size, int32_t num_blocks, float scale, void* out, int32_t partition_size,
+                   void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream);
+
+/* pa_decode_shared_prefix_e5m2 — pa_decode_shared_prefix_fp8 over e5m2 pools
+ * (same arguments, hints, checks and workspace). */
+int pa_decode_shared_prefix_e5m2(const void* q, const void* k_cache, const void* v_cache, const float* kv_scales,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                 int32_t num_seqs, int32_t max_seq_len, const int32_t* group_starts,
+                                 const int32_t* prefix_lens, int32_t num_groups, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                 float scale, void* out, int32_t partition_size, void* workspace,
+                                 size_t workspace_bytes, pa_dtype dtype, void* stream);
+
+/* pa_chunked_prefill_e5m2 — pa_chunked_prefill_fp8 over e5m2 pools (same
+ * arguments and workspace). */
+int pa_chunked_prefill_e5m2(const void* q, int32_t total_q, const int32_t* cu_q_lens, const void* k_cache,
+                            const void* v_cache, const float* kv_scales, const int32_t* block_tables,
+                            int32_t max_blocks_per_seq, const int32_t* ctx_lens, int32_t num_seqs, int32_t max_q_len,
+                            int32_t max_kv_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t num_blocks, float scale, void* out, void* workspace,
+                            size_t workspace_bytes, pa_dtype dtype, void* stream);
+
+/*
  * pa_selftest_bounded_wait — exercises the failure path every kernel relies
  * on: one warp waits on an mbarrier that nothing completes; the wait gives up
  * after limit_ns nanoseconds of device time (1 us .. 1 s, else PA_ERR_ARG),

@@ -13,16 +13,19 @@ from ._binding import (  # noqa: F401
     exported_symbols,
     load,
     pa_chunked_prefill,
+    pa_chunked_prefill_e5m2,
     pa_chunked_prefill_fp8,
     pa_chunked_prefill_workspace_size,
     pa_copy_blocks,
     pa_copy_blocks_fp8,
     pa_decode,
+    pa_decode_e5m2,
     pa_decode_fp8,
     pa_decode_noalloc,
     pa_decode_noalloc_scratch_limit,
     pa_decode_partition_size,
     pa_decode_shared_prefix,
+    pa_decode_shared_prefix_e5m2,
     pa_decode_shared_prefix_fp8,
     pa_decode_step,
     pa_selftest_bounded_wait,
@@ -31,6 +34,7 @@ from ._binding import (  # noqa: F401
     pa_decode_workspace_size,
     pa_get_status,
     pa_reshape_and_cache,
+    pa_reshape_and_cache_e5m2,
     pa_reshape_and_cache_fp8,
     pa_slot_mapping,
     pa_strerror,

@@ -29,7 +29,8 @@ EXPORTS = (
     "pa_decode_shared_prefix", "pa_decode_noalloc_scratch_limit", "pa_decode_noalloc",
     "pa_reshape_and_cache_fp8", "pa_copy_blocks_fp8", "pa_decode_fp8", "pa_swap_blocks",
     "pa_decode_step_shared_prefix", "pa_decode_step", "pa_selftest_bounded_wait", "pa_decode_shared_prefix_fp8",
-    "pa_chunked_prefill_fp8",
+    "pa_chunked_prefill_fp8", "pa_reshape_and_cache_e5m2", "pa_decode_e5m2", "pa_decode_shared_prefix_e5m2",
+    "pa_chunked_prefill_e5m2",
 )
 
 _i32, _i64, _f32, _vp, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
@@ -94,6 +95,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                                   _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _sz, ctypes.c_int,
                                                   _vp]),
     }
+    for name in ("reshape_and_cache", "decode", "decode_shared_prefix", "chunked_prefill"):
+        sig[f"pa_{name}_e5m2"] = sig[f"pa_{name}_fp8"]  # same arguments, e5m2 codes
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
         fn.restype = res
@@ -378,20 +381,31 @@ def pa_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
 
 
 # ---------------------------------------------------------------------------
-# e4m3 KV cache: uint8 code pools [P, Hkv, B, D] and float32 scales
-# [P, Hkv, 2] (K, V) per (block, KV head).
+# 8-bit KV cache: uint8 code pools [P, Hkv, B, D] and float32 scales
+# [P, Hkv, 2] (K, V) per (block, KV head). The *_fp8 calls hold e4m3 codes,
+# the *_e5m2 calls e5m2 codes; pa_copy_blocks_fp8 serves both.
 # ---------------------------------------------------------------------------
 
 def pa_reshape_and_cache_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
                              k_cache: torch.Tensor, v_cache: torch.Tensor, kv_scales: torch.Tensor,
                              stream=None) -> None:
+    _reshape_and_cache_8bit("pa_reshape_and_cache_fp8", k, v, slot_mapping, k_cache, v_cache, kv_scales, stream)
+
+
+def pa_reshape_and_cache_e5m2(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                              k_cache: torch.Tensor, v_cache: torch.Tensor, kv_scales: torch.Tensor,
+                              stream=None) -> None:
+    _reshape_and_cache_8bit("pa_reshape_and_cache_e5m2", k, v, slot_mapping, k_cache, v_cache, kv_scales, stream)
+
+
+def _reshape_and_cache_8bit(sym, k, v, slot_mapping, k_cache, v_cache, kv_scales, stream) -> None:
     P, hkv, B, D = k_cache.shape
     dt = k.dtype
-    rc = load().pa_reshape_and_cache_fp8(
+    rc = getattr(load(), sym)(
         _cuda(k, "k", dt), _cuda(v, "v", dt), _cuda(slot_mapping, "slot_mapping", torch.int64), k.shape[0],
         _cuda(k_cache, "k_cache", torch.uint8), _cuda(v_cache, "v_cache", torch.uint8),
         _cuda(kv_scales, "kv_scales", torch.float32), P, B, hkv, D, _DT[dt], _stream(stream))
-    _check(rc, "pa_reshape_and_cache_fp8")
+    _check(rc, sym)
 
 
 def pa_copy_blocks_fp8(k_cache: torch.Tensor, v_cache: torch.Tensor, kv_scales: torch.Tensor, src_dst_pairs,
@@ -410,6 +424,20 @@ def pa_decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                   block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int, scale: float,
                   out: torch.Tensor | None = None, partition_size: int = 0, workspace: torch.Tensor | None = None,
                   stream=None) -> torch.Tensor:
+    return _decode_8bit("pa_decode_fp8", q, k_cache, v_cache, kv_scales, block_tables, seq_lens, max_seq_len, scale,
+                        out, partition_size, workspace, stream)
+
+
+def pa_decode_e5m2(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, kv_scales: torch.Tensor,
+                   block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int, scale: float,
+                   out: torch.Tensor | None = None, partition_size: int = 0, workspace: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    return _decode_8bit("pa_decode_e5m2", q, k_cache, v_cache, kv_scales, block_tables, seq_lens, max_seq_len,
+                        scale, out, partition_size, workspace, stream)
+
+
+def _decode_8bit(sym, q, k_cache, v_cache, kv_scales, block_tables, seq_lens, max_seq_len, scale, out,
+                 partition_size, workspace, stream) -> torch.Tensor:
     N, hq, D = q.shape
     P, hkv, B, D2 = k_cache.shape
     if D2 != D:
@@ -422,12 +450,12 @@ def pa_decode_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    rc = load().pa_decode_fp8(
+    rc = getattr(load(), sym)(
         _cuda(q, "q", dt), _cuda(k_cache, "k_cache", torch.uint8), _cuda(v_cache, "v_cache", torch.uint8),
         _cuda(kv_scales, "kv_scales", torch.float32), _cuda(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _cuda(seq_lens, "seq_lens", torch.int32), N, int(max_seq_len), hq, hkv, D, B, P,
         float(scale), _cuda(out, "out", dt), int(partition_size), ws_ptr, ws_bytes, _DT[dt], _stream(stream))
-    _check(rc, "pa_decode_fp8")
+    _check(rc, sym)
     return out
 
 
@@ -436,6 +464,23 @@ def pa_decode_shared_prefix_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache:
                                 max_seq_len: int, group_starts: torch.Tensor, prefix_lens: torch.Tensor, scale: float,
                                 out: torch.Tensor | None = None, partition_size: int = 0,
                                 workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    return _shared_prefix_8bit("pa_decode_shared_prefix_fp8", q, k_cache, v_cache, kv_scales, block_tables,
+                               seq_lens, max_seq_len, group_starts, prefix_lens, scale, out, partition_size,
+                               workspace, stream)
+
+
+def pa_decode_shared_prefix_e5m2(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                 kv_scales: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                                 max_seq_len: int, group_starts: torch.Tensor, prefix_lens: torch.Tensor, scale: float,
+                                 out: torch.Tensor | None = None, partition_size: int = 0,
+                                 workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    return _shared_prefix_8bit("pa_decode_shared_prefix_e5m2", q, k_cache, v_cache, kv_scales, block_tables,
+                               seq_lens, max_seq_len, group_starts, prefix_lens, scale, out, partition_size,
+                               workspace, stream)
+
+
+def _shared_prefix_8bit(sym, q, k_cache, v_cache, kv_scales, block_tables, seq_lens, max_seq_len, group_starts,
+                        prefix_lens, scale, out, partition_size, workspace, stream) -> torch.Tensor:
     N, hq, D = q.shape
     P, hkv, B, _ = k_cache.shape
     G = group_starts.shape[0] - 1
@@ -447,14 +492,14 @@ def pa_decode_shared_prefix_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    rc = load().pa_decode_shared_prefix_fp8(
+    rc = getattr(load(), sym)(
         _cuda(q, "q", dt), _cuda(k_cache, "k_cache", torch.uint8), _cuda(v_cache, "v_cache", torch.uint8),
         _cuda(kv_scales, "kv_scales", torch.float32), _cuda(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _cuda(seq_lens, "seq_lens", torch.int32), N, int(max_seq_len),
         _cuda(group_starts, "group_starts", torch.int32), _cuda(prefix_lens, "prefix_lens", torch.int32), G,
         hq, hkv, D, B, P, float(scale), _cuda(out, "out", dt), int(partition_size), ws_ptr, ws_bytes, _DT[dt],
         _stream(stream))
-    _check(rc, "pa_decode_shared_prefix_fp8")
+    _check(rc, sym)
     return out
 
 
@@ -462,6 +507,20 @@ def pa_chunked_prefill_fp8(q: torch.Tensor, cu_q_lens: torch.Tensor, k_cache: to
                            kv_scales: torch.Tensor, block_tables: torch.Tensor, ctx_lens: torch.Tensor,
                            max_q_len: int, max_kv_len: int, scale: float, out: torch.Tensor | None = None,
                            workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    return _prefill_8bit("pa_chunked_prefill_fp8", q, cu_q_lens, k_cache, v_cache, kv_scales, block_tables, ctx_lens,
+                         max_q_len, max_kv_len, scale, out, workspace, stream)
+
+
+def pa_chunked_prefill_e5m2(q: torch.Tensor, cu_q_lens: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            kv_scales: torch.Tensor, block_tables: torch.Tensor, ctx_lens: torch.Tensor,
+                            max_q_len: int, max_kv_len: int, scale: float, out: torch.Tensor | None = None,
+                            workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    return _prefill_8bit("pa_chunked_prefill_e5m2", q, cu_q_lens, k_cache, v_cache, kv_scales, block_tables,
+                         ctx_lens, max_q_len, max_kv_len, scale, out, workspace, stream)
+
+
+def _prefill_8bit(sym, q, cu_q_lens, k_cache, v_cache, kv_scales, block_tables, ctx_lens, max_q_len, max_kv_len,
+                  scale, out, workspace, stream) -> torch.Tensor:
     T, hq, D = q.shape
     P, hkv, B, _ = k_cache.shape
     n = ctx_lens.shape[0]
@@ -473,13 +532,13 @@ def pa_chunked_prefill_fp8(q: torch.Tensor, cu_q_lens: torch.Tensor, k_cache: to
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    rc = load().pa_chunked_prefill_fp8(
+    rc = getattr(load(), sym)(
         _cuda(q, "q", dt), T, _cuda(cu_q_lens, "cu_q_lens", torch.int32), _cuda(k_cache, "k_cache", torch.uint8),
         _cuda(v_cache, "v_cache", torch.uint8), _cuda(kv_scales, "kv_scales", torch.float32),
         _cuda(block_tables, "block_tables", torch.int32), block_tables.shape[1],
         _cuda(ctx_lens, "ctx_lens", torch.int32), n, int(max_q_len), int(max_kv_len), hq, hkv, D, B, P,
         float(scale), _cuda(out, "out", dt), ws_ptr, ws_bytes, _DT[dt], _stream(stream))
-    _check(rc, "pa_chunked_prefill_fp8")
+    _check(rc, sym)
     return out
 
 

@@ -348,7 +348,7 @@ static int shared_prefix_decode(const void* q, const void* k_cache, const void* 
                             int32_t num_groups, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                             int32_t block_size, int32_t num_blocks, float scale, void* out, int32_t partition_size,
                             void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream,
-                            const float* kv_scales, Between&& between) {
+                            const float* kv_scales, int32_t kv_fmt, Between&& between) {
   if (num_seqs < 0 || num_groups < 0) return PA_ERR_ARG;
   if (num_seqs == 0) return between(false);
   if (num_groups < 1 || num_groups > num_seqs || !group_starts || !prefix_lens) return PA_ERR_ARG;
@@ -368,7 +368,8 @@ static int shared_prefix_decode(const void* q, const void* k_cache, const void* 
                           partition_size, 1, workspace, workspace_bytes, dtype, &dp, &wl);
   if (rc != PA_OK) return rc;
   if (kv_scales && !aligned16(kv_scales)) return PA_ERR_ALIGN;
-  dp.kv_scales = kv_scales;  // e4m3 cache (nullptr: the pools hold q's dtype)
+  dp.kv_scales = kv_scales;  // 8-bit cache (nullptr: the pools hold q's dtype)
+  dp.kv_fmt = kv_fmt;
   const CascadeWorkspace cw = cascade_workspace_layout(num_seqs, num_groups);
   uint8_t* cbase = static_cast<uint8_t*>(workspace) + wl.total;
   int32_t* prefix = reinterpret_cast<int32_t*>(cbase + cw.prefix);
@@ -416,6 +417,7 @@ static int shared_prefix_decode(const void* q, const void* k_cache, const void* 
   pp.max_parts = dp.max_parts;
   pp.status = dp.status;
   pp.kv_scales = kv_scales;
+  pp.kv_fmt = kv_fmt;
   rc = launch_prefix_pass(pp, k_cache, v_cache, dtype, s);
   if (rc != PA_OK) return rc;
   // 3. Suffix decode (split-KV over the private keys) and the merge.
@@ -538,11 +540,15 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
                        partition_size, workspace, workspace_bytes, dtype, static_cast<cudaStream_t>(stream));
 }
 
-int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const float* kv_scales,
-                  const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
-                  int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                  int32_t block_size, int32_t num_blocks, float scale, void* out, int32_t partition_size,
-                  void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
+}  // extern "C"
+
+namespace pa {
+static int decode_fp8(const void* q, const void* k_cache, const void* v_cache, const float* kv_scales,
+                      const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                      int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale, void* out,
+                      int32_t partition_size, void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream,
+                      int32_t kv_fmt) {
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_DTYPE;
   if (head_dim != 128) return PA_ERR_UNSUPPORTED;
   DecodeParams p;
@@ -554,12 +560,14 @@ int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const
   if (!kv_scales) return PA_ERR_ARG;
   if (!aligned16(kv_scales)) return PA_ERR_ALIGN;
   p.kv_scales = kv_scales;
+  p.kv_fmt = kv_fmt;
   return launch_decode(p, dtype, static_cast<cudaStream_t>(stream));
 }
 
-int pa_reshape_and_cache_fp8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
-                             void* k_cache, void* v_cache, float* kv_scales, int32_t num_blocks, int32_t block_size,
-                             int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype, void* stream) {
+static int reshape_and_cache_fp8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                                 void* k_cache, void* v_cache, float* kv_scales, int32_t num_blocks,
+                                 int32_t block_size, int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype,
+                                 void* stream, int32_t kv_fmt) {
   if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 1) return PA_ERR_ARG;
   if (block_size != 16 && block_size != 32) return PA_ERR_BLOCKSIZE;
   if (!elem_bytes(dtype)) return PA_ERR_DTYPE;
@@ -572,7 +580,44 @@ int pa_reshape_and_cache_fp8(const void* k, const void* v, const int64_t* slot_m
   if (!st) return PA_ERR_CUDA;
   return launch_reshape_and_cache_fp8(k, v, slot_mapping, num_tokens, static_cast<uint8_t*>(k_cache),
                                       static_cast<uint8_t*>(v_cache), kv_scales, num_blocks, block_size,
-                                      num_kv_heads, head_dim, dtype, st, static_cast<cudaStream_t>(stream));
+                                      num_kv_heads, head_dim, dtype, kv_fmt, st, static_cast<cudaStream_t>(stream));
+}
+}  // namespace pa
+
+extern "C" {
+
+int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const float* kv_scales,
+                  const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                  int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t block_size, int32_t num_blocks, float scale, void* out, int32_t partition_size,
+                  void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
+  return decode_fp8(q, k_cache, v_cache, kv_scales, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                    max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out,
+                    partition_size, workspace, workspace_bytes, dtype, stream, PA_KV_E4M3);
+}
+
+int pa_decode_e5m2(const void* q, const void* k_cache, const void* v_cache, const float* kv_scales,
+                   const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                   int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                   int32_t block_size, int32_t num_blocks, float scale, void* out, int32_t partition_size,
+                   void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
+  return decode_fp8(q, k_cache, v_cache, kv_scales, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                    max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, out,
+                    partition_size, workspace, workspace_bytes, dtype, stream, PA_KV_E5M2);
+}
+
+int pa_reshape_and_cache_fp8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                             void* k_cache, void* v_cache, float* kv_scales, int32_t num_blocks, int32_t block_size,
+                             int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype, void* stream) {
+  return reshape_and_cache_fp8(k, v, slot_mapping, num_tokens, k_cache, v_cache, kv_scales, num_blocks, block_size,
+                               num_kv_heads, head_dim, dtype, stream, PA_KV_E4M3);
+}
+
+int pa_reshape_and_cache_e5m2(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                              void* k_cache, void* v_cache, float* kv_scales, int32_t num_blocks, int32_t block_size,
+                              int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype, void* stream) {
+  return reshape_and_cache_fp8(k, v, slot_mapping, num_tokens, k_cache, v_cache, kv_scales, num_blocks, block_size,
+                               num_kv_heads, head_dim, dtype, stream, PA_KV_E5M2);
 }
 
 int pa_copy_blocks_fp8(void* k_cache, void* v_cache, float* kv_scales, const int64_t* src_dst_pairs,
@@ -662,7 +707,7 @@ int pa_decode_shared_prefix(const void* q, const void* k_cache, const void* v_ca
   return shared_prefix_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
                               group_starts, prefix_lens, num_groups, num_q_heads, num_kv_heads, head_dim, block_size,
                               num_blocks, scale, out, partition_size, workspace, workspace_bytes, dtype, stream,
-                              nullptr, [](bool) { return PA_OK; });
+                              nullptr, PA_KV_E4M3, [](bool) { return PA_OK; });
 }
 
 int pa_decode_shared_prefix_fp8(const void* q, const void* k_cache, const void* v_cache, const float* kv_scales,
@@ -676,7 +721,21 @@ int pa_decode_shared_prefix_fp8(const void* q, const void* k_cache, const void* 
   return shared_prefix_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
                               group_starts, prefix_lens, num_groups, num_q_heads, num_kv_heads, head_dim, block_size,
                               num_blocks, scale, out, partition_size, workspace, workspace_bytes, dtype, stream,
-                              kv_scales, [](bool) { return PA_OK; });
+                              kv_scales, PA_KV_E4M3, [](bool) { return PA_OK; });
+}
+
+int pa_decode_shared_prefix_e5m2(const void* q, const void* k_cache, const void* v_cache, const float* kv_scales,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                 int32_t num_seqs, int32_t max_seq_len, const int32_t* group_starts,
+                                 const int32_t* prefix_lens, int32_t num_groups, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                 float scale, void* out, int32_t partition_size, void* workspace,
+                                 size_t workspace_bytes, pa_dtype dtype, void* stream) {
+  if (num_seqs > 0 && !kv_scales) return PA_ERR_ARG;
+  return shared_prefix_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                              group_starts, prefix_lens, num_groups, num_q_heads, num_kv_heads, head_dim, block_size,
+                              num_blocks, scale, out, partition_size, workspace, workspace_bytes, dtype, stream,
+                              kv_scales, PA_KV_E5M2, [](bool) { return PA_OK; });
 }
 
 int pa_decode_step_shared_prefix(const int64_t* cow_pairs, int32_t num_cow_pairs, const int32_t* new_seq_ids,
@@ -704,7 +763,7 @@ int pa_decode_step_shared_prefix(const int64_t* cow_pairs, int32_t num_cow_pairs
   return shared_prefix_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
                               group_starts, prefix_lens, num_groups, num_q_heads, num_kv_heads, head_dim, block_size,
                               num_blocks, scale, out, partition_size, workspace, workspace_bytes, dtype, stream,
-                              nullptr, cache_side);
+                              nullptr, PA_KV_E4M3, cache_side);
 }
 
 int pa_decode_step(const int64_t* cow_pairs, int32_t num_cow_pairs, const int32_t* new_seq_ids,
@@ -750,10 +809,10 @@ size_t pa_chunked_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads, 
 }  // extern "C"
 
 namespace pa {
-// Mixed batch (chunks and decode rows) over 16-bit pools, or over e4m3 pools
-// when kv_scales is given.
+// Mixed batch (chunks and decode rows) over 16-bit pools, or over 8-bit
+// pools (format kv_fmt) when kv_scales is given.
 static int chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_lens, const void* k_cache,
-                           const void* v_cache, const float* kv_scales, const int32_t* block_tables,
+                           const void* v_cache, const float* kv_scales, int32_t kv_fmt, const int32_t* block_tables,
                            int32_t max_blocks_per_seq, const int32_t* ctx_lens, int32_t num_seqs, int32_t max_q_len,
                            int32_t max_kv_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                            int32_t block_size, int32_t num_blocks, float scale, void* out, void* workspace,
@@ -787,6 +846,7 @@ static int chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_l
   if (kv_scales) {
     if (!aligned16(kv_scales)) return PA_ERR_ALIGN;
     dp.kv_scales = kv_scales;
+    dp.kv_fmt = kv_fmt;
   }
   if (max_q_len <= 1) return launch_decode(dp, dtype, s);
   // Chunks (q_len > 1): tcgen05 tiles. One plan lists the chunk items and
@@ -817,6 +877,7 @@ static int chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_l
   p.decode_token_bytes = 2 * num_kv_heads * head_dim * elem_bytes(dtype);
   p.decode_bytes_per_tile = kDecodeBytesPerChunkTile;
   p.kv_scales = kv_scales;
+  p.kv_fmt = kv_fmt;
   rc = launch_prefill(p, k_cache, v_cache, dtype, s, &dp);
   if (rc != PA_OK) return rc;
   dp.planned = 1;
@@ -833,7 +894,7 @@ int pa_chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_lens,
                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                        int32_t num_blocks, float scale, void* out, void* workspace, size_t workspace_bytes,
                        pa_dtype dtype, void* stream) {
-  return chunked_prefill(q, total_q, cu_q_lens, k_cache, v_cache, nullptr, block_tables, max_blocks_per_seq,
+  return chunked_prefill(q, total_q, cu_q_lens, k_cache, v_cache, nullptr, PA_KV_E4M3, block_tables, max_blocks_per_seq,
                          ctx_lens, num_seqs, max_q_len, max_kv_len, num_q_heads, num_kv_heads, head_dim, block_size,
                          num_blocks, scale, out, workspace, workspace_bytes, dtype, stream);
 }
@@ -847,9 +908,23 @@ int pa_chunked_prefill_fp8(const void* q, int32_t total_q, const int32_t* cu_q_l
   if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_DTYPE;
   if (head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (num_seqs > 0 && total_q > 0 && !kv_scales) return PA_ERR_ARG;
-  return chunked_prefill(q, total_q, cu_q_lens, k_cache, v_cache, kv_scales, block_tables, max_blocks_per_seq,
-                         ctx_lens, num_seqs, max_q_len, max_kv_len, num_q_heads, num_kv_heads, head_dim, block_size,
-                         num_blocks, scale, out, workspace, workspace_bytes, dtype, stream);
+  return chunked_prefill(q, total_q, cu_q_lens, k_cache, v_cache, kv_scales, PA_KV_E4M3, block_tables,
+                         max_blocks_per_seq, ctx_lens, num_seqs, max_q_len, max_kv_len, num_q_heads, num_kv_heads,
+                         head_dim, block_size, num_blocks, scale, out, workspace, workspace_bytes, dtype, stream);
+}
+
+int pa_chunked_prefill_e5m2(const void* q, int32_t total_q, const int32_t* cu_q_lens, const void* k_cache,
+                            const void* v_cache, const float* kv_scales, const int32_t* block_tables,
+                            int32_t max_blocks_per_seq, const int32_t* ctx_lens, int32_t num_seqs, int32_t max_q_len,
+                            int32_t max_kv_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t num_blocks, float scale, void* out, void* workspace,
+                            size_t workspace_bytes, pa_dtype dtype, void* stream) {
+  if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_DTYPE;
+  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (num_seqs > 0 && total_q > 0 && !kv_scales) return PA_ERR_ARG;
+  return chunked_prefill(q, total_q, cu_q_lens, k_cache, v_cache, kv_scales, PA_KV_E5M2, block_tables,
+                         max_blocks_per_seq, ctx_lens, num_seqs, max_q_len, max_kv_len, num_q_heads, num_kv_heads,
+                         head_dim, block_size, num_blocks, scale, out, workspace, workspace_bytes, dtype, stream);
 }
 
 }  // extern "C"

@@ -78,20 +78,22 @@ __global__ void reshape_and_cache_kernel(const uint8_t* __restrict__ k, const ui
 }
 
 // ---------------------------------------------------------------------------
-// e4m3 cache write with one scale per (block, KV head) and pool. The rows a
+// 8-bit cache write (e4m3, or e5m2 with E5) with one scale per (block, KV
+// head) and pool. The rows a
 // call writes into one block are consecutive entries of the slot mapping
 // (padding entries may sit between them); the first of them leads a warp
 // per (KV head, pool) that
 //   1. takes a = the largest |x| of the run's rows and the lowest written
 //      offset o_min;
-//   2. forms s_new = max(s_old, a / 448), with s_old = 0 when the run
+//   2. forms s_new = max(s_old, a / fmax), fmax = 448 (e4m3) or 57344
+//      (e5m2), the format's largest finite value, with s_old = 0 when the run
 //      touches offset 0 (the block starts afresh), else the stored scale;
 //   3. if the scale grew (and s_old > 0), re-encodes the codes at offsets
 //      below o_min (the tokens already in the block) with ratio s_old / s_new;
-//   4. encodes every row of the run as e4m3(x / s_new) and stores s_new.
+//   4. encodes every row of the run as fp8(x / s_new) and stores s_new.
 // Each step is one IEEE single-precision operation (division and product
 // rounded to nearest) followed by the round-to-nearest-even, saturating
-// conversion to e4m3, so the codes are reproducible bit for bit.
+// conversion to the 8-bit format, so the codes are reproducible bit for bit.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2_c(uint16_t c) {
   uint32_t d;
@@ -99,10 +101,20 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2_c(uint16_t c) {
   return d;
 }
 
-// Two floats to two e4m3 codes: lo in the low byte.
-__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+__device__ __forceinline__ uint32_t e5m2x2_to_f16x2_c(uint16_t c) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(d) : "h"(c));
+  return d;
+}
+
+// Two floats to two 8-bit codes (e4m3, or e5m2 with E5): lo in the low byte.
+template <bool E5>
+__device__ __forceinline__ uint32_t f32x2_to_fp8x2(float lo, float hi) {
   uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  if constexpr (E5)
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
 
@@ -115,21 +127,22 @@ __device__ __forceinline__ void store_codes(uint8_t* dst, const uint32_t (&c)[VE
   }
 }
 
-template <int VEC>
+template <int VEC, bool E5>
 __device__ __forceinline__ void load_codes(const uint8_t* src, float (&x)[VEC]) {
   uint32_t w;
   if constexpr (VEC == 2) w = *reinterpret_cast<const uint16_t*>(src);
   else w = *reinterpret_cast<const uint32_t*>(src);
 #pragma unroll
   for (int i = 0; i < VEC; i += 2) {
-    const uint32_t h2 = e4m3x2_to_f16x2_c(static_cast<uint16_t>(w >> (8 * i)));
+    const uint16_t c2 = static_cast<uint16_t>(w >> (8 * i));
+    const uint32_t h2 = E5 ? e5m2x2_to_f16x2_c(c2) : e4m3x2_to_f16x2_c(c2);
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
     x[i] = f.x;
     x[i + 1] = f.y;
   }
 }
 
-template <typename TI, int VEC>
+template <typename TI, int VEC, bool E5>
 __global__ void __launch_bounds__(256) reshape_and_cache_fp8_kernel(
     const TI* __restrict__ k, const TI* __restrict__ v, const int64_t* __restrict__ slot_mapping, int64_t num_tokens,
     uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache, float* __restrict__ kv_scales, int32_t num_blocks,
@@ -197,17 +210,17 @@ __global__ void __launch_bounds__(256) reshape_and_cache_fp8_kernel(
     // 2. The block's new scale.
     float* sp = kv_scales + (blk * num_kv_heads + h) * 2 + pool;
     const float s_old = omin == 0 ? 0.f : *sp;
-    const float s_new = fmaxf(s_old, __fdiv_rn(amax, 448.f));
+    const float s_new = fmaxf(s_old, __fdiv_rn(amax, E5 ? 57344.f : 448.f));
     // 3. Re-encode the tokens already in the block if the scale grew.
     if (s_new > s_old && s_old > 0.f && omin > 0) {
       const float r = __fdiv_rn(s_old, s_new);
       for (int o = 0; o < omin; ++o) {
         uint8_t* cp = codes + (int64_t)o * D + lane * VEC;
         float x[VEC];
-        load_codes<VEC>(cp, x);
+        load_codes<VEC, E5>(cp, x);
         uint32_t c[VEC / 2];
 #pragma unroll
-        for (int i = 0; i < VEC; i += 2) c[i / 2] = f32x2_to_e4m3x2(__fmul_rn(x[i], r), __fmul_rn(x[i + 1], r));
+        for (int i = 0; i < VEC; i += 2) c[i / 2] = f32x2_to_fp8x2<E5>(__fmul_rn(x[i], r), __fmul_rn(x[i + 1], r));
         store_codes<VEC>(cp, c);
       }
     }
@@ -225,7 +238,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_fp8_kernel(
 #pragma unroll
         for (int i = 0; i < VEC; i += 2) {
           const float x0 = to_f32(row[i]), x1 = to_f32(row[i + 1]);
-          c[i / 2] = s_new > 0.f ? f32x2_to_e4m3x2(__fdiv_rn(x0, s_new), __fdiv_rn(x1, s_new)) : 0u;
+          c[i / 2] = s_new > 0.f ? f32x2_to_fp8x2<E5>(__fdiv_rn(x0, s_new), __fdiv_rn(x1, s_new)) : 0u;
         }
         store_codes<VEC>(codes + (sm - blk * block_size) * D + lane * VEC, c);
       }
@@ -392,13 +405,18 @@ int launch_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* 
 int launch_reshape_and_cache_fp8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
                                  uint8_t* k_cache, uint8_t* v_cache, float* kv_scales, int32_t num_blocks,
                                  int32_t block_size, int32_t num_kv_heads, int32_t head_dim, pa_dtype dt,
-                                 int* status, cudaStream_t stream) {
+                                 int kv_fmt, int* status, cudaStream_t stream) {
   const int64_t warps = num_tokens * num_kv_heads * 2;
   const int grid = grid_for(warps, 8);
-#define PA_RC8(TI, VEC)                                                                                          \
-  reshape_and_cache_fp8_kernel<TI, VEC><<<grid, 256, 0, stream>>>(                                               \
+#define PA_RC8_F(TI, VEC, E5)                                                                                    \
+  reshape_and_cache_fp8_kernel<TI, VEC, E5><<<grid, 256, 0, stream>>>(                                           \
       static_cast<const TI*>(k), static_cast<const TI*>(v), slot_mapping, num_tokens, k_cache, v_cache, kv_scales, \
       num_blocks, block_size, num_kv_heads, status)
+#define PA_RC8(TI, VEC)          \
+  if (kv_fmt == PA_KV_E5M2)      \
+    PA_RC8_F(TI, VEC, true);     \
+  else                           \
+    PA_RC8_F(TI, VEC, false)
   const bool d128 = head_dim == 128;
   if (dt == PA_BF16) {
     if (d128) PA_RC8(__nv_bfloat16, 4); else PA_RC8(__nv_bfloat16, 2);
@@ -408,6 +426,7 @@ int launch_reshape_and_cache_fp8(const void* k, const void* v, const int64_t* sl
     if (d128) PA_RC8(float, 4); else PA_RC8(float, 2);
   }
 #undef PA_RC8
+#undef PA_RC8_F
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -175,6 +175,21 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t codes, uint32_t& lo, ui
       : "r"(codes));
 }
 
+// Four 8-bit codes of either cache format to two fp16 pairs, exactly, in the
+// layout of e4m3x4_to_f16x4. An e5m2 code is the upper byte of the fp16 with
+// the same value (same sign bit, exponent field and bias, two of fp16's ten
+// mantissa bits; subnormals, infinities and NaNs included), so widening it
+// only moves bytes.
+template <bool E5>
+__device__ __forceinline__ void fp8x4_to_f16x4(uint32_t codes, uint32_t& lo, uint32_t& hi) {
+  if constexpr (E5) {
+    lo = __byte_perm(codes, 0u, 0x1404);  // bytes {0, c0, 0, c1}
+    hi = __byte_perm(codes, 0u, 0x3424);  // bytes {0, c2, 0, c3}
+  } else {
+    e4m3x4_to_f16x4(codes, lo, hi);
+  }
+}
+
 template <typename T>
 struct MmaOp;
 

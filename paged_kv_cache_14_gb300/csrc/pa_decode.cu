@@ -144,7 +144,7 @@ struct ItemMeta {
   int seq, qrow, h0, nrows, t_begin, t_end, nsub, jstart, part, n_parts, hg, out_mode, pad[4];
 };
 
-template <typename T, int D, int BS, int NT, bool KV8>
+template <typename T, int D, int BS, int NT, bool KV8, bool E5 = false>
 __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 : 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                      const DecodeParams p) {
@@ -666,10 +666,10 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
 #pragma unroll
             for (int q2 = 0; q2 < D / 32; ++q2) {
               uint32_t a0[4], a1[4];
-              e4m3x4_to_f16x4(kr[h][q2][0], a0[0], a0[2]);
-              e4m3x4_to_f16x4(kr[h][q2][1], a0[1], a0[3]);
-              e4m3x4_to_f16x4(kr[h][q2][2], a1[0], a1[2]);
-              e4m3x4_to_f16x4(kr[h][q2][3], a1[1], a1[3]);
+              fp8x4_to_f16x4<E5>(kr[h][q2][0], a0[0], a0[2]);
+              fp8x4_to_f16x4<E5>(kr[h][q2][1], a0[1], a0[3]);
+              fp8x4_to_f16x4<E5>(kr[h][q2][2], a1[0], a1[2]);
+              fp8x4_to_f16x4<E5>(kr[h][q2][3], a1[1], a1[3]);
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
                 MmaOp<__half>::run(acc[nt], a0, qf[2 * q2][nt][0], qf[2 * q2][nt][1]);
@@ -776,10 +776,10 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
 #pragma unroll
           for (int q2 = 0; q2 < D / 32; ++q2) {
             uint32_t a0[4], a1[4];
-            e4m3x4_to_f16x4(__byte_perm(vr[h][q2][0], 0, 0x3120), a0[0], a0[1]);
-            e4m3x4_to_f16x4(__byte_perm(vr[h][q2][1], 0, 0x3120), a0[2], a0[3]);
-            e4m3x4_to_f16x4(__byte_perm(vr[h][q2][2], 0, 0x3120), a1[0], a1[1]);
-            e4m3x4_to_f16x4(__byte_perm(vr[h][q2][3], 0, 0x3120), a1[2], a1[3]);
+            fp8x4_to_f16x4<E5>(__byte_perm(vr[h][q2][0], 0, 0x3120), a0[0], a0[1]);
+            fp8x4_to_f16x4<E5>(__byte_perm(vr[h][q2][1], 0, 0x3120), a0[2], a0[3]);
+            fp8x4_to_f16x4<E5>(__byte_perm(vr[h][q2][2], 0, 0x3120), a1[0], a1[1]);
+            fp8x4_to_f16x4<E5>(__byte_perm(vr[h][q2][3], 0, 0x3120), a1[2], a1[3]);
             a0[0] &= keep_lo, a0[1] &= keep_lo, a0[2] &= keep_hi, a0[3] &= keep_hi;
             a1[0] &= keep_lo, a1[1] &= keep_lo, a1[2] &= keep_hi, a1[3] &= keep_hi;
 #pragma unroll
@@ -1097,7 +1097,7 @@ static int launch_merge(const DecodeParams& p, pa_dtype dt, cudaStream_t stream)
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-template <typename T, int D, int BS, int NT, bool KV8>
+template <typename T, int D, int BS, int NT, bool KV8, bool E5 = false>
 static int launch_tc(const DecodeParams& p, cudaStream_t stream) {
   using C = DecCfg<D, BS, NT, KV8>;
   constexpr pa_dtype dt = std::is_same<T, __half>::value ? PA_F16 : PA_BF16;
@@ -1114,7 +1114,7 @@ static int launch_tc(const DecodeParams& p, cudaStream_t stream) {
     rc = make_kv_tensor_map(&vmap, p.v_cache, rows, D, dt, 16);
   }
   if (rc != PA_OK) return rc;
-  auto kern = decode_tc_kernel<T, D, BS, NT, KV8>;
+  auto kern = decode_tc_kernel<T, D, BS, NT, KV8, E5>;
   if (set_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)C::kSmem) != PA_OK) return PA_ERR_CUDA;
   if (!p.planned) {
     decode_plan_kernel<T><<<1, 1024, 0, stream>>>(p);
@@ -1139,13 +1139,18 @@ static int launch_simt(const DecodeParams& p, cudaStream_t stream) {
 template <typename T>
 static int launch_tc_dispatch(const DecodeParams& p, cudaStream_t stream) {
   const int nt = p.rows_per_cta <= 8 ? 1 : 2;
-  if (p.kv_scales) {  // e4m3 cache: head_dim 128 only
+  if (p.kv_scales) {  // 8-bit cache: head_dim 128 only
     if (p.head_dim != 128) return PA_ERR_UNSUPPORTED;
-    switch ((p.block_size == 16 ? 0 : 1) * 2 + (nt - 1)) {
+    const int k8 = ((p.kv_fmt == PA_KV_E5M2 ? 1 : 0) * 2 + (p.block_size == 16 ? 0 : 1)) * 2 + (nt - 1);
+    switch (k8) {
       case 0: return launch_tc<T, 128, 16, 1, true>(p, stream);
       case 1: return launch_tc<T, 128, 16, 2, true>(p, stream);
       case 2: return launch_tc<T, 128, 32, 1, true>(p, stream);
       case 3: return launch_tc<T, 128, 32, 2, true>(p, stream);
+      case 4: return launch_tc<T, 128, 16, 1, true, true>(p, stream);
+      case 5: return launch_tc<T, 128, 16, 2, true, true>(p, stream);
+      case 6: return launch_tc<T, 128, 32, 1, true, true>(p, stream);
+      case 7: return launch_tc<T, 128, 32, 2, true, true>(p, stream);
     }
     return PA_ERR_UNSUPPORTED;
   }

@@ -10,6 +10,9 @@
 
 namespace pa {
 
+// 8-bit cache formats (with kv_scales): OCP FP8 E4M3 or E5M2.
+enum KvFormat : int32_t { PA_KV_E4M3 = 0, PA_KV_E5M2 = 1 };
+
 // Largest partition (tokens) one decode CTA walks; bounds the shared-memory
 // copy of the partition's block ids.
 constexpr int kMaxPartition = 16384;
@@ -56,9 +59,10 @@ struct DecodeParams {
   // kernel start; the decode streams at once, beside it, and waits for it
   // only before exiting.
   int32_t beside;
-  // e4m3 KV cache: (K, V) scale per (block, KV head), float32
+  // 8-bit KV cache: (K, V) scale per (block, KV head), float32
   // [num_blocks][num_kv_heads][2]; nullptr when the pools hold q's dtype.
   const float* kv_scales;
+  int32_t kv_fmt;  // KvFormat of the codes when kv_scales is given
   int* status;
 };
 
@@ -117,9 +121,10 @@ struct PrefillParams {
   // and the SM-time of one chunk (item, KV tile) unit in decode KV bytes.
   int32_t decode_token_bytes;
   float decode_bytes_per_tile;
-  // e4m3 cache: (K, V) scale per (block, KV head), float32
+  // 8-bit cache: (K, V) scale per (block, KV head), float32
   // [num_blocks][num_kv_heads][2]; nullptr when the pools hold q's dtype.
   const float* kv_scales;
+  int32_t kv_fmt;  // KvFormat of the codes when kv_scales is given
   // Prefix pass of shared-prefix decode (null for chunked prefill): rows are
   // (group member, GQA head); keys are the group's shared blocks, read
   // through the table of the member with the longest verified prefix; the
@@ -189,7 +194,7 @@ int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const i
 int launch_reshape_and_cache_fp8(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
                                  uint8_t* k_cache, uint8_t* v_cache, float* kv_scales, int32_t num_blocks,
                                  int32_t block_size, int32_t num_kv_heads, int32_t head_dim, pa_dtype dt,
-                                 int* status, cudaStream_t stream);
+                                 int kv_fmt, int* status, cudaStream_t stream);
 // Whole blocks between two pools (device or pinned host memory; device-usable pointers).
 int launch_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v, const int32_t* src,
                        const int32_t* dst, int32_t num_pairs, int64_t block_bytes, int vec16, cudaStream_t stream);

@@ -88,11 +88,16 @@ constexpr int kNumBars = kBarQConv + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, item, abort
 constexpr int kOffQExp = kOffMisc + 64;           // e4m3: per-row exponent of the fp16 Q rows [kQT][kM]
 constexpr int kSmem = kOffQExp + kQT * kM * 4;
-// e4m3 cache: one more warp widens the codes of each K / V stage (TMA puts
+// 8-bit cache: converter warps widen the codes of each K / V stage (TMA puts
 // them in the upper half of the stage) into the 16-bit stage layout, and
-// moves a bf16 Q tile into fp16.
+// move a bf16 Q tile into fp16. Two warps: one left the widening on the
+// critical path (1.63 ms for the mixed 70B batch over e4m3 pools against
+// 1.52 ms with two; four gave 1.60 ms).
 constexpr int kConvWarp0 = kSoftmaxWarp0 + 4 * kQT;
-constexpr int kConvWarps = 1;
+#ifndef PA_PREFILL_CONV_WARPS
+#define PA_PREFILL_CONV_WARPS 2
+#endif
+constexpr int kConvWarps = PA_PREFILL_CONV_WARPS;
 template <bool KV8>
 __host__ __device__ constexpr int threads() { return kThreads + (KV8 ? 32 * kConvWarps : 0); }
 static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
@@ -244,9 +249,10 @@ __global__ void __launch_bounds__(1024) mixed_plan_kernel(const PrefillParams p,
 // per item (q_full, o_done), those of Q tile 1 only on items whose second
 // tile has rows, and is waited on in phase order.
 //
-// KV8 (e4m3 cache, kv_scales given): the producer loads each 16-token
-// sub-tile's codes into the upper half of its 16-bit stage; two converter
-// warps widen them (exactly) to fp16 in the stage's swizzled layout and
+// KV8 (8-bit cache, kv_scales given; e4m3 codes, or e5m2 with E5): the
+// producer loads each 16-token sub-tile's codes into the upper half of its
+// 16-bit stage; the converter warps widen them (exactly) to fp16 in the
+// stage's swizzled layout and
 // complete k_full / v_full. The MMAs run in fp16: a bf16 Q tile is moved into
 // fp16 in place once per item, each row by its own power of two. The softmax
 // multiplies a score by the K scale of its key's block (and the Q row's power
@@ -254,7 +260,7 @@ __global__ void __launch_bounds__(1024) mixed_plan_kernel(const PrefillParams p,
 // times 2^kap, kap the largest exponent keeping every weight of the item
 // seen so far below 2^7 (P stays below 2^15 in fp16); O is rescaled exactly
 // when kap drops and divided by 2^kap at the end. The row sum takes p alone.
-template <typename T, int BS, bool PREFIX, bool KV8>
+template <typename T, int BS, bool PREFIX, bool KV8, bool E5 = false>
 __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
@@ -617,10 +623,10 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
                 // Codes of head_dim 16c .. 16c + 15 -> two 16-byte chunks of
                 // 16-bit values in half c / 4 of the row.
                 uint32_t o[8];
-                e4m3x4_to_f16x4(cr[c].x, o[0], o[1]);
-                e4m3x4_to_f16x4(cr[c].y, o[2], o[3]);
-                e4m3x4_to_f16x4(cr[c].z, o[4], o[5]);
-                e4m3x4_to_f16x4(cr[c].w, o[6], o[7]);
+                fp8x4_to_f16x4<E5>(cr[c].x, o[0], o[1]);
+                fp8x4_to_f16x4<E5>(cr[c].y, o[2], o[3]);
+                fp8x4_to_f16x4<E5>(cr[c].z, o[4], o[5]);
+                fp8x4_to_f16x4<E5>(cr[c].w, o[6], o[7]);
                 uint8_t* rb = base + (c >> 2) * kKVHalf + r * 128;
                 const int cc = 2 * (c & 3);
                 *reinterpret_cast<uint4*>(rb + ((cc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -933,10 +939,10 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <typename T, int BS, bool PREFIX, bool KV8>
+template <typename T, int BS, bool PREFIX, bool KV8, bool E5>
 static int launch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                  const PrefillParams& p, int ctas, cudaStream_t stream) {
-  auto kern = prefill_tc_kernel<T, BS, PREFIX, KV8>;
+  auto kern = prefill_tc_kernel<T, BS, PREFIX, KV8, E5>;
   if (set_max_dynamic_smem(reinterpret_cast<const void*>(kern), pf::kSmem) != PA_OK) return PA_ERR_CUDA;
   return launch_dependent(kern, dim3(ctas), dim3(pf::threads<KV8>()), pf::kSmem, stream, qmap, kmap, vmap, p) ==
                  cudaSuccess
@@ -944,22 +950,23 @@ static int launch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& kma
              : PA_ERR_CUDA;
 }
 
-template <bool PREFIX, bool KV8>
+template <bool PREFIX, bool KV8, bool E5 = false>
 static int dispatch_prefill_bs(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                const PrefillParams& p, int ctas, pa_dtype dt, cudaStream_t stream) {
   const bool bf = dt == PA_BF16;
   if (p.block_size == 16)
-    return bf ? launch_prefill_kernel<__nv_bfloat16, 16, PREFIX, KV8>(qmap, kmap, vmap, p, ctas, stream)
-              : launch_prefill_kernel<__half, 16, PREFIX, KV8>(qmap, kmap, vmap, p, ctas, stream);
-  return bf ? launch_prefill_kernel<__nv_bfloat16, 32, PREFIX, KV8>(qmap, kmap, vmap, p, ctas, stream)
-            : launch_prefill_kernel<__half, 32, PREFIX, KV8>(qmap, kmap, vmap, p, ctas, stream);
+    return bf ? launch_prefill_kernel<__nv_bfloat16, 16, PREFIX, KV8, E5>(qmap, kmap, vmap, p, ctas, stream)
+              : launch_prefill_kernel<__half, 16, PREFIX, KV8, E5>(qmap, kmap, vmap, p, ctas, stream);
+  return bf ? launch_prefill_kernel<__nv_bfloat16, 32, PREFIX, KV8, E5>(qmap, kmap, vmap, p, ctas, stream)
+            : launch_prefill_kernel<__half, 32, PREFIX, KV8, E5>(qmap, kmap, vmap, p, ctas, stream);
 }
 
 template <bool PREFIX>
 static int dispatch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                    const PrefillParams& p, int ctas, pa_dtype dt, cudaStream_t stream) {
-  return p.kv_scales ? dispatch_prefill_bs<PREFIX, true>(qmap, kmap, vmap, p, ctas, dt, stream)
-                     : dispatch_prefill_bs<PREFIX, false>(qmap, kmap, vmap, p, ctas, dt, stream);
+  if (!p.kv_scales) return dispatch_prefill_bs<PREFIX, false>(qmap, kmap, vmap, p, ctas, dt, stream);
+  return p.kv_fmt == PA_KV_E5M2 ? dispatch_prefill_bs<PREFIX, true, true>(qmap, kmap, vmap, p, ctas, dt, stream)
+                                : dispatch_prefill_bs<PREFIX, true>(qmap, kmap, vmap, p, ctas, dt, stream);
 }
 
 // Tensor maps of the pools: 16-token sub-tiles of 128 16-bit columns (two

@@ -10,7 +10,8 @@ A step is what a serving engine runs per layer per iteration on the KV side:
      blocks), pa_chunked_prefill otherwise.
 With an e4m3 cache the same step runs pa_copy_blocks_fp8,
 pa_reshape_and_cache_fp8 and pa_decode_fp8 (pa_decode_shared_prefix_fp8,
-pa_chunked_prefill_fp8).
+pa_chunked_prefill_fp8); with an e5m2 cache the *_e5m2 calls
+(pa_copy_blocks_fp8 moves either format).
 This module only sequences library calls on one stream and owns the device
 buffers the calls need (slot mapping, output, split-KV workspace), allocated
 once with PyTorch.
@@ -30,11 +31,16 @@ class PagedStep:
                  new_seq_ids: torch.Tensor, new_positions: torch.Tensor, cow_pairs_host: np.ndarray,
                  scale: float, partition_size: int = 0, cu_q_lens: torch.Tensor | None = None,
                  ctx_lens: torch.Tensor | None = None, group_starts: torch.Tensor | None = None,
-                 prefix_lens: torch.Tensor | None = None, kv_scales: torch.Tensor | None = None):
+                 prefix_lens: torch.Tensor | None = None, kv_scales: torch.Tensor | None = None,
+                 kv_format: str = "e4m3"):
         self.q, self.k_cache, self.v_cache = q, k_cache, v_cache
         # e4m3 cache: k_cache / v_cache hold uint8 codes, kv_scales the
         # float32 (K, V) scale of every (block, KV head).
         self.kv_scales = kv_scales
+        if kv_format not in ("e4m3", "e5m2"):
+            raise ValueError(f"kv_format {kv_format!r}: e4m3 or e5m2")
+        self.kv_format = kv_format
+        self._f8 = "fp8" if kv_format == "e4m3" else "e5m2"  # suffix of the 8-bit calls
         self.block_tables, self.kv_lens = block_tables, kv_lens
         self.k_new, self.v_new = k_new, v_new
         self.new_seq_ids, self.new_positions = new_seq_ids, new_positions
@@ -116,23 +122,25 @@ class PagedStep:
         if self.is_decode and self.kv_scales is None and self.q.dtype != torch.float32:
             return "pa_decode_step (copy_blocks + slot_mapping + reshape_and_cache + pa_decode in one call)"
         if self.kv_scales is not None:
-            return "pa_copy_blocks_fp8 + pa_slot_mapping + pa_reshape_and_cache_fp8 + " + (
-                "pa_decode_shared_prefix_fp8" if self.shared_prefix else
-                "pa_decode_fp8" if self.is_decode else "pa_chunked_prefill_fp8")
+            f = self._f8
+            return f"pa_copy_blocks_fp8 + pa_slot_mapping + pa_reshape_and_cache_{f} + " + (
+                f"pa_decode_shared_prefix_{f}" if self.shared_prefix else
+                f"pa_decode_{f}" if self.is_decode else f"pa_chunked_prefill_{f}")
         return "pa_copy_blocks + pa_slot_mapping + pa_reshape_and_cache + " + (
             "pa_decode" if self.is_decode else "pa_chunked_prefill")
 
     @property
     def attention_kernels(self) -> str:
         """What the step's attention call (attend()) runs on the device."""
+        f, fmt = self._f8, self.kv_format
         if self.kv_scales is not None and self.shared_prefix:
-            return ("pa_decode_shared_prefix_fp8: prefix check + tcgen05 prefix pass (codes widened in shared "
-                    "memory) + e4m3 split-KV suffix decode + merge")
+            return (f"pa_decode_shared_prefix_{f}: prefix check + tcgen05 prefix pass (codes widened in shared "
+                    f"memory) + {fmt} split-KV suffix decode + merge")
         if self.kv_scales is not None and not self.is_decode:
-            return ("pa_chunked_prefill_fp8: e4m3 decode rows (decode + merge) beside the tcgen05 chunk kernel "
+            return (f"pa_chunked_prefill_{f}: {fmt} decode rows (decode + merge) beside the tcgen05 chunk kernel "
                     "(codes widened in shared memory), one plan")
         if self.kv_scales is not None:
-            return "pa_decode_fp8: plan + persistent e4m3 decode + split-KV merge"
+            return f"pa_decode_{f}: plan + persistent {fmt} decode + split-KV merge"
         if self.shared_prefix:
             return ("pa_decode_shared_prefix: prefix check + tcgen05 prefix pass + split-KV suffix decode "
                     "+ merge")
@@ -173,8 +181,8 @@ class PagedStep:
         pa.pa_slot_mapping(self.block_tables, self.new_seq_ids, self.new_positions, self.block_size,
                            self.num_blocks, slot_mapping=self.slot_mapping, stream=stream)
         if fp8:
-            pa.pa_reshape_and_cache_fp8(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
-                                        self.kv_scales, stream=stream)
+            getattr(pa, f"pa_reshape_and_cache_{self._f8}")(self.k_new, self.v_new, self.slot_mapping, self.k_cache,
+                                                            self.v_cache, self.kv_scales, stream=stream)
         else:
             pa.pa_reshape_and_cache(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
                                     stream=stream)
@@ -182,16 +190,16 @@ class PagedStep:
     def attend(self, stream=None) -> torch.Tensor:
         """The attention call of the step alone."""
         if self.kv_scales is not None and self.shared_prefix:
-            pa.pa_decode_shared_prefix_fp8(self.q, self.k_cache, self.v_cache, self.kv_scales, self.block_tables,
+            getattr(pa, f"pa_decode_shared_prefix_{self._f8}")(self.q, self.k_cache, self.v_cache, self.kv_scales, self.block_tables,
                                            self.kv_lens, self.max_seq_len, self.group_starts, self.prefix_lens,
                                            self.scale, out=self.out, partition_size=self.partition_size,
                                            workspace=self.workspace, stream=stream)
         elif self.kv_scales is not None and not self.is_decode:
-            pa.pa_chunked_prefill_fp8(self.q, self.cu_q_lens, self.k_cache, self.v_cache, self.kv_scales,
+            getattr(pa, f"pa_chunked_prefill_{self._f8}")(self.q, self.cu_q_lens, self.k_cache, self.v_cache, self.kv_scales,
                                       self.block_tables, self.ctx_lens, self.max_q_len, self.max_seq_len, self.scale,
                                       out=self.out, workspace=self.workspace, stream=stream)
         elif self.kv_scales is not None:
-            pa.pa_decode_fp8(self.q, self.k_cache, self.v_cache, self.kv_scales, self.block_tables, self.kv_lens,
+            getattr(pa, f"pa_decode_{self._f8}")(self.q, self.k_cache, self.v_cache, self.kv_scales, self.block_tables, self.kv_lens,
                              self.max_seq_len, self.scale, out=self.out, partition_size=self.partition_size,
                              workspace=self.workspace, stream=stream)
         elif self.shared_prefix:
@@ -211,12 +219,13 @@ class PagedStep:
 
 
 def step_from_host(batch, device="cuda", partition_size: int = 0, shared_prefix: bool = False,
-                   fp8_pool=None) -> PagedStep:
+                   fp8_pool=None, kv_format: str = "e4m3") -> PagedStep:
     """Build a PagedStep from a host-side batch object exposing the fields of
     a seeded workload (q, caches, tables, lengths, new tokens, CoW pairs).
     With shared_prefix, decode uses the batch's prefix-sharing groups. With
-    fp8_pool = (k_codes, v_codes, kv_scales) the step runs on an e4m3 cache
-    holding those codes instead of the batch's 16-bit pools."""
+    fp8_pool = (k_codes, v_codes, kv_scales) the step runs on an 8-bit cache
+    (kv_format "e4m3" or "e5m2") holding those codes instead of the batch's
+    16-bit pools."""
     def dev(x, dtype=None):
         t = torch.as_tensor(x)
         if dtype is not None:
@@ -236,6 +245,7 @@ def step_from_host(batch, device="cuda", partition_size: int = 0, shared_prefix:
         cu_q_lens=dev(cu, torch.int32), ctx_lens=dev(batch.kv_lens - batch.q_lens, torch.int32),
         group_starts=dev(batch.group_starts, torch.int32) if shared_prefix else None,
         prefix_lens=dev(batch.prefix_lens, torch.int32) if shared_prefix else None,
+        kv_format=kv_format,
     )
 
 

@@ -133,14 +133,15 @@ def test_prefill_host_checks(lib):
     assert call() == -5                      # workspace required
 
 
-def test_fp8_host_checks(lib):
+@pytest.mark.parametrize("fmt", ["fp8", "e5m2"])
+def test_fp8_host_checks(lib, fmt):
     def dec(**o):
         a = dict(q=0x1000, k=0x2000, v=0x3000, sc=0x8000, bt=0x4000, mb=4, sl=0x5000, n=2, maxlen=1000, hq=8, hkv=2,
                  d=128, bs=16, nb=10, scale=0.1, out=0x6000, part=64, ws=None, wsb=0, dt=pa.PA_BF16)
         a.update(o)
-        return lib.pa_decode_fp8(a["q"], a["k"], a["v"], a["sc"], a["bt"], a["mb"], a["sl"], a["n"], a["maxlen"],
-                                 a["hq"], a["hkv"], a["d"], a["bs"], a["nb"], a["scale"], a["out"], a["part"], a["ws"],
-                                 a["wsb"], a["dt"], None)
+        return getattr(lib, f"pa_decode_{fmt}")(a["q"], a["k"], a["v"], a["sc"], a["bt"], a["mb"], a["sl"], a["n"],
+                                                a["maxlen"], a["hq"], a["hkv"], a["d"], a["bs"], a["nb"], a["scale"],
+                                                a["out"], a["part"], a["ws"], a["wsb"], a["dt"], None)
     assert dec(dt=pa.PA_F32) == -2           # q/out must be fp16 or bf16
     assert dec(d=64) == -10                  # head_dim 128 only
     assert dec(hq=6, hkv=4) == -3
@@ -153,8 +154,8 @@ def test_fp8_host_checks(lib):
         a = dict(k=0x1000, v=0x2000, sl=0x3000, n=4, kc=0x4000, vc=0x5000, sc=0x6000, nb=10, bs=16, hkv=2, d=128,
                  dt=pa.PA_BF16)
         a.update(o)
-        return lib.pa_reshape_and_cache_fp8(a["k"], a["v"], a["sl"], a["n"], a["kc"], a["vc"], a["sc"], a["nb"],
-                                            a["bs"], a["hkv"], a["d"], a["dt"], None)
+        return getattr(lib, f"pa_reshape_and_cache_{fmt}")(a["k"], a["v"], a["sl"], a["n"], a["kc"], a["vc"],
+                                                           a["sc"], a["nb"], a["bs"], a["hkv"], a["d"], a["dt"], None)
     assert rc8(dt=9) == -2
     assert rc8(bs=12) == -4
     assert rc8(d=96) == -10

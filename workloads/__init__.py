@@ -9,6 +9,7 @@ from .generate import (  # noqa: F401
     PagedBatch,
     build_batch,
     e4m3_pool,
+    e5m2_pool,
     make_config,
     random_lengths,
 )

@@ -386,6 +386,28 @@ def e4m3_pool(seed: int, num_blocks: int, num_kv_heads: int, block_size: int, he
     return k, v, torch.from_numpy(sc)
 
 
+def e5m2_pool(seed: int, num_blocks: int, num_kv_heads: int, block_size: int, head_dim: int,
+              log2_scale_range: tuple[float, float] = (-17.0, -14.0)):
+    """A synthetic e5m2 KV pool drawn directly as codes: K and V codes uniform
+    over the 248 byte values whose exponent field is not all ones (e5m2's
+    infinities and NaNs), and one K and one V scale per (block, KV head),
+    log-uniform over 2^log2_scale_range (the default keeps stored magnitudes
+    below 57344 * 2^-14 = 3.5, like unit-normal data).
+    Returns (k_codes, v_codes) uint8 [P, Hkv, B, D] and kv_scales float32
+    [P, Hkv, 2] (CPU tensors). Random structure only: no value is encoded."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 5011]))
+    shape = (num_blocks, num_kv_heads, block_size, head_dim)
+    finite = np.array([c for c in range(256) if (c >> 2) & 0x1F != 0x1F], dtype=np.uint8)
+
+    def codes():
+        return torch.from_numpy(finite[rng.integers(0, finite.size, size=shape)])
+
+    k, v = codes(), codes()
+    lo, hi = log2_scale_range
+    sc = np.exp2(rng.uniform(lo, hi, size=(num_blocks, num_kv_heads, 2))).astype(np.float32)
+    return k, v, torch.from_numpy(sc)
+
+
 def random_lengths(seed: int, n: int, lo: int, hi: int) -> np.ndarray:
     """Uniform integer lengths in [lo, hi] (structure helper for small cases)."""
     rng = np.random.default_rng(np.random.SeedSequence([seed, 77]))
