@@ -61,6 +61,7 @@ PER_CONFIG = (
     ("llama3_70b_prefix_bf16", "e4m3"),
     ("long_splitkv_bf16", "e4m3"),
     ("mixed_prefill_fp16", "e4m3"),
+    ("llama3_70b_prefix_bf16", "e5m2"),
 )
 
 
@@ -261,8 +262,8 @@ def source_sha256() -> str:
 def profile_summary(config: str, kv_cache: str = "native") -> str:
     """The committed ncu summary of the attention call on this workload."""
     kind = "prefill" if config.startswith("mixed_prefill") else "decode"
-    if kv_cache == "e4m3":
-        return os.path.join(PROFILES, f"{kind}_e4m3_{config}.md")
+    if kv_cache in ("e4m3", "e5m2"):
+        return os.path.join(PROFILES, f"{kind}_{kv_cache}_{config}.md")
     if kind == "prefill":
         return os.path.join(PROFILES, f"prefill_{config}.md")
     return os.path.join(PROFILES, f"decode_{config}.md")
@@ -572,8 +573,9 @@ def chunk_only_entry(pa, torch, st, batch, timer, calls: int) -> dict:
 
     def call():
         if st.kv_scales is not None:
-            pa.pa_chunked_prefill_fp8(q, cuq, st.k_cache, st.v_cache, st.kv_scales, tables, ctx, max_q,
-                                      st.max_seq_len, batch.scale, out=out, workspace=ws)
+            chunked_8bit = getattr(pa, f"pa_chunked_prefill_{st._f8}")  # e4m3 (_fp8) or e5m2 codes
+            chunked_8bit(q, cuq, st.k_cache, st.v_cache, st.kv_scales, tables, ctx, max_q, st.max_seq_len,
+                         batch.scale, out=out, workspace=ws)
         else:
             pa.pa_chunked_prefill(q, cuq, st.k_cache, st.v_cache, tables, ctx, max_q, st.max_seq_len, batch.scale,
                                   out=out, workspace=ws)
@@ -593,19 +595,19 @@ def chunk_only_entry(pa, torch, st, batch, timer, calls: int) -> dict:
 def per_config_entry(pa, torch, batch, kv_cache: str, timer, steps: int, warmup: int) -> dict:
     """Step and attention-call measurements of one more workload."""
     from paged_kv_cache_14_gb300.step import step_from_host
-    from workloads import e4m3_pool
-    fp8 = kv_cache == "e4m3"
-    pool = e4m3_pool(batch.meta["seed"], batch.num_blocks, batch.num_kv_heads, batch.block_size,
-                     batch.head_dim) if fp8 else None
+    from workloads import e4m3_pool, e5m2_pool
+    fp8 = kv_cache in ("e4m3", "e5m2")
+    pool = (e5m2_pool if kv_cache == "e5m2" else e4m3_pool)(
+        batch.meta["seed"], batch.num_blocks, batch.num_kv_heads, batch.block_size, batch.head_dim) if fp8 else None
     shared = batch.is_decode and batch.prefix_lens is not None and bool(batch.prefix_lens.any())
-    st = step_from_host(batch, shared_prefix=shared, fp8_pool=pool)
+    st = step_from_host(batch, shared_prefix=shared, fp8_pool=pool, kv_format=kv_cache if fp8 else "e4m3")
     kv_es = 1 if fp8 else None
     for _ in range(warmup):
         st.run()
     n = max(steps, 50)
     ms_block, _, _ = timer.block(st.run, n)
     step_bytes = decode_algorithmic_bytes(batch, kv_es)["total"] + step_extra_bytes(batch, kv_es)
-    entry = {"workload": batch.name, "kv_cache": "e4m3 codes + fp32 (K, V) scale per (block, KV head)"
+    entry = {"workload": batch.name, "kv_cache": f"{kv_cache} codes + fp32 (K, V) scale per (block, KV head)"
              if fp8 else batch.dtype, "step": st.step_calls, "steps": n,
              "ms_per_step": round(ms_block / n, 5),
              "roofline": attention_entry(pa, st, batch, kv_es, timer, n, batch.name, kv_cache)}

@@ -251,9 +251,9 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
  *                  sequence (same result, no saving). Malformed group_starts
  *                  record PA_ERR_ARG and disable every hint.
  *   workspace    : pa_decode_shared_prefix_workspace_size() bytes.
- * Other arguments as pa_decode. fp16/bf16, head_dim 128, GQA group a power
- * of two up to 128 (up to 256/group members per tensor-core work item, in
- * two tiles; larger groups take several items), scale > 0.
+ * Other arguments as pa_decode. fp16/bf16, head_dim 128, GQA group G of at
+ * most 128 (2 * floor(128 / G) members per tensor-core work item, in two
+ * tiles; larger groups take several items), scale > 0.
  */
 size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                               int32_t head_dim, int32_t block_size, int32_t max_seq_len,
@@ -374,7 +374,8 @@ int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, c
  *                no initialisation needed; not shared by overlapping calls
  * Rows with q_len == 1 go through the decode path (any supported dtype and
  * head_dim); longer chunks through a tcgen05 tensor-core kernel that needs
- * fp16/bf16, head_dim 128, a power-of-two GQA group of at most 128
+ * fp16/bf16, head_dim 128, a GQA group G of at most 128 (a tensor-core tile
+ * holds floor(128 / G) query positions x G heads)
  * (PA_ERR_DTYPE / PA_ERR_UNSUPPORTED otherwise) and scale > 0 (PA_ERR_ARG).
  */
 size_t pa_chunked_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
@@ -470,7 +471,7 @@ int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache, const
  *                  NULL with num_seqs > 0: PA_ERR_ARG)
  * Other arguments, hints, checks and errors as pa_decode_shared_prefix; the
  * workspace is pa_decode_shared_prefix_workspace_size() bytes. q/out fp16
- * or bf16, head_dim 128, GQA group a power of two up to 128, scale > 0.
+ * or bf16, head_dim 128, GQA group up to 128, scale > 0.
  * The codes are widened to fp16 exactly (a bf16 query row is moved into fp16
  * by a power of two); scores, softmax and accumulation are fp32.
  */
@@ -492,7 +493,7 @@ int pa_decode_shared_prefix_fp8(const void* q, const void* k_cache, const void* 
  * pa_chunked_prefill plus kv_scales (as pa_decode_fp8); the workspace is
  * pa_chunked_prefill_workspace_size() bytes. q/out fp16 or bf16 (else
  * PA_ERR_DTYPE), head_dim 128 (else PA_ERR_UNSUPPORTED); chunks need a
- * power-of-two GQA group up to 128 and scale > 0.
+ * GQA group up to 128 and scale > 0.
  */
 int pa_chunked_prefill_fp8(const void* q, int32_t total_q, const int32_t* cu_q_lens, const void* k_cache,
                            const void* v_cache, const float* kv_scales, const int32_t* block_tables,

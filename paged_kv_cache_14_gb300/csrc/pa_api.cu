@@ -357,7 +357,7 @@ static int shared_prefix_decode(const void* q, const void* k_cache, const void* 
   if (head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads) return PA_ERR_HEADS;
   const int32_t g = num_q_heads / num_kv_heads;
-  if (g > 128 || (g & (g - 1))) return PA_ERR_UNSUPPORTED;
+  if (g > 128) return PA_ERR_UNSUPPORTED;
   const size_t need = pa_decode_shared_prefix_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                                             block_size, max_seq_len, partition_size, num_groups);
   if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
@@ -382,8 +382,8 @@ static int shared_prefix_decode(const void* q, const void* k_cache, const void* 
   dp.prefix = prefix;
   decode_set_rows(dp, dtype);
   // 1. Verify the hints, list the prefix pass's work and the suffix decode's.
-  rc = launch_cascade_prep(dp, dtype, group_starts, prefix_lens, num_groups, kPrefillRowsPerItem / g, prefix, group_ref,
-                           group_of_seq, pwork, ppairs, pkeys, s);
+  rc = launch_cascade_prep(dp, dtype, group_starts, prefix_lens, num_groups, prefill_positions_per_item(g), prefix,
+                           group_ref, group_of_seq, pwork, ppairs, pkeys, s);
   dp.planned = 1;
   if (rc != PA_OK) return rc;
   // Whatever the caller launches here runs beside the check: it must not
@@ -826,7 +826,7 @@ static int chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_l
     if (head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads) return PA_ERR_HEADS;
     const int32_t g = num_q_heads / num_kv_heads;
-    if (g > 128 || (g & (g - 1))) return PA_ERR_UNSUPPORTED;
+    if (g > 128) return PA_ERR_UNSUPPORTED;
     if (max_q_len > total_q) return PA_ERR_ARG;
   }
   const size_t dec_ws =

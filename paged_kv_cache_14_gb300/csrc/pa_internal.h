@@ -93,6 +93,10 @@ inline DecodeWorkspace decode_workspace_layout(int64_t num_seqs, int64_t num_q_h
 // Packed (position, GQA head) rows per work item of the tcgen05 prefill
 // kernel (chunks and the shared-prefix pass).
 constexpr int kPrefillRowsPerItem = 256;
+// Query positions (chunked prefill) or group members (prefix pass) of one
+// tcgen05 work item: two Q tiles of floor(128 / group) positions, each
+// position's `group` query heads adjacent.
+inline int prefill_positions_per_item(int group) { return 2 * (128 / group); }
 
 struct PrefillParams {
   const void* q;
@@ -111,7 +115,7 @@ struct PrefillParams {
   int32_t max_q_len;
   int32_t max_kv_len;
   int32_t total_q;   // rows of q / out
-  int32_t gshift;    // log2(group)
+  int32_t tile_pos;  // query positions (or group members) per 128-row Q tile: floor(128 / group)
   float scale_log2;
   int32_t* work;     // [0] next work item, [1] number of work items, [2] CTAs that run items (chunks)
   int32_t* pairs;    // (seq << 16 | row tile), longest first; prefix pass: (group << 16 | member tile)

@@ -119,7 +119,7 @@ __device__ __forceinline__ int64_t prefill_plan_body(const PrefillParams& p) {
   __shared__ int hist[kBins];
   __shared__ int total;
   __shared__ int scratch[33];
-  const int pp = pf::kRows >> p.gshift;  // query positions per work item
+  const int pp = pf::kQT * p.tile_pos;  // query positions per work item
   for (int i = threadIdx.x; i < kBins; i += blockDim.x) hist[i] = 0;
   if (threadIdx.x == 0) total = 0;
   __syncthreads();
@@ -326,8 +326,8 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
       return;
     }
   }
-  const int G = 1 << p.gshift;
-  const int pp = kM >> p.gshift;  // query positions (or group members) per Q tile
+  const int G = p.group;
+  const int pp = p.tile_pos;  // query positions (or group members) per Q tile: pp * G <= 128 rows
   const int total = p.work[1];
 
   int tile_base = 0;  // KV tiles processed by this CTA before the current item
@@ -377,7 +377,9 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
       bool bad = false;
       int k_issued = 0, v_issued = 0;  // tiles of this item whose K / V copies were issued
       if (lane == 0) {
-        mbar_arrive_expect_tx(b_q, kQT * kQBytes);
+        // The box holds pp * G of the tile's 128 rows (all of them when G
+        // divides 128); the rest of the tile is never read into an output.
+        mbar_arrive_expect_tx(b_q, kQT * 2 * pp * G * 128);
 #pragma unroll
         for (int t = 0; t < kQT; ++t)
 #pragma unroll
@@ -648,13 +650,14 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
       const uint32_t tl = (uint32_t)(q * 32) << 16;
       const uint32_t ts = tmem + tl + col_s(t), to = tmem + tl + col_o(t);
       const uint32_t b_sfull = b_sfull0 + 8 * t, b_pfull = b_pfull0 + 8 * t, b_odone = b_odone0 + 8 * t;
-      const int pos = pos_lo + t * pp + (row >> p.gshift);  // query position (chunk) or group member (prefix)
-      const int head = row & (G - 1);
+      const int pos = pos_lo + t * pp + row / G;  // query position (chunk) or group member (prefix)
+      const int head = row - (row / G) * G;
+      const bool row_used = row < pp * G;  // rows past pp * G hold no (position, head)
       int lim;  // last key this row may see (-1: none)
       if constexpr (!PREFIX) {
-        lim = min(ctx + pos, kv_len - 1);
+        lim = row_used ? min(ctx + pos, kv_len - 1) : -1;
       } else {
-        lim = pos < m_hi ? p.prefix[s0 + pos] - 1 : -1;
+        lim = row_used && pos < m_hi ? p.prefix[s0 + pos] - 1 : -1;
       }
       // e4m3: scores are scaled to log2 units before the max (sl2 then 1).
       const float sl2 = KV8 ? 1.f : p.scale_log2;
@@ -884,7 +887,7 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
         if constexpr (!PREFIX) {
           const float inv = 1.f / (l * pw);  // pw = 2^kap with an e4m3 cache, else 1
           T* orow = static_cast<T*>(p.out) + ((int64_t)(q0 + pos) * p.num_q_heads + kvh * G + head) * kD;
-          const bool valid = pos < ql;
+          const bool valid = row_used && pos < ql;
 #pragma unroll
           for (int cc = 0; cc < kD / 32; ++cc) {
             uint32_t ov[32];
@@ -985,10 +988,8 @@ int launch_prefill(const PrefillParams& p0, const void* k_cache, const void* v_c
                    cudaStream_t stream, const DecodeParams* beside) {
   PrefillParams p = p0;
   if (p.head_dim != pf::kD) return PA_ERR_UNSUPPORTED;
-  if (p.group < 1 || p.group > pf::kM || (p.group & (p.group - 1))) return PA_ERR_UNSUPPORTED;
-  int gs = 0;
-  while ((1 << gs) < p.group) ++gs;
-  p.gshift = gs;
+  if (p.group < 1 || p.group > pf::kM) return PA_ERR_UNSUPPORTED;
+  p.tile_pos = pf::kM / p.group;
   CUtensorMap qmap, kmap, vmap;
   {
     // q seen as [total_q][num_q_heads][head_dim]; box = 64 columns x G heads x 128/G positions.
@@ -1020,10 +1021,8 @@ int launch_prefix_pass(const PrefillParams& p0, const void* k_cache, const void*
                        cudaStream_t stream) {
   PrefillParams p = p0;
   if (p.head_dim != pf::kD) return PA_ERR_UNSUPPORTED;
-  if (p.group < 1 || p.group > pf::kM || (p.group & (p.group - 1))) return PA_ERR_UNSUPPORTED;
-  int gs = 0;
-  while ((1 << gs) < p.group) ++gs;
-  p.gshift = gs;
+  if (p.group < 1 || p.group > pf::kM) return PA_ERR_UNSUPPORTED;
+  p.tile_pos = pf::kM / p.group;
   CUtensorMap qmap, kmap, vmap;
   // Decode queries [num_seqs][num_q_heads][head_dim]: members of a group are
   // consecutive sequences, so a tile is one box of 128/G sequences x G heads.

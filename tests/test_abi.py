@@ -127,7 +127,8 @@ def test_prefill_host_checks(lib):
     assert call(n=0) == 0                    # empty batch
     assert call(tq=0) == 0
     assert call(d=64) == -10                 # chunk kernel needs head_dim 128
-    assert call(hq=12, hkv=4) == -10         # group 3 is not a power of two
+    assert call(hq=12, hkv=4) == -5          # group 3 is supported: only the workspace is missing
+    assert call(hq=258, hkv=2) == -10        # group 129: above the 128 rows of a tensor-core tile
     assert call(hq=6, hkv=4) == -3
     assert call(mq=100, tq=64) == -1         # max_q_len above total_q
     assert call() == -5                      # workspace required

@@ -76,6 +76,7 @@ SP_CASES = [
     ("bf16", 32, 32, 8, [300] * 20 + [20, 700], 20, 256),               # group 4: 32 members per tile
     ("bf16", 16, 64, 8, list(range(100, 100 + 37 * 45, 45)), 37, 512),  # 37 members: 3 tiles of 16
     ("f16", 16, 128, 8, [129, 400, 1024, 77], 2, 128),                  # group 16: 8 members per tile
+    ("bf16", 16, 48, 8, list(range(90, 90 + 45 * 30, 30)), 45, 64),     # GQA group 6: 21 members per tile
 ]
 
 
@@ -193,6 +194,7 @@ PF_CASES = [
     ("bf16", 32, 16, 8, [64, 9], [65, 0]),              # group 2
     ("bf16", 32, 64, 8, [512, 1, 1], [1000, 700, 30]),  # a long chunk over a long context
     ("f16", 16, 128, 1, [3, 2, 5, 1], [7, 40, 0, 9]),   # group 128: one position per Q tile
+    ("bf16", 16, 28, 4, [50, 1, 130], [20, 9, 0]),      # group 7: 18 positions, 126 rows per tile
 ]
 
 

@@ -32,6 +32,12 @@ CASES = [
     ("f16", 32, 64, 8, [512], [1000]),               # a long chunk over a long context
     ("bf16", 16, 64, 2, [9, 4, 13], [30, 0, 100]),   # group 32: 4 positions per Q tile
     ("f16", 16, 128, 1, [3, 2, 5, 1], [7, 40, 0, 9]),  # group 128: one position per Q tile
+    # Groups that do not divide 128: a Q tile holds floor(128 / G) positions
+    # x G heads and its last rows hold nothing.
+    ("bf16", 16, 24, 8, [33, 1, 70, 130], [10, 50, 0, 3]),  # group 3: 42 positions, 126 rows
+    ("f16", 32, 28, 4, [100, 9, 1, 37], [0, 200, 31, 64]),  # group 7: 18 positions, 126 rows
+    ("bf16", 32, 96, 8, [20, 5, 23], [100, 7, 0]),          # group 12: 10 positions, 120 rows
+    ("f16", 16, 80, 8, [13, 1, 25], [3, 9, 40]),            # group 10: 12 positions, 120 rows
 ]
 
 

@@ -39,6 +39,8 @@ CASES = [
     ("bf16", 16, 32, 8, [300] * 20 + [20, 700], 20, 256),      # group 4: 20 members > 32/tile? no: 32/tile
     ("bf16", 16, 64, 8, list(range(100, 100 + 37 * 45, 45)), 37, 512),  # 37 members: 3 tiles of 16
     ("f16", 16, 128, 8, [129, 400, 1024, 77], 2, 128),        # group 16: 8 members per tile
+    ("bf16", 16, 48, 8, list(range(90, 90 + 45 * 30, 30)), 45, 64),  # GQA group 6: 21 members per tile
+    ("f16", 32, 96, 8, [300, 40, 900, 64, 65, 500, 33, 128] * 3, 12, 64),  # GQA group 12: 10 per tile
 ]
 
 
