@@ -138,6 +138,7 @@ enum ItemOut : int {
   kOutPartial = 0,     // fp32 partial into its slot (merged later)
   kOutDirect = 1,      // the sequence's only partition: normalised output
   kOutWithPrefix = 2,  // the only suffix partition: merged here with the prefix pass's partial (slot 0)
+  kOutSkip = 3,        // a row with an illegal length (its output was zeroed by the plan): nothing to write
 };
 
 struct ItemMeta {
@@ -188,7 +189,10 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
   // beside the chunk kernel, and wait for it before exiting; they let the
   // merge kernel launch only as they exit, so its CTAs take no SM that a
   // decode CTA could use once a chunk CTA leaves.
-  const bool overlap = p.planned && (p.prefix || p.beside);
+  // Standalone plain decode runs each CTA's first work item (known without
+  // the plan, see DecodeParams::static_first) while the plan runs; the
+  // producer waits for the plan before it takes further items.
+  const bool overlap = (p.planned && (p.prefix || p.beside)) || p.static_first;
   if (!overlap) pdl_wait();
   if (!p.beside) pdl_trigger();
   const uint32_t ring0 = smem_u32(smem + C::kRing);
@@ -199,15 +203,28 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
     }
-    const int total = p.work[1];
+    // First item: CTA c < first_static runs item c (row c / hr, its first
+    // partition) before the plan has finished; every other CTA, and every
+    // later item, comes from the plan's list and the work counter.
+    const bool stat = p.static_first && (int)blockIdx.x < p.first_static;
+    bool planned_now = !p.static_first;  // the plan's results are visible to this warp
+    if (p.static_first && !stat) {
+      pdl_wait();
+      planned_now = true;
+    }
+    int total = planned_now ? p.work[1] : 0x7fffffff;
     int next = 0;
-    if (lane == 0) next = atomicAdd(&p.work[0], 1);
-    next = __shfl_sync(0xffffffffu, next, 0);
+    if (stat) {
+      next = blockIdx.x;
+    } else {
+      if (lane == 0) next = atomicAdd(&p.work[0], 1);
+      next = __shfl_sync(0xffffffffu, next, 0);
+    }
     // The (sequence, partition) pair and length of the next item are loaded
     // one item ahead, so the item switch costs no dependent global loads.
     int next_pr = 0, next_qrow = 0, next_len = 0, next_pfx = 0;
     if (next < total) {
-      next_pr = p.pairs[next / hr];
+      next_pr = stat ? (next / hr) << 16 : p.pairs[next / hr];
       decode_row(p, next_pr >> 16, next_qrow, next_len);
       next_pfx = p.prefix ? p.prefix[next_pr >> 16] : 0;
     }
@@ -232,12 +249,17 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
         break;
       }
       const int pr = next_pr, qrow = next_qrow, len = next_len, pfx = next_pfx;
-      if (lane == 0) next = atomicAdd(&p.work[0], 1);  // fetch the following item
+      // fetch the following item (a CTA that started ahead of the plan does
+      // so once its first item is issued)
+      if (planned_now && lane == 0) next = atomicAdd(&p.work[0], 1);
       const int hg = item - (item / hr) * hr;
       const int seq = pr >> 16, part = pr & 0xffff;
       const int kvh = hg / p.row_groups, rgi = hg - kvh * p.row_groups;
       const int t_begin = pfx + part * p.partition;  // the suffix starts after the shared prefix
-      const int t_end = min(t_begin + p.partition, len);
+      // A row of illegal length (listed only so that first partitions keep
+      // their places) gets no stages and no output.
+      const bool skip = p.static_first && !len_ok(p, len);
+      const int t_end = skip ? t_begin : min(t_begin + p.partition, len);
       const int nsub16 = (t_end - t_begin + 15) / 16;                 // 16-token sub-tiles
       const int nsub = (nsub16 + C::kSubTiles - 1) / C::kSubTiles;    // stages
       // Items are padded to a multiple of 4 stages with empty stages, so
@@ -260,7 +282,7 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
         m.part = p.slot0 + part;
         const int ns = (len - pfx + p.partition - 1) / p.partition;  // suffix partitions
         m.n_parts = ns + (pfx > 0 ? 1 : 0);
-        m.out_mode = ns > 1 ? kOutPartial : (pfx > 0 ? kOutWithPrefix : kOutDirect);
+        m.out_mode = skip ? kOutSkip : ns > 1 ? kOutPartial : (pfx > 0 ? kOutWithPrefix : kOutDirect);
         m.hg = seq * hr + hg;
         const uint32_t fb = smem_u32(&ifull[slot]);
         mbar_arrive_expect_tx(fb, nrows * D * 2);
@@ -367,7 +389,7 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
           }
           jg += n;
         }
-        if (ub == 0) {
+        if (ub == 0 && planned_now) {
           // The counter has answered by now: load the next item's metadata
           // while the rest of this item is issued.
           next = __shfl_sync(0xffffffffu, next, 0);
@@ -385,6 +407,20 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
         }
       }
       if (bad) break;
+      if (!planned_now) {
+        // The first item is issued: wait for the plan, then take the next
+        // item from its list.
+        pdl_wait();
+        planned_now = true;
+        total = p.work[1];
+        if (lane == 0) next = atomicAdd(&p.work[0], 1);
+        next = __shfl_sync(0xffffffffu, next, 0);
+        if (next < total) {
+          next_pr = p.pairs[next / hr];
+          decode_row(p, next_pr >> 16, next_qrow, next_len);
+          next_pfx = p.prefix ? p.prefix[next_pr >> 16] : 0;
+        }
+      }
     }
     if (bad && lane < C::kStages) {
       // Let copies still in flight land before the CTA exits: lane s waits
@@ -853,7 +889,9 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
         acc.z += v.z;
         acc.w += v.w;
       }
-      if (mt.out_mode == kOutWithPrefix) {
+      if (mt.out_mode == kOutSkip) {
+        // nothing to write
+      } else if (mt.out_mode == kOutWithPrefix) {
         // Merge with the prefix pass's partial (written by the previous
         // launch on this stream): M' = max(M, m0), weights 2^(M - M'), 2^(m0 - M').
         pdl_wait();
@@ -1116,16 +1154,23 @@ static int launch_tc(const DecodeParams& p, cudaStream_t stream) {
   if (rc != PA_OK) return rc;
   auto kern = decode_tc_kernel<T, D, BS, NT, KV8, E5>;
   if (set_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)C::kSmem) != PA_OK) return PA_ERR_CUDA;
-  if (!p.planned) {
-    decode_plan_kernel<T><<<1, 1024, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-  }
   const int64_t upper = (int64_t)p.num_seqs * p.max_parts * p.num_kv_heads * p.row_groups;
   const int64_t resident = (NT == 1 ? 2LL : 1LL) * num_sms_current_device();
   const int ctas = (int)(upper < resident ? upper : resident);
-  if (launch_dependent(kern, dim3(ctas), dim3(C::kThreads), C::kSmem, stream, kmap, vmap, p) != cudaSuccess)
+  DecodeParams pk = p;
+  if (!p.planned) {
+    // Standalone plain decode: the first items run while the plan runs.
+    if (!p.cu_q_lens && !p.prefix) {
+      const int64_t firsts = (int64_t)p.num_seqs * p.num_kv_heads * p.row_groups;
+      pk.static_first = 1;
+      pk.first_static = (int32_t)(firsts < ctas ? firsts : ctas);
+    }
+    decode_plan_kernel<T><<<1, 1024, 0, stream>>>(pk);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  }
+  if (launch_dependent(kern, dim3(ctas), dim3(C::kThreads), C::kSmem, stream, kmap, vmap, pk) != cudaSuccess)
     return PA_ERR_CUDA;
-  return launch_merge(p, dt, stream);
+  return launch_merge(pk, dt, stream);
 }
 
 template <int VEC>

@@ -59,6 +59,13 @@ struct DecodeParams {
   // kernel start; the decode streams at once, beside it, and waits for it
   // only before exiting.
   int32_t beside;
+  // Standalone plain decode: the plan lists every row's first partition
+  // first, in row order (rows with an illegal length too, as items the
+  // kernel skips), so work item i < num_seqs * heads_per_row is known
+  // without the plan: CTA c < first_static runs item c while the plan runs,
+  // and the plan starts the work counter at first_static.
+  int32_t static_first;
+  int32_t first_static;
   // 8-bit KV cache: (K, V) scale per (block, KV head), float32
   // [num_blocks][num_kv_heads][2]; nullptr when the pools hold q's dtype.
   const float* kv_scales;

@@ -80,6 +80,7 @@ __device__ __forceinline__ void decode_plan_body(const DecodeParams& p, const in
     int qrow, len;
     if (!row(s, qrow, len)) continue;
     if (!len_ok(p, len)) {
+      if (p.static_first) ++cnt0;  // keeps its place in the first section; the kernel skips it
       record_error(p.status, PA_ERR_SEQLEN);
       T* out = static_cast<T*>(p.out) + (int64_t)qrow * p.num_q_heads * p.head_dim;
       for (int i = 0; i < p.num_q_heads * p.head_dim; ++i) out[i] = T(0.0f);
@@ -104,7 +105,11 @@ __device__ __forceinline__ void decode_plan_body(const DecodeParams& p, const in
   const int total = total0 + nbin_total;
   for (int s = s0; s < s1; ++s) {
     int qrow, len;
-    if (!row(s, qrow, len) || !len_ok(p, len)) continue;
+    if (!row(s, qrow, len)) continue;
+    if (!len_ok(p, len)) {
+      if (p.static_first) p.pairs[base0++] = s << 16;
+      continue;
+    }
     const int sl = len - prefix_of(s);
     const int n = (sl + P - 1) / P;
     const int first_binned = p.prefix ? 0 : 1;
@@ -120,7 +125,7 @@ __device__ __forceinline__ void decode_plan_body(const DecodeParams& p, const in
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    p.work[0] = 0;
+    p.work[0] = p.static_first ? p.first_static : 0;  // items below first_static are taken already
     p.work[1] = total * p.num_kv_heads * p.row_groups;
     p.work[2] = n_merge;
   }
