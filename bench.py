@@ -342,15 +342,19 @@ import numpy as np
 sys.path.insert(0, {root!r})
 import oracle
 import oracle.fp8_kv as f8
-from workloads import make_config, e4m3_pool
+from workloads import make_config, e4m3_pool, e5m2_pool
 b = make_config({config!r})
-fp8 = {fp8!r}
+fmt = {fmt!r}  # "native", "e4m3" or "e5m2"
+fp8 = fmt != "native"
 if fp8:
-    kc, vc, sc = (x.numpy() for x in e4m3_pool(b.meta.get("seed", 0), b.num_blocks, b.num_kv_heads,
-                                               b.block_size, b.head_dim))
+    pool_of = e5m2_pool if fmt == "e5m2" else e4m3_pool
+    write8 = f8.reshape_and_cache_e5m2 if fmt == "e5m2" else f8.reshape_and_cache_fp8
+    deq = f8.dequantize_e5m2 if fmt == "e5m2" else f8.dequantize
+    kc, vc, sc = (x.numpy() for x in pool_of(b.meta.get("seed", 0), b.num_blocks, b.num_kv_heads,
+                                             b.block_size, b.head_dim))
     f8.copy_blocks_fp8(kc, vc, sc, b.cow_pairs)
     slots = oracle.slot_mapping(b.block_tables, b.new_seq_ids, b.new_positions, b.block_size)
-    f8.reshape_and_cache_fp8(b.k_new.float().numpy(), b.v_new.float().numpy(), slots, kc, vc, sc, b.block_size)
+    write8(b.k_new.float().numpy(), b.v_new.float().numpy(), slots, kc, vc, sc, b.block_size)
 else:
     kc = b.k_cache.clone(); vc = b.v_cache.clone()
     oracle.copy_blocks(kc, vc, b.cow_pairs)
@@ -362,11 +366,11 @@ def decode_one(i):
     if not fp8:
         oracle.decode(b.q, kc, vc, b.block_tables, b.kv_lens, b.scale, b.block_size, seqs=[i])
         return i
-    # e4m3: dequantise the sequence's blocks, then the same decode.
+    # 8-bit pools: dequantise the sequence's blocks, then the same decode.
     nb = -(-int(b.kv_lens[i]) // b.block_size)
     blocks = b.block_tables[i][:nb]
-    kd = f8.dequantize(kc[blocks], sc[blocks, :, 0])
-    vd = f8.dequantize(vc[blocks], sc[blocks, :, 1])
+    kd = deq(kc[blocks], sc[blocks, :, 0])
+    vd = deq(vc[blocks], sc[blocks, :, 1])
     tables = np.zeros_like(b.block_tables)
     tables[i, :nb] = np.arange(nb)
     oracle.decode(b.q, kd, vd, tables, b.kv_lens, b.scale, b.block_size, seqs=[i])
@@ -408,7 +412,7 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def run_oracle_sample(config: str, budget_s: float, reps: int, fp8: bool = False,
+def run_oracle_sample(config: str, budget_s: float, reps: int, fmt: str = "native",
                       workers: int | None = None, total_s: float = 1e9) -> list[dict]:
     """Up to `reps` timed passes of the oracle over the workload's sequences
     (each cut at budget_s), stopping once total_s seconds have been timed."""
@@ -416,7 +420,7 @@ def run_oracle_sample(config: str, budget_s: float, reps: int, fp8: bool = False
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
-    code = ORACLE_SNIPPET.format(root=ROOT, config=config, budget=budget_s, reps=reps, fp8=fp8,
+    code = ORACLE_SNIPPET.format(root=ROOT, config=config, budget=budget_s, reps=reps, fmt=fmt,
                                  workers=workers or host_cores(), total=total_s)
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
     for line in r.stdout.splitlines():
@@ -440,12 +444,12 @@ def per_seq_decode_bytes(batch, kv_esize: int | None = None) -> np.ndarray:
     return batch.kv_lens.astype(np.float64) * per_tok + qo
 
 
-def cpu_baseline_entry(res: dict, value: float, unit: str, fp8: bool, num_seqs: int) -> dict:
+def cpu_baseline_entry(res: dict, value: float, unit: str, fmt: str, num_seqs: int) -> dict:
     return {"value": round(value, 6), "unit": unit, "cores": res["workers"], "kind": "oracle",
             "host_cores": host_cores(), "blas_threads_per_worker": 1,
             "sample": f"decode of {len(res['seqs'])} of {num_seqs} sequences ({res['tokens']} keys) in "
                       f"{res['seconds']:.2f} s, fp64 numpy, {res['workers']} worker processes x 1 thread, "
-                      "one sequence per task" + (" (e4m3 pools dequantised per sequence)" if fp8 else "")}
+                      "one sequence per task" + (f" ({fmt} pools dequantised per sequence)" if fmt != "native" else "")}
 
 
 # ---------------------------------------------------------------------------
@@ -469,7 +473,7 @@ def reference_arm(args) -> None:
     value = byts / secs / 1e9
     merged = {"seconds": secs, "seqs": [i for r in timed for i in r["seqs"]],
               "tokens": sum(r["tokens"] for r in timed), "workers": timed[0]["workers"]}
-    cpu = cpu_baseline_entry(merged, value, "GB/s", False, batch.num_seqs * len(timed))
+    cpu = cpu_baseline_entry(merged, value, "GB/s", "native", batch.num_seqs * len(timed))
     cpu["sample"] = (f"{len(timed)} steps, each one pass over the {batch.num_seqs} sequences in a seeded order "
                      f"(cut at ~{budget:.1f} s): " + cpu["sample"])
     line = {
@@ -630,7 +634,7 @@ def native_arm(args) -> None:
 
     import paged_kv_cache_14_gb300 as pa
     from paged_kv_cache_14_gb300.step import HostPipeline, step_from_host
-    from workloads import e4m3_pool, make_config
+    from workloads import e4m3_pool, e5m2_pool, make_config
 
     rank, world, local = dist_info()
     torch.cuda.set_device(local)
@@ -638,12 +642,29 @@ def native_arm(args) -> None:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     pa.load()
     batch = make_config(args.config)
-    fp8 = args.kv_cache == "e4m3"
+    fp8 = args.kv_cache in ("e4m3", "e5m2")
     shared = batch.is_decode and (args.decode == "shared_prefix" or (
         args.decode == "auto" and batch.prefix_lens is not None and bool(batch.prefix_lens.any())))
-    pool = e4m3_pool(batch.meta["seed"], batch.num_blocks, batch.num_kv_heads, batch.block_size,
-                     batch.head_dim) if fp8 else None
-    st = step_from_host(batch, partition_size=args.partition, shared_prefix=shared, fp8_pool=pool)
+    pool = (e5m2_pool if args.kv_cache == "e5m2" else e4m3_pool)(
+        batch.meta["seed"], batch.num_blocks, batch.num_kv_heads, batch.block_size, batch.head_dim) if fp8 else None
+    st = step_from_host(batch, partition_size=args.partition, shared_prefix=shared, fp8_pool=pool,
+                        kv_format=args.kv_cache if fp8 else "e4m3")
+    if args.attention_once:
+        # One attention call after warm-up steps, nothing timed: the command
+        # the committed ncu summaries capture (its last launches are one
+        # cache side and one attention call).
+        for _ in range(args.warmup):
+            st.run()
+        torch.cuda.synchronize()
+        st.prepare()
+        st.attend()
+        torch.cuda.synchronize()
+        status = pa.pa_get_status()
+        print(json.dumps({"attention_once": args.config, "kv_cache": args.kv_cache, "kernels": st.attention_kernels,
+                          "status": status}), flush=True)
+        if status != 0:
+            raise RuntimeError(f"device status: {pa.pa_strerror(status)}")
+        return
     kv_es = 1 if fp8 else None
     dec_bytes = decode_algorithmic_bytes(batch, kv_es)
     step_bytes = dec_bytes["total"] + step_extra_bytes(batch, kv_es)
@@ -745,12 +766,12 @@ def native_arm(args) -> None:
     if rank == 0 and not args.no_cpu_baseline and st.is_decode:
         # Passes over the batch until about cpu_seconds are timed; the first
         # pass (worker start-up, first touch of the pools) is not counted.
-        runs = run_oracle_sample(args.config, args.cpu_seconds, 1000, fp8=fp8, total_s=args.cpu_seconds)
+        runs = run_oracle_sample(args.config, args.cpu_seconds, 1000, fmt=args.kv_cache, total_s=args.cpu_seconds)
         timed = runs[1:] or runs
         res = {"seconds": sum(r["seconds"] for r in timed), "seqs": [i for r in timed for i in r["seqs"]],
                "tokens": sum(r["tokens"] for r in timed), "workers": timed[0]["workers"]}
         gbs, sps = oracle_rate(res, per_seq_decode_bytes(batch, kv_es))
-        cpu = cpu_baseline_entry(res, gbs, "GB/s", fp8, batch.num_seqs * len(timed))
+        cpu = cpu_baseline_entry(res, gbs, "GB/s", args.kv_cache, batch.num_seqs * len(timed))
         cpu["sample"] = f"{len(timed)} passes over the batch after one untimed pass: " + cpu["sample"]
         cpu["seq_steps_per_s"] = round(sps, 4)
     if rank == 0:
@@ -758,8 +779,8 @@ def native_arm(args) -> None:
             "metric": METRIC,
             "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else batch.dtype,
-            "data": "synthetic (seeded)" + (", e4m3 pools drawn as codes + per-block scales" if fp8 else ""),
+            "scaling": "weak", "vs_baseline": None, "dtype": args.kv_cache if fp8 else batch.dtype,
+            "data": "synthetic (seeded)" + (f", {args.kv_cache} pools drawn as codes + per-block scales" if fp8 else ""),
             "pct_of_peak": round(100.0 * value / world / peak, 2),
             "seq_steps_per_s": round(world * batch.num_seqs / (ms_step * 1e-3), 1),
             "timing": {"timed_blocks": reps, "steps_per_block": args.steps,
@@ -773,7 +794,7 @@ def native_arm(args) -> None:
                 "cow_pairs": int(len(batch.cow_pairs)), "partition": pa.pa_decode_partition_size(
                     batch.num_seqs, batch.num_q_heads, batch.num_kv_heads, batch.block_size, batch.max_seq_len,
                     args.partition),
-                "kv_cache": ("e4m3 codes + fp32 (K, V) scale per (block, KV head); q/out " + batch.dtype)
+                "kv_cache": (f"{args.kv_cache} codes + fp32 (K, V) scale per (block, KV head); q/out " + batch.dtype)
                 if fp8 else batch.dtype,
                 "step": st.step_calls, "step_bytes": step_bytes, "decode_bytes": dec_bytes,
                 "launches_per_step": st.launches,
@@ -807,8 +828,10 @@ def main():
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--decode", choices=("auto", "plain", "shared_prefix"), default="auto",
                     help="auto: shared-prefix decode when the workload's sequences share prefix blocks")
-    ap.add_argument("--kv-cache", choices=("native", "e4m3"), default="native",
-                    help="native: the pools hold q's dtype; e4m3: e4m3 codes with per-block scales")
+    ap.add_argument("--kv-cache", choices=("native", "e4m3", "e5m2"), default="native",
+                    help="native: the pools hold q's dtype; e4m3 / e5m2: 8-bit codes with per-block scales")
+    ap.add_argument("--attention-once", action="store_true",
+                    help="run warm-up steps, then one cache side and one attention call, and exit (for ncu)")
     ap.add_argument("--min-timed-ms", type=float, default=1000.0,
                     help="device time the repeated K-step blocks cover")
     ap.add_argument("--e2e-steps", type=int, default=400)

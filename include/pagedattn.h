@@ -251,7 +251,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache, const int
  *                  sequence (same result, no saving). Malformed group_starts
  *                  record PA_ERR_ARG and disable every hint.
  *   workspace    : pa_decode_shared_prefix_workspace_size() bytes.
- * Other arguments as pa_decode. fp16/bf16, head_dim 128, GQA group G of at
+ * Other arguments as pa_decode. fp16/bf16, head_dim 64 or 128, GQA group G of at
  * most 128 (2 * floor(128 / G) members per tensor-core work item, in two
  * tiles; larger groups take several items), scale > 0.
  */
@@ -374,7 +374,7 @@ int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, c
  *                no initialisation needed; not shared by overlapping calls
  * Rows with q_len == 1 go through the decode path (any supported dtype and
  * head_dim); longer chunks through a tcgen05 tensor-core kernel that needs
- * fp16/bf16, head_dim 128, a GQA group G of at most 128 (a tensor-core tile
+ * fp16/bf16, head_dim 64 or 128, a GQA group G of at most 128 (a tensor-core tile
  * holds floor(128 / G) query positions x G heads)
  * (PA_ERR_DTYPE / PA_ERR_UNSUPPORTED otherwise) and scale > 0 (PA_ERR_ARG).
  */

@@ -354,7 +354,7 @@ static int shared_prefix_decode(const void* q, const void* k_cache, const void* 
   if (num_groups < 1 || num_groups > num_seqs || !group_starts || !prefix_lens) return PA_ERR_ARG;
   if (dtype == PA_F32) return PA_ERR_DTYPE;
   if (!(scale > 0.f)) return PA_ERR_ARG;  // the prefix pass needs scale > 0
-  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (head_dim != 128 && !(head_dim == 64 && !kv_scales)) return PA_ERR_UNSUPPORTED;
   if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads) return PA_ERR_HEADS;
   const int32_t g = num_q_heads / num_kv_heads;
   if (g > 128) return PA_ERR_UNSUPPORTED;
@@ -823,7 +823,7 @@ static int chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_l
   if (dtype == PA_F32 && max_q_len > 1) return PA_ERR_DTYPE;
   if (max_q_len > 1 && !(scale > 0.f)) return PA_ERR_ARG;  // the chunk kernel needs scale > 0
   if (max_q_len > 1) {
-    if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 128 && !(head_dim == 64 && !kv_scales)) return PA_ERR_UNSUPPORTED;
     if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads) return PA_ERR_HEADS;
     const int32_t g = num_q_heads / num_kv_heads;
     if (g > 128) return PA_ERR_UNSUPPORTED;

@@ -49,7 +49,7 @@ namespace pf {
 constexpr int kM = 128;          // rows per Q tile (tensor-memory lanes)
 constexpr int kQT = 2;           // Q tiles per work item, one softmax warpgroup each
 constexpr int kRows = kM * kQT;  // packed rows per work item
-constexpr int kD = 128;          // head_dim
+constexpr int kD = 128;          // largest head_dim: the shared-memory tiles are laid out for it
 constexpr int kN = 128;          // keys per KV tile
 constexpr int kSubTiles = kN / 16;  // 16-token sub-tiles per KV tile
 constexpr int kThreads = 64 + kQT * 128;  // producer, MMA, one softmax warpgroup per Q tile
@@ -260,15 +260,20 @@ __global__ void __launch_bounds__(1024) mixed_plan_kernel(const PrefillParams p,
 // times 2^kap, kap the largest exponent keeping every weight of the item
 // seen so far below 2^7 (P stays below 2^15 in fp16); O is rescaled exactly
 // when kap drops and divided by 2^kap at the end. The row sum takes p alone.
-template <typename T, int BS, bool PREFIX, bool KV8, bool E5 = false>
+// D = head_dim, 128 or 64 (16-bit caches): a tile is D / 64 swizzled
+// 64-column halves of 128-byte rows (the layout is sized for 128).
+template <typename T, int BS, bool PREFIX, bool KV8, bool E5 = false, int D = 128>
 __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
   using namespace pf;
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static_assert(!KV8 || D == 128, "8-bit caches at head_dim 128");
+  constexpr int kH = D / 64;  // 64-column halves per row
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value && !KV8;  // the MMA's 16-bit type
   using MT = typename std::conditional<KV8, __half, T>::type;             // P's 16-bit type
   constexpr uint32_t kIdescS = idesc_f16(kM, kN, kBf16, false);  // S = Q K^T
-  constexpr uint32_t kIdescO = idesc_f16(kM, kD, kBf16, true);   // O += P V (V MN-major)
+  constexpr uint32_t kIdescO = idesc_f16(kM, D, kBf16, true);    // O += P V (V MN-major)
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   const uint32_t b_q = smem_u32(&bars[kBarQ]);
@@ -379,11 +384,11 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
       if (lane == 0) {
         // The box holds pp * G of the tile's 128 rows (all of them when G
         // divides 128); the rest of the tile is never read into an output.
-        mbar_arrive_expect_tx(b_q, kQT * 2 * pp * G * 128);
+        mbar_arrive_expect_tx(b_q, kQT * kH * pp * G * 128);
 #pragma unroll
         for (int t = 0; t < kQT; ++t)
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
+          for (int h = 0; h < kH; ++h)
             tma_load_3d(sbase + kOffQ + t * kQBytes + h * kQHalf, &qmap, h * 64, kvh * G, q_z + t * pp, b_q);
       }
       const int32_t* bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
@@ -433,7 +438,7 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
         const int id = id_of(x);
         if (lane == 0) {
           if (g >= ns && !mbar_wait(b_empty, ((g / ns) & 1) ^ 1, p.status)) bad = true;
-          else mbar_arrive_expect_tx(b_full, KV8 ? kKVHalf : kKBytes);
+          else mbar_arrive_expect_tx(b_full, KV8 ? kKVHalf : kH * kKVHalf);
         }
         bad = __shfl_sync(0xffffffffu, bad, 0);
         if (bad) return;
@@ -446,7 +451,7 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
           } else {
             const uint32_t dst = sbase + (is_v ? kOffV : kOffK) + st * kKBytes + lane * 2048;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) tma_load_2d(dst + h * kKVHalf, is_v ? &vmap : &kmap, h * 64, row, b_full);
+            for (int h = 0; h < kH; ++h) tma_load_2d(dst + h * kKVHalf, is_v ? &vmap : &kmap, h * 64, row, b_full);
           }
         }
         if (is_v) v_issued = x + 1;
@@ -491,7 +496,7 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
           const uint64_t ka = dk + (uint64_t)((g % NK) * (kKBytes >> 4));
           const uint64_t qa = dq + (uint64_t)(t * (kQBytes >> 4));
 #pragma unroll
-          for (int k = 0; k < kD / 16; ++k)
+          for (int k = 0; k < D / 16; ++k)
             tc_mma_f16(tmem + col_s(t), qa + (((k >> 2) * kQHalf + (k & 3) * 32) >> 4),
                        ka + (((k >> 2) * kKVHalf + (k & 3) * 32) >> 4), kIdescS, k > 0);
           tc_commit(b_sfull0 + 8 * t);
@@ -750,8 +755,8 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
             if (!mbar_wait(b_vfull0 + 8 * sv, (g / NV) & 1, p.status)) return false;
             uint8_t* vst = smem + kOffV + sv * kKBytes;
             const int first = max(kv_len - k0, 0);
-            for (int idx = threadIdx.x - 32 * kSoftmaxWarp0 - 128 * t; idx < (kN - first) * 16; idx += 128) {
-              const int r = first + idx / 16, c = idx % 16;  // row, 16-byte chunk over both halves
+            for (int idx = threadIdx.x - 32 * kSoftmaxWarp0 - 128 * t; idx < (kN - first) * 8 * kH; idx += 128) {
+              const int r = first + idx / (8 * kH), c = idx % (8 * kH);  // row, 16-byte chunk over the halves
               *reinterpret_cast<int4*>(vst + (c >> 3) * kKVHalf + r * 128 + (c & 7) * 16) = make_int4(0, 0, 0, 0);
             }
             fence_async_shared();
@@ -763,7 +768,7 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
         // preceded S_t(g)'s.
         auto rescale_o = [&](float f) {
 #pragma unroll 1
-          for (int cc = 0; cc < kD / 16; ++cc) {
+          for (int cc = 0; cc < D / 16; ++cc) {
             uint32_t orow[16];
             tmem_ld16(to + cc * 16, orow);
             tmem_ld_wait();
@@ -886,10 +891,10 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
         tc_fence_after();
         if constexpr (!PREFIX) {
           const float inv = 1.f / (l * pw);  // pw = 2^kap with an e4m3 cache, else 1
-          T* orow = static_cast<T*>(p.out) + ((int64_t)(q0 + pos) * p.num_q_heads + kvh * G + head) * kD;
+          T* orow = static_cast<T*>(p.out) + ((int64_t)(q0 + pos) * p.num_q_heads + kvh * G + head) * D;
           const bool valid = row_used && pos < ql;
 #pragma unroll
-          for (int cc = 0; cc < kD / 32; ++cc) {
+          for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t ov[32];
             tmem_ld32(to + cc * 32, ov);
             tmem_ld_wait();
@@ -909,14 +914,14 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
           const int64_t base = ((int64_t)(s0 + pos) * p.num_q_heads + kvh * G + head) * p.max_parts;
           const float ipw = 1.f / pw;  // exact: a power of two
 #pragma unroll
-          for (int cc = 0; cc < kD / 32; ++cc) {
+          for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t ov[32];
             tmem_ld32(to + cc * 32, ov);
             tmem_ld_wait();
             if (valid) {
 #pragma unroll
               for (int c = 0; c < 32; c += 4)
-                __stcg(reinterpret_cast<float4*>(p.part_o + base * kD + cc * 32 + c),
+                __stcg(reinterpret_cast<float4*>(p.part_o + base * D + cc * 32 + c),
                        make_float4(__uint_as_float(ov[c]) * ipw, __uint_as_float(ov[c + 1]) * ipw,
                                    __uint_as_float(ov[c + 2]) * ipw, __uint_as_float(ov[c + 3]) * ipw));
             }
@@ -942,10 +947,10 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <typename T, int BS, bool PREFIX, bool KV8, bool E5>
+template <typename T, int BS, bool PREFIX, bool KV8, bool E5, int D>
 static int launch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                  const PrefillParams& p, int ctas, cudaStream_t stream) {
-  auto kern = prefill_tc_kernel<T, BS, PREFIX, KV8, E5>;
+  auto kern = prefill_tc_kernel<T, BS, PREFIX, KV8, E5, D>;
   if (set_max_dynamic_smem(reinterpret_cast<const void*>(kern), pf::kSmem) != PA_OK) return PA_ERR_CUDA;
   return launch_dependent(kern, dim3(ctas), dim3(pf::threads<KV8>()), pf::kSmem, stream, qmap, kmap, vmap, p) ==
                  cudaSuccess
@@ -953,21 +958,23 @@ static int launch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& kma
              : PA_ERR_CUDA;
 }
 
-template <bool PREFIX, bool KV8, bool E5 = false>
+template <bool PREFIX, bool KV8, bool E5 = false, int D = 128>
 static int dispatch_prefill_bs(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                const PrefillParams& p, int ctas, pa_dtype dt, cudaStream_t stream) {
   const bool bf = dt == PA_BF16;
   if (p.block_size == 16)
-    return bf ? launch_prefill_kernel<__nv_bfloat16, 16, PREFIX, KV8, E5>(qmap, kmap, vmap, p, ctas, stream)
-              : launch_prefill_kernel<__half, 16, PREFIX, KV8, E5>(qmap, kmap, vmap, p, ctas, stream);
-  return bf ? launch_prefill_kernel<__nv_bfloat16, 32, PREFIX, KV8, E5>(qmap, kmap, vmap, p, ctas, stream)
-            : launch_prefill_kernel<__half, 32, PREFIX, KV8, E5>(qmap, kmap, vmap, p, ctas, stream);
+    return bf ? launch_prefill_kernel<__nv_bfloat16, 16, PREFIX, KV8, E5, D>(qmap, kmap, vmap, p, ctas, stream)
+              : launch_prefill_kernel<__half, 16, PREFIX, KV8, E5, D>(qmap, kmap, vmap, p, ctas, stream);
+  return bf ? launch_prefill_kernel<__nv_bfloat16, 32, PREFIX, KV8, E5, D>(qmap, kmap, vmap, p, ctas, stream)
+            : launch_prefill_kernel<__half, 32, PREFIX, KV8, E5, D>(qmap, kmap, vmap, p, ctas, stream);
 }
 
 template <bool PREFIX>
 static int dispatch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                    const PrefillParams& p, int ctas, pa_dtype dt, cudaStream_t stream) {
-  if (!p.kv_scales) return dispatch_prefill_bs<PREFIX, false>(qmap, kmap, vmap, p, ctas, dt, stream);
+  if (!p.kv_scales)
+    return p.head_dim == 64 ? dispatch_prefill_bs<PREFIX, false, false, 64>(qmap, kmap, vmap, p, ctas, dt, stream)
+                            : dispatch_prefill_bs<PREFIX, false>(qmap, kmap, vmap, p, ctas, dt, stream);
   return p.kv_fmt == PA_KV_E5M2 ? dispatch_prefill_bs<PREFIX, true, true>(qmap, kmap, vmap, p, ctas, dt, stream)
                                 : dispatch_prefill_bs<PREFIX, true>(qmap, kmap, vmap, p, ctas, dt, stream);
 }
@@ -977,23 +984,23 @@ static int dispatch_prefill_kernel(const CUtensorMap& qmap, const CUtensorMap& k
 static int make_pool_maps(const PrefillParams& p, const void* k_cache, const void* v_cache, pa_dtype dt,
                           CUtensorMap* kmap, CUtensorMap* vmap) {
   const int64_t rows = (int64_t)p.num_blocks * p.num_kv_heads * p.block_size;
-  int rc = p.kv_scales ? make_u8_tensor_map(kmap, k_cache, rows, pf::kD, 16)
-                       : make_kv_tensor_map(kmap, k_cache, rows, pf::kD, dt, 16);
+  int rc = p.kv_scales ? make_u8_tensor_map(kmap, k_cache, rows, p.head_dim, 16)
+                       : make_kv_tensor_map(kmap, k_cache, rows, p.head_dim, dt, 16);
   if (rc != PA_OK) return rc;
-  return p.kv_scales ? make_u8_tensor_map(vmap, v_cache, rows, pf::kD, 16)
-                     : make_kv_tensor_map(vmap, v_cache, rows, pf::kD, dt, 16);
+  return p.kv_scales ? make_u8_tensor_map(vmap, v_cache, rows, p.head_dim, 16)
+                     : make_kv_tensor_map(vmap, v_cache, rows, p.head_dim, dt, 16);
 }
 
 int launch_prefill(const PrefillParams& p0, const void* k_cache, const void* v_cache, pa_dtype dt,
                    cudaStream_t stream, const DecodeParams* beside) {
   PrefillParams p = p0;
-  if (p.head_dim != pf::kD) return PA_ERR_UNSUPPORTED;
+  if (!(p.head_dim == 128 || (p.head_dim == 64 && !p.kv_scales))) return PA_ERR_UNSUPPORTED;
   if (p.group < 1 || p.group > pf::kM) return PA_ERR_UNSUPPORTED;
   p.tile_pos = pf::kM / p.group;
   CUtensorMap qmap, kmap, vmap;
   {
     // q seen as [total_q][num_q_heads][head_dim]; box = 64 columns x G heads x 128/G positions.
-    int rc = make_3d_tensor_map(&qmap, p.q, p.total_q, p.num_q_heads, pf::kD, dt, pf::kM / p.group, p.group, 64);
+    int rc = make_3d_tensor_map(&qmap, p.q, p.total_q, p.num_q_heads, p.head_dim, dt, pf::kM / p.group, p.group, 64);
     if (rc != PA_OK) return rc;
     rc = make_pool_maps(p, k_cache, v_cache, dt, &kmap, &vmap);
     if (rc != PA_OK) return rc;
@@ -1020,13 +1027,13 @@ int launch_prefill(const PrefillParams& p0, const void* k_cache, const void* v_c
 int launch_prefix_pass(const PrefillParams& p0, const void* k_cache, const void* v_cache, pa_dtype dt,
                        cudaStream_t stream) {
   PrefillParams p = p0;
-  if (p.head_dim != pf::kD) return PA_ERR_UNSUPPORTED;
+  if (!(p.head_dim == 128 || (p.head_dim == 64 && !p.kv_scales))) return PA_ERR_UNSUPPORTED;
   if (p.group < 1 || p.group > pf::kM) return PA_ERR_UNSUPPORTED;
   p.tile_pos = pf::kM / p.group;
   CUtensorMap qmap, kmap, vmap;
   // Decode queries [num_seqs][num_q_heads][head_dim]: members of a group are
   // consecutive sequences, so a tile is one box of 128/G sequences x G heads.
-  int rc = make_3d_tensor_map(&qmap, p.q, p.num_seqs, p.num_q_heads, pf::kD, dt, pf::kM / p.group, p.group, 64);
+  int rc = make_3d_tensor_map(&qmap, p.q, p.num_seqs, p.num_q_heads, p.head_dim, dt, pf::kM / p.group, p.group, 64);
   if (rc != PA_OK) return rc;
   rc = make_pool_maps(p, k_cache, v_cache, dt, &kmap, &vmap);
   if (rc != PA_OK) return rc;

@@ -126,7 +126,8 @@ def test_prefill_host_checks(lib):
     assert call(dt=pa.PA_F32) == -2          # fp32 chunks are not on the tensor-core path
     assert call(n=0) == 0                    # empty batch
     assert call(tq=0) == 0
-    assert call(d=64) == -10                 # chunk kernel needs head_dim 128
+    assert call(d=64) == -5                  # head_dim 64 is supported: only the workspace is missing
+    assert call(d=96) == -10                 # the chunk kernel takes head_dim 64 or 128
     assert call(hq=12, hkv=4) == -5          # group 3 is supported: only the workspace is missing
     assert call(hq=258, hkv=2) == -10        # group 129: above the 128 rows of a tensor-core tile
     assert call(hq=6, hkv=4) == -3

@@ -53,6 +53,26 @@ def test_prefill_small(lib, case):
     assert_attention_close(out, ref, dtype, str(case))
 
 
+CASES_D64 = [
+    # dtype, B, Hq, Hkv, q_lens, ctx_lens: head_dim 64 (one 64-column half per tile row)
+    ("f16", 16, 32, 8, [17, 1, 130, 40], [5, 60, 0, 300]),   # group 4
+    ("bf16", 32, 24, 8, [64, 3, 1], [100, 0, 7]),           # group 3
+    ("f16", 16, 8, 8, [129, 1], [10, 20]),                  # group 1
+    ("bf16", 16, 64, 8, [512, 1], [600, 33]),               # group 8, a long chunk
+]
+
+
+@pytest.mark.parametrize("case", CASES_D64, ids=lambda c: f"{c[0]}-B{c[1]}-G{c[2] // c[3]}-q{sum(c[4])}-D64")
+def test_prefill_head_dim_64(lib, case):
+    dtype, B, hq, hkv, qls, ctxs = case
+    kv = [c + q for c, q in zip(ctxs, qls)]
+    b = build_batch(name="pf64", seed=CASES_D64.index(case) + 150, dtype=dtype, block_size=B, num_q_heads=hq,
+                    num_kv_heads=hkv, head_dim=64, q_lens=qls, kv_lens=kv)
+    _, out = run_step(lib, b)
+    kc, vc, _ = oracle_caches_after_step(b)
+    assert_attention_close(out, oracle_prefill(b, kc, vc), dtype, f"{case} head_dim 64")
+
+
 def test_prefill_garbage_in_unused_slots(lib):
     qls, ctxs = [40, 7], [10, 90]
     b = build_batch(name="pfnan", seed=9, dtype="f16", block_size=32, num_q_heads=64, num_kv_heads=8,

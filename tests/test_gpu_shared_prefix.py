@@ -61,6 +61,23 @@ def test_shared_prefix_matches_oracle_and_decode(lib, case, partition):
     assert_attention_close(out, ref_plain, dtype, f"{case} vs pa_decode")
 
 
+@pytest.mark.parametrize("case", [("bf16", 16, 32, 8, [5, 64, 300, 65, 700, 31, 1000, 129], 4, 64),
+                                  ("f16", 32, 24, 8, [200, 40, 900, 64, 65, 500] * 2, 6, 128)],
+                         ids=["bf16-B16-G4-D64", "f16-B32-G3-D64"])
+def test_shared_prefix_head_dim_64(lib, case):
+    dtype, B, hq, hkv, lens, grp, pref = case
+    b = build_batch(name="cascade64", seed=len(lens) + 160, dtype=dtype, block_size=B, num_q_heads=hq,
+                    num_kv_heads=hkv, head_dim=64, q_lens=np.ones(len(lens), np.int32), kv_lens=lens,
+                    share_group=grp, share_prefix_tokens=pref, cow_per_seq=True)
+    assert (b.prefix_lens > 0).any()
+    st = _device_step(lib, b)
+    out = to_f64(_shared(lib, st, b))
+    assert lib.pa_get_status() == 0
+    kc, vc, _ = oracle_caches_after_step(b)
+    assert_attention_close(out, oracle_decode(b, kc, vc), dtype, f"{case} vs oracle")
+    assert_attention_close(out, to_f64(st.out), dtype, f"{case} vs pa_decode")
+
+
 def test_shared_prefix_bad_hints_still_correct(lib):
     lens = [300, 300, 900, 64, 500, 33]
     b = build_batch(name="cascade_bad", seed=81, dtype="bf16", block_size=16, num_q_heads=64, num_kv_heads=8,
