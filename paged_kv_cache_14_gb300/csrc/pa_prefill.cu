@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
   using namespace pf;
-  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static_assert(D == 64 || D == kD, "head_dim 64 or 128");
   static_assert(!KV8 || D == 128, "8-bit caches at head_dim 128");
   constexpr int kH = D / 64;  // 64-column halves per row
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value && !KV8;  // the MMA's 16-bit type
@@ -826,30 +826,41 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
             tmem_st32(ts + hh * 32, pk);
           }
         } else {
-          // e4m3: two passes over the S row in tensor memory, 32 keys at a
-          // time, so only 32 scores are held in registers. A score is
-          // s * s_K(block) * rf (log2 units). Pass 1: the row max. Pass 2:
-          // p, the row sum, and P = p * s_V(block) * 2^kap over the S columns
-          // already read (P of keys 32h.. goes to columns 16h..).
-          auto scaled = [&](uint32_t (&v)[32], int h) {
+          // 8-bit cache: two passes over the S row in tensor memory, 32 keys
+          // at a time, so only 32 scores are held in registers. A score is
+          // s * f(group), f = s_K(block) * rf >= 0 per 16-key group (log2
+          // units). Pass 1: the row max, taken on the raw scores of each
+          // group and scaled once (rounding is monotonic, so this equals the
+          // largest scaled score exactly). Pass 2: p = 2^(s * f - m) in one
+          // fused multiply-add, the row sum, and P = p * s_V(block) * 2^kap
+          // over the S columns already read (P of keys 32h.. goes to columns
+          // 16h..). Keys past the row's limit get p = 0 (their scores may be
+          // anything, NaN included).
+          auto load = [&](uint32_t (&v)[32], int h, float& f0, float& f1) {
             tmem_ld32(ts + h * 32, v);
+            f0 = __shfl_sync(0xffffffffu, csc.x, 2 * h) * rf;
+            f1 = __shfl_sync(0xffffffffu, csc.x, 2 * h + 1) * rf;
             tmem_ld_wait();
-            const float f0 = __shfl_sync(0xffffffffu, csc.x, 2 * h) * rf;
-            const float f1 = __shfl_sync(0xffffffffu, csc.x, 2 * h + 1) * rf;
+          };
+          // max_c(s_c) * f over a group; -inf if every key is masked (also when f == 0).
+          auto group_max = [&](const uint32_t (&v)[32], int c0, int key0, float f) -> float {
+            float r = -CUDART_INF_F;
+            if (full_vis) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const int key = k0 + h * 32 + c;
-              const float x = __uint_as_float(v[c]) * (c < 16 ? f0 : f1);
-              v[c] = __float_as_uint(!full_vis && key > lim ? -CUDART_INF_F : x);
+              for (int c = 0; c < 16; c += 2) r = fmax3(r, __uint_as_float(v[c0 + c]), __uint_as_float(v[c0 + c + 1]));
+            } else {
+#pragma unroll
+              for (int c = 0; c < 16; ++c) r = key0 + c > lim ? r : fmaxf(r, __uint_as_float(v[c0 + c]));
             }
+            return r == -CUDART_INF_F ? r : r * f;
           };
           float mx = -CUDART_INF_F;
 #pragma unroll 1
           for (int h = 0; h < kN / 32; ++h) {
             uint32_t v[32];
-            scaled(v, h);
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) mx = fmax3(mx, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+            float f0, f1;
+            load(v, h, f0, f1);
+            mx = fmax3(mx, group_max(v, 0, k0 + h * 32, f0), group_max(v, 16, k0 + h * 32 + 16, f1));
           }
           update_max(mx);
           if (!zero_v_tail()) { bad = true; break; }
@@ -857,22 +868,33 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
           const float oalpha = alpha * kap_r;
           const bool rescale = j > 0 && __any_sync(0xffffffffu, oalpha != 1.f);
           const float neg = m == -CUDART_INF_F ? 0.f : -m;
-          const uint64_t onex2 = f2_pack(1.f, 1.f), negx2 = f2_pack(neg, neg);
+          const uint64_t negx2 = f2_pack(neg, neg);
 #pragma unroll 1
           for (int h = 0; h < kN / 32; ++h) {
             uint32_t v[32];
-            scaled(v, h);
+            float f0, f1;
+            load(v, h, f0, f1);
             const float fv0 = __shfl_sync(0xffffffffu, csc.y, 2 * h) * pw;
             const float fv1 = __shfl_sync(0xffffffffu, csc.y, 2 * h + 1) * pw;
+            const uint64_t f0x2 = f2_pack(f0, f0), f1x2 = f2_pack(f1, f1);
+            const uint64_t fv0x2 = f2_pack(fv0, fv0), fv1x2 = f2_pack(fv1, fv1);
             uint32_t pk[16];
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
               float x0, x1;
-              f2_unpack(f2_fma(f2_pack(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), onex2, negx2), x0, x1);
-              const float a = fast_exp2(x0), b = fast_exp2(x1);
-              rs2 = f2_add(rs2, f2_pack(a, b));
-              const float f = c < 16 ? fv0 : fv1;
-              pk[c / 2] = MmaOp<MT>::pack(a * f, b * f);
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), c < 16 ? f0x2 : f1x2, negx2),
+                        x0, x1);
+              float a = fast_exp2(x0), b = fast_exp2(x1);
+              if (!full_vis) {
+                const int key = k0 + h * 32 + c;
+                a = key > lim ? 0.f : a;
+                b = key + 1 > lim ? 0.f : b;
+              }
+              const uint64_t ab = f2_pack(a, b);
+              rs2 = f2_add(rs2, ab);
+              float pa, pb;
+              f2_unpack(f2_mul(ab, c < 16 ? fv0x2 : fv1x2), pa, pb);
+              pk[c / 2] = MmaOp<MT>::pack(pa, pb);
             }
             if (h == 1 && rescale) rescale_o(oalpha);
             tmem_st16(ts + h * 16, pk);
