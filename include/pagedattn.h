@@ -373,10 +373,12 @@ int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, c
  *   workspace  : pa_chunked_prefill_workspace_size() bytes, 16-byte aligned,
  *                no initialisation needed; not shared by overlapping calls
  * Rows with q_len == 1 go through the decode path (any supported dtype and
- * head_dim); longer chunks through a tcgen05 tensor-core kernel that needs
- * fp16/bf16, head_dim 64 or 128, a GQA group G of at most 128 (a tensor-core tile
- * holds floor(128 / G) query positions x G heads)
- * (PA_ERR_DTYPE / PA_ERR_UNSUPPORTED otherwise) and scale > 0 (PA_ERR_ARG).
+ * head_dim). Longer chunks in fp16/bf16 go through a tcgen05 tensor-core
+ * kernel that needs head_dim 64 or 128, a GQA group G of at most 128 (a
+ * tensor-core tile holds floor(128 / G) query positions x G heads)
+ * (PA_ERR_UNSUPPORTED otherwise) and scale > 0 (PA_ERR_ARG); fp32 chunks go
+ * through a CUDA-core kernel with exact fp32 arithmetic (head_dim as for
+ * fp32 decode, any scale), one query row at a time: exact, not fast.
  */
 size_t pa_chunked_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t block_size, int32_t total_q,

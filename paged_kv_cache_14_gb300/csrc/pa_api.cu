@@ -820,15 +820,16 @@ static int chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_l
   if (num_seqs < 0 || max_q_len < 0 || max_kv_len < 0 || total_q < 0) return PA_ERR_ARG;
   if (num_seqs == 0 || max_q_len == 0 || total_q == 0) return PA_OK;
   if (!cu_q_lens || !ctx_lens) return PA_ERR_ARG;
-  if (dtype == PA_F32 && max_q_len > 1) return PA_ERR_DTYPE;
-  if (max_q_len > 1 && !(scale > 0.f)) return PA_ERR_ARG;  // the chunk kernel needs scale > 0
-  if (max_q_len > 1) {
+  // Chunks (q_len > 1): fp16 / bf16 on the tensor-core kernel, fp32 on the
+  // CUDA-core kernel (exact fp32; any scale and decode head_dim).
+  if (max_q_len > 1 && dtype != PA_F32) {
+    if (!(scale > 0.f)) return PA_ERR_ARG;  // the tensor-core chunk kernel needs scale > 0
     if (head_dim != 128 && !(head_dim == 64 && !kv_scales)) return PA_ERR_UNSUPPORTED;
     if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads) return PA_ERR_HEADS;
     const int32_t g = num_q_heads / num_kv_heads;
     if (g > 128) return PA_ERR_UNSUPPORTED;
-    if (max_q_len > total_q) return PA_ERR_ARG;
   }
+  if (max_q_len > 1 && max_q_len > total_q) return PA_ERR_ARG;
   const size_t dec_ws =
       pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_kv_len, 0);
   if (!workspace ||
@@ -849,6 +850,12 @@ static int chunked_prefill(const void* q, int32_t total_q, const int32_t* cu_q_l
     dp.kv_fmt = kv_fmt;
   }
   if (max_q_len <= 1) return launch_decode(dp, dtype, s);
+  if (dtype == PA_F32) {
+    // Decode rows on the fp32 decode path, then the chunk rows.
+    rc = launch_decode(dp, dtype, s);
+    if (rc != PA_OK) return rc;
+    return launch_prefill_simt(dp, total_q, s);
+  }
   // Chunks (q_len > 1): tcgen05 tiles. One plan lists the chunk items and
   // the decode rows' partitions and splits the SMs between them; the chunk
   // kernel runs on its share and the decode kernel beside it on the rest.

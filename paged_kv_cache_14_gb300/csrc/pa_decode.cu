@@ -1173,6 +1173,150 @@ static int launch_tc(const DecodeParams& p, cudaStream_t stream) {
   return launch_merge(pk, dt, stream);
 }
 
+// fp32 I/O chunk rows (q_len > 1) of a mixed batch: a CUDA-core path with
+// exact fp32 FMAs (the tensor cores' fp32 input kind rounds to TF32). One
+// CTA per (query row, KV-head row group); its four warps take the row's keys
+// 0 .. ctx + r round-robin, each lane holding head_dim / 32 dimensions, and
+// merge through shared memory. Every row reads its keys itself (no reuse
+// across the rows of a chunk): a path for exactness, not speed.
+template <int VEC>
+__global__ void __launch_bounds__(128) prefill_simt_kernel(const DecodeParams p) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int D = VEC * 32;
+  constexpr int ROWS = 8;
+  constexpr int NW = 4;
+  __shared__ float mls[NW][ROWS][2];
+  __shared__ float ob[NW][ROWS][D];
+
+  const int t = blockIdx.x;  // query row
+  const int kvh = blockIdx.y / p.row_groups;
+  const int rg = blockIdx.y - kvh * p.row_groups;
+  // The row's sequence: the last s with cu_q_lens[s] <= t.
+  int lo = 0, hi = p.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.cu_q_lens[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  const int seq = lo;
+  const int q0 = p.cu_q_lens[seq], ql = p.cu_q_lens[seq + 1] - q0;
+  if (ql <= 1 || t < q0 || t >= q0 + ql) return;  // decode rows go through the decode kernels
+  const int ctx = p.lens[seq];
+  const int BS = p.block_size;
+  if (ctx < 0 || ctx + ql > p.len_cap || ctx + ql > p.max_blocks_per_seq * BS) {
+    if (threadIdx.x == 0 && blockIdx.y == 0 && t == q0) record_error(p.status, PA_ERR_SEQLEN);
+    return;
+  }
+  const int nkeys = ctx + (t - q0) + 1;  // causal: keys 0 .. ctx + r
+  const int h0 = kvh * p.group + rg * p.rows_per_cta;
+  const int nrows = min(p.rows_per_cta, p.group - rg * p.rows_per_cta);
+  const int32_t* bt = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* qb = static_cast<const float*>(p.q) + ((int64_t)t * p.num_q_heads + h0) * D;
+  float q[ROWS][VEC], o[ROWS][VEC], m[ROWS], l[ROWS];
+#pragma unroll
+  for (int g = 0; g < ROWS; ++g) {
+    m[g] = -CUDART_INF_F;
+    l[g] = 0.f;
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+      q[g][v] = g < nrows ? qb[g * D + lane + 32 * v] : 0.f;
+      o[g][v] = 0.f;
+    }
+  }
+  const float* kc = static_cast<const float*>(p.k_cache);
+  const float* vc = static_cast<const float*>(p.v_cache);
+  for (int key = warp; key < nkeys; key += NW) {
+    const int id = bt[key / BS];
+    if (id < 0 || id >= p.num_blocks) {
+      if (lane == 0) record_error(p.status, PA_ERR_BLOCK_OOB);
+      continue;
+    }
+    const int64_t row = ((int64_t)id * p.num_kv_heads + kvh) * BS + (key % BS);
+    float kv[VEC], vv[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+      kv[v] = kc[row * D + lane + 32 * v];
+      vv[v] = vc[row * D + lane + 32 * v];
+    }
+#pragma unroll
+    for (int g = 0; g < ROWS; ++g) {
+      if (g >= nrows) break;
+      float d = 0.f;
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) d = fmaf(q[g][v], kv[v], d);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+      const float sc = d * p.scale_log2;
+      const float mn = fmaxf(m[g], sc);
+      const float a = exp2f(m[g] - mn);
+      const float e = exp2f(sc - mn);
+      l[g] = l[g] * a + e;
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) o[g][v] = fmaf(e, vv[v], o[g][v] * a);
+      m[g] = mn;
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int g = 0; g < ROWS; ++g) {
+      mls[warp][g][0] = m[g];
+      mls[warp][g][1] = l[g];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int g = 0; g < ROWS; ++g) {
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, mls[w][g][0]);
+    const float f = m[g] == -CUDART_INF_F ? 0.f : exp2f(m[g] - M);
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) ob[warp][g][lane + 32 * v] = o[g][v] * f;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < nrows * D; idx += blockDim.x) {
+    const int g = idx / D, d = idx - g * D;
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, mls[w][g][0]);
+    float L = 0.f, acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float mw = mls[w][g][0];
+      L += mw == -CUDART_INF_F ? 0.f : mls[w][g][1] * exp2f(mw - M);
+      acc += ob[w][g][d];
+    }
+    static_cast<float*>(p.out)[((int64_t)t * p.num_q_heads + h0 + g) * D + d] = acc / L;
+  }
+}
+
+template <int VEC>
+static int launch_prefill_simt_vec(const DecodeParams& p, int32_t total_q, cudaStream_t stream) {
+  const dim3 grid((unsigned)total_q, (unsigned)(p.num_kv_heads * p.row_groups));
+  return launch_dependent(prefill_simt_kernel<VEC>, grid, dim3(128), 0, stream, p) == cudaSuccess ? PA_OK
+                                                                                               : PA_ERR_CUDA;
+}
+
+int launch_prefill_simt(const DecodeParams& p0, int32_t total_q, cudaStream_t stream) {
+  DecodeParams p = p0;
+  decode_set_rows(p, PA_F32);
+  if ((int64_t)p.num_kv_heads * p.row_groups > 65535) return PA_ERR_UNSUPPORTED;
+  switch (p.head_dim) {
+    case 32: return launch_prefill_simt_vec<1>(p, total_q, stream);
+    case 64: return launch_prefill_simt_vec<2>(p, total_q, stream);
+    case 96: return launch_prefill_simt_vec<3>(p, total_q, stream);
+    case 128: return launch_prefill_simt_vec<4>(p, total_q, stream);
+    case 160: return launch_prefill_simt_vec<5>(p, total_q, stream);
+    case 192: return launch_prefill_simt_vec<6>(p, total_q, stream);
+    case 224: return launch_prefill_simt_vec<7>(p, total_q, stream);
+    case 256: return launch_prefill_simt_vec<8>(p, total_q, stream);
+  }
+  return PA_ERR_UNSUPPORTED;
+}
+
 template <int VEC>
 static int launch_simt(const DecodeParams& p, cudaStream_t stream) {
   decode_plan_kernel<float><<<1, 1024, 0, stream>>>(p);

@@ -215,6 +215,9 @@ int launch_copy_scales(float* kv_scales, const int32_t* src, const int32_t* dst,
 
 // Decode: split-KV main pass (+ merge pass when max_parts > 1).
 int launch_decode(const DecodeParams& p, pa_dtype dt, cudaStream_t stream);
+// fp32 I/O chunk rows (q_len > 1) of a mixed batch on CUDA cores (exact
+// fp32); the decode rows are launched separately (launch_decode).
+int launch_prefill_simt(const DecodeParams& p, int32_t total_q, cudaStream_t stream);
 // The decode plan alone (fp16/bf16), for a step that launches other kernels
 // between the plan and the decode: launch_decode then runs with
 // planned = 1 and its first kernel waits for the ones before it.

@@ -123,7 +123,7 @@ def test_prefill_host_checks(lib):
         a.update(o)
         return f(a["q"], a["tq"], a["cu"], a["k"], a["v"], a["bt"], a["mb"], a["ctx"], a["n"], a["mq"], a["mkv"],
                  a["hq"], a["hkv"], a["d"], a["bs"], a["nb"], a["scale"], a["out"], a["ws"], a["wsb"], a["dt"], None)
-    assert call(dt=pa.PA_F32) == -2          # fp32 chunks are not on the tensor-core path
+    assert call(dt=pa.PA_F32) == -5          # fp32 chunks run on CUDA cores: only the workspace is missing
     assert call(n=0) == 0                    # empty batch
     assert call(tq=0) == 0
     assert call(d=64) == -5                  # head_dim 64 is supported: only the workspace is missing

@@ -73,6 +73,25 @@ def test_prefill_head_dim_64(lib, case):
     assert_attention_close(out, oracle_prefill(b, kc, vc), dtype, f"{case} head_dim 64")
 
 
+CASES_F32 = [
+    # B, Hq, Hkv, D, q_lens, ctx_lens: fp32 I/O (chunk rows on the exact fp32 CUDA-core kernel)
+    (16, 8, 2, 64, [17, 1, 40], [5, 30, 100]),
+    (32, 32, 8, 128, [70, 1, 3, 129], [200, 10, 0, 31]),
+    (16, 12, 4, 96, [9, 130, 1], [0, 33, 64]),   # group 3, head_dim 96
+]
+
+
+@pytest.mark.parametrize("case", CASES_F32, ids=lambda c: f"f32-B{c[0]}-G{c[1] // c[2]}-D{c[3]}-q{sum(c[4])}")
+def test_prefill_fp32(lib, case):
+    B, hq, hkv, D, qls, ctxs = case
+    kv = [c + q for c, q in zip(ctxs, qls)]
+    b = build_batch(name="pf32", seed=CASES_F32.index(case) + 170, dtype="f32", block_size=B, num_q_heads=hq,
+                    num_kv_heads=hkv, head_dim=D, q_lens=qls, kv_lens=kv)
+    _, out = run_step(lib, b)
+    kc, vc, _ = oracle_caches_after_step(b)
+    assert_attention_close(out, oracle_prefill(b, kc, vc), "f32", f"{case} fp32")
+
+
 def test_prefill_garbage_in_unused_slots(lib):
     qls, ctxs = [40, 7], [10, 90]
     b = build_batch(name="pfnan", seed=9, dtype="f16", block_size=32, num_q_heads=64, num_kv_heads=8,
