@@ -577,7 +577,7 @@ def chunk_only_entry(pa, torch, st, batch, timer, calls: int) -> dict:
 
     def call():
         if st.kv_scales is not None:
-            chunked_8bit = getattr(pa, f"pa_chunked_prefill_{st._f8}")  # e4m3 (_fp8) or e5m2 codes
+            chunked_8bit = st.call_8bit("pa_chunked_prefill")  # e4m3 (_fp8) or e5m2 codes
             chunked_8bit(q, cuq, st.k_cache, st.v_cache, st.kv_scales, tables, ctx, max_q, st.max_seq_len,
                          batch.scale, out=out, workspace=ws)
         else:
@@ -780,7 +780,8 @@ def native_arm(args) -> None:
             "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": args.kv_cache if fp8 else batch.dtype,
-            "data": "synthetic (seeded)" + (f", {args.kv_cache} pools drawn as codes + per-block scales" if fp8 else ""),
+            "data": "synthetic (seeded)"
+                    + (f", {args.kv_cache} pools drawn as codes + per-block scales" if fp8 else ""),
             "pct_of_peak": round(100.0 * value / world / peak, 2),
             "seq_steps_per_s": round(world * batch.num_seqs / (ms_step * 1e-3), 1),
             "timing": {"timed_blocks": reps, "steps_per_block": args.steps,

@@ -40,7 +40,9 @@ class PagedStep:
         if kv_format not in ("e4m3", "e5m2"):
             raise ValueError(f"kv_format {kv_format!r}: e4m3 or e5m2")
         self.kv_format = kv_format
-        self._f8 = "fp8" if kv_format == "e4m3" else "e5m2"  # suffix of the 8-bit calls
+        # Suffix of the library's 8-bit calls for this format: pa_decode_fp8
+        # and friends hold e4m3 codes, the *_e5m2 calls e5m2 codes.
+        self.kv_call_suffix = "fp8" if kv_format == "e4m3" else "e5m2"
         self.block_tables, self.kv_lens = block_tables, kv_lens
         self.k_new, self.v_new = k_new, v_new
         self.new_seq_ids, self.new_positions = new_seq_ids, new_positions
@@ -122,7 +124,7 @@ class PagedStep:
         if self.is_decode and self.kv_scales is None and self.q.dtype != torch.float32:
             return "pa_decode_step (copy_blocks + slot_mapping + reshape_and_cache + pa_decode in one call)"
         if self.kv_scales is not None:
-            f = self._f8
+            f = self.kv_call_suffix
             return f"pa_copy_blocks_fp8 + pa_slot_mapping + pa_reshape_and_cache_{f} + " + (
                 f"pa_decode_shared_prefix_{f}" if self.shared_prefix else
                 f"pa_decode_{f}" if self.is_decode else f"pa_chunked_prefill_{f}")
@@ -132,7 +134,7 @@ class PagedStep:
     @property
     def attention_kernels(self) -> str:
         """What the step's attention call (attend()) runs on the device."""
-        f, fmt = self._f8, self.kv_format
+        f, fmt = self.kv_call_suffix, self.kv_format
         if self.kv_scales is not None and self.shared_prefix:
             return (f"pa_decode_shared_prefix_{f}: prefix check + tcgen05 prefix pass (codes widened in shared "
                     f"memory) + {fmt} split-KV suffix decode + merge")
@@ -181,27 +183,32 @@ class PagedStep:
         pa.pa_slot_mapping(self.block_tables, self.new_seq_ids, self.new_positions, self.block_size,
                            self.num_blocks, slot_mapping=self.slot_mapping, stream=stream)
         if fp8:
-            getattr(pa, f"pa_reshape_and_cache_{self._f8}")(self.k_new, self.v_new, self.slot_mapping, self.k_cache,
-                                                            self.v_cache, self.kv_scales, stream=stream)
+            write_8bit = self.call_8bit("pa_reshape_and_cache")
+            write_8bit(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache, self.kv_scales,
+                       stream=stream)
         else:
             pa.pa_reshape_and_cache(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
                                     stream=stream)
 
+    def call_8bit(self, name: str):
+        """The binding's 8-bit form of a call for this cache's format."""
+        return getattr(pa, f"{name}_{self.kv_call_suffix}")
+
     def attend(self, stream=None) -> torch.Tensor:
         """The attention call of the step alone."""
         if self.kv_scales is not None and self.shared_prefix:
-            getattr(pa, f"pa_decode_shared_prefix_{self._f8}")(self.q, self.k_cache, self.v_cache, self.kv_scales, self.block_tables,
-                                           self.kv_lens, self.max_seq_len, self.group_starts, self.prefix_lens,
-                                           self.scale, out=self.out, partition_size=self.partition_size,
-                                           workspace=self.workspace, stream=stream)
+            self.call_8bit("pa_decode_shared_prefix")(
+                self.q, self.k_cache, self.v_cache, self.kv_scales, self.block_tables, self.kv_lens, self.max_seq_len,
+                self.group_starts, self.prefix_lens, self.scale, out=self.out, partition_size=self.partition_size,
+                workspace=self.workspace, stream=stream)
         elif self.kv_scales is not None and not self.is_decode:
-            getattr(pa, f"pa_chunked_prefill_{self._f8}")(self.q, self.cu_q_lens, self.k_cache, self.v_cache, self.kv_scales,
-                                      self.block_tables, self.ctx_lens, self.max_q_len, self.max_seq_len, self.scale,
-                                      out=self.out, workspace=self.workspace, stream=stream)
+            self.call_8bit("pa_chunked_prefill")(
+                self.q, self.cu_q_lens, self.k_cache, self.v_cache, self.kv_scales, self.block_tables, self.ctx_lens,
+                self.max_q_len, self.max_seq_len, self.scale, out=self.out, workspace=self.workspace, stream=stream)
         elif self.kv_scales is not None:
-            getattr(pa, f"pa_decode_{self._f8}")(self.q, self.k_cache, self.v_cache, self.kv_scales, self.block_tables, self.kv_lens,
-                             self.max_seq_len, self.scale, out=self.out, partition_size=self.partition_size,
-                             workspace=self.workspace, stream=stream)
+            self.call_8bit("pa_decode")(
+                self.q, self.k_cache, self.v_cache, self.kv_scales, self.block_tables, self.kv_lens, self.max_seq_len,
+                self.scale, out=self.out, partition_size=self.partition_size, workspace=self.workspace, stream=stream)
         elif self.shared_prefix:
             pa.pa_decode_shared_prefix(self.q, self.k_cache, self.v_cache, self.block_tables, self.kv_lens,
                                        self.max_seq_len, self.group_starts, self.prefix_lens, self.scale,
