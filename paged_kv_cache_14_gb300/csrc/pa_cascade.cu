@@ -97,7 +97,10 @@ __global__ void __launch_bounds__(1024) cascade_prep_kernel(const DecodeParams p
   // 2. Reference member of every group: the longest requested prefix.
   for (int s = tid; s < N && groups_ok; s += nt) {
     const int g = gof[s];
-    atomicMax(&ref[g], ((pfx[s] / B) << 16) | (s - gs[g]));
+    // Key: prefix blocks (clamped to 16 bits; beyond that a tie, which can
+    // only drop hints) above the member index, compared as unsigned.
+    const uint32_t key = ((uint32_t)min(pfx[s] / B, 65535) << 16) | (uint32_t)(s - gs[g]);
+    atomicMax(reinterpret_cast<unsigned int*>(&ref[g]), key);
   }
   __syncthreads();
   for (int g = tid; g < num_groups && groups_ok; g += nt) ref[g] = gs[g] + (ref[g] & 0xffff);
@@ -141,7 +144,7 @@ __global__ void __launch_bounds__(1024) cascade_prep_kernel(const DecodeParams p
     for (int t = s; t < end; ++t) keys = max(keys, pfx[t]);
     if (keys > 0) {
       const int slot = atomicAdd(&count, 1);
-      pairs[slot] = (g << 16) | (m / members_per_tile);
+      pairs[slot] = pack_pair(g, m / members_per_tile);
       pair_keys[slot] = keys;
     }
   }

@@ -224,9 +224,9 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
     // one item ahead, so the item switch costs no dependent global loads.
     int next_pr = 0, next_qrow = 0, next_len = 0, next_pfx = 0;
     if (next < total) {
-      next_pr = stat ? (next / hr) << 16 : p.pairs[next / hr];
-      decode_row(p, next_pr >> 16, next_qrow, next_len);
-      next_pfx = p.prefix ? p.prefix[next_pr >> 16] : 0;
+      next_pr = stat ? pack_pair(next / hr, 0) : p.pairs[next / hr];
+      decode_row(p, pair_hi(next_pr), next_qrow, next_len);
+      next_pfx = p.prefix ? p.prefix[pair_hi(next_pr)] : 0;
     }
     int jg = 0;  // stages issued so far (global stage sequence)
     bool bad = false;
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
       // so once its first item is issued)
       if (planned_now && lane == 0) next = atomicAdd(&p.work[0], 1);
       const int hg = item - (item / hr) * hr;
-      const int seq = pr >> 16, part = pr & 0xffff;
+      const int seq = pair_hi(pr), part = pair_lo(pr);
       const int kvh = hg / p.row_groups, rgi = hg - kvh * p.row_groups;
       const int t_begin = pfx + part * p.partition;  // the suffix starts after the shared prefix
       // A row of illegal length (listed only so that first partitions keep
@@ -395,8 +395,8 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
           next = __shfl_sync(0xffffffffu, next, 0);
           if (next < total) {
             next_pr = p.pairs[next / hr];
-            decode_row(p, next_pr >> 16, next_qrow, next_len);
-            next_pfx = p.prefix ? p.prefix[next_pr >> 16] : 0;
+            decode_row(p, pair_hi(next_pr), next_qrow, next_len);
+            next_pfx = p.prefix ? p.prefix[pair_hi(next_pr)] : 0;
           }
         }
 #pragma unroll
@@ -417,8 +417,8 @@ __global__ void __launch_bounds__(DecCfg<D, BS, NT, KV8>::kThreads, NT == 1 ? 2 
         next = __shfl_sync(0xffffffffu, next, 0);
         if (next < total) {
           next_pr = p.pairs[next / hr];
-          decode_row(p, next_pr >> 16, next_qrow, next_len);
-          next_pfx = p.prefix ? p.prefix[next_pr >> 16] : 0;
+          decode_row(p, pair_hi(next_pr), next_qrow, next_len);
+          next_pfx = p.prefix ? p.prefix[pair_hi(next_pr)] : 0;
         }
       }
     }

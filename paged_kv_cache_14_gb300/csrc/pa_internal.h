@@ -13,6 +13,16 @@ namespace pa {
 // 8-bit cache formats (with kv_scales): OCP FP8 E4M3 or E5M2.
 enum KvFormat : int32_t { PA_KV_E4M3 = 0, PA_KV_E5M2 = 1 };
 
+// Work-list entries: a sequence (or sharing group) index below 65536 in the
+// upper 16 bits and a partition or tile index below 65536 in the lower 16,
+// packed and unpacked as unsigned so that indices from 32768 up stay
+// positive.
+__host__ __device__ __forceinline__ int32_t pack_pair(int hi, int lo) {
+  return (int32_t)(((uint32_t)hi << 16) | ((uint32_t)lo & 0xffffu));
+}
+__host__ __device__ __forceinline__ int pair_hi(int32_t v) { return (int)((uint32_t)v >> 16); }
+__host__ __device__ __forceinline__ int pair_lo(int32_t v) { return (int)((uint32_t)v & 0xffffu); }
+
 // Largest partition (tokens) one decode CTA walks; bounds the shared-memory
 // copy of the partition's block ids.
 constexpr int kMaxPartition = 16384;
@@ -47,7 +57,7 @@ struct DecodeParams {
   // sequences with more than one split-KV partition (written by the plan).
   int4* merge_list;
   int32_t* work;         // [0] next work item, [1] number of work items, [2] sequences to merge (plan)
-  int32_t* pairs;        // [num_seqs * max_parts] (seq << 16 | partition), in work order
+  int32_t* pairs;        // [num_seqs * max_parts] pack_pair(seq, partition), in work order
   // Shared-prefix (cascade) decode: tokens [0, prefix[i]) of sequence i were
   // attended by the prefix pass, whose partial sits in slot 0; the suffix
   // partitions use slots 1.. . nullptr / 0 for plain decode.
@@ -125,7 +135,7 @@ struct PrefillParams {
   int32_t tile_pos;  // query positions (or group members) per 128-row Q tile: floor(128 / group)
   float scale_log2;
   int32_t* work;     // [0] next work item, [1] number of work items, [2] CTAs that run items (chunks)
-  int32_t* pairs;    // (seq << 16 | row tile), longest first; prefix pass: (group << 16 | member tile)
+  int32_t* pairs;    // pack_pair(seq, row tile), longest first; prefix pass: pack_pair(group, member tile)
   int32_t ctas;      // grid of the chunk kernel
   int32_t num_sms;
   // Mixed batches: KV bytes of one decode-row token (K and V, all KV heads)

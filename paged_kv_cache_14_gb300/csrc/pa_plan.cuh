@@ -107,15 +107,15 @@ __device__ __forceinline__ void decode_plan_body(const DecodeParams& p, const in
     int qrow, len;
     if (!row(s, qrow, len)) continue;
     if (!len_ok(p, len)) {
-      if (p.static_first) p.pairs[base0++] = s << 16;
+      if (p.static_first) p.pairs[base0++] = pack_pair(s, 0);
       continue;
     }
     const int sl = len - prefix_of(s);
     const int n = (sl + P - 1) / P;
     const int first_binned = p.prefix ? 0 : 1;
-    if (!p.prefix) p.pairs[base0++] = s << 16;
+    if (!p.prefix) p.pairs[base0++] = pack_pair(s, 0);
     for (int part = first_binned; part < n; ++part)
-      p.pairs[atomicAdd(&hist[bin_of(sl, part)], 1)] = (s << 16) | part;
+      p.pairs[atomicAdd(&hist[bin_of(sl, part)], 1)] = pack_pair(s, part);
     // One suffix partition: written by the decode kernel (alone, or merged
     // there with the prefix partial); more: listed for the merge kernel.
     if (n > 1 && p.merge_list) {

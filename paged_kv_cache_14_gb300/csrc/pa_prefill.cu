@@ -170,7 +170,7 @@ __device__ __forceinline__ int64_t prefill_plan_body(const PrefillParams& p) {
     const int nm = (ql + pp - 1) / pp;
     for (int mt = 0; mt < nm; ++mt) {
       const int slot = atomicAdd(&hist[tiles_of(s, mt)], 1);
-      p.pairs[slot] = (s << 16) | mt;
+      p.pairs[slot] = pack_pair(s, mt);
     }
   }
   if (threadIdx.x == 0) {
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
     const int pi = item / p.num_kv_heads;
     const int pr = p.pairs[pi];
     const int kvh = item - pi * p.num_kv_heads;
-    const int mt = pr & 0xffff;
+    const int mt = pair_lo(pr);
     // Item geometry (kQT * pp positions from pos_lo). Chunk: rows are query
     // positions of sequence `seq`; prefix pass: rows are members of group
     // `grp`, keys are the group's shared prefix read through the reference
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
     int seq, q_z, q0 = 0, ql = 0, ctx = 0, kv_len, keys, grp = 0, s0 = 0, m_hi = 0;
     const int pos_lo = mt * kQT * pp;
     if constexpr (!PREFIX) {
-      seq = pr >> 16;
+      seq = pair_hi(pr);
       q0 = p.cu_q_lens[seq];
       ql = p.cu_q_lens[seq + 1] - q0;
       ctx = p.ctx_lens[seq];
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(pf::threads<KV8>(), 1)
       keys = ctx + min(pos_lo + kQT * pp, ql);  // keys the item's last row needs
       q_z = q0 + pos_lo;
     } else {
-      grp = pr >> 16;
+      grp = pair_hi(pr);
       s0 = p.group_starts[grp];
       m_hi = min(pos_lo + kQT * pp, p.group_starts[grp + 1] - s0);
       seq = p.group_ref[grp];

@@ -70,6 +70,12 @@ def test_decode_host_checks(lib):
     assert _decode_raw(lib, part=24) == -1              # partition not a multiple of block_size
     assert _decode_raw(lib, maxlen=1000) == -5          # a workspace is always needed
     assert _decode_raw(lib, maxlen=1000, ws=0x7000, wsb=10) == -5
+    # Limits: 65535 sequences and 12288 split-KV partitions are accepted (the
+    # call then asks for its workspace); one more of either is refused.
+    assert _decode_raw(lib, n=65535, maxlen=1000) == -5
+    assert _decode_raw(lib, n=65536) == -10             # PA_ERR_UNSUPPORTED
+    assert _decode_raw(lib, maxlen=12288 * 16, part=16) == -5
+    assert _decode_raw(lib, maxlen=12289 * 16, part=16) == -1
 
 
 def test_partition_and_workspace_sizes(lib):
