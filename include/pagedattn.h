@@ -379,6 +379,10 @@ int pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, c
  * (PA_ERR_UNSUPPORTED otherwise) and scale > 0 (PA_ERR_ARG); fp32 chunks go
  * through a CUDA-core kernel with exact fp32 arithmetic (head_dim as for
  * fp32 decode, any scale), one query row at a time: exact, not fast.
+ * Precondition of the tensor-core kernel, not checked by this version: one
+ * chunk holds at most 65536 work items of two tiles, i.e. max_q_len <=
+ * 65536 * 2 * floor(128 / G) (131072 rows at G = 128, 2097152 at G = 8);
+ * rows of a longer chunk past that bound are not computed.
  */
 size_t pa_chunked_prefill_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t block_size, int32_t total_q,
